@@ -1,0 +1,204 @@
+"""CPU oracle for the speculative-decoding verification row (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+binding) never does.  The arithmetic lives in ``spec_oracle.c`` (plain C,
+double precision, single-threaded); this module compiles it with gcc on first
+use and exposes numpy-friendly wrappers through ctypes.
+
+Each wrapper names the passage it follows in the C source header.  Pins that
+tie the oracle to the pages and to mathematics (closed forms, exact enumerated
+distributions, a chi-square test, library special cases, brute force) are in
+``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "spec_oracle.c")
+LIB = os.path.join(HERE, "libspec_oracle.so")
+
+OK, EINVAL, EBADINDEX = 0, -1, -2
+ACCEPT_TIE = 1e-5   # |r - p/q| window of a flagged accept test
+SAMPLE_TIE = 1e-6   # window (in units of Z) of a flagged final sample
+DTYPE_CODE = {"f32": 0, "bf16": 1}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(src: str = SRC, out: str = LIB, force: bool = False) -> str:
+    """Compile the oracle C source into a shared library (gcc, -O2, no fast-math)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.oracle_softmax.argtypes = [P, I, ctypes.c_double, I, P]
+    lib.oracle_inverse_cdf.argtypes = [P, I, ctypes.c_double, ctypes.c_double, P]
+    lib.oracle_argmax.argtypes = [P, I, I]
+    lib.oracle_verify_chain.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P]
+    lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P]
+    lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
+    lib.oracle_rollback.argtypes = [P, P, I, I, P, P]
+    for f in ("oracle_softmax", "oracle_inverse_cdf", "oracle_argmax", "oracle_verify_chain",
+              "oracle_verify_greedy", "oracle_verify_tree", "oracle_rollback"):
+        getattr(lib, f).restype = I
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library; ``path`` loads another build."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _logits(a, dtype: str):
+    return _c(a, np.uint16 if dtype == "bf16" else np.float32)
+
+
+def softmax(x, temperature: float, dtype: str = "f32", lib=None) -> np.ndarray:
+    """softmax(x / T) in double (vLLM learning book, section 2).
+
+    T is rounded to float32 first, as the verify calls take it."""
+    lib = lib or load()
+    x = _logits(x, dtype)
+    p = np.empty(x.shape[-1], dtype=np.float64)
+    rc = lib.oracle_softmax(_ptr(x), DTYPE_CODE[dtype], float(np.float32(temperature)),
+                            x.shape[-1], _ptr(p))
+    if rc != OK:
+        raise ValueError(f"oracle_softmax rc={rc}")
+    return p
+
+
+def inverse_cdf(w, u: float, tol: float = SAMPLE_TIE, lib=None):
+    """(token, near_tie) of the inverse-CDF draw from weights ``w`` at uniform ``u``."""
+    lib = lib or load()
+    w = _c(w, np.float64)
+    tie = np.zeros(1, dtype=np.int32)
+    t = lib.oracle_inverse_cdf(_ptr(w), w.shape[0], float(u), float(tol), _ptr(tie))
+    return int(t), bool(tie[0])
+
+
+def argmax(x, dtype: str = "f32", lib=None) -> int:
+    lib = lib or load()
+    x = _logits(x, dtype)
+    return int(lib.oracle_argmax(_ptr(x), DTYPE_CODE[dtype], x.shape[-1]))
+
+
+def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, dtype: str = "f32",
+                 lib=None) -> dict:
+    """Chain rejection-sampling verify (vLLM anatomy page, "Speculative Decoding").
+
+    target [B,k+1,V], draft [B,k,V] (fp32 values or raw bf16 bits),
+    draft_tokens int [B,k], uniforms float32 [B,k+1].  Returns a dict with
+    tokens [B,k+1], num_accepted [B], probs [B,k,2] (p_i(x_i), q_i(x_i)),
+    flags [B,k+1] and the return code.
+    """
+    lib = lib or load()
+    target = _logits(target, dtype)
+    draft = _logits(draft, dtype)
+    B, k1, V = target.shape
+    k = k1 - 1
+    assert draft.shape == (B, k, V)
+    x = _c(draft_tokens, np.int32)
+    r = _c(uniforms, np.float32)
+    assert x.shape == (B, k) and r.shape == (B, k + 1)
+    tokens = np.empty((B, k + 1), dtype=np.int32)
+    n_acc = np.empty(B, dtype=np.int32)
+    probs = np.empty((B, k, 2), dtype=np.float64)
+    flags = np.empty((B, k + 1), dtype=np.int32)
+    rc = lib.oracle_verify_chain(_ptr(target), _ptr(draft), DTYPE_CODE[dtype], _ptr(x), _ptr(r),
+                                 float(temperature), B, k, V, _ptr(tokens), _ptr(n_acc),
+                                 _ptr(probs), _ptr(flags))
+    if rc not in (OK, EBADINDEX):
+        raise ValueError(f"oracle_verify_chain rc={rc}")
+    return dict(tokens=tokens, num_accepted=n_acc, probs=probs, flags=flags, rc=rc)
+
+
+def verify_greedy(target, draft_tokens, dtype: str = "f32", lib=None) -> dict:
+    """Greedy chain verify (Kestrel article, section 3.3)."""
+    lib = lib or load()
+    target = _logits(target, dtype)
+    B, k1, V = target.shape
+    k = k1 - 1
+    d = _c(draft_tokens, np.int32)
+    assert d.shape == (B, k)
+    tokens = np.empty((B, k + 1), dtype=np.int32)
+    n_acc = np.empty(B, dtype=np.int32)
+    rc = lib.oracle_verify_greedy(_ptr(target), DTYPE_CODE[dtype], _ptr(d), B, k, V,
+                                  _ptr(tokens), _ptr(n_acc))
+    if rc not in (OK, EBADINDEX):
+        raise ValueError(f"oracle_verify_greedy rc={rc}")
+    return dict(tokens=tokens, num_accepted=n_acc, rc=rc)
+
+
+def verify_tree(target, tree_tokens, paths, dtype: str = "f32", lib=None) -> dict:
+    """Greedy tree verify (TensorRT-LLM deployment page, "Eagle-2" section)."""
+    lib = lib or load()
+    target = _logits(target, dtype)
+    B, N, V = target.shape
+    tok = _c(tree_tokens, np.int32)
+    pth = _c(paths, np.int32)
+    _, P, L = pth.shape
+    assert tok.shape == (B, N) and pth.shape[0] == B
+    tokens = np.empty((B, L), dtype=np.int32)
+    n_acc = np.empty(B, dtype=np.int32)
+    best = np.empty(B, dtype=np.int32)
+    nodes = np.empty((B, L), dtype=np.int32)
+    rc = lib.oracle_verify_tree(_ptr(target), DTYPE_CODE[dtype], _ptr(tok), _ptr(pth), B, N, P, L,
+                                V, _ptr(tokens), _ptr(n_acc), _ptr(best), _ptr(nodes))
+    if rc not in (OK, EBADINDEX):
+        raise ValueError(f"oracle_verify_tree rc={rc}")
+    return dict(tokens=tokens, num_accepted=n_acc, best_path=best, accepted_nodes=nodes, rc=rc)
+
+
+def rollback(old_lens, num_accepted, k: int, lib=None) -> dict:
+    """KV cursor rollback (TensorRT-LLM walkthrough, update_requests / rewind_cache)."""
+    lib = lib or load()
+    old = _c(old_lens, np.int32)
+    n = _c(num_accepted, np.int32)
+    B = old.shape[0]
+    new = np.empty(B, dtype=np.int32)
+    rew = np.empty(B, dtype=np.int32)
+    rc = lib.oracle_rollback(_ptr(old), _ptr(n), int(k), B, _ptr(new), _ptr(rew))
+    if rc not in (OK, EBADINDEX):
+        raise ValueError(f"oracle_rollback rc={rc}")
+    return dict(new_lens=new, rewind_lens=rew, rc=rc)
+
+
+def verify(w: dict, greedy: bool = False, lib=None) -> dict:
+    """Run the oracle on a workload dict from ``workloads.make``."""
+    if w["kind"] == "tree":
+        return verify_tree(w["target"], w["tree_tokens"], w["paths"], w["dtype"], lib=lib)
+    if greedy:
+        return verify_greedy(w["target"], w["draft_tokens"], w["dtype"], lib=lib)
+    return verify_chain(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
+                        w["temperature"], w["dtype"], lib=lib)

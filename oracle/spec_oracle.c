@@ -1,0 +1,412 @@
+/*
+ * CPU oracle for the speculative-decoding verification row.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header or constant with the CUDA
+ * library; it is plain, single-threaded C in double precision, written so that
+ * each step can be read against the pages:
+ *
+ *   - softmax of logits / T ........ vLLM learning book, section 2 (algorithm
+ *                                     flowchart: p and q are the target and
+ *                                     draft distributions); TensorRT-LLM
+ *                                     walkthrough, rejection-sampling section
+ *                                     (target and draft filtered alike).
+ *   - left-to-right accept scan .... vLLM anatomy page, "Speculative Decoding"
+ *                                     (accept/reject steps); vLLM learning
+ *                                     book, section 2 (r < min(1, p/q)).
+ *   - residual / bonus sample ....... vLLM anatomy page, same list (rebalanced
+ *                                     distribution max(0, p - q) normalised;
+ *                                     bonus token from row k+1).
+ *   - output row, -1 padded ........ TensorRT-LLM walkthrough, rejection-
+ *                                     sampling section (accepted_tokens
+ *                                     [batch, D+1]).
+ *   - greedy verify ................. Kestrel article, section 3.3 (accept
+ *                                     while argmax equals the draft; emit the
+ *                                     target's own token).
+ *   - tree verify ................... TensorRT-LLM deployment page, "Eagle-2"
+ *                                     section (paths [batch, max_decoding_
+ *                                     tokens, max_path_len]).
+ *   - rollback lengths .............. TensorRT-LLM walkthrough, update_requests
+ *                                     and rewind_cache sections (rewind =
+ *                                     verified - accepted; cursor truncation).
+ *
+ * Readings taken where the pages are silent:
+ *   target row i and draft row i both describe token x_i; row k is the bonus
+ *   row; uniforms[b, 0..k-1] drive the accept tests and uniforms[b, k] drives
+ *   the single final sample; accept iff r < p/q (q == 0 accepts); the inverse
+ *   CDF picks the smallest t with C(t) > u*Z; argmax ties go to the lowest id.
+ *
+ * Precision: every logit is widened exactly to double, z = x / T in double,
+ * exp() from libm, all sums sequential in token order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+#define ORC_EBADINDEX (-2)
+#define ORC_ENOMEM (-6)
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* Near-tie windows: an accept test with |r - p/q| below ACCEPT_TIE, or a final
+ * sample whose u*Z lies within SAMPLE_TIE*Z of a CDF boundary, is flagged. */
+static const double ACCEPT_TIE = 1e-5;
+static const double SAMPLE_TIE = 1e-6;
+
+/* One stored logit, widened exactly to double. */
+static double logit_at(const void *base, int dtype, size_t i)
+{
+    if (dtype == ORC_F32)
+        return (double)((const float *)base)[i];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* p(t) = exp(z_t - max z) / sum_s exp(z_s - max z), z = x / T. */
+int oracle_softmax(const void *x, int dtype, double temperature, int V, double *p)
+{
+    if (!x || !p || V < 1 || !(temperature > 0.0) || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_EINVAL;
+    double zmax = -INFINITY;
+    for (int t = 0; t < V; ++t) {
+        p[t] = logit_at(x, dtype, (size_t)t) / temperature;
+        if (p[t] > zmax)
+            zmax = p[t];
+    }
+    double sum = 0.0;
+    for (int t = 0; t < V; ++t) {
+        p[t] = exp(p[t] - zmax);
+        sum += p[t];
+    }
+    for (int t = 0; t < V; ++t)
+        p[t] /= sum;
+    return ORC_OK;
+}
+
+/* Inverse-CDF draw from non-negative weights w[0..V).
+ * Returns the smallest t with C(t) = w_0 + ... + w_t > u * Z, Z = C(V-1); when
+ * rounding leaves no such t, the last t with w_t > 0.  Returns -1 if Z == 0.
+ * *near_tie is set when u*Z lies within tol*Z of C(t) or of C(t-1). */
+int oracle_inverse_cdf(const double *w, int V, double u, double tol, int32_t *near_tie)
+{
+    if (near_tie)
+        *near_tie = 0;
+    if (!w || V < 1)
+        return ORC_EINVAL;
+    double Z = 0.0;
+    for (int t = 0; t < V; ++t)
+        Z += w[t];
+    if (!(Z > 0.0))
+        return -1;
+    double target = u * Z;
+    double c_prev = 0.0, c = 0.0;
+    int tok = -1;
+    for (int t = 0; t < V; ++t) {
+        c_prev = c;
+        c += w[t];
+        if (c > target) {
+            tok = t;
+            break;
+        }
+    }
+    if (tok < 0) {
+        for (int t = V - 1; t >= 0; --t)
+            if (w[t] > 0.0) {
+                tok = t;
+                break;
+            }
+        c = Z;
+        c_prev = Z - w[tok];
+    }
+    if (near_tie)
+        *near_tie = (fabs(c - target) <= tol * Z) || (fabs(c_prev - target) <= tol * Z);
+    return tok;
+}
+
+/* First index of the largest stored value (ties: lowest index). */
+int oracle_argmax(const void *x, int dtype, int V)
+{
+    if (!x || V < 1)
+        return ORC_EINVAL;
+    int best = 0;
+    double bv = logit_at(x, dtype, 0);
+    for (int t = 1; t < V; ++t) {
+        double v = logit_at(x, dtype, (size_t)t);
+        if (v > bv) {
+            bv = v;
+            best = t;
+        }
+    }
+    return best;
+}
+
+static void fail_closed_row(int32_t *row, int width, int32_t *n_acc)
+{
+    for (int i = 0; i < width; ++i)
+        row[i] = -1;
+    *n_acc = -1;
+}
+
+/* Chain rejection-sampling verify for B requests with k drafts each.
+ *   target:  [B, k+1, V] logits (row k is the bonus row)
+ *   draft:   [B, k, V] logits
+ *   draft_tokens [B, k], uniforms [B, k+1] (column k drives the final sample)
+ *   out_tokens [B, k+1]: accepted drafts, then the corrected/bonus token, -1 pad
+ *   out_num_accepted [B]: n_acc in [0, k]; -1 for a request whose draft token
+ *     lies outside [0, V) (its row is all -1 and the call returns EBADINDEX)
+ *   out_probs [B, k, 2] (nullable): p_i(x_i), q_i(x_i)
+ *   out_flags [B, k+1] (nullable): 1 at each accept test that is a near-tie
+ *     (positions 0..n_acc), and at column k when the final sample is one. */
+int oracle_verify_chain(const void *target, const void *draft, int dtype,
+                        const int32_t *draft_tokens, const float *uniforms,
+                        float temperature, int B, int k, int V,
+                        int32_t *out_tokens, int32_t *out_num_accepted,
+                        double *out_probs, int32_t *out_flags)
+{
+    if (!target || !draft || !draft_tokens || !uniforms || !out_tokens || !out_num_accepted ||
+        B < 1 || k < 1 || V < 2 || !(temperature > 0.0f) || !isfinite(temperature) ||
+        (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_EINVAL;
+    const double T = (double)temperature;
+    double *p = malloc(sizeof(double) * (size_t)V);
+    double *q = malloc(sizeof(double) * (size_t)V);
+    double *w = malloc(sizeof(double) * (size_t)V);
+    double *ratio = malloc(sizeof(double) * (size_t)k);
+    if (!p || !q || !w || !ratio) {
+        free(p), free(q), free(w), free(ratio);
+        return ORC_ENOMEM;
+    }
+    const size_t es = dtype == ORC_F32 ? 4 : 2;
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)b * (size_t)(k + 1) * (size_t)V * es;
+        const char *db = (const char *)draft + (size_t)b * (size_t)k * (size_t)V * es;
+        const int32_t *x = draft_tokens + (size_t)b * k;
+        const float *r = uniforms + (size_t)b * (k + 1);
+        int32_t *out = out_tokens + (size_t)b * (k + 1);
+        int32_t *flags = out_flags ? out_flags + (size_t)b * (k + 1) : NULL;
+        if (flags)
+            for (int i = 0; i <= k; ++i)
+                flags[i] = 0;
+        int bad = 0;
+        for (int i = 0; i < k; ++i)
+            if (x[i] < 0 || x[i] >= V)
+                bad = 1;
+        if (bad) {
+            fail_closed_row(out, k + 1, &out_num_accepted[b]);
+            if (out_probs)
+                for (int i = 0; i < 2 * k; ++i)
+                    out_probs[(size_t)b * 2 * k + i] = NAN;
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        /* p_i(x_i) and q_i(x_i) for every draft position. */
+        for (int i = 0; i < k; ++i) {
+            oracle_softmax(tb + (size_t)i * V * es, dtype, T, V, p);
+            oracle_softmax(db + (size_t)i * V * es, dtype, T, V, q);
+            double pi = p[x[i]], qi = q[x[i]];
+            if (out_probs) {
+                out_probs[((size_t)b * k + i) * 2 + 0] = pi;
+                out_probs[((size_t)b * k + i) * 2 + 1] = qi;
+            }
+            ratio[i] = qi > 0.0 ? pi / qi : INFINITY;
+        }
+        /* Left to right: accept x_i while r_i < p_i(x_i) / q_i(x_i). */
+        int j = k;
+        for (int i = 0; i < k; ++i) {
+            if (flags && fabs((double)r[i] - ratio[i]) < ACCEPT_TIE)
+                flags[i] = 1;
+            if (!((double)r[i] < ratio[i])) {
+                j = i;
+                break;
+            }
+        }
+        /* Final token: residual max(0, p_j - q_j) after a rejection, else p_k. */
+        oracle_softmax(tb + (size_t)j * V * es, dtype, T, V, p);
+        if (j < k) {
+            oracle_softmax(db + (size_t)j * V * es, dtype, T, V, q);
+            for (int t = 0; t < V; ++t)
+                w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0;
+        } else {
+            memcpy(w, p, sizeof(double) * (size_t)V);
+        }
+        int32_t tie = 0;
+        int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);
+        if (tok < 0) /* residual mass vanished numerically: fall back to p_j */
+            tok = oracle_inverse_cdf(p, V, (double)r[k], SAMPLE_TIE, &tie);
+        if (flags)
+            flags[k] = tie;
+        for (int i = 0; i < j; ++i)
+            out[i] = x[i];
+        out[j] = tok;
+        for (int i = j + 1; i <= k; ++i)
+            out[i] = -1;
+        out_num_accepted[b] = j;
+    }
+    free(p), free(q), free(w), free(ratio);
+    return rc;
+}
+
+/* Greedy chain verify: g_i = argmax target[b,i,:]; n_acc = the longest prefix
+ * with g_i == d_i; output d_0..d_{n_acc-1}, g_{n_acc}, -1 pad. */
+int oracle_verify_greedy(const void *target, int dtype, const int32_t *draft_tokens,
+                         int B, int k, int V, int32_t *out_tokens, int32_t *out_num_accepted)
+{
+    if (!target || !draft_tokens || !out_tokens || !out_num_accepted || B < 1 || k < 1 || V < 2 ||
+        (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_EINVAL;
+    const size_t es = dtype == ORC_F32 ? 4 : 2;
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)b * (size_t)(k + 1) * (size_t)V * es;
+        const int32_t *d = draft_tokens + (size_t)b * k;
+        int32_t *out = out_tokens + (size_t)b * (k + 1);
+        int bad = 0;
+        for (int i = 0; i < k; ++i)
+            if (d[i] < 0 || d[i] >= V)
+                bad = 1;
+        if (bad) {
+            fail_closed_row(out, k + 1, &out_num_accepted[b]);
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        int j = 0;
+        while (j < k && oracle_argmax(tb + (size_t)j * V * es, dtype, V) == d[j])
+            ++j;
+        for (int i = 0; i < j; ++i)
+            out[i] = d[i];
+        out[j] = oracle_argmax(tb + (size_t)j * V * es, dtype, V);
+        for (int i = j + 1; i <= k; ++i)
+            out[i] = -1;
+        out_num_accepted[b] = j;
+    }
+    return rc;
+}
+
+/* Greedy tree verify over EAGLE-style paths.
+ *   target [B, N, V]: row n is the distribution after node n (node 0 = root)
+ *   tree_tokens [B, N]: node n's token; paths [B, P, L]: root-to-leaf node
+ *   lists, -1 padded; a path whose first entry is -1 is unused, a used path
+ *   starts at node 0.
+ * For each used path walk j = 1..L-1 while the node is >= 0 and its token
+ * equals argmax of its parent's row; keep the path with the most accepted
+ * steps (ties: lowest path index).  Outputs: out_tokens [B, L] = accepted
+ * tokens then argmax of the last accepted node's row, -1 pad;
+ * out_best_path [B] (nullable, -1 when no path is used);
+ * out_accepted_nodes [B, L] (nullable) = root and accepted nodes, -1 pad.
+ * A request with a node id outside [-1, N), a path that starts elsewhere than
+ * 0 or -1, or a token outside [0, V) fails closed (n_acc -1, rows all -1). */
+int oracle_verify_tree(const void *target, int dtype, const int32_t *tree_tokens,
+                       const int32_t *paths, int B, int N, int P, int L, int V,
+                       int32_t *out_tokens, int32_t *out_num_accepted,
+                       int32_t *out_best_path, int32_t *out_accepted_nodes)
+{
+    if (!target || !tree_tokens || !paths || !out_tokens || !out_num_accepted || B < 1 ||
+        N < 1 || P < 1 || L < 2 || V < 2 || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_EINVAL;
+    const size_t es = dtype == ORC_F32 ? 4 : 2;
+    int *g = malloc(sizeof(int) * (size_t)N);
+    if (!g)
+        return ORC_ENOMEM;
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)b * (size_t)N * (size_t)V * es;
+        const int32_t *tok = tree_tokens + (size_t)b * N;
+        const int32_t *pb = paths + (size_t)b * P * L;
+        int32_t *out = out_tokens + (size_t)b * L;
+        int32_t *nodes = out_accepted_nodes ? out_accepted_nodes + (size_t)b * L : NULL;
+        int bad = 0;
+        for (int n = 0; n < N; ++n)
+            if (tok[n] < 0 || tok[n] >= V)
+                bad = 1;
+        for (int pth = 0; pth < P; ++pth) {
+            if (pb[(size_t)pth * L] != 0 && pb[(size_t)pth * L] != -1)
+                bad = 1;
+            for (int j = 0; j < L; ++j) {
+                int32_t nd = pb[(size_t)pth * L + j];
+                if (nd < -1 || nd >= N)
+                    bad = 1;
+            }
+        }
+        if (bad) {
+            fail_closed_row(out, L, &out_num_accepted[b]);
+            if (nodes)
+                for (int j = 0; j < L; ++j)
+                    nodes[j] = -1;
+            if (out_best_path)
+                out_best_path[b] = -1;
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        for (int n = 0; n < N; ++n)
+            g[n] = oracle_argmax(tb + (size_t)n * V * es, dtype, V);
+        int best = -1, best_acc = -1;
+        for (int pth = 0; pth < P; ++pth) {
+            const int32_t *path = pb + (size_t)pth * L;
+            if (path[0] < 0)
+                continue;
+            int acc = 0;
+            for (int j = 1; j < L; ++j) {
+                int32_t node = path[j];
+                if (node < 0 || tok[node] != g[path[j - 1]])
+                    break;
+                ++acc;
+            }
+            if (acc > best_acc) {
+                best_acc = acc;
+                best = pth;
+            }
+        }
+        int n_acc = best < 0 ? 0 : best_acc;
+        int last = best < 0 ? 0 : pb[(size_t)best * L + n_acc];
+        for (int j = 0; j < n_acc; ++j)
+            out[j] = tok[pb[(size_t)best * L + j + 1]];
+        out[n_acc] = g[last];
+        for (int j = n_acc + 1; j < L; ++j)
+            out[j] = -1;
+        if (nodes) {
+            for (int j = 0; j <= n_acc; ++j)
+                nodes[j] = best < 0 ? 0 : pb[(size_t)best * L + j];
+            for (int j = n_acc + 1; j < L; ++j)
+                nodes[j] = -1;
+        }
+        if (out_best_path)
+            out_best_path[b] = best;
+        out_num_accepted[b] = n_acc;
+    }
+    free(g);
+    return rc;
+}
+
+/* KV cursor rollback: new_len = old_len + n_acc + 1 (the last committed token
+ * plus the accepted drafts stay visible), rewind = k - n_acc (rows written by
+ * the verify window but not kept).  An entry with n_acc outside [0, k] is left
+ * unchanged (new_len = old_len, rewind 0) and the call returns EBADINDEX. */
+int oracle_rollback(const int32_t *old_lens, const int32_t *num_accepted, int k, int B,
+                    int32_t *new_lens, int32_t *rewind_lens)
+{
+    if (!old_lens || !num_accepted || !new_lens || B < 1 || k < 0)
+        return ORC_EINVAL;
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        int32_t n = num_accepted[b];
+        if (n < 0 || n > k) {
+            new_lens[b] = old_lens[b];
+            if (rewind_lens)
+                rewind_lens[b] = 0;
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        new_lens[b] = old_lens[b] + n + 1;
+        if (rewind_lens)
+            rewind_lens[b] = k - n;
+    }
+    return rc;
+}

@@ -1,0 +1,387 @@
+"""Checks that tie the CPU oracle to the pages and to mathematics.
+
+Each ``pin_*`` function runs the oracle (optionally a rebuilt copy, ``lib``)
+and returns a list of failure messages (empty = the pin holds).  The regular
+tests assert that every pin holds for the committed oracle; the mutation test
+plants plausible mistakes in a copy of the oracle source and asserts that some
+pin catches each of them.
+
+None of these checks re-types the oracle's formulas: they use closed forms,
+exact enumeration of the method's branch probabilities against the
+equivalence theorem, library routines (scipy softmax, numpy argmax and
+searchsorted), brute force over tree chains, and the worked examples printed
+on the pages.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+
+import numpy as np
+from scipy.special import softmax as sp_softmax
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _softmax_T(x, T):
+    return sp_softmax(np.asarray(x, dtype=np.float64) / np.float64(np.float32(T)))
+
+
+# --------------------------------------------------------------------------- softmax
+def pin_softmax(lib=None) -> list[str]:
+    """Closed forms and the scipy special case of softmax(x / T)."""
+    errs = []
+    # uniform logits -> 1/V
+    p = oracle.softmax(np.full(7, 3.25, np.float32), 0.7, lib=lib)
+    if np.max(np.abs(p - 1.0 / 7)) > 1e-15:
+        errs.append("uniform logits do not give 1/V")
+    # two tokens [a, 0] -> logistic(a / T)
+    for a, T in [(1.5, 1.0), (-2.0, 0.5), (4.0, 0.8)]:
+        p = oracle.softmax(np.array([a, 0.0], np.float32), T, lib=lib)
+        want = 1.0 / (1.0 + np.exp(-a / np.float64(np.float32(T))))
+        if abs(p[0] - want) > 1e-14 or abs(p.sum() - 1.0) > 1e-15:
+            errs.append(f"two-token closed form fails at a={a} T={T}")
+    # bf16 widening: 1.0 (0x3F80) and -2.0 (0xC000) -> logistic(3)
+    p = oracle.softmax(np.array([0x3F80, 0xC000], np.uint16), 1.0, dtype="bf16", lib=lib)
+    if abs(p[0] - 1.0 / (1.0 + np.exp(-3.0))) > 1e-14:
+        errs.append("bf16 widening wrong")
+    # library special case: scipy softmax of x / T in float64
+    rng = np.random.default_rng(5)
+    for T in (1.0, 0.7, 2.5):
+        x = (rng.standard_normal(513) * 4).astype(np.float32)
+        p = oracle.softmax(x, T, lib=lib)
+        if np.max(np.abs(p - _softmax_T(x, T))) > 1e-14 or abs(p.sum() - 1) > 1e-12:
+            errs.append(f"disagrees with scipy softmax at T={T}")
+    return errs
+
+
+# --------------------------------------------------------------------------- inverse CDF
+def pin_inverse_cdf(lib=None) -> list[str]:
+    """numpy searchsorted(side='right') special case; zero weights never drawn."""
+    errs = []
+    rng = np.random.default_rng(11)
+    for trial in range(200):
+        V = int(rng.integers(1, 40))
+        w = rng.random(V) * (rng.random(V) < 0.7)
+        if w.sum() == 0:
+            w[int(rng.integers(0, V))] = 0.5
+        u = float(rng.random())
+        t, tie = oracle.inverse_cdf(w, u, lib=lib)
+        c = np.cumsum(w)
+        want = int(np.searchsorted(c, u * c[-1], side="right"))
+        if not tie and t != want:
+            errs.append(f"searchsorted mismatch V={V} u={u}: {t} vs {want}")
+            break
+        if w[t] <= 0:
+            errs.append("zero-weight token drawn")
+            break
+    w = np.array([0.0, 0.0, 0.3, 0.0, 0.7, 0.0])
+    if oracle.inverse_cdf(w, 0.0, lib=lib)[0] != 2:
+        errs.append("u=0 must draw the first positive-weight token")
+    if oracle.inverse_cdf(w, np.nextafter(1.0, 0.0), lib=lib)[0] != 4:
+        errs.append("u->1 must draw the last positive-weight token")
+    if oracle.inverse_cdf(np.zeros(4), 0.3, lib=lib)[0] != -1:
+        errs.append("Z == 0 must return -1")
+    return errs
+
+
+# --------------------------------------------------------------------------- exact distribution
+def enumerate_chain(target, draft, T, lib=None):
+    """Drive the oracle through every branch of the chain verify for one small problem.
+
+    For every draft tuple x in [V]^k (weight prod q_i(x_i)), every stopping
+    position j, and every final token t with positive weight, build uniforms
+    that take that branch: r_i = min(1,a_i)/2 accepts (weight min(1,a_i)),
+    r_j = (1+a_j)/2 rejects (weight 1-a_j), and u at the midpoint of t's CDF
+    interval (weight w_t/Z).  Returns (weights, expected rows, oracle result).
+    """
+    k1, V = target.shape
+    k = k1 - 1
+    p = [_softmax_T(target[i], T) for i in range(k + 1)]
+    q = [_softmax_T(draft[i], T) for i in range(k)]
+    reqs_x, reqs_r, weights, expect = [], [], [], []
+    for x in itertools.product(range(V), repeat=k):
+        wx = np.prod([q[i][x[i]] for i in range(k)])
+        a = [p[i][x[i]] / q[i][x[i]] for i in range(k)]
+        for j in range(k + 1):
+            wb = wx
+            r = np.full(k + 1, 0.5)
+            for i in range(j):
+                wb *= min(1.0, a[i])
+                r[i] = min(1.0, a[i]) / 2
+            if j < k:
+                if a[j] >= 1.0:
+                    continue
+                wb *= 1.0 - a[j]
+                r[j] = (1.0 + a[j]) / 2
+                wts = np.maximum(p[j] - q[j], 0.0)
+            else:
+                wts = p[k]
+            Z = wts.sum()
+            c = np.concatenate([[0.0], np.cumsum(wts)])
+            for t in range(V):
+                if wts[t] <= 0:
+                    continue
+                rr = r.copy()
+                rr[k] = (c[t] + c[t + 1]) / (2 * Z)
+                reqs_x.append(x)
+                reqs_r.append(rr)
+                weights.append(wb * wts[t] / Z)
+                expect.append((j, list(x[:j]) + [t] + [-1] * (k - j)))
+    Bn = len(weights)
+    tgt = np.broadcast_to(target, (Bn, k + 1, V)).astype(np.float32)
+    drf = np.broadcast_to(draft, (Bn, k, V)).astype(np.float32)
+    res = oracle.verify_chain(tgt, drf, np.array(reqs_x, np.int32).reshape(Bn, k),
+                              np.array(reqs_r, np.float32), T, lib=lib)
+    return np.array(weights), expect, res, p
+
+
+def pin_exact_distribution(lib=None) -> list[str]:
+    """The equivalence theorem on enumerated branches (vLLM anatomy page,
+    "Why this works"; vLLM learning book, section 2 and question 2):
+    P(y_i = t | n_acc >= i) = p_i(t) and P(n_acc >= i+1 | n_acc >= i) =
+    sum_t min(p_i, q_i), to 1e-12, plus the exact branch outcome per request."""
+    errs = []
+    rng = np.random.default_rng(2024)
+    for (k, V, T) in [(1, 5, 1.0), (2, 4, 0.7), (3, 3, 1.3), (2, 6, 1.0), (3, 5, 0.9)]:
+        target = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+        draft = (target[:k] + rng.standard_normal((k, V)) * 0.8).astype(np.float32)
+        wts, expect, res, p = enumerate_chain(target, draft, T, lib=lib)
+        for e, (j, row) in enumerate(expect):
+            if res["num_accepted"][e] != j or list(res["tokens"][e]) != row:
+                errs.append(f"k={k} V={V}: branch {e} gave {res['tokens'][e]} want {row}")
+                break
+        n_acc = res["num_accepted"]
+        toks = res["tokens"]
+        if abs(wts.sum() - 1.0) > 1e-12:
+            errs.append(f"k={k} V={V}: branch weights sum to {wts.sum()}")
+        q = [_softmax_T(draft[i], T) for i in range(k)]
+        for i in range(k + 1):
+            reach = n_acc >= i
+            pr = wts[reach].sum()
+            dist = np.array([wts[reach & (toks[:, i] == t)].sum() for t in range(V)]) / pr
+            if np.max(np.abs(dist - p[i])) > 1e-12:
+                errs.append(f"k={k} V={V}: emitted token at {i} is not distributed as p_{i}")
+            if i < k:
+                beta = np.minimum(p[i], q[i]).sum()
+                if abs(wts[n_acc >= i + 1].sum() / pr - beta) > 1e-12:
+                    errs.append(f"k={k} V={V}: acceptance at {i} is not sum min(p,q)")
+    return errs
+
+
+# --------------------------------------------------------------------------- invariants
+def pin_invariants(lib=None) -> list[str]:
+    """q == p accepts all k; r == 0 accepts all k; output-row structure."""
+    errs = []
+    rng = np.random.default_rng(7)
+    B, k, V = 64, 4, 50
+    target = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    draft = (target[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, k)).astype(np.int32)
+    r = rng.random((B, k + 1)).astype(np.float32)
+    same = oracle.verify_chain(target, target[:, :k].copy(), x, r, 0.9, lib=lib)
+    if not np.all(same["num_accepted"] == k):
+        errs.append("identical draft and target must accept every draft")
+    zero = r.copy()
+    zero[:, :k] = 0.0
+    if not np.all(oracle.verify_chain(target, draft, x, zero, 0.9, lib=lib)["num_accepted"] == k):
+        errs.append("uniforms of 0 must accept every draft")
+    res = oracle.verify_chain(target, draft, x, r, 0.9, lib=lib)
+    for b in range(B):
+        n = res["num_accepted"][b]
+        row = res["tokens"][b]
+        if not (0 <= n <= k):
+            errs.append("n_acc outside [0, k]")
+            break
+        if np.count_nonzero(row >= 0) != n + 1 or np.any(row[: n + 1] < 0):
+            errs.append("row must hold exactly n_acc+1 tokens then -1")
+            break
+        if list(row[:n]) != list(x[b, :n]):
+            errs.append("the first n_acc tokens must be the drafts")
+            break
+    bad = x.copy()
+    bad[3, 1] = V
+    res = oracle.verify_chain(target, draft, bad, r, 0.9, lib=lib)
+    if res["rc"] != oracle.EBADINDEX or res["num_accepted"][3] != -1 or np.any(res["tokens"][3] != -1):
+        errs.append("an out-of-range draft token must fail that request closed")
+    return errs
+
+
+# --------------------------------------------------------------------------- greedy
+def pin_greedy(lib=None) -> list[str]:
+    """argmax = numpy argmax (first occurrence); greedy verify emits the argmax chain."""
+    errs = []
+    rng = np.random.default_rng(3)
+    for dtype in ("f32", "bf16"):
+        for _ in range(50):
+            V = int(rng.integers(2, 300))
+            vals = rng.integers(-4, 5, V).astype(np.float32)  # many exact ties
+            raw = vals if dtype == "f32" else (vals.view(np.uint32) >> 16).astype(np.uint16)
+            if oracle.argmax(raw, dtype, lib=lib) != int(np.argmax(vals)):
+                errs.append(f"argmax tie-break differs from numpy ({dtype})")
+                break
+    B, k, V = 40, 5, 64
+    target = rng.integers(-3, 4, (B, k + 1, V)).astype(np.float32)
+    g = np.argmax(target, axis=2)
+    d = g[:, :k].copy()
+    cut = rng.integers(0, k + 1, B)
+    for b in range(B):
+        if cut[b] < k:
+            d[b, cut[b]] = (g[b, cut[b]] + 1) % V
+    res = oracle.verify_greedy(target, d, lib=lib)
+    for b in range(B):
+        want = list(g[b, : cut[b] + 1]) + [-1] * (k - cut[b])
+        if res["num_accepted"][b] != cut[b] or list(res["tokens"][b]) != want:
+            errs.append("greedy verify does not emit the target's argmax chain")
+            break
+    return errs
+
+
+# --------------------------------------------------------------------------- tree
+def _random_tree(rng, N, V, accept_bias):
+    parent = np.full(N, -1)
+    for n in range(1, N):
+        parent[n] = int(rng.integers(0, n))
+    target = rng.integers(-3, 4, (N, V)).astype(np.float32)
+    g = np.argmax(target, axis=1)
+    tokens = np.zeros(N, np.int32)
+    tokens[0] = int(rng.integers(0, V))
+    for n in range(1, N):
+        sib_used = {int(tokens[m]) for m in range(1, n) if parent[m] == parent[n]}
+        want = int(g[parent[n]])
+        if rng.random() < accept_bias and want not in sib_used:
+            tokens[n] = want
+        else:
+            choices = [t for t in range(V) if t not in sib_used]
+            tokens[n] = choices[int(rng.integers(0, len(choices)))]
+    return parent, target, tokens
+
+
+def _paths_from_parents(parent, L, P):
+    N = len(parent)
+    kids = {n: [] for n in range(N)}
+    for n in range(1, N):
+        kids[int(parent[n])].append(n)
+    paths = np.full((P, L), -1, np.int32)
+    leaves = [n for n in range(N) if not kids[n]]
+    for i, leaf in enumerate(leaves):
+        chain = [leaf]
+        while chain[-1] != 0:
+            chain.append(int(parent[chain[-1]]))
+        chain = chain[::-1][:L]
+        paths[i, : len(chain)] = chain
+    return paths
+
+
+def _depth(parent, n):
+    d = 0
+    while n != 0:
+        n = int(parent[n])
+        d += 1
+    return d
+
+
+def pin_tree(lib=None) -> list[str]:
+    """Brute force over root-to-node chains; a one-chain tree equals chain greedy."""
+    errs = []
+    rng = np.random.default_rng(17)
+    for trial in range(60):
+        N = int(rng.integers(2, 14))
+        V = int(rng.integers(N + 2, N + 12))
+        parent, target, tokens = _random_tree(rng, N, V, accept_bias=0.6)
+        depth = max(_depth(parent, n) for n in range(N))
+        L = depth + 1
+        paths = _paths_from_parents(parent, L, N)
+        g = np.argmax(target, axis=1)
+        # brute force: a node is reachable when every edge on its root chain is accepted
+        ok = [True] + [False] * (N - 1)
+        for n in range(1, N):  # parents have lower ids
+            ok[n] = ok[int(parent[n])] and tokens[n] == g[int(parent[n])]
+        best_depth = max(_depth(parent, n) for n in range(N) if ok[n])
+        res = oracle.verify_tree(target[None], tokens[None], paths[None], lib=lib)
+        n_acc = int(res["num_accepted"][0])
+        if n_acc != best_depth:
+            errs.append(f"tree n_acc {n_acc} != brute-force depth {best_depth}")
+            break
+        nodes = [int(v) for v in res["accepted_nodes"][0] if v >= 0]
+        if nodes[0] != 0 or len(nodes) != n_acc + 1 or any(
+                parent[nodes[i + 1]] != nodes[i] or not ok[nodes[i + 1]] for i in range(n_acc)):
+            errs.append("accepted nodes are not an accepted root chain")
+            break
+        row = res["tokens"][0]
+        want = [int(tokens[n]) for n in nodes[1:]] + [int(g[nodes[-1]])]
+        if list(row[: n_acc + 1]) != want or np.any(row[n_acc + 1:] != -1):
+            errs.append("tree output row wrong")
+            break
+    # one-chain tree == chain greedy
+    B, k, V = 16, 4, 20
+    target = rng.integers(-3, 4, (B, k + 1, V)).astype(np.float32)
+    g = np.argmax(target, axis=2)
+    d = np.where(rng.random((B, k)) < 0.7, g[:, :k], rng.integers(0, V, (B, k))).astype(np.int32)
+    tree_tokens = np.concatenate([np.zeros((B, 1), np.int32), d], axis=1)
+    paths = np.tile(np.arange(k + 1, dtype=np.int32), (B, 1, 1))
+    t = oracle.verify_tree(target, tree_tokens, paths, lib=lib)
+    c = oracle.verify_greedy(target, d, lib=lib)
+    if not (np.array_equal(t["tokens"], c["tokens"]) and np.array_equal(t["num_accepted"], c["num_accepted"])):
+        errs.append("one-chain tree differs from chain greedy")
+    return errs
+
+
+# --------------------------------------------------------------------------- rollback
+def pin_rollback(lib=None) -> list[str]:
+    """Closed form and the boundaries of the TensorRT-LLM walkthrough (update_requests:
+    all accepted -> rewind 0; all rejected -> rewind = whole window)."""
+    errs = []
+    rng = np.random.default_rng(1)
+    k = 7
+    old = rng.integers(0, 100000, 500).astype(np.int32)
+    n = rng.integers(0, k + 1, 500).astype(np.int32)
+    res = oracle.rollback(old, n, k, lib=lib)
+    for b in range(500):
+        if res["new_lens"][b] != old[b] + n[b] + 1 or res["rewind_lens"][b] != k - n[b]:
+            errs.append("rollback closed form fails")
+            break
+    edge = oracle.rollback(np.array([10, 10], np.int32), np.array([k, 0], np.int32), k, lib=lib)
+    if list(edge["rewind_lens"]) != [0, k] or list(edge["new_lens"]) != [10 + k + 1, 11]:
+        errs.append("rewind boundaries wrong")
+    return errs
+
+
+# --------------------------------------------------------------------------- worked example
+def pin_worked_example(lib=None) -> list[str]:
+    """The FGH example of the TensorRT-LLM walkthrough (MTP section, generation
+    phase 1): drafts F G H, target samples F G X (Y discarded) -> accepted F G X,
+    H's KV row invalid (rewind 1), two drafts accepted."""
+    errs = []
+    with open(os.path.join(GOLDEN, "fgh_worked_example.json")) as f:
+        ex = json.load(f)
+    tok = ex["tokens"]
+    target = np.array(ex["target_logits"], np.float32)[None]
+    draft = np.array(ex["draft_logits"], np.float32)[None]
+    drafts = np.array([[tok["F"], tok["G"], tok["H"]]], np.int32)
+    r = np.array([ex["uniforms"]], np.float32)
+    want = [tok[c] if c != "-" else -1 for c in ex["expect"]["tokens"]]
+    for name, res in (("stochastic", oracle.verify_chain(target, draft, drafts, r, ex["temperature"], lib=lib)),
+                      ("greedy", oracle.verify_greedy(target, drafts, lib=lib))):
+        if list(res["tokens"][0]) != want or res["num_accepted"][0] != ex["expect"]["num_accepted"]:
+            errs.append(f"{name} verify of the FGH example gave {res['tokens'][0]}")
+    rb = oracle.rollback(np.array([ex["old_len"]], np.int32),
+                         np.array([ex["expect"]["num_accepted"]], np.int32), 3, lib=lib)
+    if rb["rewind_lens"][0] != ex["expect"]["rewind"] or rb["new_lens"][0] != ex["expect"]["new_len"]:
+        errs.append("FGH rollback wrong")
+    return errs
+
+
+ALL_PINS = {
+    "softmax": pin_softmax,
+    "inverse_cdf": pin_inverse_cdf,
+    "exact_distribution": pin_exact_distribution,
+    "invariants": pin_invariants,
+    "greedy": pin_greedy,
+    "tree": pin_tree,
+    "rollback": pin_rollback,
+    "worked_example": pin_worked_example,
+}

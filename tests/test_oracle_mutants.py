@@ -1,0 +1,49 @@
+"""Negative controls: plant plausible mistakes in a copy of the oracle source,
+rebuild it, and check that at least one pin catches each mistake (the Kestrel
+article's section 3.2.1 makes the same point: a check that still passes with
+the mechanism removed proves nothing)."""
+import os
+import shutil
+
+import pytest
+
+import _pins
+import oracle
+
+MUTANTS = {
+    "ratio_inverted": ("ratio[i] = qi > 0.0 ? pi / qi : INFINITY;",
+                       "ratio[i] = qi > 0.0 ? qi / pi : INFINITY;"),
+    "accept_wrong_row": ("oracle_softmax(tb + (size_t)i * V * es, dtype, T, V, p);",
+                         "oracle_softmax(tb + (size_t)(i + 1) * V * es, dtype, T, V, p);"),
+    "residual_without_clamp_resamples_p": ("w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0;",
+                                           "w[t] = p[t];"),
+    "residual_sign_flipped": ("w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0;",
+                              "w[t] = q[t] - p[t] > 0.0 ? q[t] - p[t] : 0.0;"),
+    "bonus_from_draft_row": ("memcpy(w, p, sizeof(double) * (size_t)V);",
+                             "oracle_softmax(db + (size_t)(j - 1) * V * es, dtype, T, V, w);"),
+    "inverse_cdf_non_strict": ("if (c > target) {", "if (c >= target) {"),
+    "argmax_last_tie": ("if (v > bv) {", "if (v >= bv) {"),
+    "tree_compares_own_row": ("if (node < 0 || tok[node] != g[path[j - 1]])",
+                              "if (node < 0 || tok[node] != g[node])"),
+    "temperature_multiplies": ("p[t] = logit_at(x, dtype, (size_t)t) / temperature;",
+                               "p[t] = logit_at(x, dtype, (size_t)t) * temperature;"),
+    "softmax_unnormalised": ("p[t] /= sum;", "p[t] /= 1.0;"),
+    "rollback_drops_committed_token": ("new_lens[b] = old_lens[b] + n + 1;",
+                                       "new_lens[b] = old_lens[b] + n;"),
+    "scan_does_not_stop": ("j = i;\n                break;", "j = i;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle.SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor missing: {old!r}"
+    mutated = src.replace(old, new)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    so = str(tmp_path / "libmutant.so")
+    oracle.build(src=str(path), out=so, force=True)
+    lib = oracle.load(so)
+    caught = [n for n, pin in _pins.ALL_PINS.items() if pin(lib=lib)]
+    assert caught, f"no pin catches mutant {name}"
