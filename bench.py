@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verification row on GB300.
+
+One step = one verify call over one batch (chain: both passes plus the fused
+KV cursor update) on seeded synthetic logits already resident in HBM.  The
+headline workload is chain stochastic verify with B=64 requests, k=7 drafts,
+V=128256, bf16 logits, T=0.7.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Under torchrun each rank verifies its own batch on its own GPU (weak scaling,
+no collective on the data path); the timed region is bracketed by barriers
+and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import shutil
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verified positions/sec and achieved HBM GB/s (B=64,k=7,V=128256 bf16)"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_row_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--greedy", action="store_true", help="greedy chain verify instead of stochastic")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) stamped on arrival."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return
+        self.proc = subprocess.Popen(
+            [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", str(index),
+             "-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi not found"}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = None
+        if not inside:  # region shorter than the sampling period: nearest samples
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
+            inside = [s for _, s in near]
+            note = "timed region shorter than the sampling period; nearest samples used"
+        sm = [float(s[0]) for s in inside if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        out = {"sm_mhz": float(np.median(sm)) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# --------------------------------------------------------------------- helpers
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes per call from the committed ncu summary, if taken on this source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("csrc_sha256") != csrc_digest():
+        return None
+    return rec.get("dram_bytes_per_call")
+
+
+def positions_per_call(w, greedy):
+    return w["B"] * (w["L"] - 1) if w["kind"] == "tree" else w["B"] * w["k"]
+
+
+def dev_logits(arr, dtype, device):
+    import torch
+    if dtype == workloads.BF16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr)).to(device)
+
+
+# --------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+    import speculative_decoding_verification_row_gb300 as sv
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    w = workloads.make(args.config, seed=args.seed + 1000 * rank)
+    tree = w["kind"] == "tree"
+    greedy = args.greedy and not tree
+    lib = sv.lib()
+    stream = torch.cuda.current_stream(device)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)  # noqa: E731
+    code = workloads.DTYPE_CODE[w["dtype"]]
+    B, V = w["B"], w["V"]
+
+    # Two resident copies of the inputs, used alternately: each step reads
+    # logits the previous step did not touch (2x the input size > L2).
+    copies = []
+    for _ in range(2):
+        c = {"target": dev_logits(w["target"], w["dtype"], device)}
+        if tree:
+            c["tree_tokens"], c["paths"] = i32(w["tree_tokens"]), i32(w["paths"])
+        else:
+            c["tokens"] = i32(w["draft_tokens"])
+            if not greedy:
+                c["draft"] = dev_logits(w["draft"], w["dtype"], device)
+                c["uniforms"] = torch.from_numpy(w["uniforms"]).to(device)
+        copies.append(c)
+    seq = i32(w["seq_lens"])
+    k = w["L"] - 1 if tree else w["k"]
+    rows = w["N"] if tree else (k + 1 if greedy else 2 * k + 1)
+    ws = sv.Workspace(device)
+    buf = ws.ensure(B, rows, V, sh)
+    out_tok = torch.empty((B, w["L"] if tree else k + 1), dtype=torch.int32, device=device)
+    out_n = torch.empty(B, dtype=torch.int32, device=device)
+    P = ctypes.c_void_p
+    ptr = lambda t: P(t.data_ptr())  # noqa: E731
+    call_args = []
+    for c in copies:
+        if tree:
+            best = torch.empty(B, dtype=torch.int32, device=device)
+            nodes = torch.empty((B, w["L"]), dtype=torch.int32, device=device)
+            fn = lib.spec_verify_tree
+            call_args.append((ptr(c["target"]), code, ptr(c["tree_tokens"]), ptr(c["paths"]), B, w["N"],
+                              w["P"], w["L"], V, ptr(out_tok), ptr(out_n), ptr(best), ptr(nodes),
+                              ptr(seq), ptr(buf), buf.numel(), sh))
+        elif greedy:
+            fn = lib.spec_verify_greedy
+            call_args.append((ptr(c["target"]), code, ptr(c["tokens"]), B, k, V, ptr(out_tok),
+                              ptr(out_n), ptr(seq), ptr(buf), buf.numel(), sh))
+        else:
+            fn = lib.spec_verify_chain
+            call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
+                              ptr(c["uniforms"]), ctypes.c_float(w["temperature"]), B, k, V,
+                              ptr(out_tok), ptr(out_n), None, ptr(seq), ptr(buf), buf.numel(), sh))
+    launches_per_step = 1 if (tree or greedy) else 2
+
+    for i in range(args.warmup):
+        rc = fn(*call_args[i & 1])
+        assert rc == 0, sv.status_string(rc)
+    torch.cuda.synchronize()
+    n_first = out_n.cpu().numpy()
+    assert sv.last_error(ws) == sv.SPEC_OK
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    start.record(stream)
+    bad = 0
+    for i in range(args.steps):
+        bad |= fn(*call_args[i & 1])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    if dist:
+        dist.barrier()
+    clocks.stop()
+    assert bad == 0
+    ms_total = start.elapsed_time(end)
+    if dist:
+        tt = torch.tensor([ms_total], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+
+    # End to end through the public binding: pinned host inputs copied in and
+    # results read back inside every step.
+    host = {key: torch.from_numpy(np.ascontiguousarray(
+        w[key].view(np.int16) if (w["dtype"] == workloads.BF16 and key in ("target", "draft")) else w[key])).pin_memory()
+        for key in (["target", "tree_tokens", "paths"] if tree else
+                    ["target", "draft_tokens"] + ([] if greedy else ["draft", "uniforms"]))}
+    host["seq_lens"] = torch.from_numpy(w["seq_lens"].copy()).pin_memory()
+    dev_in = {key: torch.empty(t.shape, dtype=t.dtype, device=device) for key, t in host.items()}
+    res_tok = torch.empty(tuple(out_tok.shape), dtype=torch.int32).pin_memory()
+    res_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    res_seq = torch.empty(B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in (res_tok, res_n, res_seq))
+
+    def e2e_step():
+        for key, t in host.items():
+            dev_in[key].copy_(t, non_blocking=True)
+        lg = (lambda t: t.view(torch.bfloat16)) if w["dtype"] == workloads.BF16 else (lambda t: t)
+        if tree:
+            tk, nn, _, _ = sv.verify_tree(lg(dev_in["target"]), dev_in["tree_tokens"], dev_in["paths"],
+                                          seq_lens=dev_in["seq_lens"], workspace=ws)
+        elif greedy:
+            tk, nn = sv.verify_greedy(lg(dev_in["target"]), dev_in["draft_tokens"],
+                                      seq_lens=dev_in["seq_lens"], workspace=ws)
+        else:
+            tk, nn, _ = sv.verify_chain(lg(dev_in["target"]), lg(dev_in["draft"]), dev_in["draft_tokens"],
+                                        dev_in["uniforms"], w["temperature"], seq_lens=dev_in["seq_lens"],
+                                        workspace=ws)
+        res_tok.copy_(tk, non_blocking=True)
+        res_n.copy_(nn, non_blocking=True)
+        res_seq.copy_(dev_in["seq_lens"], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if dist:
+        dist.barrier()
+    te0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    te = time.perf_counter() - te0
+    if dist:
+        tt = torch.tensor([te], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        te = float(tt.item())
+
+    pos = positions_per_call(w, greedy)
+    value = world * pos / (ms_step * 1e-3)
+    algo_bytes = workloads.algorithmic_bytes(w, greedy=greedy or tree)
+    achieved = algo_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_src = peak_hbm()
+    kernel_key = "tree" if tree else ("greedy" if greedy else "chain")
+    traffic = recorded_traffic(f"{args.config}/{kernel_key}")
+    stats = sv.acceptance_stats(n_first, k)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, greedy, args.cpu_seconds)
+
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": args.config + ("/greedy" if greedy else ""),
+            "B": B, "k": k, "V": V, "logits": w["dtype"],
+            "temperature": None if (tree or greedy) else w["temperature"],
+            "requests_per_step": B * world,
+            "l2": "inputs larger than L2: two resident copies of the logits used alternately",
+        },
+        "achieved_hbm_gbs": achieved,
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+            "kernel": {"chain": "spec_verify_chain call (chain_stats_kernel + chain_sample_kernel)",
+                       "greedy": "spec_verify_greedy call (argmax_kernel)",
+                       "tree": "spec_verify_tree call (argmax_kernel)"}[kernel_key],
+            "algorithmic_bytes_per_call": algo_bytes,
+        },
+        "e2e": {"value": world * pos * args.e2e_steps / te, "unit": "positions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(t0, t1),
+        "acceptance": stats,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, greedy, seconds):
+    import oracle
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify(w, greedy=greedy)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    pos = positions_per_call(w, greedy) * reps
+    return {"value": pos / el, "unit": "positions/s", "cores": 1, "kind": "oracle",
+            "sample": f"the full batch ({w['B']} requests) verified {reps} times by the single-threaded "
+                      f"fp64 oracle ({el:.1f} s)"}
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle timed as the reference arm: each step verifies one
+    request of the workload (cycling through the batch)."""
+    if rank != 0:
+        return
+    import oracle
+    w = workloads.make(args.config, seed=args.seed)
+    tree = w["kind"] == "tree"
+    greedy = args.greedy and not tree
+
+    def one(b):
+        sub = {key: (v[b:b + 1] if isinstance(v, np.ndarray) and v.shape[:1] == (w["B"],) else v)
+               for key, v in w.items()}
+        sub["B"] = 1
+        return oracle.verify(sub, greedy=greedy)
+
+    for i in range(args.warmup):
+        one(i % w["B"])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i % w["B"])
+    el = time.perf_counter() - t0
+    per = (w["L"] - 1) if tree else w["k"]
+    value = per * args.steps / el
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.config + ("/greedy" if greedy else ""), "B": w["B"],
+                   "k": per, "V": w["V"], "logits": w["dtype"]},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                         "sample": "one request per step, cycling through the batch"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * spec_verify.h — C ABI of the speculative-decoding verification library
+ * (libspecverify.so, sm_103a).
+ *
+ * One call verifies the draft tokens of B requests against the target model's
+ * logits on the caller's CUDA stream.  Sources of each operation:
+ *
+ *   chain verify   vLLM anatomy page ("Inside vLLM", part 3), section
+ *                  "Speculative Decoding": accept/reject left to right, stop
+ *                  at the first rejection, sample the rebalanced distribution
+ *                  max(0, p_large - p_draft) normalised, or the bonus token
+ *                  from the extra row when all k drafts are accepted.  The
+ *                  vLLM learning book, section 2 (Leviathan 2023 flowchart),
+ *                  gives the test r < min(1, p(x_i)/q(x_i)).  The TensorRT-LLM
+ *                  walkthrough (part 10), rejection-sampling section, fixes the
+ *                  shapes draft [batch, D, vocab], target [batch, D+1, vocab]
+ *                  and the output accepted_tokens [batch, D+1] padded with -1.
+ *   greedy verify  Kestrel article 32, section 3.3: accept while the target's
+ *                  argmax equals the draft; the emitted stream is the target's
+ *                  own argmax chain.  TensorRT-LLM walkthrough, rejection-
+ *                  sampling section: an all-greedy batch takes the base path.
+ *   tree verify    TensorRT-LLM deployment page ("05-TensorRT-LLM 推测解码"),
+ *                  section "Eagle-2 多层级树状草稿生成": paths tensor
+ *                  [batch, max_decoding_tokens, max_path_len].
+ *   rollback       TensorRT-LLM walkthrough, update_requests section
+ *                  (py_rewind_len = verified_len - accepted) and the paged
+ *                  rewind_cache section (only the logical length moves; rows
+ *                  are not cleared).  Kestrel article 32, section 3.1
+ *                  (truncate = move the cursor, copy nothing).
+ *
+ * Conventions for every call
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates or frees memory and keeps no global state.  Arrays are
+ *     dense, row-major, with the shapes given below.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     A host-detectable error (bad size, null pointer, small workspace)
+ *     returns before any launch and writes nothing.  A failed launch returns
+ *     SPEC_ECUDA.
+ *   - Data-dependent errors (a token or node id out of range) do not stop the
+ *     call: the affected request fails closed (its num_accepted is -1, its
+ *     token row is all -1, its seq_len is left unchanged) and the status word
+ *     in the workspace records SPEC_EBADINDEX; read it with spec_last_error().
+ *   - Logits must be finite or -inf (masked), with at least one finite value
+ *     per row; NaN and +inf are outside the contract and are not checked.
+ *   - One workspace serves one stream at a time: calls that overlap on the GPU
+ *     must not share a workspace.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_EINVAL = -1,      /* bad size, dtype, temperature or null pointer */
+    SPEC_EBADINDEX = -2,   /* a token or node id was out of range (device status) */
+    SPEC_ECUDA = -3,       /* a CUDA launch or copy failed */
+    SPEC_EWORKSPACE = -4,  /* workspace missing or smaller than spec_workspace_size() */
+    SPEC_ETIMEOUT = -5     /* reserved: a bounded device wait ran out */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Largest supported draft length k of a chain call, and the largest tree
+ * (N nodes, L path length) of a tree call. */
+#define SPEC_MAX_DRAFT 64
+#define SPEC_MAX_TREE_NODES 1024
+#define SPEC_MAX_PATH_LEN 64
+
+/* Bytes of scratch one call needs for B requests of `rows_per_request` logit
+ * rows of width V (chain: 2k+1, greedy: k+1, tree: N).  Returns 0 for invalid
+ * sizes.  The same workspace may be reused by any call whose own size is not
+ * larger. */
+size_t spec_workspace_size(int B, int rows_per_request, int V);
+
+/* Zero a workspace (asynchronously, on `stream`).  Call once after allocating
+ * it; every verify call leaves it ready for the next. */
+int spec_workspace_init(void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Chain rejection-sampling verify.
+ *   target_logits  [B, k+1, V] of `dtype`: row i (i < k) is the target
+ *                  distribution of draft position i, row k the bonus row.
+ *   draft_logits   [B, k, V] of `dtype`: row i is the draft distribution
+ *                  that draft token i was sampled from.
+ *   draft_tokens   [B, k] int32 in [0, V).
+ *   uniforms       [B, k+1] float32 in [0, 1): column i < k is the accept
+ *                  test of position i, column k drives the final sample.
+ *   temperature    > 0 and finite; both rows are softmax(logits / T).
+ * Accepts x_i while uniforms[b,i] < p_i(x_i) / q_i(x_i) (q == 0 accepts).
+ * At the first rejection j the last token is drawn from max(0, p_j - q_j)
+ * normalised; when all k are accepted it is drawn from p_k.  The draw takes
+ * the smallest t whose cumulative weight exceeds uniforms[b,k] times the
+ * total.
+ *   out_tokens       [B, k+1] int32: x_0..x_{n-1}, the final token, -1 pad.
+ *   out_num_accepted [B] int32: n in [0, k] (-1 for a failed request).
+ *   out_probs        [B, k, 2] float32 or NULL: p_i(x_i), q_i(x_i) for every i.
+ *   seq_lens         [B] int32 or NULL: KV cursor, updated in place to
+ *                    seq_len + n + 1 (see spec_rollback_lengths).
+ * Probabilities are accumulated in fp32. */
+int spec_verify_chain(const void *target_logits, const void *draft_logits, int dtype,
+                      const int32_t *draft_tokens, const float *uniforms, float temperature,
+                      int B, int k, int V,
+                      int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                      int32_t *seq_lens,
+                      void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Greedy chain verify.
+ *   target_logits [B, k+1, V], draft_tokens [B, k] in [0, V).
+ * g_i = argmax_t target[b,i,t] on the stored values, lowest id on ties;
+ * n = the longest prefix with g_i == d_i; out_tokens [B, k+1] =
+ * d_0..d_{n-1}, g_n, -1 pad; out_num_accepted [B]; seq_lens as above. */
+int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draft_tokens,
+                       int B, int k, int V,
+                       int32_t *out_tokens, int32_t *out_num_accepted, int32_t *seq_lens,
+                       void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Greedy tree verify over EAGLE-style paths.
+ *   target_logits [B, N, V]: row n is the target distribution after node n;
+ *                 node 0 is the root (the last committed token).
+ *   tree_tokens   [B, N] int32 in [0, V): node n's token.
+ *   paths         [B, P, L] int32 in [-1, N): root-to-leaf node lists padded
+ *                 with -1; a used path starts with 0, an unused one with -1.
+ * For every used path, step j = 1..L-1 is accepted while its node is >= 0 and
+ * its token equals argmax of its parent's row; the path with the most
+ * accepted steps wins (lowest path index on ties).
+ *   out_tokens         [B, L] int32: accepted tokens, then argmax of the last
+ *                      accepted node's row, -1 pad.
+ *   out_num_accepted   [B] int32 (-1 for a failed request).
+ *   out_best_path      [B] int32 or NULL (-1 when no path is used).
+ *   out_accepted_nodes [B, L] int32 or NULL: the root and the accepted node
+ *                      ids (the KV rows to keep), -1 pad.
+ *   seq_lens           [B] int32 or NULL, updated to seq_len + n + 1. */
+int spec_verify_tree(const void *target_logits, int dtype, const int32_t *tree_tokens,
+                     const int32_t *paths, int B, int N, int P, int L, int V,
+                     int32_t *out_tokens, int32_t *out_num_accepted, int32_t *out_best_path,
+                     int32_t *out_accepted_nodes, int32_t *seq_lens,
+                     void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* KV cursor rollback as length arithmetic only (no KV row is copied or
+ * cleared; rows past the new length become invisible and are overwritten
+ * later).
+ *   old_lens [B]: cursor before the verify window was written.
+ *   num_accepted [B]: n per request; k = draft rows in the verify window
+ *   (chain: k; tree: N - 1).
+ *   new_lens [B] = old_lens + n + 1 (may alias old_lens);
+ *   rewind_lens [B] or NULL = k - n (rows written but not kept).
+ * An entry with n outside [0, k] keeps its length (rewind 0) and sets
+ * SPEC_EBADINDEX in no workspace: this call returns SPEC_OK and leaves the
+ * entry unchanged. */
+int spec_rollback_lengths(const int32_t *old_lens, const int32_t *num_accepted, int k, int B,
+                          int32_t *new_lens, int32_t *rewind_lens, spec_stream_t stream);
+
+/* Synchronise `stream`, read the workspace status word into *status_out
+ * (SPEC_OK or SPEC_EBADINDEX) and clear it.  Returns SPEC_OK, SPEC_EINVAL or
+ * SPEC_ECUDA. */
+int spec_last_error(void *workspace, size_t workspace_bytes, spec_stream_t stream,
+                    int *status_out);
+
+/* Static text for a status code. */
+const char *spec_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

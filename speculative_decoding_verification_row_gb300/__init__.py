@@ -1,0 +1,277 @@
+"""GB300-native speculative-decoding verification row.
+
+A thin ctypes binding over ``libspecverify.so`` (C ABI in
+``include/spec_verify.h``).  The functions here only check and marshal
+arguments: every step of verification runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  If the library has
+not been built the first call raises; there is no CPU fallback.
+
+Calls (same names as the C ABI):
+  verify_chain     chain rejection-sampling verify (vLLM anatomy page,
+                   "Speculative Decoding")
+  verify_greedy    greedy chain verify (Kestrel article 32, section 3.3)
+  verify_tree      greedy EAGLE tree verify (TensorRT-LLM deployment page,
+                   "Eagle-2" section)
+  rollback_lengths KV cursor rollback (TensorRT-LLM walkthrough,
+                   update_requests / rewind_cache)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .stats import acceptance_stats, anchored_emitted  # noqa: F401  (host bookkeeping)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
+
+SPEC_OK, SPEC_EINVAL, SPEC_EBADINDEX, SPEC_ECUDA, SPEC_EWORKSPACE, SPEC_ETIMEOUT = 0, -1, -2, -3, -4, -5
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_MAX_DRAFT = 64
+SPEC_MAX_TREE_NODES = 1024
+SPEC_MAX_PATH_LEN = 64
+
+# Every entry point the header declares.
+SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
+           "spec_verify_greedy", "spec_verify_tree", "spec_rollback_lengths",
+           "spec_last_error", "spec_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+def _bind(lib):
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.spec_workspace_size.argtypes = [I, I, I]
+    lib.spec_workspace_size.restype = S
+    lib.spec_workspace_init.argtypes = [P, S, P]
+    lib.spec_verify_chain.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P, S, P]
+    lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
+    lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P, P, P, S, P]
+    lib.spec_rollback_lengths.argtypes = [P, P, I, I, P, P, P]
+    lib.spec_last_error.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int)]
+    lib.spec_status_string.argtypes = [I]
+    lib.spec_status_string.restype = ctypes.c_char_p
+    for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
+              "spec_rollback_lengths", "spec_last_error"):
+        getattr(lib, f).restype = I
+    return lib
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+                _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().spec_status_string(int(code)).decode()
+
+
+# ---------------------------------------------------------------- marshalling helpers
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream), stream
+    return ctypes.c_void_p(int(stream)), None
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _logit_code(t: torch.Tensor, name: str) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise ValueError(f"{name} must be bfloat16 or float32, got {t.dtype}")
+
+
+def _out(t, name, shape, dtype, device):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _dev(t, name, dtype, shape)
+
+
+class Workspace:
+    """Device scratch for verify calls on one stream (grown on demand).
+
+    A workspace must not be shared by calls that may overlap on the GPU."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device if device is not None else "cuda")
+        self.buf = None
+
+    def ensure(self, B: int, rows: int, V: int, stream_handle) -> torch.Tensor:
+        need = lib().spec_workspace_size(B, rows, V)
+        if need == 0:
+            raise SpecError("spec_workspace_size", SPEC_EINVAL)
+        if self.buf is None or self.buf.numel() < need:
+            self.buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+            rc = lib().spec_workspace_init(_ptr(self.buf), self.buf.numel(), stream_handle)
+            if rc != SPEC_OK:
+                raise SpecError("spec_workspace_init", rc)
+        return self.buf
+
+    @property
+    def nbytes(self) -> int:
+        return 0 if self.buf is None else self.buf.numel()
+
+
+_default_ws: dict = {}
+
+
+def default_workspace(device, stream_handle) -> Workspace:
+    key = (torch.device(device).index, int(stream_handle.value or 0))
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = _default_ws[key] = Workspace(device)
+    return ws
+
+
+# ---------------------------------------------------------------- calls
+def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                 out_tokens=None, out_num_accepted=None, out_probs=None, want_probs=False,
+                 seq_lens=None, workspace: Workspace | None = None, stream=None):
+    """Chain rejection-sampling verify; returns (tokens [B,k+1], num_accepted [B], probs [B,k,2] or None).
+
+    seq_lens (int32 [B], optional) is advanced in place by n_acc + 1."""
+    t = _dev(target_logits, "target_logits")
+    if t.dim() != 3:
+        raise ValueError("target_logits must be [B, k+1, V]")
+    B, k1, V = t.shape
+    k = k1 - 1
+    code = _logit_code(t, "target_logits")
+    d = _dev(draft_logits, "draft_logits", t.dtype, (B, k, V))
+    x = _dev(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    u = _dev(uniforms, "uniforms", torch.float32, (B, k + 1))
+    dev = t.device
+    tok = _out(out_tokens, "out_tokens", (B, k + 1), torch.int32, dev)
+    n = _out(out_num_accepted, "out_num_accepted", (B,), torch.int32, dev)
+    probs = None
+    if out_probs is not None or want_probs:
+        probs = _out(out_probs, "out_probs", (B, k, 2), torch.float32, dev)
+    if seq_lens is not None:
+        _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    sh, _ = _stream_handle(stream, dev)
+    ws = workspace or default_workspace(dev, sh)
+    buf = ws.ensure(B, 2 * k + 1, V, sh)
+    rc = lib().spec_verify_chain(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
+                                 B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens),
+                                 _ptr(buf), buf.numel(), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_chain", rc)
+    return tok, n, probs
+
+
+def verify_greedy(target_logits, draft_tokens, *, out_tokens=None, out_num_accepted=None,
+                  seq_lens=None, workspace: Workspace | None = None, stream=None):
+    """Greedy chain verify; returns (tokens [B,k+1], num_accepted [B])."""
+    t = _dev(target_logits, "target_logits")
+    if t.dim() != 3:
+        raise ValueError("target_logits must be [B, k+1, V]")
+    B, k1, V = t.shape
+    k = k1 - 1
+    code = _logit_code(t, "target_logits")
+    x = _dev(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    dev = t.device
+    tok = _out(out_tokens, "out_tokens", (B, k + 1), torch.int32, dev)
+    n = _out(out_num_accepted, "out_num_accepted", (B,), torch.int32, dev)
+    if seq_lens is not None:
+        _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    sh, _ = _stream_handle(stream, dev)
+    ws = workspace or default_workspace(dev, sh)
+    buf = ws.ensure(B, k + 1, V, sh)
+    rc = lib().spec_verify_greedy(_ptr(t), code, _ptr(x), B, k, V, _ptr(tok), _ptr(n),
+                                  _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_greedy", rc)
+    return tok, n
+
+
+def verify_tree(target_logits, tree_tokens, paths, *, out_tokens=None, out_num_accepted=None,
+                out_best_path=None, out_accepted_nodes=None, seq_lens=None,
+                workspace: Workspace | None = None, stream=None):
+    """Greedy tree verify; returns (tokens [B,L], num_accepted [B], best_path [B], accepted_nodes [B,L])."""
+    t = _dev(target_logits, "target_logits")
+    if t.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = t.shape
+    code = _logit_code(t, "target_logits")
+    tt = _dev(tree_tokens, "tree_tokens", torch.int32, (B, N))
+    p = _dev(paths, "paths", torch.int32)
+    if p.dim() != 3 or p.shape[0] != B:
+        raise ValueError("paths must be [B, P, L]")
+    P, L = p.shape[1], p.shape[2]
+    dev = t.device
+    tok = _out(out_tokens, "out_tokens", (B, L), torch.int32, dev)
+    n = _out(out_num_accepted, "out_num_accepted", (B,), torch.int32, dev)
+    best = _out(out_best_path, "out_best_path", (B,), torch.int32, dev)
+    nodes = _out(out_accepted_nodes, "out_accepted_nodes", (B, L), torch.int32, dev)
+    if seq_lens is not None:
+        _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    sh, _ = _stream_handle(stream, dev)
+    ws = workspace or default_workspace(dev, sh)
+    buf = ws.ensure(B, N, V, sh)
+    rc = lib().spec_verify_tree(_ptr(t), code, _ptr(tt), _ptr(p), B, N, P, L, V, _ptr(tok),
+                                _ptr(n), _ptr(best), _ptr(nodes), _ptr(seq_lens), _ptr(buf),
+                                buf.numel(), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_tree", rc)
+    return tok, n, best, nodes
+
+
+def rollback_lengths(old_lens, num_accepted, k: int, *, new_lens=None, rewind_lens=None,
+                     stream=None):
+    """KV cursor rollback lengths; returns (new_lens [B], rewind_lens [B])."""
+    o = _dev(old_lens, "old_lens", torch.int32)
+    B = o.shape[0]
+    n = _dev(num_accepted, "num_accepted", torch.int32, (B,))
+    new = _out(new_lens, "new_lens", (B,), torch.int32, o.device)
+    rew = _out(rewind_lens, "rewind_lens", (B,), torch.int32, o.device)
+    sh, _ = _stream_handle(stream, o.device)
+    rc = lib().spec_rollback_lengths(_ptr(o), _ptr(n), int(k), B, _ptr(new), _ptr(rew), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_rollback_lengths", rc)
+    return new, rew
+
+
+def last_error(workspace: Workspace, stream=None) -> int:
+    """Synchronise, read and clear the workspace's data-dependent status."""
+    if workspace.buf is None:
+        return SPEC_OK
+    sh, _ = _stream_handle(stream, workspace.buf.device)
+    out = ctypes.c_int(0)
+    rc = lib().spec_last_error(_ptr(workspace.buf), workspace.buf.numel(), sh, ctypes.byref(out))
+    if rc != SPEC_OK:
+        raise SpecError("spec_last_error", rc)
+    return out.value

@@ -1,0 +1,210 @@
+// C ABI of libspecverify.so: host-side validation, workspace carving and
+// dispatch.  Every computation of the verification row runs in the kernels of
+// chain.cu and argmax.cu; this file only checks arguments and launches.
+#include <float.h>
+#include <math.h>
+
+#include "kernels.cuh"
+
+namespace {
+
+using namespace sv;
+
+constexpr double kLog2e = 1.4426950408889634073599246810019;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int esize(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+
+// log2(e)/T as c_hi + c_lo with c_hi rounded down and c_lo > 0.
+bool temperature_consts(float T, float* hi, float* lo) {
+  if (!(T > 0.f) || !isfinite(T)) return false;
+  const double c = kLog2e / (double)T;
+  if (!(c < (double)FLT_MAX) || !(c > (double)FLT_MIN)) return false;
+  float h = (float)c;
+  if ((double)h > c) h = nextafterf(h, 0.f);
+  float l = (float)(c - (double)h);
+  if (!(l > 0.f)) l = FLT_MIN;
+  *hi = h;
+  *lo = l;
+  return true;
+}
+
+// Units of one row: vectors per row, units per row and vectors per unit.
+void row_units(int V, int dtype, bool vec, int* nvec, int* nsplit, int* vps) {
+  *nvec = vec ? (int)((size_t)V * esize(dtype) / 16) : V;
+  *nsplit = ceil_div(*nvec, kUnitVecs);
+  *vps = ceil_div(*nvec, *nsplit);
+}
+
+int check_ws(void* ws, size_t bytes, int B, int rows, int V) {
+  if (!ws || !aligned16(ws)) return SPEC_EWORKSPACE;
+  if (bytes < WsLayout(B, rows, V).total) return SPEC_EWORKSPACE;
+  return SPEC_OK;
+}
+
+__global__ void rollback_kernel(const int32_t* old_lens, const int32_t* n_acc, int k, int B,
+                                int32_t* new_lens, int32_t* rewind_lens) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int32_t n = n_acc[b], old = old_lens[b];
+  if (n < 0 || n > k) {
+    new_lens[b] = old;
+    if (rewind_lens) rewind_lens[b] = 0;
+    return;
+  }
+  new_lens[b] = old + n + 1;
+  if (rewind_lens) rewind_lens[b] = k - n;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_size(int B, int rows_per_request, int V) {
+  if (B < 1 || rows_per_request < 1 || V < 2) return 0;
+  return WsLayout(B, rows_per_request, V).total;
+}
+
+int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  if (!workspace || workspace_bytes == 0) return SPEC_EINVAL;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) != cudaSuccess)
+    return SPEC_ECUDA;
+  return SPEC_OK;
+}
+
+int spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype,
+                      const int32_t* draft_tokens, const float* uniforms, float temperature,
+                      int B, int k, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                      float* out_probs, int32_t* seq_lens, void* workspace,
+                      size_t workspace_bytes, spec_stream_t stream) {
+  if (!target_logits || !draft_logits || !draft_tokens || !uniforms || !out_tokens ||
+      !out_num_accepted)
+    return SPEC_EINVAL;
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || k < 1 || k > SPEC_MAX_DRAFT ||
+      V < 2)
+    return SPEC_EINVAL;
+  ChainArgs a{};
+  if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
+  const int R = 2 * k + 1;
+  if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
+  const bool vec = aligned16(target_logits) && aligned16(draft_logits) &&
+                   ((size_t)V * esize(dtype)) % 16 == 0;
+  row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
+  a.nchunks = num_chunks(V);
+  a.cpc = kChunksPerCta;
+  a.nsplit2 = ceil_div(a.nchunks, a.cpc);
+  if ((long)B * R * a.nsplit > INT_MAX || (long)B * a.nsplit2 > INT_MAX) return SPEC_EINVAL;
+  a.target = static_cast<const char*>(target_logits);
+  a.draft = static_cast<const char*>(draft_logits);
+  a.tokens = draft_tokens;
+  a.uniforms = uniforms;
+  a.B = B;
+  a.k = k;
+  a.V = V;
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.out_probs = out_probs;
+  a.seq_lens = seq_lens;
+  a.ws = ws_views(workspace, WsLayout(B, R, V));
+  return launch_chain(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
+                                                                          : SPEC_ECUDA;
+}
+
+int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens, int B,
+                       int k, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                       int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                       spec_stream_t stream) {
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || k < 1 || k > SPEC_MAX_DRAFT ||
+      V < 2)
+    return SPEC_EINVAL;
+  const int R = k + 1;
+  if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
+  ArgmaxArgs a{};
+  const bool vec = aligned16(target_logits) && ((size_t)V * esize(dtype)) % 16 == 0;
+  row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
+  if ((long)B * R * a.nsplit > INT_MAX) return SPEC_EINVAL;
+  a.target = static_cast<const char*>(target_logits);
+  a.B = B;
+  a.R = R;
+  a.V = V;
+  a.tree = 0;
+  a.draft_tokens = draft_tokens;
+  a.k = k;
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.seq_lens = seq_lens;
+  a.ws = ws_views(workspace, WsLayout(B, R, V));
+  return launch_argmax(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
+                                                                           : SPEC_ECUDA;
+}
+
+int spec_verify_tree(const void* target_logits, int dtype, const int32_t* tree_tokens,
+                     const int32_t* paths, int B, int N, int P, int L, int V,
+                     int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_best_path,
+                     int32_t* out_accepted_nodes, int32_t* seq_lens, void* workspace,
+                     size_t workspace_bytes, spec_stream_t stream) {
+  if (!target_logits || !tree_tokens || !paths || !out_tokens || !out_num_accepted)
+    return SPEC_EINVAL;
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || N < 1 || N > SPEC_MAX_TREE_NODES ||
+      P < 1 || L < 2 || L > SPEC_MAX_PATH_LEN || V < 2 || (long)P * L > INT_MAX)
+    return SPEC_EINVAL;
+  if (const int rc = check_ws(workspace, workspace_bytes, B, N, V)) return rc;
+  ArgmaxArgs a{};
+  const bool vec = aligned16(target_logits) && ((size_t)V * esize(dtype)) % 16 == 0;
+  row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
+  if ((long)B * N * a.nsplit > INT_MAX) return SPEC_EINVAL;
+  a.target = static_cast<const char*>(target_logits);
+  a.B = B;
+  a.R = N;
+  a.V = V;
+  a.tree = 1;
+  a.tree_tokens = tree_tokens;
+  a.paths = paths;
+  a.P = P;
+  a.L = L;
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.out_best = out_best_path;
+  a.out_nodes = out_accepted_nodes;
+  a.seq_lens = seq_lens;
+  a.ws = ws_views(workspace, WsLayout(B, N, V));
+  return launch_argmax(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
+                                                                           : SPEC_ECUDA;
+}
+
+int spec_rollback_lengths(const int32_t* old_lens, const int32_t* num_accepted, int k, int B,
+                          int32_t* new_lens, int32_t* rewind_lens, spec_stream_t stream) {
+  if (!old_lens || !num_accepted || !new_lens || B < 1 || k < 0) return SPEC_EINVAL;
+  rollback_kernel<<<ceil_div(B, 256), 256, 0, (cudaStream_t)stream>>>(old_lens, num_accepted, k,
+                                                                       B, new_lens, rewind_lens);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int spec_last_error(void* workspace, size_t workspace_bytes, spec_stream_t stream,
+                    int* status_out) {
+  if (!workspace || !status_out || workspace_bytes < sizeof(int)) return SPEC_EINVAL;
+  const cudaStream_t st = (cudaStream_t)stream;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess)
+    return SPEC_ECUDA;
+  *status_out = h;
+  return SPEC_OK;
+}
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument";
+    case SPEC_EBADINDEX: return "token or node id out of range";
+    case SPEC_ECUDA: return "CUDA error";
+    case SPEC_EWORKSPACE: return "workspace missing or too small";
+    case SPEC_ETIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,240 @@
+// Greedy verify: chain (Kestrel article 32, section 3.3: accept while the
+// target's argmax equals the draft, emit the target's own token) and EAGLE
+// tree (TensorRT-LLM deployment page, "Eagle-2" section: paths
+// [batch, max_decoding_tokens, max_path_len]).
+//
+// One CTA per (request, row, unit) streams its slice of a target row once and
+// keeps the first position of its largest stored value (compared exactly as
+// fp32, lowest index on ties).  The request's last CTA merges the units of all
+// rows, then either scans the chain (greedy) or walks every path of the tree,
+// one path per thread, and keeps the longest accepted path.
+#include "kernels.cuh"
+
+namespace sv {
+
+// (value, index) order: larger value first, then lower index.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// Fail-closed outputs of one request.
+__device__ void argmax_fail(const ArgmaxArgs& a, int b) {
+  const int W = a.tree ? a.L : a.k + 1;
+  for (int i = threadIdx.x; i < W; i += kThreads) {
+    a.out_tokens[(size_t)b * W + i] = -1;
+    if (a.tree && a.out_nodes) a.out_nodes[(size_t)b * a.L + i] = -1;
+  }
+  if (threadIdx.x == 0) {
+    a.out_n[b] = -1;
+    if (a.tree && a.out_best) a.out_best[b] = -1;
+    set_status(a.ws.status, SPEC_EBADINDEX);
+  }
+}
+
+__device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
+  __shared__ int sArg[SPEC_MAX_TREE_NODES];
+  __shared__ int sBad;
+  __shared__ int sAcc[kWarps], sPath[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) sBad = 0;
+  for (int r = warp; r < a.R; r += kWarps) {
+    float v = -INFINITY;
+    int i = INT_MAX;
+    const float2* pr = a.ws.part + ((size_t)b * a.R + r) * a.nsplit;
+    for (int u = lane; u < a.nsplit; u += 32) {
+      const float2 p = __ldcg(pr + u);
+      if (better(p.x, __float_as_int(p.y), v, i)) {
+        v = p.x;
+        i = __float_as_int(p.y);
+      }
+    }
+    warp_argmax(v, i);
+    if (lane == 0) sArg[r] = i;
+  }
+  __syncthreads();
+
+  if (!a.tree) {  // ---------------------------------------------- greedy chain
+    const int k = a.k;
+    const int32_t* d = a.draft_tokens + (size_t)b * k;
+    for (int i = threadIdx.x; i < k; i += kThreads)
+      if (d[i] < 0 || d[i] >= a.V) sBad = 1;
+    __syncthreads();
+    if (sBad) {
+      argmax_fail(a, b);
+      return;
+    }
+    if (threadIdx.x == 0) {
+      int j = 0;
+      while (j < k && sArg[j] == d[j]) ++j;
+      int32_t* out = a.out_tokens + (size_t)b * (k + 1);
+      for (int i = 0; i <= k; ++i) out[i] = i < j ? d[i] : (i == j ? sArg[j] : -1);
+      a.out_n[b] = j;
+      if (a.seq_lens) a.seq_lens[b] += j + 1;
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- tree
+  const int N = a.R, P = a.P, L = a.L;
+  const int32_t* tok = a.tree_tokens + (size_t)b * N;
+  const int32_t* pb = a.paths + (size_t)b * P * L;
+  for (int n = threadIdx.x; n < N; n += kThreads)
+    if (tok[n] < 0 || tok[n] >= a.V) sBad = 1;
+  for (int e = threadIdx.x; e < P * L; e += kThreads) {
+    const int32_t nd = pb[e];
+    if (nd < -1 || nd >= N || (e % L == 0 && nd > 0)) sBad = 1;
+  }
+  __syncthreads();
+  if (sBad) {
+    argmax_fail(a, b);
+    return;
+  }
+  // One path per thread; paths in increasing order so a strict '>' keeps the
+  // lowest index among equally long paths.
+  int best_acc = -1, best_p = INT_MAX;
+  for (int p = threadIdx.x; p < P; p += kThreads) {
+    const int32_t* path = pb + (size_t)p * L;
+    if (path[0] < 0) continue;
+    int acc = 0;
+    for (int j = 1; j < L; ++j) {
+      const int32_t node = path[j];
+      if (node < 0 || tok[node] != sArg[path[j - 1]]) break;
+      ++acc;
+    }
+    if (acc > best_acc) {
+      best_acc = acc;
+      best_p = p;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const int oa = __shfl_xor_sync(0xffffffffu, best_acc, off);
+    const int op = __shfl_xor_sync(0xffffffffu, best_p, off);
+    if (oa > best_acc || (oa == best_acc && op < best_p)) {
+      best_acc = oa;
+      best_p = op;
+    }
+  }
+  if (lane == 0) {
+    sAcc[warp] = best_acc;
+    sPath[warp] = best_p;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kWarps; ++w)
+      if (sAcc[w] > best_acc || (sAcc[w] == best_acc && sPath[w] < best_p)) {
+        best_acc = sAcc[w];
+        best_p = sPath[w];
+      }
+    const bool none = best_acc < 0;
+    const int n = none ? 0 : best_acc;
+    const int32_t* path = none ? nullptr : pb + (size_t)best_p * L;
+    const int last = none ? 0 : path[n];
+    int32_t* out = a.out_tokens + (size_t)b * L;
+    for (int j = 0; j < L; ++j) out[j] = j < n ? tok[path[j + 1]] : (j == n ? sArg[last] : -1);
+    if (a.out_nodes)
+      for (int j = 0; j < L; ++j)
+        a.out_nodes[(size_t)b * L + j] = j <= n ? (none ? 0 : path[j]) : -1;
+    if (a.out_best) a.out_best[b] = none ? -1 : best_p;
+    a.out_n[b] = n;
+    if (a.seq_lens) a.seq_lens[b] += n + 1;
+  }
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) argmax_kernel(const ArgmaxArgs a) {
+  using IO = Io<DT, VEC>;
+  const int per_req = a.R * a.nsplit;
+  const int b = blockIdx.x / per_req;
+  const int rem = blockIdx.x - b * per_req;
+  const int r = rem / a.nsplit;
+  const int s = rem - r * a.nsplit;
+  const char* row = a.target + ((size_t)b * a.R + r) * (size_t)a.V * IO::ES;
+  const int vbeg = s * a.vps;
+  const int vend = min(a.nvec, vbeg + a.vps);
+
+  uint32_t w[kVecPerThread][IO::NW];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int v = vbeg + (int)threadIdx.x + u * kThreads;
+    if (v < vend) IO::load(row, v, w[u]);
+  }
+  // Largest value per vector; the first vector that reaches the thread's
+  // maximum holds its first occurrence (vectors are visited in order).
+  float best = -INFINITY;
+  int bu = -1;
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int v = vbeg + (int)threadIdx.x + u * kThreads;
+    if (v < vend) {
+      const float vm = IO::vmax(w[u]);
+      if (bu < 0 || vm > best) {
+        best = vm;
+        bu = u;
+      }
+    }
+  }
+  int idx = INT_MAX;
+  if (bu >= 0) {
+    uint32_t sel[IO::NW];
+#pragma unroll
+    for (int i = 0; i < IO::NW; ++i) sel[i] = w[0][i];
+#pragma unroll
+    for (int u = 1; u < kVecPerThread; ++u)
+      if (u == bu)
+#pragma unroll
+        for (int i = 0; i < IO::NW; ++i) sel[i] = w[u][i];
+    float e[IO::EPV];
+    IO::unpack(sel, e);
+    int first = 0;
+#pragma unroll
+    for (int i = IO::EPV - 1; i >= 0; --i)
+      if (e[i] == best) first = i;
+    idx = (vbeg + (int)threadIdx.x + bu * kThreads) * IO::EPV + first;
+  }
+  // Block reduce (value, index).
+  __shared__ float sv_[kWarps];
+  __shared__ int si_[kWarps];
+  warp_argmax(best, idx);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sv_[warp] = best;
+    si_[warp] = idx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < kWarps ? sv_[lane] : -INFINITY;
+    idx = lane < kWarps ? si_[lane] : INT_MAX;
+    warp_argmax(best, idx);
+    if (lane == 0) a.ws.part[blockIdx.x] = make_float2(best, __int_as_float(idx));
+  }
+  if (!last_arrival(a.ws.tick1 + b, per_req)) return;
+  argmax_epilogue(a, b);
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_argmax_t(const ArgmaxArgs& a, cudaStream_t st) {
+  const long g = (long)a.B * a.R * a.nsplit;
+  argmax_kernel<DT, VEC><<<(unsigned)g, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st) {
+  if (dtype == SPEC_BF16)
+    return vec ? launch_argmax_t<SPEC_BF16, true>(a, st) : launch_argmax_t<SPEC_BF16, false>(a, st);
+  return vec ? launch_argmax_t<SPEC_F32, true>(a, st) : launch_argmax_t<SPEC_F32, false>(a, st);
+}
+
+}  // namespace sv

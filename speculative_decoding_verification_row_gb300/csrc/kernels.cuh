@@ -1,0 +1,46 @@
+// Launch arguments and launchers of the verification kernels (internal).
+#pragma once
+
+#include "common.cuh"
+
+namespace sv {
+
+struct ChainArgs {
+  const char* target;
+  const char* draft;
+  const int32_t* tokens;
+  const float* uniforms;
+  float c_hi, c_lo;  // log2(e)/T split as hi + lo
+  int B, k, V;
+  int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
+  int nchunks, cpc, nsplit2;   // sampler: chunks per row, per CTA, CTAs per request
+  int32_t* out_tokens;
+  int32_t* out_n;
+  float* out_probs;
+  int32_t* seq_lens;
+  Ws ws;
+};
+
+struct ArgmaxArgs {
+  const char* target;
+  int B, R, V;                 // R rows per request (k+1 or N)
+  int nvec, nsplit, vps;
+  int tree;                    // 0: greedy chain, 1: tree
+  const int32_t* draft_tokens; // greedy: [B, k]
+  int k;
+  const int32_t* tree_tokens;  // tree: [B, N]
+  const int32_t* paths;        // tree: [B, P, L]
+  int P, L;
+  int32_t* out_tokens;
+  int32_t* out_n;
+  int32_t* out_best;
+  int32_t* out_nodes;
+  int32_t* seq_lens;
+  Ws ws;
+};
+
+// Enqueue the two chain passes / the argmax pass on `st`.
+cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
+cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st);
+
+}  // namespace sv

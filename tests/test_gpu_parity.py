@@ -1,0 +1,314 @@
+"""Parity of the CUDA path (through the C ABI binding) with the CPU oracle.
+
+Token ids, accept counts, best paths, accepted nodes and sequence lengths must
+match the oracle exactly, except at near-ties the oracle flags: an accept test
+with |r - p/q| < 1e-5, or a final draw whose u*Z lies within 1e-6*Z of a CDF
+boundary.  Every mismatch must be flagged; flagged and mismatched counts are
+reported.  p_i(x_i) and q_i(x_i) must agree with the oracle to 1e-5 relative
+(fp32 accumulation against fp64).  Greedy and tree verify involve no rounding
+and must match exactly everywhere.
+
+Sizes: small cases that span several units and ragged tails (including the
+element-wise path for rows that are not 16-byte aligned), then every named
+workload at full size and seeds 0, 1, 2 in the launch configuration the
+benchmark times.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import speculative_decoding_verification_row_gb300 as sv
+
+pytestmark = pytest.mark.gpu
+
+PROB_RTOL = 1e-5
+REPORT = []
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _report():
+    yield
+    path = os.environ.get("SPEC_PARITY_REPORT")
+    if path:
+        with open(path, "w") as f:
+            json.dump(REPORT, f, indent=1)
+
+
+def to_dev(arr, dtype):
+    if dtype == workloads.BF16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).cuda()
+
+
+def i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def run_chain(w, misalign=False, workspace=None):
+    t, d = to_dev(w["target"], w["dtype"]), to_dev(w["draft"], w["dtype"])
+    if misalign:  # same values one element past a 16-byte boundary
+        t, d = _offset_copy(t), _offset_copy(d)
+    seq = i32(w["seq_lens"])
+    tok, n, probs = sv.verify_chain(t, d, i32(w["draft_tokens"]),
+                                    torch.from_numpy(w["uniforms"]).cuda(), w["temperature"],
+                                    want_probs=True, seq_lens=seq, workspace=workspace)
+    torch.cuda.synchronize()
+    return dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(),
+                probs=probs.cpu().numpy(), seq_lens=seq.cpu().numpy())
+
+
+def _offset_copy(t):
+    flat = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    view = flat.as_strided(t.shape, t.stride(), storage_offset=1)
+    view.copy_(t)
+    assert view.data_ptr() % 16 != 0 and view.is_contiguous()
+    return view
+
+
+def check_chain(w, g, o, label):
+    k, B = w["k"], w["B"]
+    flags, n_o, tok_o = o["flags"], o["num_accepted"], o["tokens"]
+    flagged = mism = 0
+    for b in range(B):
+        tested = min(max(int(n_o[b]), 0), k - 1)
+        f = bool(flags[b, : tested + 1].any() or flags[b, k])
+        flagged += f
+        if g["num_accepted"][b] != n_o[b] or not np.array_equal(g["tokens"][b], tok_o[b]):
+            mism += 1
+            assert f, (f"{label}: unflagged mismatch at request {b}: gpu {g['tokens'][b]} "
+                       f"(n={g['num_accepted'][b]}) oracle {tok_o[b]} (n={n_o[b]})")
+    ok = n_o >= 0
+    po = o["probs"][ok]
+    pg = g["probs"][ok].astype(np.float64)
+    big = po > 1e-30
+    rel = np.abs(pg[big] - po[big]) / po[big]
+    assert np.all(np.abs(pg[~big] - po[~big]) <= 1e-30)
+    assert rel.max(initial=0.0) <= PROB_RTOL, f"{label}: p/q relative error {rel.max()}"
+    want_seq = oracle.rollback(w["seq_lens"], g["num_accepted"], k)["new_lens"]
+    assert np.array_equal(g["seq_lens"], want_seq), f"{label}: seq_lens"
+    REPORT.append(dict(case=label, kind="chain", requests=B, flagged=flagged, mismatched=mism,
+                       max_prob_rel_err=float(rel.max(initial=0.0)),
+                       mean_accepted=float(np.mean(n_o[ok])) if ok.any() else 0.0))
+    return flagged, mism
+
+
+def run_greedy(w, misalign=False):
+    t = to_dev(w["target"], w["dtype"])
+    if misalign:
+        t = _offset_copy(t)
+    seq = i32(w["seq_lens"])
+    tok, n = sv.verify_greedy(t, i32(w["draft_tokens"]), seq_lens=seq)
+    torch.cuda.synchronize()
+    return dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(), seq_lens=seq.cpu().numpy())
+
+
+def check_greedy(w, g, o, label):
+    assert np.array_equal(g["tokens"], o["tokens"]), label
+    assert np.array_equal(g["num_accepted"], o["num_accepted"]), label
+    want_seq = oracle.rollback(w["seq_lens"], o["num_accepted"], w["k"])["new_lens"]
+    assert np.array_equal(g["seq_lens"], want_seq), label
+    REPORT.append(dict(case=label, kind="greedy", requests=w["B"], flagged=0, mismatched=0))
+
+
+def run_tree(w, misalign=False):
+    t = to_dev(w["target"], w["dtype"])
+    if misalign:
+        t = _offset_copy(t)
+    seq = i32(w["seq_lens"])
+    tok, n, best, nodes = sv.verify_tree(t, i32(w["tree_tokens"]), i32(w["paths"]), seq_lens=seq)
+    torch.cuda.synchronize()
+    return dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(), best_path=best.cpu().numpy(),
+                accepted_nodes=nodes.cpu().numpy(), seq_lens=seq.cpu().numpy())
+
+
+def check_tree(w, g, o, label):
+    for key in ("tokens", "num_accepted", "best_path", "accepted_nodes"):
+        assert np.array_equal(g[key], o[key]), f"{label}: {key}\n{g[key]}\n{o[key]}"
+    want_seq = oracle.rollback(w["seq_lens"], o["num_accepted"], w["N"] - 1)["new_lens"]
+    assert np.array_equal(g["seq_lens"], want_seq), label
+    REPORT.append(dict(case=label, kind="tree", requests=w["B"], flagged=0, mismatched=0,
+                       mean_accepted=float(np.mean(o["num_accepted"]))))
+
+
+# ------------------------------------------------------------------ small cases
+SMALL_CHAIN = [
+    # (name, overrides) — units per row, chunk tails and the element-wise path
+    ("chain_b1_k4_v1024_f32", dict(B=3, V=9000)),
+    ("chain_b8_k4_v32000_f32", dict(B=4, V=4097)),            # V*4 % 16 != 0: element path
+    ("chain_b64_k7_v128256_bf16", dict(B=5, V=40000)),
+    ("chain_b64_k7_v128256_bf16", dict(B=3, V=5001)),          # element path, ragged
+    ("chain_b256_k3_v129280_bf16", dict(B=6, V=33000)),
+    ("chain_b1_k4_v1024_f32", dict(B=2, k=1, V=2)),            # smallest problem
+    ("chain_b1_k4_v1024_f32", dict(B=2, k=64, V=300)),         # longest draft
+]
+
+
+@pytest.mark.parametrize("name,over", SMALL_CHAIN, ids=lambda v: str(v))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_chain_small(name, over, seed):
+    w = workloads.make(name, seed=seed, **over)
+    check_chain(w, run_chain(w), oracle.verify(w), f"{name}{over}/s{seed}")
+
+
+@pytest.mark.parametrize("dtype_name", ["chain_b8_k4_v32000_f32", "chain_b64_k7_v128256_bf16"])
+def test_chain_misaligned_rows(dtype_name):
+    w = workloads.make(dtype_name, seed=4, B=3, V=6000)
+    check_chain(w, run_chain(w, misalign=True), oracle.verify(w), f"{dtype_name}/misaligned")
+
+
+@pytest.mark.parametrize("name,over", [("chain_b8_k4_v32000_f32", dict(B=6, V=30011)),
+                                       ("chain_b64_k7_v128256_bf16", dict(B=4, V=50000)),
+                                       ("chain_b64_k7_v128256_bf16", dict(B=2, k=1, V=2))])
+def test_greedy_small(name, over):
+    w = workloads.make(name, seed=3, **over)
+    check_greedy(w, run_greedy(w), oracle.verify(w, greedy=True), f"greedy {name}{over}")
+
+
+def test_greedy_ties_and_misaligned():
+    """Many exactly equal maxima: the lowest index must win (bf16 and fp32)."""
+    rng = np.random.default_rng(9)
+    for dtype in (workloads.F32, workloads.BF16):
+        B, k, V = 4, 6, 20000
+        vals = rng.integers(-2, 3, (B, k + 1, V)).astype(np.float32)
+        target = workloads.f32_to_bf16_bits(vals) if dtype == workloads.BF16 else vals
+        g = np.argmax(vals, axis=2)
+        drafts = np.where(rng.random((B, k)) < 0.8, g[:, :k], (g[:, :k] + 1) % V).astype(np.int32)
+        w = dict(kind="chain", dtype=dtype, B=B, k=k, V=V, target=target, draft_tokens=drafts,
+                 seq_lens=np.arange(B, dtype=np.int32) * 10)
+        o = oracle.verify_greedy(target, drafts, dtype)
+        check_greedy(w, run_greedy(w), o, f"greedy ties {dtype}")
+        check_greedy(w, run_greedy(w, misalign=True), o, f"greedy ties {dtype} misaligned")
+
+
+@pytest.mark.parametrize("over", [dict(B=4, N=30, L=5, V=7777, level_sizes=[8, 10, 7, 4]),
+                                  dict(B=3, V=8192), dict(B=2, N=2, L=2, V=64, level_sizes=[1])])
+def test_tree_small(over):
+    w = workloads.make("tree_b16_n60_l4_v151936_bf16", seed=2, **over)
+    check_tree(w, run_tree(w), oracle.verify(w), f"tree {over}")
+    check_tree(w, run_tree(w, misalign=True), oracle.verify(w), f"tree {over} misaligned")
+
+
+# ------------------------------------------------------------------ edge cases
+def test_chain_identical_draft_accepts_all():
+    w = workloads.make("chain_b64_k7_v128256_bf16", seed=5, B=4, V=12000)
+    w["draft"] = np.ascontiguousarray(w["target"][:, : w["k"]])
+    g, o = run_chain(w), oracle.verify(w)
+    assert np.all(o["num_accepted"] == w["k"])
+    check_chain(w, g, o, "identical draft")
+
+
+def test_chain_masked_vocab():
+    """-inf logits (masked tokens) in both rows: they carry no probability."""
+    w = workloads.make("chain_b8_k4_v32000_f32", seed=6, B=4, V=8000)
+    mask = np.random.default_rng(6).random(8000) < 0.5
+    w["target"][:, :, mask] = -np.inf
+    w["draft"][:, :, mask] = -np.inf
+    free = np.flatnonzero(~mask)
+    w["draft_tokens"] = free[np.random.default_rng(7).integers(0, free.size, (4, 4))].astype(np.int32)
+    g, o = run_chain(w), oracle.verify(w)
+    check_chain(w, g, o, "masked vocab")
+    emitted = g["tokens"][g["tokens"] >= 0]
+    assert not np.any(mask[emitted])
+
+
+def test_chain_bad_token_fails_closed():
+    w = workloads.make("chain_b1_k4_v1024_f32", seed=8, B=5, V=3000)
+    w["draft_tokens"][2, 1] = 3000
+    w["draft_tokens"][4, 0] = -1
+    ws = sv.Workspace()
+    seq0 = w["seq_lens"].copy()
+    g = run_chain(w, workspace=ws)
+    assert sv.last_error(ws) == sv.SPEC_EBADINDEX
+    assert sv.last_error(ws) == sv.SPEC_OK  # cleared by the read
+    o = oracle.verify(w)
+    assert o["rc"] == oracle.EBADINDEX
+    for b in (2, 4):
+        assert g["num_accepted"][b] == -1 and np.all(g["tokens"][b] == -1)
+        assert g["seq_lens"][b] == seq0[b] and np.all(np.isnan(g["probs"][b]))
+    keep = [0, 1, 3]
+    sub = {key: (w[key][keep] if isinstance(w[key], np.ndarray) else w[key]) for key in w}
+    sub["B"] = 3
+    check_chain(sub, {key: v[keep] for key, v in g.items()},
+                {key: (v[keep] if isinstance(v, np.ndarray) else v) for key, v in o.items()},
+                "bad token (others)")
+
+
+def test_tree_bad_indices_fail_closed():
+    w = workloads.make("tree_b16_n60_l4_v151936_bf16", seed=3, B=4, V=4096)
+    w["paths"][1, 0, 2] = 60      # node id out of range
+    w["paths"][2, 3, 0] = 5       # path that does not start at the root
+    w["tree_tokens"][3, 7] = 4096  # token out of range
+    ws = sv.Workspace()
+    t = to_dev(w["target"], w["dtype"])
+    seq = i32(w["seq_lens"])
+    tok, n, best, nodes = sv.verify_tree(t, i32(w["tree_tokens"]), i32(w["paths"]), seq_lens=seq,
+                                         workspace=ws)
+    assert sv.last_error(ws) == sv.SPEC_EBADINDEX
+    o = oracle.verify(w)
+    assert np.array_equal(tok.cpu().numpy(), o["tokens"])
+    assert np.array_equal(n.cpu().numpy(), o["num_accepted"])
+    assert list(o["num_accepted"][1:]) == [-1, -1, -1]
+    assert np.array_equal(seq.cpu().numpy()[1:], w["seq_lens"][1:])
+
+
+def test_tree_without_used_paths():
+    w = workloads.make("tree_b16_n60_l4_v151936_bf16", seed=4, B=2, V=1024)
+    w["paths"][0, :, :] = -1
+    g, o = run_tree(w), oracle.verify(w)
+    check_tree(w, g, o, "tree without paths")
+    assert g["best_path"][0] == -1 and g["num_accepted"][0] == 0
+
+
+def test_rollback_kernel_matches_oracle():
+    rng = np.random.default_rng(12)
+    k, B = 7, 5000
+    old = rng.integers(0, 1 << 20, B).astype(np.int32)
+    n = rng.integers(-2, k + 3, B).astype(np.int32)
+    new, rew = sv.rollback_lengths(i32(old), i32(n), k)
+    o = oracle.rollback(old, n, k)
+    assert np.array_equal(new.cpu().numpy(), o["new_lens"])
+    assert np.array_equal(rew.cpu().numpy(), o["rewind_lens"])
+    lens = i32(old)  # in place (new_lens aliases old_lens)
+    sv.rollback_lengths(lens, i32(n), k, new_lens=lens)
+    assert np.array_equal(lens.cpu().numpy(), o["new_lens"])
+
+
+def test_repeat_calls_are_deterministic_and_workspace_reusable():
+    ws = sv.Workspace()
+    w = workloads.make("chain_b64_k7_v128256_bf16", seed=9, B=6, V=30000)
+    a = run_chain(w, workspace=ws)
+    b = run_chain(w, workspace=ws)
+    for key in a:
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+    w2 = workloads.make("chain_b1_k4_v1024_f32", seed=9, B=2, V=777)
+    check_chain(w2, run_chain(w2, workspace=ws), oracle.verify(w2), "reuse smaller")
+    check_chain(w, run_chain(w, workspace=ws), oracle.verify(w), "reuse again")
+
+
+# ------------------------------------------------------------------ full sizes
+FULL_CHAIN = ["chain_b1_k4_v1024_f32", "chain_b8_k4_v32000_f32", "chain_b64_k7_v128256_bf16",
+              "chain_b256_k3_v129280_bf16"]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("name", FULL_CHAIN)
+def test_chain_full(name, seed):
+    w = workloads.make(name, seed=seed)
+    check_chain(w, run_chain(w), oracle.verify(w), f"{name}/s{seed}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_greedy_full(seed):
+    w = workloads.make("chain_b8_k4_v32000_f32", seed=seed)
+    check_greedy(w, run_greedy(w), oracle.verify(w, greedy=True), f"greedy chain_b8_k4_v32000_f32/s{seed}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tree_full(seed):
+    w = workloads.make("tree_b16_n60_l4_v151936_bf16", seed=seed)
+    check_tree(w, run_tree(w), oracle.verify(w), f"tree_b16_n60_l4_v151936_bf16/s{seed}")
