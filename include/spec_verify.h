@@ -30,7 +30,8 @@
  *
  * Conventions for every call
  *   - All array pointers are DEVICE pointers owned by the caller; the library
- *     never allocates or frees memory and keeps no global state.  Arrays are
+ *     never allocates or frees memory.  It keeps no global state apart from
+ *     the fixed scratch array of spec_verify_chain_noalloc.  Arrays are
  *     dense, row-major, with the shapes given below.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     A host-detectable error (bad size, null pointer, small workspace)
@@ -158,6 +159,31 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *tree_t
  * entry unchanged. */
 int spec_rollback_lengths(const int32_t *old_lens, const int32_t *num_accepted, int k, int B,
                           int32_t *new_lens, int32_t *rewind_lens, spec_stream_t stream);
+
+/* Chain verify without a caller-provided workspace, for callers that cannot
+ * allocate device memory (code whose allocator forbids allocations while a
+ * step runs, or host code that owns no CUDA allocator).  The pages have no
+ * counterpart: it is an addition of this library.
+ *   Arguments and results are those of spec_verify_chain; inputs and outputs
+ *   are still the caller's device arrays.
+ *   Scratch: a file-scope device array of SPEC_NOALLOC_SCRATCH_BYTES that
+ *   every GPU loading the library holds until the process exits.  A problem
+ *   whose spec_workspace_size(B, 2k+1, V) exceeds it returns SPEC_EWORKSPACE
+ *   before any launch.  The first call on a device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   Every call on a device shares the one array: calls that can overlap on the
+ *   GPU (other streams, other threads) race and must be serialised by the
+ *   caller.  Each call clears the array's counters and status word on
+ *   `stream` before launching, so the data-dependent status is not kept: a
+ *   request that fails closed shows num_accepted == -1.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define SPEC_NOALLOC_SCRATCH_BYTES (4u << 20)
+int spec_verify_chain_noalloc(const void *target_logits, const void *draft_logits, int dtype,
+                              const int32_t *draft_tokens, const float *uniforms,
+                              float temperature, int B, int k, int V,
+                              int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                              int32_t *seq_lens, spec_stream_t stream);
 
 /* Synchronise `stream`, read the workspace status word into *status_out
  * (SPEC_OK or SPEC_EBADINDEX) and clear it.  Returns SPEC_OK, SPEC_EINVAL or

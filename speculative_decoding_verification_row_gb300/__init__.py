@@ -36,7 +36,8 @@ SPEC_MAX_PATH_LEN = 64
 # Every entry point the header declares.
 SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_greedy", "spec_verify_tree", "spec_rollback_lengths",
-           "spec_last_error", "spec_status_string")
+           "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc")
+SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -57,11 +58,12 @@ def _bind(lib):
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
     lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P, P, P, S, P]
     lib.spec_rollback_lengths.argtypes = [P, P, I, I, P, P, P]
+    lib.spec_verify_chain_noalloc.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P]
     lib.spec_last_error.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int)]
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
-              "spec_rollback_lengths", "spec_last_error"):
+              "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc"):
         getattr(lib, f).restype = I
     return lib
 
@@ -190,6 +192,38 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
                                  _ptr(buf), buf.numel(), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_verify_chain", rc)
+    return tok, n, probs
+
+
+def verify_chain_noalloc(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                         out_tokens=None, out_num_accepted=None, out_probs=None, want_probs=False,
+                         seq_lens=None, stream=None):
+    """verify_chain without a workspace: for callers that cannot allocate device
+    scratch.  The library's fixed device array serves as scratch (problems up to
+    SPEC_NOALLOC_SCRATCH_BYTES of scratch); calls that overlap on the GPU race.
+    Output tensors are allocated here unless passed in."""
+    t = _dev(target_logits, "target_logits")
+    if t.dim() != 3:
+        raise ValueError("target_logits must be [B, k+1, V]")
+    B, k1, V = t.shape
+    k = k1 - 1
+    code = _logit_code(t, "target_logits")
+    d = _dev(draft_logits, "draft_logits", t.dtype, (B, k, V))
+    x = _dev(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    u = _dev(uniforms, "uniforms", torch.float32, (B, k + 1))
+    dev = t.device
+    tok = _out(out_tokens, "out_tokens", (B, k + 1), torch.int32, dev)
+    n = _out(out_num_accepted, "out_num_accepted", (B,), torch.int32, dev)
+    probs = None
+    if out_probs is not None or want_probs:
+        probs = _out(out_probs, "out_probs", (B, k, 2), torch.float32, dev)
+    if seq_lens is not None:
+        _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    sh, _ = _stream_handle(stream, dev)
+    rc = lib().spec_verify_chain_noalloc(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
+                                         B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_chain_noalloc", rc)
     return tok, n, probs
 
 
