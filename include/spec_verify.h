@@ -74,13 +74,16 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 /* Largest supported draft length k of a chain call, and the largest tree
  * (N nodes, L path length) of a tree call. */
 #define SPEC_MAX_DRAFT 64
+/* Largest batch B of any call. */
+#define SPEC_MAX_BATCH 8192
 #define SPEC_MAX_TREE_NODES 1024
 #define SPEC_MAX_PATH_LEN 64
 
 /* Bytes of scratch one call needs for B requests of `rows_per_request` logit
  * rows of width V (chain: 2k+1, greedy: k+1, tree: N).  Returns 0 for invalid
  * sizes.  The same workspace may be reused by any call whose own size is not
- * larger. */
+ * larger.  Every workspace starts with a fixed 512 KB block of per-request
+ * sync lines (SPEC_MAX_BATCH of them). */
 size_t spec_workspace_size(int B, int rows_per_request, int V);
 
 /* Zero a workspace (asynchronously, on `stream`).  Call once after allocating

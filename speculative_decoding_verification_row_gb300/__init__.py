@@ -30,6 +30,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecveri
 SPEC_OK, SPEC_EINVAL, SPEC_EBADINDEX, SPEC_ECUDA, SPEC_EWORKSPACE, SPEC_ETIMEOUT = 0, -1, -2, -3, -4, -5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_MAX_DRAFT = 64
+SPEC_MAX_BATCH = 8192
 SPEC_MAX_TREE_NODES = 1024
 SPEC_MAX_PATH_LEN = 64
 

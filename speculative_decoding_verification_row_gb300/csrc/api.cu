@@ -62,7 +62,7 @@ __global__ void rollback_kernel(const int32_t* old_lens, const int32_t* n_acc, i
 extern "C" {
 
 size_t spec_workspace_size(int B, int rows_per_request, int V) {
-  if (B < 1 || rows_per_request < 1 || V < 2) return 0;
+  if (B < 1 || B > SPEC_MAX_BATCH || rows_per_request < 1 || V < 2) return 0;
   return WsLayout(B, rows_per_request, V).total;
 }
 
@@ -81,8 +81,8 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   if (!target_logits || !draft_logits || !draft_tokens || !uniforms || !out_tokens ||
       !out_num_accepted)
     return SPEC_EINVAL;
-  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || k < 1 || k > SPEC_MAX_DRAFT ||
-      V < 2)
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || k < 1 ||
+      k > SPEC_MAX_DRAFT || V < 2)
     return SPEC_EINVAL;
   ChainArgs a{};
   if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
@@ -93,8 +93,8 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
-  a.nsplit2 = ceil_div(a.nchunks, a.cpc);
-  if ((long)B * R * a.nsplit > INT_MAX || (long)B * a.nsplit2 > INT_MAX) return SPEC_EINVAL;
+  a.nsplit2 = num_items(V);
+  if ((long)B * (R * (long)a.nsplit + a.nsplit2) > INT_MAX) return SPEC_EINVAL;
   a.target = static_cast<const char*>(target_logits);
   a.draft = static_cast<const char*>(draft_logits);
   a.tokens = draft_tokens;
@@ -116,8 +116,8 @@ int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draf
                        int32_t* seq_lens, void* workspace, size_t workspace_bytes,
                        spec_stream_t stream) {
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
-  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || k < 1 || k > SPEC_MAX_DRAFT ||
-      V < 2)
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || k < 1 ||
+      k > SPEC_MAX_DRAFT || V < 2)
     return SPEC_EINVAL;
   const int R = k + 1;
   if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
@@ -147,7 +147,8 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* tree_t
                      size_t workspace_bytes, spec_stream_t stream) {
   if (!target_logits || !tree_tokens || !paths || !out_tokens || !out_num_accepted)
     return SPEC_EINVAL;
-  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || N < 1 || N > SPEC_MAX_TREE_NODES ||
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || N < 1 ||
+      N > SPEC_MAX_TREE_NODES ||
       P < 1 || L < 2 || L > SPEC_MAX_PATH_LEN || V < 2 || (long)P * L > INT_MAX)
     return SPEC_EINVAL;
   if (const int rc = check_ws(workspace, workspace_bytes, B, N, V)) return rc;

@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 4) argmax_kernel(const ArgmaxArgs a)
     warp_argmax(best, idx);
     if (lane == 0) a.ws.part[blockIdx.x] = make_float2(best, __int_as_float(idx));
   }
-  if (!last_arrival(a.ws.tick1 + b, per_req)) return;
+  if (!last_arrival(&a.ws.sync[b].tick1, per_req)) return;
   argmax_epilogue(a, b);
 }
 

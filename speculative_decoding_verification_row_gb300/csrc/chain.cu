@@ -3,45 +3,32 @@
 // max(0, p - q) normalised, or take a bonus token from the extra row; vLLM
 // learning book, section 2: accept iff r < min(1, p(x_i)/q(x_i))).
 //
-// Pass 1, chain_stats_kernel: one CTA per (request, row, unit) streams its
-// slice of a target or draft row once and reduces it to the softmax statistics
-// (max m, S = sum 2^(log2(e)/T * (x - m))).  The request's last CTA merges the
-// units of all 2k+1 rows, gathers p_i(x_i) and q_i(x_i), and runs the
-// accept scan; it stores the stopping position and the statistics of the
-// row(s) the final draw needs.
+// Pass 1, chain_rowstats_kernel: one short-lived CTA per 32 KB slice of a
+// target or draft row.  It reads its slice once with 128-bit loads and
+// reduces it to softmax statistics: each warp takes its own max, sums
+// 2^(c(x - max)) (c = log2(e)/T) with packed fp32x2 arithmetic and one exp
+// per logit, and thread 0 merges the eight warp pairs into the slice's (M, S).
+// Slices are ordered by descending draft position, so the rows the draw most
+// often needs (the first positions) are read last and are still in L2 when
+// pass 2 runs.  No CTA waits for another.
 //
-// Pass 2, chain_sample_kernel: the final token is drawn by inverse CDF from
-// w_t = max(0, p_j(t) - q_j(t)) (rejection at j) or w_t = p_k(t) (bonus).
-// CTAs of a request split the row(s) into 256-token chunks and store each
-// chunk's weight sum; the request's last CTA prefix-sums the chunk sums in
-// fp64, finds the chunk holding u * Z, re-reads only that chunk and scans it
-// with a warp prefix sum to find the token.
+// Pass 2, chain_draw_kernel: launched as a programmatic dependent of pass 1,
+// one wave of persistent CTAs taking draw items (64 chunks of 256 tokens of
+// one request) in grid-stride order.  For each item a CTA gathers x_i's
+// logits, merges the request's slice statistics and runs the accept scan
+// (tiny; every CTA of the request repeats it).  It then sums the draw weights
+// of its chunks: w_t = max(0, p_j(t) - q_j(t)) after a rejection at j,
+// w_t = p_k(t) when all k are accepted.  The request's last item (atomic
+// ticket, no waiting) prefix-sums the chunk sums exactly in 64-bit fixed
+// point, finds the chunk holding u*Z, re-reads only that chunk, scans it with
+// a warp prefix sum and writes the outputs.
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace sv {
 
-// Block-wide merge of (m, s); the result is valid in thread 0.
-__device__ __forceinline__ void block_lse(float& m, float& s, float c_hi, float c_lo) {
-  __shared__ float sm[kWarps], ss[kWarps];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-    lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, s, off),
-              c_hi, c_lo);
-  if (lane == 0) {
-    sm[warp] = m;
-    ss[warp] = s;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    m = lane < kWarps ? sm[lane] : -INFINITY;
-    s = lane < kWarps ? ss[lane] : 0.f;
-#pragma unroll
-    for (int off = kWarps / 2; off > 0; off >>= 1)
-      lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, s, off),
-                c_hi, c_lo);
-  }
-}
+namespace {
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -49,139 +36,125 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// ------------------------------------------------------------------ pass 1 epilogue
-template <int DT>
-__device__ void chain_scan(const ChainArgs& a, int b) {
-  __shared__ float sM[2 * SPEC_MAX_DRAFT + 1], sS[2 * SPEC_MAX_DRAFT + 1];
-  __shared__ float sRatio[SPEC_MAX_DRAFT];
-  __shared__ int sBad;
-  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
-  const int k = a.k, R = 2 * k + 1;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) sBad = 0;
-  // Merge the units of every row, in unit order.
-  for (int r = warp; r < R; r += kWarps) {
-    float m = -INFINITY, s = 0.f;
-    const float2* pr = a.ws.part + ((size_t)b * R + r) * a.nsplit;
-    for (int u = lane; u < a.nsplit; u += 32) {
-      const float2 v = __ldcg(pr + u);
-      lse_merge(m, s, v.x, v.y, a.c_hi, a.c_lo);
-    }
+__device__ __forceinline__ const char* row_ptr(const ChainArgs& a, int b, int r, size_t row_bytes) {
+  return r <= a.k ? a.target + ((size_t)b * (a.k + 1) + r) * row_bytes
+                  : a.draft + ((size_t)b * a.k + (r - a.k - 1)) * row_bytes;
+}
+
+// Sum of 2^(c (x - M)) over one vector, as a pair of partial sums.
+template <int DT, bool VEC>
+__device__ __forceinline__ float2 vec_expsum(const uint32_t (&w)[Io<DT, VEC>::NW], float2 nm,
+                                             float2 ch, float2 cl) {
+  if constexpr (VEC && DT == SPEC_BF16) {
+    float2 e[4];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, s, off),
-                a.c_hi, a.c_lo);
-    if (lane == 0) {
-      sM[r] = m;
-      sS[r] = s;
+    for (int j = 0; j < 4; ++j) {
+      const float2 d = add2(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), nm);
+      const float2 y = fma2(d, ch, mul2(d, cl));
+      e[j] = make_float2(ex2(y.x), ex2(y.y));
     }
-  }
-  __syncthreads();
-  const size_t row_bytes = (size_t)a.V * ES;
-  for (int i = threadIdx.x; i < k; i += kThreads) {
-    const int x = a.tokens[(size_t)b * k + i];
-    if (x < 0 || x >= a.V) {
-      sBad = 1;
-      sRatio[i] = 0.f;
-      continue;
+    return add2(add2(e[0], e[1]), add2(e[2], e[3]));
+  } else if constexpr (VEC) {
+    float2 e[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 d = add2(make_float2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])), nm);
+      const float2 y = fma2(d, ch, mul2(d, cl));
+      e[j] = make_float2(ex2(y.x), ex2(y.y));
     }
-    const float xp = load_logit<DT>(a.target + ((size_t)b * (k + 1) + i) * row_bytes, x);
-    const float xq = load_logit<DT>(a.draft + ((size_t)b * k + i) * row_bytes, x);
-    const float p = ex2(scaled(xp - sM[i], a.c_hi, a.c_lo)) / sS[i];
-    const float q = ex2(scaled(xq - sM[k + 1 + i], a.c_hi, a.c_lo)) / sS[k + 1 + i];
-    if (a.out_probs) {
-      a.out_probs[((size_t)b * k + i) * 2] = p;
-      a.out_probs[((size_t)b * k + i) * 2 + 1] = q;
-    }
-    sRatio[i] = q > 0.f ? p / q : INFINITY;
-  }
-  __syncthreads();
-  if (sBad) {
-    if (a.out_probs)
-      for (int i = threadIdx.x; i < 2 * k; i += kThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
-    if (threadIdx.x == 0) {
-      set_status(a.ws.status, SPEC_EBADINDEX);
-      ReqInfo ri{};
-      ri.j = -1;
-      a.ws.req[b] = ri;
-    }
-    return;
-  }
-  if (threadIdx.x == 0) {
-    const float* r = a.uniforms + (size_t)b * (k + 1);
-    int j = k;
-    for (int i = 0; i < k; ++i)
-      if (!(r[i] < sRatio[i])) {
-        j = i;
-        break;
-      }
-    ReqInfo ri{};
-    ri.j = j;
-    ri.mp = sM[j];
-    ri.sp = sS[j];
-    if (j < k) {
-      ri.mq = sM[k + 1 + j];
-      ri.sq = sS[k + 1 + j];
-    }
-    a.ws.req[b] = ri;
+    return add2(e[0], e[1]);
+  } else {
+    float x[1];
+    Io<DT, false>::unpack(w, x);
+    return make_float2(ex2(scaled(x[0] + nm.x, ch.x, cl.x)), 0.f);
   }
 }
 
 // ------------------------------------------------------------------ pass 1
+// Row of slice-row index rr in pass-1 order: the B bonus rows first, then,
+// for p = k-1 down to 0, the target and draft rows of position p of every
+// request.  r < k+1 is target row r, r > k is draft row r-k-1.
+__device__ __forceinline__ void slice_row(const ChainArgs& a, int rr, int& b, int& r) {
+  if (rr < a.B) {
+    b = rr;
+    r = a.k;
+    return;
+  }
+  rr -= a.B;
+  const int q = rr / (2 * a.B);
+  const int rem = rr - q * 2 * a.B;
+  const int p = a.k - 1 - q;
+  b = rem >> 1;
+  r = (rem & 1) ? a.k + 1 + p : p;
+}
+
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4) chain_stats_kernel(const ChainArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) chain_rowstats_kernel(const ChainArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;");
   using IO = Io<DT, VEC>;
-  const int R = 2 * a.k + 1;
-  const int per_req = R * a.nsplit;
-  const int b = blockIdx.x / per_req;
-  const int rem = blockIdx.x - b * per_req;
-  const int r = rem / a.nsplit;
-  const int s = rem - r * a.nsplit;
-  const size_t row_bytes = (size_t)a.V * IO::ES;
-  const char* row = r <= a.k ? a.target + ((size_t)b * (a.k + 1) + r) * row_bytes
-                             : a.draft + ((size_t)b * a.k + (r - a.k - 1)) * row_bytes;
+  const int tid = threadIdx.x;
+  const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
+  int b, r;
+  slice_row(a, rr, b, r);
+  const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
   const int vbeg = s * a.vps;
   const int vend = min(a.nvec, vbeg + a.vps);
 
   uint32_t w[kVecPerThread][IO::NW];
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
-    const int v = vbeg + (int)threadIdx.x + u * kThreads;
+    const int v = vbeg + tid + u * kThreads;
     if (v < vend) IO::load(row, v, w[u]);
   }
   float m = -INFINITY;
+  if constexpr (VEC && DT == SPEC_BF16) {
+    uint32_t mx = 0xff80ff80u;  // (-inf, -inf)
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int v = vbeg + (int)threadIdx.x + u * kThreads;
-    if (v < vend) m = fmaxf(m, IO::vmax(w[u]));
+    for (int u = 0; u < kVecPerThread; ++u)
+      if (vbeg + tid + u * kThreads < vend)
+        mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(w[u][0], w[u][1]), bf16x2_max(w[u][2], w[u][3])));
+    m = fmaxf(bf16_lo(mx), bf16_hi(mx));
+  } else {
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u)
+      if (vbeg + tid + u * kThreads < vend) m = fmaxf(m, IO::vmax(w[u]));
   }
-  const float ms = m == -INFINITY ? 0.f : m;
-  float acc = 0.f;
+  // Warp max, then this warp's sum relative to it; thread 0 merges the warps.
+  __shared__ float s_wm[kWarps], s_ws[kWarps];
+  const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int v = vbeg + (int)threadIdx.x + u * kThreads;
-    if (v < vend) {
-      float e[IO::EPV];
-      IO::unpack(w[u], e);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float Ms = m == -INFINITY ? 0.f : m;
+  const float2 nm = make_float2(-Ms, -Ms), ch = make_float2(a.c_hi, a.c_hi),
+               cl = make_float2(a.c_lo, a.c_lo);
+  float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < IO::EPV; ++i) e[i] = ex2(scaled(e[i] - ms, a.c_hi, a.c_lo));
+  for (int u = 0; u < kVecPerThread; ++u)
+    if (vbeg + tid + u * kThreads < vend) acc = add2(acc, vec_expsum<DT, VEC>(w[u], nm, ch, cl));
+  const float ssum = warp_sum(acc.x + acc.y);
+  if (lane == 0) {
+    s_wm[warp] = m;
+    s_ws[warp] = ssum;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float M = s_wm[0];
 #pragma unroll
-      for (int h = IO::EPV / 2; h > 0; h >>= 1)
+    for (int i = 1; i < kWarps; ++i) M = fmaxf(M, s_wm[i]);
+    float S = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
-        for (int i = 0; i < h; ++i) e[i] += e[i + h];
-      acc += e[0];
+      for (int i = 0; i < kWarps; ++i)
+        if (s_ws[i] > 0.f) S += s_ws[i] * ex2(scaled(s_wm[i] - M, a.c_hi, a.c_lo));
     }
+    a.ws.part[((size_t)b * (2 * a.k + 1) + r) * a.nsplit + s] = make_float2(M, S);
   }
-  block_lse(m, acc, a.c_hi, a.c_lo);
-  if (threadIdx.x == 0) a.ws.part[blockIdx.x] = make_float2(m, acc);
-  if (!last_arrival(a.ws.tick1 + b, per_req)) return;
-  chain_scan<DT>(a, b);
 }
 
 // ------------------------------------------------------------------ pass 2
 // The 8 draw weights of lane `lane` in chunk `c` (0 past the row's end):
 // residual: 2^(c(xp - mp)) - lam * 2^(c(xq - mq)) clamped at 0, lam = Sp/Sq
-// (that is Sp * max(0, p - q)); bonus: 2^(c(xp - mp)) (Sp * p).
+// (that is Sp * max(0, p - q)); bonus (qrow == nullptr): 2^(c(xp - mp)).
 template <int DT, bool VEC>
 __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow, int c, int lane,
                                               int V, float mp, float mq, float lam, float c_hi,
@@ -192,18 +165,22 @@ __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow
     constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
     constexpr int LOADS = 8 * ES / 16;  // 16-byte loads per row per lane
     using IO = Io<DT, true>;
+    uint32_t P[LOADS][4], Q[LOADS][4];
+#pragma unroll
+    for (int h = 0; h < LOADS; ++h) {  // issue every load first
+      const long th = t0 + h * IO::EPV;
+      if (th < V) {
+        ld_stream_v4(prow + th * ES, P[h]);
+        if (qrow) ld_stream_v4(qrow + th * ES, Q[h]);
+      }
+    }
 #pragma unroll
     for (int h = 0; h < LOADS; ++h) {
       const long th = t0 + h * IO::EPV;
       float ep[IO::EPV], eq[IO::EPV];
       if (th < V) {
-        uint32_t w[4];
-        ld_stream_v4(prow + th * ES, w);
-        IO::unpack(w, ep);
-        if (qrow) {
-          ld_stream_v4(qrow + th * ES, w);
-          IO::unpack(w, eq);
-        }
+        IO::unpack(P[h], ep);
+        if (qrow) IO::unpack(Q[h], eq);
       } else {
 #pragma unroll
         for (int i = 0; i < IO::EPV; ++i) ep[i] = eq[i] = -INFINITY;
@@ -234,90 +211,212 @@ __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow
   }
 }
 
+// A non-negative weight sum (at most 256) as an integer number of 2^-32.
+__device__ __forceinline__ unsigned long long to_fixed(float x) {
+  return __float2ull_rn(x * 4294967296.0f);
+}
+
 __device__ __forceinline__ float tree8(const float (&v)[8]) {
   return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
 }
 
-// Epilogue of pass 2: find the token and write the request's outputs.
-template <int DT, bool VEC>
-__device__ void chain_finish(const ChainArgs& a, int b, const ReqInfo& ri, const char* prow,
-                             const char* qrow, float lam) {
-  __shared__ double sTarget, sPre;
-  __shared__ int sChunk, sTok, sRetry;
-  const int k = a.k, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j = ri.j;
-  float* chunks = a.ws.chunks + (size_t)b * a.nchunks;
-  if (j < 0) {  // failed request: nothing is emitted and the cursor does not move
-    for (int i = threadIdx.x; i <= k; i += kThreads) a.out_tokens[(size_t)b * (k + 1) + i] = -1;
-    if (threadIdx.x == 0) a.out_n[b] = -1;
-    return;
+// Draw weights of one 16-byte vector pair of bf16 (8 tokens) with packed
+// fp32x2 arithmetic; the same operations as chunk_weights, lane by lane.
+__device__ __forceinline__ void weights8_bf16(const uint32_t (&P)[4], const uint32_t (&Q)[4],
+                                              bool resid, float2 nmp, float2 nmq, float2 nlam,
+                                              float2 ch, float2 cl, float (&wv)[8]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 dp = add2(make_float2(bf16_lo(P[j]), bf16_hi(P[j])), nmp);
+    const float2 yp = fma2(dp, ch, mul2(dp, cl));
+    const float2 ep = make_float2(ex2(yp.x), ex2(yp.y));
+    if (resid) {
+      const float2 dq = add2(make_float2(bf16_lo(Q[j]), bf16_hi(Q[j])), nmq);
+      const float2 yq = fma2(dq, ch, mul2(dq, cl));
+      const float2 eq = make_float2(ex2(yq.x), ex2(yq.y));
+      const float2 w = fma2(nlam, eq, ep);
+      wv[2 * j] = fmaxf(w.x, 0.f);
+      wv[2 * j + 1] = fmaxf(w.y, 0.f);
+    } else {
+      wv[2 * j] = ep.x;
+      wv[2 * j + 1] = ep.y;
+    }
   }
-  const double u = (double)a.uniforms[(size_t)b * (k + 1) + k];
-  if (threadIdx.x == 0) {
+}
+
+// Draw-weight sums of chunks [c0, c1) (warp w takes c0+w, c0+w+8, ...).
+// Each warp issues the loads of four chunks before using any.  The weights
+// are those of chunk_weights, computed with the same operations.
+// Returns, in lane 0 of each warp, the fixed-point total of that warp's chunks.
+template <int DT, bool VEC>
+__device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, const char* prow,
+                                                         const char* qrow, int c0, int c1, float mp,
+                                                         float mq, float lam,
+                                                         unsigned long long* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long wtot = 0;
+  if constexpr (VEC && DT == SPEC_BF16) {
+    constexpr int GRP = 4;
+    const bool resid = qrow != nullptr;
+    const float2 nmp = make_float2(-mp, -mp), nmq = make_float2(-mq, -mq),
+                 nlam = make_float2(-lam, -lam), ch = make_float2(a.c_hi, a.c_hi),
+                 cl = make_float2(a.c_lo, a.c_lo);
+#pragma unroll 1
+    for (int cb = c0 + warp; cb < c1; cb += GRP * kWarps) {
+      uint32_t P[GRP][4], Q[GRP][4];
+#pragma unroll
+      for (int i = 0; i < GRP; ++i) {
+        const int c = cb + i * kWarps;
+        const long t = (long)c * kChunk + lane * 8;
+        if (c < c1 && t < a.V) {
+          ld_stream_v4(prow + t * 2, P[i]);
+          if (resid) ld_stream_v4(qrow + t * 2, Q[i]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) P[i][e] = Q[i][e] = 0xff80ff80u;  // -inf: zero weight
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < GRP; ++i) {
+        const int c = cb + i * kWarps;
+        if (c >= c1) continue;
+        float wv[8];
+        weights8_bf16(P[i], Q[i], resid, nmp, nmq, nlam, ch, cl, wv);
+        const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
+        if (lane == 0) out[c] = f;
+        wtot += f;
+      }
+    }
+  } else {
+    for (int c = c0 + warp; c < c1; c += kWarps) {
+      float wv[8];
+      chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, wv);
+      const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
+      if (lane == 0) out[c] = f;
+      wtot += f;
+    }
+  }
+  return wtot;
+}
+
+// The request's last CTA: locate u*Z among the chunk sums, scan that chunk,
+// return the token (all threads call it; the result is valid in every thread).
+template <int DT, bool VEC>
+__device__ int draw_token(const ChainArgs& a, int b, const char* prow, const char* qrow,
+                          float mp, float mq, float lam, double u) {
+  __shared__ unsigned long long sTarget, sPre;
+  __shared__ int sChunk, sTok, sRetry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = a.nchunks, ni = a.nsplit2;
+  unsigned long long* chunks = a.ws.chunks + (size_t)b * n;
+  unsigned long long* items = a.ws.items + (size_t)b * ni;
+  if (tid == 0) {
     sChunk = 0;
-    sPre = 0.0;
-    sTarget = 0.0;
+    sPre = 0;
+    sTarget = 0;
     sRetry = 0;
   }
-  __syncthreads();
   for (int attempt = 0; attempt < 2; ++attempt) {
+    __syncthreads();
     if (warp == 0) {
-      // fp64 prefix over chunk sums: lane l owns a contiguous run of chunks.
-      const int n = a.nchunks, per = (n + 31) / 32;
-      const int c_lo = min(n, lane * per), c_hi = min(n, c_lo + per);
-      double tot = 0.0;
-      for (int c = c_lo; c < c_hi; ++c) tot += (double)__ldcg(chunks + c);
-      double incl = tot;
+      // Level 1: exact prefix over the item totals (lane l owns a run of items).
+      const int per = (ni + 31) / 32;
+      const int i_lo = min(ni, lane * per), i_hi = min(ni, i_lo + per);
+      unsigned long long tot = 0;
+      for (int i = i_lo; i < i_hi; ++i) tot += __ldcg(items + i);
+      unsigned long long incl = tot;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const double o = __shfl_up_sync(0xffffffffu, incl, off);
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
       }
-      const double Z = __shfl_sync(0xffffffffu, incl, 31);
-      if (lane == 0) sRetry = !(Z > 0.0);
-      if (Z > 0.0) {
-        const double target = u * Z;
+      const unsigned long long Z = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) sRetry = Z == 0;
+      if (Z > 0) {
+        const unsigned long long target = (unsigned long long)(u * (double)Z);
         const unsigned hit = __ballot_sync(0xffffffffu, incl > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, tot > 0.0);
+        const unsigned pos = __ballot_sync(0xffffffffu, tot > 0);
         const int L = hit ? __ffs(hit) - 1 : 31 - __clz(pos);  // u*Z >= Z only if u >= 1
+        unsigned long long pre = 0;
+        int item = 0;
         if (lane == L) {
-          double pre = incl - tot;
-          int chosen = -1;
-          double chosen_pre = pre;
-          for (int c = c_lo; c < c_hi; ++c) {
-            const double v = (double)__ldcg(chunks + c);
-            if (v > 0.0) {
-              chosen = c;  // keeps the last positive chunk if rounding finds none
+          pre = incl - tot;
+          int chosen = i_lo;
+          unsigned long long chosen_pre = pre;
+          for (int i = i_lo; i < i_hi; ++i) {
+            const unsigned long long v = __ldcg(items + i);
+            if (v > 0) {
+              chosen = i;  // keeps the last positive item if none is hit
               chosen_pre = pre;
             }
-            if (pre + v > target && v > 0.0) break;
+            if (pre + v > target && v > 0) break;
             pre += v;
           }
-          sChunk = chosen;
-          sPre = chosen_pre;
+          item = chosen;
+          pre = chosen_pre;
+        }
+        item = __shfl_sync(0xffffffffu, item, L);
+        pre = __shfl_sync(0xffffffffu, pre, L);
+        // Level 2: the item's chunks, two per lane (an item has at most 64).
+        const int c_base = item * a.cpc, c_cnt = min(n - c_base, a.cpc);
+        unsigned long long v0 = 2 * lane < c_cnt ? __ldcg(chunks + c_base + 2 * lane) : 0;
+        unsigned long long v1 = 2 * lane + 1 < c_cnt ? __ldcg(chunks + c_base + 2 * lane + 1) : 0;
+        unsigned long long cin = v0 + v1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const unsigned long long o = __shfl_up_sync(0xffffffffu, cin, off);
+          if (lane >= off) cin += o;
+        }
+        const unsigned long long base = pre + cin - (v0 + v1);  // before this lane's first chunk
+        int hit_c = -1;
+        if (v0 > 0 && base + v0 > target) hit_c = 0;
+        else if (v1 > 0 && base + v0 + v1 > target) hit_c = 1;
+        const unsigned hc = __ballot_sync(0xffffffffu, hit_c >= 0);
+        const unsigned pc = __ballot_sync(0xffffffffu, v0 + v1 > 0);
+        int Lc, off_c;
+        unsigned long long cpre;
+        if (hc) {
+          Lc = __ffs(hc) - 1;
+          off_c = __shfl_sync(0xffffffffu, hit_c, Lc);
+        } else {  // rounding left u*Z past the item: its last positive chunk
+          Lc = pc ? 31 - __clz(pc) : 0;
+          off_c = __shfl_sync(0xffffffffu, v1 > 0 ? 1 : 0, Lc);
+        }
+        cpre = __shfl_sync(0xffffffffu, base, Lc) + (off_c ? __shfl_sync(0xffffffffu, v0, Lc) : 0);
+        if (lane == 0) {
+          sChunk = c_base + 2 * Lc + off_c;
+          sPre = cpre;
           sTarget = target;
         }
       }
     }
     __syncthreads();
     if (!sRetry) break;
-    // The residual vanished numerically: draw from p_j instead (every CTA
-    // chunk sum is recomputed here by this CTA; a rare path).
+    // The residual vanished numerically: draw from p_j instead (this CTA
+    // recomputes every chunk and item sum; a rare path).
     qrow = nullptr;
     lam = 0.f;
-    for (int c = warp; c < a.nchunks; c += kWarps) {
+    for (int c = warp; c < n; c += kWarps) {
       float wv[8];
-      chunk_weights<DT, VEC>(prow, nullptr, c, lane, a.V, ri.mp, 0.f, 0.f, a.c_hi, a.c_lo, wv);
-      const float s = warp_sum(tree8(wv));
-      if (lane == 0) chunks[c] = s;
+      chunk_weights<DT, VEC>(prow, nullptr, c, lane, a.V, mp, 0.f, 0.f, a.c_hi, a.c_lo, wv);
+      const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
+      if (lane == 0) chunks[c] = f;
     }
     __threadfence();
     __syncthreads();
+    if (tid == 0) {
+      for (int i = 0; i < ni; ++i) {
+        unsigned long long t = 0;
+        for (int c = i * a.cpc; c < min(n, (i + 1) * a.cpc); ++c) t += __ldcg(chunks + c);
+        items[i] = t;
+      }
+      __threadfence();
+    }
   }
   if (warp == 0) {
     const int c = sChunk;
     float wv[8];
-    chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, ri.mp, ri.mq, lam, a.c_hi, a.c_lo, wv);
+    chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, wv);
     float loc[8];
     loc[0] = wv[0];
 #pragma unroll
@@ -330,11 +429,11 @@ __device__ void chain_finish(const ChainArgs& a, int b, const ReqInfo& ri, const
     }
     float excl = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) excl = 0.f;
-    const double pre = sPre, target = sTarget;
+    const unsigned long long pre = sPre, target = sTarget;
     int first = 8;
 #pragma unroll
     for (int i = 7; i >= 0; --i)
-      if (wv[i] > 0.f && pre + (double)(excl + loc[i]) > target) first = i;
+      if (wv[i] > 0.f && pre + to_fixed(excl + loc[i]) > target) first = i;
     const unsigned hit = __ballot_sync(0xffffffffu, first < 8);
     int tok;
     if (hit) {
@@ -353,64 +452,224 @@ __device__ void chain_finish(const ChainArgs& a, int b, const ReqInfo& ri, const
     if (lane == 0) sTok = tok;
   }
   __syncthreads();
-  const int tok = sTok;
-  for (int i = threadIdx.x; i <= k; i += kThreads)
-    a.out_tokens[(size_t)b * (k + 1) + i] =
-        i < j ? a.tokens[(size_t)b * k + i] : (i == j ? tok : -1);
-  if (threadIdx.x == 0) {
+  return sTok;
+}
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
+  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
+  __shared__ float sM[2 * SPEC_MAX_DRAFT + 1], sS[2 * SPEC_MAX_DRAFT + 1];
+  __shared__ float sP[SPEC_MAX_DRAFT], sQ[SPEC_MAX_DRAFT];
+  __shared__ int sJ, sBad, sLast;
+  __shared__ unsigned long long sWT[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k, R = 2 * k + 1;
+  const size_t row_bytes = (size_t)a.V * ES;
+
+  // Gather the logits of x_i (inputs only, so before the wait on pass 1).
+  float xp = 0.f, xq = 0.f;
+  bool bad = false;
+  if (tid < k) {
+    const int x = a.tokens[(size_t)b * k + tid];
+    bad = x < 0 || x >= a.V;
+    if (!bad) {
+      xp = load_logit<DT>(a.target + ((size_t)b * (k + 1) + tid) * row_bytes, x);
+      xq = load_logit<DT>(a.draft + ((size_t)b * k + tid) * row_bytes, x);
+    }
+  }
+  if (tid == 0) sBad = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1 has finished
+  // Merge the slice statistics of every row of the request, in a fixed
+  // order: warp w takes rows w, w+8, ...; it loads four rows' partials before
+  // using any, takes each row max with shuffles, then adds S_s * 2^(c(m_s -
+  // M)) with one exp per partial (no chain of exps).
+  for (int r0 = warp; r0 < R; r0 += 4 * kWarps) {
+    float2 v[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q * kWarps;
+      const float2* pr = a.ws.part + ((size_t)b * R + min(r, R - 1)) * a.nsplit;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int u = lane + 32 * h;
+        v[q][h] = (r < R && u < a.nsplit) ? __ldcg(pr + u) : make_float2(-INFINITY, 0.f);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q * kWarps;
+      if (r >= R) continue;  // the same for the whole warp
+      const float2* pr = a.ws.part + ((size_t)b * R + r) * a.nsplit;
+      float m = fmaxf(v[q][0].x, v[q][1].x);
+      for (int u = lane + 64; u < a.nsplit; u += 32) m = fmaxf(m, __ldcg(pr + u).x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      float sum = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (v[q][h].y > 0.f) sum += v[q][h].y * ex2(scaled(v[q][h].x - m, a.c_hi, a.c_lo));
+        for (int u = lane + 64; u < a.nsplit; u += 32) {
+          const float2 e = __ldcg(pr + u);
+          if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - m, a.c_hi, a.c_lo));
+        }
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) {
+        sM[r] = m;
+        sS[r] = sum;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < k) {
+    if (bad) {
+      sBad = 1;
+    } else {
+      sP[tid] = ex2(scaled(xp - sM[tid], a.c_hi, a.c_lo)) / sS[tid];
+      sQ[tid] = ex2(scaled(xq - sM[k + 1 + tid], a.c_hi, a.c_lo)) / sS[k + 1 + tid];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {  // accept scan: r_i < p_i(x_i) / q_i(x_i), q == 0 accepts
+    int j = k;
+    if (sBad) {
+      j = -1;
+    } else {
+      const float* r = a.uniforms + (size_t)b * (k + 1);
+      for (int i = 0; i < k; ++i) {
+        const float ratio = sQ[i] > 0.f ? sP[i] / sQ[i] : INFINITY;
+        if (!(r[i] < ratio)) {
+          j = i;
+          break;
+        }
+      }
+    }
+    sJ = j;
+  }
+  __syncthreads();
+  const int j = sJ;
+  const char* prow = nullptr;
+  const char* qrow = nullptr;
+  float mp = 0.f, mq = 0.f, lam = 0.f;
+  if (j >= 0) {
+    prow = a.target + ((size_t)b * (k + 1) + j) * row_bytes;
+    mp = sM[j];
+    if (j < k) {
+      qrow = a.draft + ((size_t)b * k + j) * row_bytes;
+      mq = sM[k + 1 + j];
+      lam = sS[j] / sS[k + 1 + j];
+    }
+    const int c0 = part * a.cpc, c1 = min(a.nchunks, c0 + a.cpc);
+    const unsigned long long wt =
+        chunk_sums<DT, VEC>(a, prow, qrow, c0, c1, mp, mq, lam, a.ws.chunks + (size_t)b * a.nchunks);
+    if (lane == 0) sWT[warp] = wt;
+    __syncthreads();
+    if (tid == 0) {  // the item's total (exact in fixed point) for the two-level search
+      unsigned long long t = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) t += sWT[w];
+      a.ws.items[(size_t)b * a.nsplit2 + part] = t;
+    }
+  }
+  if (lane == 0) __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(&a.ws.sync[b].tick2, 1);
+    sLast = t == a.nsplit2 - 1;
+    if (sLast) {
+      a.ws.sync[b].tick2 = 0;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!sLast) return;
+
+  // ---------------------------------------------------------- outputs
+  int32_t* out = a.out_tokens + (size_t)b * (k + 1);
+  if (j < 0) {  // a draft token was out of range: the request fails closed
+    for (int i = tid; i <= k; i += kThreads) out[i] = -1;
+    if (a.out_probs)
+      for (int i = tid; i < 2 * k; i += kThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
+    if (tid == 0) {
+      a.out_n[b] = -1;
+      set_status(a.ws.status, SPEC_EBADINDEX);
+    }
+    return;
+  }
+  if (a.out_probs && tid < k) {
+    a.out_probs[((size_t)b * k + tid) * 2] = sP[tid];
+    a.out_probs[((size_t)b * k + tid) * 2 + 1] = sQ[tid];
+  }
+  const double u = (double)a.uniforms[(size_t)b * (k + 1) + k];
+  const int tok = draw_token<DT, VEC>(a, b, prow, qrow, mp, mq, lam, u);
+  for (int i = tid; i <= k; i += kThreads)
+    out[i] = i < j ? a.tokens[(size_t)b * k + i] : (i == j ? tok : -1);
+  if (tid == 0) {
     a.out_n[b] = j;
     if (a.seq_lens) a.seq_lens[b] += j + 1;
   }
 }
 
+
+
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) chain_sample_kernel(const ChainArgs a) {
-  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
-  const int b = blockIdx.x / a.nsplit2;
-  const int sp = blockIdx.x - b * a.nsplit2;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  ReqInfo ri;
-  {
-    const int4 w0 = __ldcg(reinterpret_cast<const int4*>(a.ws.req + b));
-    const int4 w1 = __ldcg(reinterpret_cast<const int4*>(a.ws.req + b) + 1);
-    ri.j = w0.x;
-    ri.mp = __int_as_float(w0.z);
-    ri.sp = __int_as_float(w0.w);
-    ri.mq = __int_as_float(w1.x);
-    ri.sq = __int_as_float(w1.y);
+__global__ void __launch_bounds__(kThreads, 4) chain_draw_kernel(const ChainArgs a) {
+  const int items = a.B * a.nsplit2;
+  for (int h = blockIdx.x; h < items; h += gridDim.x) {
+    const int b = h / a.nsplit2;
+    draw_item<DT, VEC>(a, b, h - b * a.nsplit2);
+    __syncthreads();  // shared state of this item is no longer read
   }
-  const size_t row_bytes = (size_t)a.V * ES;
-  const int j = ri.j;
-  const char* prow = nullptr;
-  const char* qrow = nullptr;
-  float lam = 0.f;
-  if (j >= 0) {
-    prow = a.target + ((size_t)b * (a.k + 1) + j) * row_bytes;
-    if (j < a.k) {
-      qrow = a.draft + ((size_t)b * a.k + j) * row_bytes;
-      lam = ri.sp / ri.sq;
-    }
-    const int c0 = sp * a.cpc, c1 = min(a.nchunks, c0 + a.cpc);
-    for (int c = c0 + warp; c < c1; c += kWarps) {
-      float wv[8];
-      chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, ri.mp, ri.mq, lam, a.c_hi, a.c_lo, wv);
-      const float s = warp_sum(tree8(wv));
-      if (lane == 0) a.ws.chunks[(size_t)b * a.nchunks + c] = s;
-    }
-  }
-  if (!last_arrival(a.ws.tick2 + b, a.nsplit2)) return;
-  chain_finish<DT, VEC>(a, b, ri, prow, qrow, lam);
 }
 
-// ------------------------------------------------------------------ launch
+template <int DT, bool VEC>
+cudaError_t draw_grid(int* grid) {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_draw_kernel<DT, VEC>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    cached[dev] = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  *grid = cached[dev];
+  return cudaSuccess;
+}
+
 template <int DT, bool VEC>
 cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t st) {
   const long g1 = (long)a.B * (2 * a.k + 1) * a.nsplit;
-  chain_stats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
-  const long g2 = (long)a.B * a.nsplit2;
-  chain_sample_kernel<DT, VEC><<<(unsigned)g2, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  chain_rowstats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int slots = 0;
+  e = draw_grid<DT, VEC>(&slots);
+  if (e != cudaSuccess) return e;
+  const long items = (long)a.B * a.nsplit2;
+  // Pass 2 may be scheduled while pass 1 drains; it waits for pass 1's
+  // results with griddepcontrol.wait.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(items < slots ? items : slots));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chain_draw_kernel<DT, VEC>, a);
 }
+
+}  // namespace
 
 cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st) {
   if (dtype == SPEC_BF16)

@@ -25,52 +25,58 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerThread = 8;    // vectors a thread holds in registers
 constexpr int kUnitVecs = kThreads * kVecPerThread;
 constexpr int kChunk = 256;         // elements per inverse-CDF chunk (32 lanes x 8)
-constexpr int kChunksPerCta = 32;   // chunks one sampling CTA sums (4 per warp)
+constexpr int kChunksPerCta = 64;   // chunks of one draw item (8 per warp)
 
-struct ReqInfo {        // per-request result of the accept scan, read by the sampler
-  int j;                // first rejected position, k = all accepted, -1 = failed
-  int pad;
-  float mp, sp;         // max and sum-exp of target row j
-  float mq, sq;         // max and sum-exp of draft row j (residual only)
-  float pad2[2];
-};
-static_assert(sizeof(ReqInfo) == 32, "ReqInfo layout");
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 __host__ __device__ inline int ceil_div(long a, long b) { return (int)((a + b - 1) / b); }
 // Units per row for the worst case (one element per vector).
 __host__ __device__ inline int max_splits(int V) { return ceil_div(V, kUnitVecs); }
 __host__ __device__ inline int num_chunks(int V) { return ceil_div(V, kChunk); }
+static_assert(kChunksPerCta <= 64, "the draw search scans an item's chunks two per lane");
+__host__ __device__ inline int num_items(int V) { return ceil_div(num_chunks(V), kChunksPerCta); }
 
-// Byte offsets of the workspace regions for one call's sizes.
+// Per-request synchronisation words, 64 bytes apart so that the CTAs of
+// different requests rarely share a line.
+struct ReqSync {
+  int tick1;  // pass-1 units of the request that have finished
+  int tick2;  // pass-2 (draw) items of the request that have finished
+  int pad[14];
+};
+static_assert(sizeof(ReqSync) == 64, "ReqSync layout");
+
+// Byte offsets of the workspace regions for one call's sizes.  The status
+// word and the sync lines of SPEC_MAX_BATCH requests come first, at offsets
+// that do not depend on the call, so no call's scratch ever lands on them;
+// they must be zero when a call starts and the kernels return every line
+// they use to zero.
 struct WsLayout {
-  size_t status, tick1, tick2, part, req, chunks, total;
+  size_t status, sync, part, chunks, items, total;
   __host__ __device__ WsLayout(int B, int rows, int V) {
     size_t off = 0;
     status = off; off += 256;
-    tick1 = off; off += align256(sizeof(int) * (size_t)B);
-    tick2 = off; off += align256(sizeof(int) * (size_t)B);
+    sync = off; off += sizeof(ReqSync) * (size_t)SPEC_MAX_BATCH;
     part = off; off += align256(sizeof(float2) * (size_t)B * rows * max_splits(V));
-    req = off; off += align256(sizeof(ReqInfo) * (size_t)B);
-    chunks = off; off += align256(sizeof(float) * (size_t)B * num_chunks(V));
+    chunks = off; off += align256(sizeof(unsigned long long) * (size_t)B * num_chunks(V));
+    items = off; off += align256(sizeof(unsigned long long) * (size_t)B * num_items(V));
     total = off;
   }
 };
 
 struct Ws {  // typed views of one call's workspace
   int* status;
-  int* tick1;
-  int* tick2;
+  ReqSync* sync;
   float2* part;
-  ReqInfo* req;
-  float* chunks;
+  unsigned long long* chunks;  // draw-weight sum of each 256-token chunk, in 2^-32 units
+  unsigned long long* items;   // sum of each draw item's chunks, in 2^-32 units
 };
 
 inline Ws ws_views(void* base, const WsLayout& l) {
   char* p = static_cast<char*>(base);
-  return Ws{reinterpret_cast<int*>(p + l.status), reinterpret_cast<int*>(p + l.tick1),
-            reinterpret_cast<int*>(p + l.tick2), reinterpret_cast<float2*>(p + l.part),
-            reinterpret_cast<ReqInfo*>(p + l.req), reinterpret_cast<float*>(p + l.chunks)};
+  return Ws{reinterpret_cast<int*>(p + l.status), reinterpret_cast<ReqSync*>(p + l.sync),
+            reinterpret_cast<float2*>(p + l.part),
+            reinterpret_cast<unsigned long long*>(p + l.chunks),
+            reinterpret_cast<unsigned long long*>(p + l.items)};
 }
 
 // ---------------------------------------------------------------- loads
@@ -182,8 +188,131 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = M;
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// Blackwell executes add/mul/fma on fp32 pairs as one instruction.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mov.b64 c, {%6, %7};\n fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+// ---------------------------------------------------------------- mbarrier / bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+// Make barrier initialisation visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
+// 16) that reports its bytes to `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Upper bound of every device-side wait (about one second at 2 GHz).  A wait
+// that runs out sets SPEC_ETIMEOUT instead of spinning forever.
+constexpr long long kWaitCycles = 2000000000LL;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+__device__ __forceinline__ int ld_volatile(const int* p) {
+  return *reinterpret_cast<const volatile int*>(p);
+}
+// Device-scope atomic add with release semantics: this thread's earlier writes
+// (and those ordered before it by a CTA barrier) are visible before the add.
+__device__ __forceinline__ int atom_add_release(int* p, int v) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Barrier of the 256 compute threads (kThreads).  In a block of exactly
+// kThreads threads it is the same as __syncthreads(); in the persistent
+// kernel it leaves the producer warp out.
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 // Record the first data-dependent error of a call.
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Ticket for a CTA whose only global write to publish was made by thread 0:
+// thread 0 fences, counts itself in and learns whether it arrived last.
+__device__ __forceinline__ bool last_arrival_t0(int* counter, int expected) {
+  __shared__ int s_last0;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int t = atomicAdd(counter, 1);
+    s_last0 = (t == expected - 1);
+    if (s_last0) {
+      *counter = 0;
+      __threadfence();
+    }
+  }
+  csync();
+  return s_last0 != 0;
+}
 
 // Ticket of the threadfence-reduction pattern: returns true in exactly one CTA
 // of the `expected` CTAs that call it for the same counter (the last to
@@ -191,13 +320,13 @@ __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(st
 __device__ __forceinline__ bool last_arrival(int* counter, int expected) {
   __shared__ int s_last;
   __threadfence();  // this thread's global writes are visible device-wide
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
     const int t = atomicAdd(counter, 1);
     s_last = (t == expected - 1);
     if (s_last) *counter = 0;
   }
-  __syncthreads();
+  csync();
   if (s_last) __threadfence();  // order the epilogue's reads after the ticket
   return s_last != 0;
 }

@@ -13,7 +13,7 @@ struct ChainArgs {
   float c_hi, c_lo;  // log2(e)/T split as hi + lo
   int B, k, V;
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
-  int nchunks, cpc, nsplit2;   // sampler: chunks per row, per CTA, CTAs per request
+  int nchunks, cpc, nsplit2;   // draw: chunks per row, per item, items per request
   int32_t* out_tokens;
   int32_t* out_n;
   float* out_probs;
@@ -39,7 +39,8 @@ struct ArgmaxArgs {
   Ws ws;
 };
 
-// Enqueue the two chain passes / the argmax pass on `st`.
+// Enqueue the two chain passes (pass 2 as a programmatic dependent launch) /
+// the argmax pass on `st`.
 cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
 cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st);
 

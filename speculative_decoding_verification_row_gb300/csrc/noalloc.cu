@@ -43,14 +43,15 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
                                          int V, int32_t* out_tokens, int32_t* out_num_accepted,
                                          float* out_probs, int32_t* seq_lens,
                                          spec_stream_t stream) {
-  if (B < 1 || k < 1 || k > SPEC_MAX_DRAFT || V < 2) return SPEC_EINVAL;
+  if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2) return SPEC_EINVAL;
   const WsLayout layout(B, 2 * k + 1, V);
   if (layout.total > (size_t)SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_EWORKSPACE;
   void* scratch = nullptr;
   if (const int rc = scratch_address(&scratch)) return rc;
-  // Counters and the status word must start at zero; the rest is written
-  // before it is read within the call.
-  if (cudaMemsetAsync(scratch, 0, layout.part, (cudaStream_t)stream) != cudaSuccess)
+  // The status word and this call's sync lines must start at zero; the rest
+  // is written before it is read within the call.
+  if (cudaMemsetAsync(scratch, 0, layout.sync + sizeof(ReqSync) * (size_t)B,
+                      (cudaStream_t)stream) != cudaSuccess)
     return SPEC_ECUDA;
   return spec_verify_chain(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                            temperature, B, k, V, out_tokens, out_num_accepted, out_probs,
