@@ -45,6 +45,9 @@
  *     per row; NaN and +inf are outside the contract and are not checked.
  *   - One workspace serves one stream at a time: calls that overlap on the GPU
  *     must not share a workspace.
+ *   - Every call leaves its workspace ready for the next.  After a call that
+ *     returned SPEC_ECUDA, or whose status word reads SPEC_ETIMEOUT, zero the
+ *     workspace again with spec_workspace_init before reusing it.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -66,7 +69,7 @@ typedef enum {
     SPEC_EBADINDEX = -2,   /* a token or node id was out of range (device status) */
     SPEC_ECUDA = -3,       /* a CUDA launch or copy failed */
     SPEC_EWORKSPACE = -4,  /* workspace missing or smaller than spec_workspace_size() */
-    SPEC_ETIMEOUT = -5     /* reserved: a bounded device wait ran out */
+    SPEC_ETIMEOUT = -5     /* a bounded device wait ran out (device status) */
 } spec_status_t;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
@@ -189,7 +192,7 @@ int spec_verify_chain_noalloc(const void *target_logits, const void *draft_logit
                               int32_t *seq_lens, spec_stream_t stream);
 
 /* Synchronise `stream`, read the workspace status word into *status_out
- * (SPEC_OK or SPEC_EBADINDEX) and clear it.  Returns SPEC_OK, SPEC_EINVAL or
+ * (SPEC_OK, SPEC_EBADINDEX or SPEC_ETIMEOUT) and clear it.  Returns SPEC_OK, SPEC_EINVAL or
  * SPEC_ECUDA. */
 int spec_last_error(void *workspace, size_t workspace_bytes, spec_stream_t stream,
                     int *status_out);

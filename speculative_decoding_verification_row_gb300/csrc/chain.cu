@@ -7,21 +7,24 @@
 // target or draft row.  It reads its slice once with 128-bit loads and
 // reduces it to softmax statistics: each warp takes its own max, sums
 // 2^(c(x - max)) (c = log2(e)/T) with packed fp32x2 arithmetic and one exp
-// per logit, and thread 0 merges the eight warp pairs into the slice's (M, S).
-// Slices are ordered by descending draft position, so the rows the draw most
-// often needs (the first positions) are read last and are still in L2 when
-// pass 2 runs.  No CTA waits for another.
+// per logit, and thread 0 merges the eight warp pairs into the slice's (M, S)
+// and publishes it as one 64-bit word (no fence, no counter).  Slices are ordered by
+// descending draft position, so the rows the draw most often needs (the
+// first positions) are read last and are still in L2 when the draw reads
+// them again.  No pass-1 CTA waits for another.
 //
-// Pass 2, chain_draw_kernel: launched as a programmatic dependent of pass 1,
-// one wave of persistent CTAs taking draw items (64 chunks of 256 tokens of
-// one request) in grid-stride order.  For each item a CTA gathers x_i's
-// logits, merges the request's slice statistics and runs the accept scan
-// (tiny; every CTA of the request repeats it).  It then sums the draw weights
-// of its chunks: w_t = max(0, p_j(t) - q_j(t)) after a rejection at j,
-// w_t = p_k(t) when all k are accepted.  The request's last item (atomic
-// ticket, no waiting) prefix-sums the chunk sums exactly in 64-bit fixed
-// point, finds the chunk holding u*Z, re-reads only that chunk, scans it with
-// a warp prefix sum and writes the outputs.
+// Pass 2, chain_draw_kernel: launched as a programmatic dependent of pass 1
+// (scheduled once every pass-1 CTA has started), one wave of CTAs taking
+// draw items (64 chunks of 256 tokens of one request) in grid-stride order.
+// For each item a CTA gathers x_i's logits, merges its request's slice
+// statistics as their words arrive (requests finish one after another during
+// pass 1's last wave; no grid-wide wait) and runs the accept scan (tiny;
+// every CTA of the request repeats it).  It then sums the draw weights of its
+// chunks: w_t = max(0, p_j(t) - q_j(t)) after a rejection at j, w_t = p_k(t)
+// when all k are accepted, and publishes each chunk sum and the item total in
+// 64-bit fixed point.  The request's last item (atomic ticket, no waiting)
+// searches the item totals, then the chunk sums, re-reads only the chunk
+// holding u*Z, scans it with a warp prefix sum and writes the outputs.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -68,6 +71,34 @@ __device__ __forceinline__ float2 vec_expsum(const uint32_t (&w)[Io<DT, VEC>::NW
     Io<DT, false>::unpack(w, x);
     return make_float2(ex2(scaled(x[0] + nm.x, ch.x, cl.x)), 0.f);
   }
+}
+
+// Slice statistics (M, S) as one 64-bit word: M in the low half, S in the
+// high half.  A written word is never 0: a finite M comes with S >= 1 (the
+// slice maximum contributes 2^0), M = -inf and NaN have nonzero bits.  So 0
+// means "not yet written"; kNoStats stands for an absent slice (-inf, 0).
+constexpr unsigned long long kNoStats = 0xff800000ull;
+__device__ __forceinline__ unsigned long long stats_pack(float M, float S) {
+  return ((unsigned long long)__float_as_uint(S) << 32) | __float_as_uint(M);
+}
+__device__ __forceinline__ float2 stats_unpack(unsigned long long v) {
+  return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+// Poll a slice's word until pass 1 has written it.  Pass 1 was scheduled in
+// full before the draw grid, so the wait ends; the bound only turns a broken
+// invariant into an error instead of a hang.
+__device__ __noinline__ unsigned long long wait_stats(const unsigned long long* p, int* status) {
+  unsigned long long v = ld_relaxed_u64(p);
+  const long long t0 = clock64();
+  while (!v) {
+    if (clock64() - t0 > kWaitCycles) {
+      set_status(status, SPEC_ETIMEOUT);
+      return kNoStats;
+    }
+    __nanosleep(64);
+    v = ld_relaxed_u64(p);
+  }
+  return v;
 }
 
 // ------------------------------------------------------------------ pass 1
@@ -147,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 4) chain_rowstats_kernel(const Chain
       for (int i = 0; i < kWarps; ++i)
         if (s_ws[i] > 0.f) S += s_ws[i] * ex2(scaled(s_wm[i] - M, a.c_hi, a.c_lo));
     }
-    a.ws.part[((size_t)b * (2 * a.k + 1) + r) * a.nsplit + s] = make_float2(M, S);
+    // One 64-bit store publishes the pair; the draw polls for it (no fence).
+    st_relaxed_u64(a.ws.stats + ((size_t)b * (2 * a.k + 1) + r) * a.nsplit + s, stats_pack(M, S));
   }
 }
 
@@ -459,7 +491,7 @@ template <int DT, bool VEC>
 __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
   __shared__ float sM[2 * SPEC_MAX_DRAFT + 1], sS[2 * SPEC_MAX_DRAFT + 1];
-  __shared__ float sP[SPEC_MAX_DRAFT], sQ[SPEC_MAX_DRAFT];
+  __shared__ float sP[SPEC_MAX_DRAFT], sQ[SPEC_MAX_DRAFT], sU[SPEC_MAX_DRAFT + 1];
   __shared__ int sJ, sBad, sLast;
   __shared__ unsigned long long sWT[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -477,40 +509,48 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
       xq = load_logit<DT>(a.draft + ((size_t)b * k + tid) * row_bytes, x);
     }
   }
+  if (tid <= k) sU[tid] = a.uniforms[(size_t)b * (k + 1) + tid];
   if (tid == 0) sBad = 0;
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1 has finished
   // Merge the slice statistics of every row of the request, in a fixed
-  // order: warp w takes rows w, w+8, ...; it loads four rows' partials before
-  // using any, takes each row max with shuffles, then adds S_s * 2^(c(m_s -
-  // M)) with one exp per partial (no chain of exps).
+  // order, as they arrive: warp w takes rows w, w+8, ...; it issues the loads
+  // of four rows' words before using any (waiting only for words still 0),
+  // takes each row max with shuffles, then adds S_s * 2^(c(m_s - M)) with one
+  // exp per slice (no chain of exps).
+  const unsigned long long* sb = a.ws.stats + (size_t)b * R * a.nsplit;
   for (int r0 = warp; r0 < R; r0 += 4 * kWarps) {
-    float2 v[4][2];
+    unsigned long long v[4][2];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int r = r0 + q * kWarps;
-      const float2* pr = a.ws.part + ((size_t)b * R + min(r, R - 1)) * a.nsplit;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int u = lane + 32 * h;
-        v[q][h] = (r < R && u < a.nsplit) ? __ldcg(pr + u) : make_float2(-INFINITY, 0.f);
+        v[q][h] = (r < R && u < a.nsplit) ? ld_relaxed_u64(sb + (size_t)r * a.nsplit + u) : kNoStats;
       }
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (!v[q][h])  // only a present slice reads 0
+          v[q][h] = wait_stats(sb + (size_t)(r0 + q * kWarps) * a.nsplit + lane + 32 * h, a.ws.status);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int r = r0 + q * kWarps;
       if (r >= R) continue;  // the same for the whole warp
-      const float2* pr = a.ws.part + ((size_t)b * R + r) * a.nsplit;
-      float m = fmaxf(v[q][0].x, v[q][1].x);
-      for (int u = lane + 64; u < a.nsplit; u += 32) m = fmaxf(m, __ldcg(pr + u).x);
+      const unsigned long long* pr = sb + (size_t)r * a.nsplit;
+      const float2 e0 = stats_unpack(v[q][0]), e1 = stats_unpack(v[q][1]);
+      float m = fmaxf(e0.x, e1.x);
+      for (int u = lane + 64; u < a.nsplit; u += 32)
+        m = fmaxf(m, stats_unpack(wait_stats(pr + u, a.ws.status)).x);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       float sum = 0.f;
       if (m != -INFINITY) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (v[q][h].y > 0.f) sum += v[q][h].y * ex2(scaled(v[q][h].x - m, a.c_hi, a.c_lo));
+        if (e0.y > 0.f) sum += e0.y * ex2(scaled(e0.x - m, a.c_hi, a.c_lo));
+        if (e1.y > 0.f) sum += e1.y * ex2(scaled(e1.x - m, a.c_hi, a.c_lo));
         for (int u = lane + 64; u < a.nsplit; u += 32) {
-          const float2 e = __ldcg(pr + u);
+          const float2 e = stats_unpack(ld_relaxed_u64(pr + u));  // written: seen above
           if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - m, a.c_hi, a.c_lo));
         }
       }
@@ -531,21 +571,20 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
     }
   }
   __syncthreads();
-  if (tid == 0) {  // accept scan: r_i < p_i(x_i) / q_i(x_i), q == 0 accepts
-    int j = k;
-    if (sBad) {
-      j = -1;
-    } else {
-      const float* r = a.uniforms + (size_t)b * (k + 1);
-      for (int i = 0; i < k; ++i) {
+  if (warp == 0) {  // accept scan: r_i < p_i(x_i) / q_i(x_i), q == 0 accepts; j = first reject
+    unsigned rej[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      bool rj = false;
+      if (i < k) {
         const float ratio = sQ[i] > 0.f ? sP[i] / sQ[i] : INFINITY;
-        if (!(r[i] < ratio)) {
-          j = i;
-          break;
-        }
+        rj = !(sU[i] < ratio);
       }
+      rej[h] = __ballot_sync(0xffffffffu, rj);
     }
-    sJ = j;
+    if (lane == 0)
+      sJ = sBad ? -1 : rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : k;
   }
   __syncthreads();
   const int j = sJ;
@@ -586,6 +625,9 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   if (!sLast) return;
 
   // ---------------------------------------------------------- outputs
+  // Every item has merged: return the request's statistics words to 0.
+  for (int i = tid; i < R * a.nsplit; i += kThreads)
+    const_cast<unsigned long long*>(sb)[i] = 0;
   int32_t* out = a.out_tokens + (size_t)b * (k + 1);
   if (j < 0) {  // a draft token was out of range: the request fails closed
     for (int i = tid; i <= k; i += kThreads) out[i] = -1;
@@ -601,7 +643,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
     a.out_probs[((size_t)b * k + tid) * 2] = sP[tid];
     a.out_probs[((size_t)b * k + tid) * 2 + 1] = sQ[tid];
   }
-  const double u = (double)a.uniforms[(size_t)b * (k + 1) + k];
+  const double u = (double)sU[k];
   const int tok = draw_token<DT, VEC>(a, b, prow, qrow, mp, mq, lam, u);
   for (int i = tid; i <= k; i += kThreads)
     out[i] = i < j ? a.tokens[(size_t)b * k + i] : (i == j ? tok : -1);
@@ -621,6 +663,9 @@ __global__ void __launch_bounds__(kThreads, 4) chain_draw_kernel(const ChainArgs
     draw_item<DT, VEC>(a, b, h - b * a.nsplit2);
     __syncthreads();  // shared state of this item is no longer read
   }
+  // Completion of this grid then implies completion of pass 1, which stream
+  // order relies on (nothing above waits for the whole of pass 1).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int DT, bool VEC>
@@ -654,8 +699,8 @@ cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t st) {
   e = draw_grid<DT, VEC>(&slots);
   if (e != cudaSuccess) return e;
   const long items = (long)a.B * a.nsplit2;
-  // Pass 2 may be scheduled while pass 1 drains; it waits for pass 1's
-  // results with griddepcontrol.wait.
+  // Pass 2 may be scheduled once every pass-1 CTA has started; each draw
+  // item waits only for its own request's slices.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(items < slots ? items : slots));
   cfg.blockDim = dim3(kThreads);

@@ -39,23 +39,30 @@ __host__ __device__ inline int num_items(int V) { return ceil_div(num_chunks(V),
 // Per-request synchronisation words, 64 bytes apart so that the CTAs of
 // different requests rarely share a line.
 struct ReqSync {
-  int tick1;  // pass-1 units of the request that have finished
-  int tick2;  // pass-2 (draw) items of the request that have finished
+  int tick1;  // argmax: units of the request that have finished
+  int tick2;  // chain: draw items of the request that have finished
   int pad[14];
 };
 static_assert(sizeof(ReqSync) == 64, "ReqSync layout");
+
+__host__ __device__ inline size_t stats_bytes(int B, int rows, int V) {
+  return sizeof(unsigned long long) * (size_t)B * rows * max_splits(V);
+}
 
 // Byte offsets of the workspace regions for one call's sizes.  The status
 // word and the sync lines of SPEC_MAX_BATCH requests come first, at offsets
 // that do not depend on the call, so no call's scratch ever lands on them;
 // they must be zero when a call starts and the kernels return every line
-// they use to zero.
+// they use to zero.  The chain path's slice statistics follow; an entry is
+// zero until pass 1 writes it (a written entry never is: see stats_pack) and
+// the chain kernels return every entry they use to zero.
 struct WsLayout {
-  size_t status, sync, part, chunks, items, total;
+  size_t status, sync, stats, part, chunks, items, total;
   __host__ __device__ WsLayout(int B, int rows, int V) {
     size_t off = 0;
     status = off; off += 256;
     sync = off; off += sizeof(ReqSync) * (size_t)SPEC_MAX_BATCH;
+    stats = off; off += align256(stats_bytes(B, rows, V));
     part = off; off += align256(sizeof(float2) * (size_t)B * rows * max_splits(V));
     chunks = off; off += align256(sizeof(unsigned long long) * (size_t)B * num_chunks(V));
     items = off; off += align256(sizeof(unsigned long long) * (size_t)B * num_items(V));
@@ -66,6 +73,7 @@ struct WsLayout {
 struct Ws {  // typed views of one call's workspace
   int* status;
   ReqSync* sync;
+  unsigned long long* stats;   // chain: packed (M, S) of each row slice, 0 = not yet written
   float2* part;
   unsigned long long* chunks;  // draw-weight sum of each 256-token chunk, in 2^-32 units
   unsigned long long* items;   // sum of each draw item's chunks, in 2^-32 units
@@ -74,6 +82,7 @@ struct Ws {  // typed views of one call's workspace
 inline Ws ws_views(void* base, const WsLayout& l) {
   char* p = static_cast<char*>(base);
   return Ws{reinterpret_cast<int*>(p + l.status), reinterpret_cast<ReqSync*>(p + l.sync),
+            reinterpret_cast<unsigned long long*>(p + l.stats),
             reinterpret_cast<float2*>(p + l.part),
             reinterpret_cast<unsigned long long*>(p + l.chunks),
             reinterpret_cast<unsigned long long*>(p + l.items)};
@@ -282,6 +291,15 @@ __device__ __forceinline__ void red_add_release(int* p, int v) {
 }
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Device-scope relaxed 64-bit accesses (single-copy atomic, no fence).
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;

@@ -48,10 +48,13 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   if (layout.total > (size_t)SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_EWORKSPACE;
   void* scratch = nullptr;
   if (const int rc = scratch_address(&scratch)) return rc;
-  // The status word and this call's sync lines must start at zero; the rest
-  // is written before it is read within the call.
+  // The status word, this call's sync lines and its slice-statistics words
+  // must start at zero; the rest is written before it is read within the
+  // call.
   if (cudaMemsetAsync(scratch, 0, layout.sync + sizeof(ReqSync) * (size_t)B,
-                      (cudaStream_t)stream) != cudaSuccess)
+                      (cudaStream_t)stream) != cudaSuccess ||
+      cudaMemsetAsync(static_cast<char*>(scratch) + layout.stats, 0,
+                      stats_bytes(B, 2 * k + 1, V), (cudaStream_t)stream) != cudaSuccess)
     return SPEC_ECUDA;
   return spec_verify_chain(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                            temperature, B, k, V, out_tokens, out_num_accepted, out_probs,
