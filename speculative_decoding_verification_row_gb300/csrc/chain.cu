@@ -8,18 +8,17 @@
 // reduces it to softmax statistics: each warp takes its own max, sums
 // 2^(c(x - max)) (c = log2(e)/T) with packed fp32x2 arithmetic and one exp
 // per logit, and thread 0 merges the eight warp pairs into the slice's (M, S)
-// and publishes it as one 64-bit word (no fence, no counter).  Slices are ordered by
-// descending draft position, so the rows the draw most often needs (the
-// first positions) are read last and are still in L2 when the draw reads
-// them again.  No pass-1 CTA waits for another.
+// and publishes it as one 64-bit word (no fence, no counter).  Slices run in
+// request order, so requests complete one after another.  No pass-1 CTA
+// waits for another.
 //
 // Pass 2, chain_draw_kernel: launched as a programmatic dependent of pass 1
 // (scheduled once every pass-1 CTA has started), one wave of CTAs taking
 // draw items (64 chunks of 256 tokens of one request) in grid-stride order.
 // For each item a CTA gathers x_i's logits, merges its request's slice
-// statistics as their words arrive (requests finish one after another during
-// pass 1's last wave; no grid-wide wait) and runs the accept scan (tiny;
-// every CTA of the request repeats it).  It then sums the draw weights of its
+// statistics as their words arrive (no grid-wide wait: most requests are
+// complete when the grid starts, the rest finish during pass 1's last wave)
+// and runs the accept scan (tiny; every CTA of the request repeats it).  It then sums the draw weights of its
 // chunks: w_t = max(0, p_j(t) - q_j(t)) after a rejection at j, w_t = p_k(t)
 // when all k are accepted, and publishes each chunk sum and the item total in
 // 64-bit fixed point.  The request's last item (atomic ticket, no waiting)
@@ -102,21 +101,14 @@ __device__ __noinline__ unsigned long long wait_stats(const unsigned long long* 
 }
 
 // ------------------------------------------------------------------ pass 1
-// Row of slice-row index rr in pass-1 order: the B bonus rows first, then,
-// for p = k-1 down to 0, the target and draft rows of position p of every
-// request.  r < k+1 is target row r, r > k is draft row r-k-1.
+// Row of slice-row index rr in pass-1 order: request-major, so requests
+// finish one after another and most are complete when the draw grid is
+// scheduled (during pass 1's last wave).  r < k+1 is target row r, r > k is
+// draft row r-k-1.
 __device__ __forceinline__ void slice_row(const ChainArgs& a, int rr, int& b, int& r) {
-  if (rr < a.B) {
-    b = rr;
-    r = a.k;
-    return;
-  }
-  rr -= a.B;
-  const int q = rr / (2 * a.B);
-  const int rem = rr - q * 2 * a.B;
-  const int p = a.k - 1 - q;
-  b = rem >> 1;
-  r = (rem & 1) ? a.k + 1 + p : p;
+  const int R = 2 * a.k + 1;
+  b = rr / R;
+  r = rr - b * R;
 }
 
 template <int DT, bool VEC>
@@ -243,9 +235,15 @@ __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow
   }
 }
 
-// A non-negative weight sum (at most 256) as an integer number of 2^-32.
+// A non-negative weight sum (below 2^32) as an integer number of 2^-32,
+// rounded to nearest even, with 32-bit conversions only (64-bit ones run on
+// the FP64 pipe, which is narrow on this GPU).  x = h + f with h = trunc(x)
+// and f = x - h exact; f * 2^32 < 2^32 - 255 is exact too, so rounding it
+// rounds x * 2^32, and the tie parity is that of the low word.
 __device__ __forceinline__ unsigned long long to_fixed(float x) {
-  return __float2ull_rn(x * 4294967296.0f);
+  const unsigned h = __float2uint_rz(x);
+  const unsigned l = __float2uint_rn((x - (float)h) * 4294967296.0f);
+  return ((unsigned long long)h << 32) + l;
 }
 
 __device__ __forceinline__ float tree8(const float (&v)[8]) {
@@ -354,8 +352,15 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
       // Level 1: exact prefix over the item totals (lane l owns a run of items).
       const int per = (ni + 31) / 32;
       const int i_lo = min(ni, lane * per), i_hi = min(ni, i_lo + per);
+      constexpr int kHeld = 4;  // item totals a lane keeps in registers
+      unsigned long long held[kHeld];
       unsigned long long tot = 0;
-      for (int i = i_lo; i < i_hi; ++i) tot += __ldcg(items + i);
+#pragma unroll
+      for (int e = 0; e < kHeld; ++e) {
+        held[e] = i_lo + e < i_hi ? __ldcg(items + i_lo + e) : 0;
+        tot += held[e];
+      }
+      for (int i = i_lo + kHeld; i < i_hi; ++i) tot += __ldcg(items + i);
       unsigned long long incl = tot;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -376,7 +381,11 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
           int chosen = i_lo;
           unsigned long long chosen_pre = pre;
           for (int i = i_lo; i < i_hi; ++i) {
-            const unsigned long long v = __ldcg(items + i);
+            unsigned long long v = 0;
+#pragma unroll
+            for (int e = 0; e < kHeld; ++e)
+              if (i == i_lo + e) v = held[e];
+            if (i >= i_lo + kHeld) v = __ldcg(items + i);
             if (v > 0) {
               chosen = i;  // keeps the last positive item if none is hit
               chosen_pre = pre;
