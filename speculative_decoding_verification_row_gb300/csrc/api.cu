@@ -94,7 +94,9 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
   a.nsplit2 = num_items(V);
-  if ((long)B * (R * (long)a.nsplit + a.nsplit2) > INT_MAX) return SPEC_EINVAL;
+  // The chain kernel's work queue counts units in 32 bits (plus one ticket
+  // per CTA past the end).
+  if ((long)B * (R * (long)a.nsplit + a.nsplit2) > INT_MAX / 2) return SPEC_EINVAL;
   a.target = static_cast<const char*>(target_logits);
   a.draft = static_cast<const char*>(draft_logits);
   a.tokens = draft_tokens;

@@ -64,6 +64,9 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
     if (lane == 0) sArg[r] = i;
   }
   __syncthreads();
+  // Every call leaves the workspace zero: clear this request's partials.
+  float2* pz = a.ws.part + (size_t)b * a.R * a.nsplit;
+  for (int i = threadIdx.x; i < a.R * a.nsplit; i += kThreads) pz[i] = make_float2(0.f, 0.f);
 
   if (!a.tree) {  // ---------------------------------------------- greedy chain
     const int k = a.k;

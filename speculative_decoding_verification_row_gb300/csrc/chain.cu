@@ -493,6 +493,9 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
     if (lane == 0) sTok = tok;
   }
   __syncthreads();
+  // Every call leaves the workspace zero: clear this request's sums.
+  for (int i = tid; i < n; i += kThreads) chunks[i] = 0;
+  for (int i = tid; i < ni; i += kThreads) items[i] = 0;
   return sTok;
 }
 

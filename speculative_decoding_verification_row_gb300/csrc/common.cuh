@@ -51,11 +51,13 @@ __host__ __device__ inline size_t stats_bytes(int B, int rows, int V) {
 
 // Byte offsets of the workspace regions for one call's sizes.  The status
 // word and the sync lines of SPEC_MAX_BATCH requests come first, at offsets
-// that do not depend on the call, so no call's scratch ever lands on them;
-// they must be zero when a call starts and the kernels return every line
-// they use to zero.  The chain path's slice statistics follow; an entry is
-// zero until pass 1 writes it (a written entry never is: see stats_pack) and
-// the chain kernels return every entry they use to zero.
+// that do not depend on the call.  The regions after them move with the
+// call's sizes, so one call's scratch may sit where another call's slice
+// statistics sit; hence every call returns everything it writes (sync lines,
+// statistics, partials, sums) to zero before it ends, and the whole
+// workspace but the status word is zero between calls.  The chain path's
+// statistics words rely on it: an entry is zero until its slice writes it
+// (a written entry never is: see stats_pack).
 struct WsLayout {
   size_t status, sync, stats, part, chunks, items, total;
   __host__ __device__ WsLayout(int B, int rows, int V) {
@@ -71,7 +73,9 @@ struct WsLayout {
 };
 
 struct Ws {  // typed views of one call's workspace
-  int* status;
+  int* status;                 // first word of the 256-byte status block
+  unsigned* ticket;            // chain: next unit of the work queue (status block + 64)
+  unsigned* exits;             // chain: CTAs that have left the queue (status block + 128)
   ReqSync* sync;
   unsigned long long* stats;   // chain: packed (M, S) of each row slice, 0 = not yet written
   float2* part;
@@ -81,7 +85,9 @@ struct Ws {  // typed views of one call's workspace
 
 inline Ws ws_views(void* base, const WsLayout& l) {
   char* p = static_cast<char*>(base);
-  return Ws{reinterpret_cast<int*>(p + l.status), reinterpret_cast<ReqSync*>(p + l.sync),
+  return Ws{reinterpret_cast<int*>(p + l.status),
+            reinterpret_cast<unsigned*>(p + l.status + 64),
+            reinterpret_cast<unsigned*>(p + l.status + 128), reinterpret_cast<ReqSync*>(p + l.sync),
             reinterpret_cast<unsigned long long*>(p + l.stats),
             reinterpret_cast<float2*>(p + l.part),
             reinterpret_cast<unsigned long long*>(p + l.chunks),

@@ -97,12 +97,12 @@ def check_chain(w, g, o, label):
     return flagged, mism
 
 
-def run_greedy(w, misalign=False):
+def run_greedy(w, misalign=False, workspace=None):
     t = to_dev(w["target"], w["dtype"])
     if misalign:
         t = _offset_copy(t)
     seq = i32(w["seq_lens"])
-    tok, n = sv.verify_greedy(t, i32(w["draft_tokens"]), seq_lens=seq)
+    tok, n = sv.verify_greedy(t, i32(w["draft_tokens"]), seq_lens=seq, workspace=workspace)
     torch.cuda.synchronize()
     return dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(), seq_lens=seq.cpu().numpy())
 
@@ -115,12 +115,13 @@ def check_greedy(w, g, o, label):
     REPORT.append(dict(case=label, kind="greedy", requests=w["B"], flagged=0, mismatched=0))
 
 
-def run_tree(w, misalign=False):
+def run_tree(w, misalign=False, workspace=None):
     t = to_dev(w["target"], w["dtype"])
     if misalign:
         t = _offset_copy(t)
     seq = i32(w["seq_lens"])
-    tok, n, best, nodes = sv.verify_tree(t, i32(w["tree_tokens"]), i32(w["paths"]), seq_lens=seq)
+    tok, n, best, nodes = sv.verify_tree(t, i32(w["tree_tokens"]), i32(w["paths"]), seq_lens=seq,
+                                         workspace=workspace)
     torch.cuda.synchronize()
     return dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(), best_path=best.cpu().numpy(),
                 accepted_nodes=nodes.cpu().numpy(), seq_lens=seq.cpu().numpy())
@@ -288,6 +289,23 @@ def test_repeat_calls_are_deterministic_and_workspace_reusable():
     w2 = workloads.make("chain_b1_k4_v1024_f32", seed=9, B=2, V=777)
     check_chain(w2, run_chain(w2, workspace=ws), oracle.verify(w2), "reuse smaller")
     check_chain(w, run_chain(w, workspace=ws), oracle.verify(w), "reuse again")
+
+
+def test_workspace_shared_across_paths_and_sizes():
+    # Scratch regions move with each call's sizes, so one call's partials or
+    # sums can sit where the next call's chain statistics words live; every
+    # call must leave the workspace zero for the next one to be correct.
+    ws = sv.Workspace()
+    wc = workloads.make("chain_b64_k7_v128256_bf16", seed=11, B=5, V=20000)
+    wg = workloads.make("chain_b8_k4_v32000_f32", seed=11, B=7, V=9000)
+    wt = workloads.make("tree_b16_n60_l4_v151936_bf16", seed=11, B=3, V=7000)
+    ws_small = workloads.make("chain_b1_k4_v1024_f32", seed=11, B=3, V=1500)
+    for step in range(2):
+        check_greedy(wg, run_greedy(wg, workspace=ws), oracle.verify(wg, greedy=True), f"shared greedy {step}")
+        check_chain(wc, run_chain(wc, workspace=ws), oracle.verify(wc), f"shared chain {step}")
+        check_tree(wt, run_tree(wt, workspace=ws), oracle.verify(wt), f"shared tree {step}")
+        check_chain(ws_small, run_chain(ws_small, workspace=ws), oracle.verify(ws_small), f"shared small {step}")
+        check_chain(wc, run_chain(wc, workspace=ws), oracle.verify(wc), f"shared chain again {step}")
 
 
 # ------------------------------------------------------------------ full sizes
