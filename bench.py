@@ -339,7 +339,7 @@ def run_ours(args, rank, world, local):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
-            "kernel": {"chain": "spec_verify_chain call (chain_stats_kernel + chain_sample_kernel)",
+            "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
                        "greedy": "spec_verify_greedy call (argmax_kernel)",
                        "tree": "spec_verify_tree call (argmax_kernel)"}[kernel_key],
             "algorithmic_bytes_per_call": algo_bytes,

@@ -22,8 +22,9 @@
 // chunks: w_t = max(0, p_j(t) - q_j(t)) after a rejection at j, w_t = p_k(t)
 // when all k are accepted, and publishes each chunk sum and the item total in
 // 64-bit fixed point.  The request's last item (atomic ticket, no waiting)
-// searches the item totals, then the chunk sums, re-reads only the chunk
-// holding u*Z, scans it with a warp prefix sum and writes the outputs.
+// loads every chunk sum at once, finds the chunk holding u*Z with a
+// block-wide exact prefix sum, re-reads only that chunk, scans it with a
+// warp prefix sum and writes the outputs.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -112,7 +113,7 @@ __device__ __forceinline__ void slice_row(const ChainArgs& a, int rr, int& b, in
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4) chain_rowstats_kernel(const ChainArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) chain_rowstats_kernel(const ChainArgs a) {
   asm volatile("griddepcontrol.launch_dependents;");
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x;
@@ -246,6 +247,17 @@ __device__ __forceinline__ unsigned long long to_fixed(float x) {
   return ((unsigned long long)h << 32) + l;
 }
 
+// Warp-wide inclusive prefix sum of 64-bit values.
+__device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
 __device__ __forceinline__ float tree8(const float (&v)[8]) {
   return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
 }
@@ -329,110 +341,82 @@ __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, con
   return wtot;
 }
 
-// The request's last CTA: locate u*Z among the chunk sums, scan that chunk,
-// return the token (all threads call it; the result is valid in every thread).
+// The request's last CTA: locate u*Z among the chunk sums (one round trip for
+// all of them), re-read and scan that chunk, return the token (all threads
+// call it; the result is valid in every thread).
 template <int DT, bool VEC>
 __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const char* qrow,
                           float mp, float mq, float lam, double u) {
-  __shared__ unsigned long long sTarget, sPre;
-  __shared__ int sChunk, sTok, sRetry;
+  __shared__ unsigned long long sTarget, sPre, sZ;
+  __shared__ unsigned long long sWarpTot[kWarps];
+  __shared__ int sChunk, sTok, sRetry, sLastPos;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = a.nchunks, ni = a.nsplit2;
   unsigned long long* chunks = a.ws.chunks + (size_t)b * n;
   unsigned long long* items = a.ws.items + (size_t)b * ni;
-  if (tid == 0) {
-    sChunk = 0;
-    sPre = 0;
-    sTarget = 0;
-    sRetry = 0;
-  }
   for (int attempt = 0; attempt < 2; ++attempt) {
-    __syncthreads();
+    // One round trip: every thread loads two chunk sums while warp 0 adds
+    // the item totals into the exact total Z.
+    unsigned long long v0 = 2 * tid < n ? __ldcg(chunks + 2 * tid) : 0;
+    unsigned long long v1 = 2 * tid + 1 < n ? __ldcg(chunks + 2 * tid + 1) : 0;
     if (warp == 0) {
-      // Level 1: exact prefix over the item totals (lane l owns a run of items).
-      const int per = (ni + 31) / 32;
-      const int i_lo = min(ni, lane * per), i_hi = min(ni, i_lo + per);
-      constexpr int kHeld = 4;  // item totals a lane keeps in registers
-      unsigned long long held[kHeld];
-      unsigned long long tot = 0;
+      unsigned long long t = 0;
+      for (int i = lane; i < ni; i += 32) t += __ldcg(items + i);
 #pragma unroll
-      for (int e = 0; e < kHeld; ++e) {
-        held[e] = i_lo + e < i_hi ? __ldcg(items + i_lo + e) : 0;
-        tot += held[e];
-      }
-      for (int i = i_lo + kHeld; i < i_hi; ++i) tot += __ldcg(items + i);
-      unsigned long long incl = tot;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      const unsigned long long Z = __shfl_sync(0xffffffffu, incl, 31);
-      if (lane == 0) sRetry = Z == 0;
-      if (Z > 0) {
-        const unsigned long long target = (unsigned long long)(u * (double)Z);
-        const unsigned hit = __ballot_sync(0xffffffffu, incl > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, tot > 0);
-        const int L = hit ? __ffs(hit) - 1 : 31 - __clz(pos);  // u*Z >= Z only if u >= 1
-        unsigned long long pre = 0;
-        int item = 0;
-        if (lane == L) {
-          pre = incl - tot;
-          int chosen = i_lo;
-          unsigned long long chosen_pre = pre;
-          for (int i = i_lo; i < i_hi; ++i) {
-            unsigned long long v = 0;
-#pragma unroll
-            for (int e = 0; e < kHeld; ++e)
-              if (i == i_lo + e) v = held[e];
-            if (i >= i_lo + kHeld) v = __ldcg(items + i);
-            if (v > 0) {
-              chosen = i;  // keeps the last positive item if none is hit
-              chosen_pre = pre;
-            }
-            if (pre + v > target && v > 0) break;
-            pre += v;
-          }
-          item = chosen;
-          pre = chosen_pre;
-        }
-        item = __shfl_sync(0xffffffffu, item, L);
-        pre = __shfl_sync(0xffffffffu, pre, L);
-        // Level 2: the item's chunks, two per lane (an item has at most 64).
-        const int c_base = item * a.cpc, c_cnt = min(n - c_base, a.cpc);
-        unsigned long long v0 = 2 * lane < c_cnt ? __ldcg(chunks + c_base + 2 * lane) : 0;
-        unsigned long long v1 = 2 * lane + 1 < c_cnt ? __ldcg(chunks + c_base + 2 * lane + 1) : 0;
-        unsigned long long cin = v0 + v1;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const unsigned long long o = __shfl_up_sync(0xffffffffu, cin, off);
-          if (lane >= off) cin += o;
-        }
-        const unsigned long long base = pre + cin - (v0 + v1);  // before this lane's first chunk
-        int hit_c = -1;
-        if (v0 > 0 && base + v0 > target) hit_c = 0;
-        else if (v1 > 0 && base + v0 + v1 > target) hit_c = 1;
-        const unsigned hc = __ballot_sync(0xffffffffu, hit_c >= 0);
-        const unsigned pc = __ballot_sync(0xffffffffu, v0 + v1 > 0);
-        int Lc, off_c;
-        unsigned long long cpre;
-        if (hc) {
-          Lc = __ffs(hc) - 1;
-          off_c = __shfl_sync(0xffffffffu, hit_c, Lc);
-        } else {  // rounding left u*Z past the item: its last positive chunk
-          Lc = pc ? 31 - __clz(pc) : 0;
-          off_c = __shfl_sync(0xffffffffu, v1 > 0 ? 1 : 0, Lc);
-        }
-        cpre = __shfl_sync(0xffffffffu, base, Lc) + (off_c ? __shfl_sync(0xffffffffu, v0, Lc) : 0);
-        if (lane == 0) {
-          sChunk = c_base + 2 * Lc + off_c;
-          sPre = cpre;
-          sTarget = target;
-        }
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (lane == 0) {
+        sZ = t;
+        sRetry = t == 0;
+        sTarget = t ? (unsigned long long)(u * (double)t) : 0;  // < Z: u < 1
+        sChunk = -1;
+        sLastPos = -1;
       }
     }
     __syncthreads();
-    if (!sRetry) break;
+    if (!sRetry) {
+      // The chunk holding the target: block-wide exact prefix sums, 2 * kThreads
+      // chunks at a time; exactly one thread sees the running sum cross it.
+      const unsigned long long target = sTarget;
+      unsigned long long carry = 0;
+      for (int base = 0; base < n; base += 2 * kThreads) {
+        const int i0 = base + 2 * tid;
+        if (base > 0) {
+          v0 = i0 < n ? __ldcg(chunks + i0) : 0;
+          v1 = i0 + 1 < n ? __ldcg(chunks + i0 + 1) : 0;
+        }
+        const unsigned long long mine = v0 + v1;
+        const unsigned long long incl = warp_incl_u64(mine);
+        if (lane == 31) sWarpTot[warp] = incl;
+        __syncthreads();
+        unsigned long long wbase = 0, seg = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const unsigned long long t = sWarpTot[w];
+          wbase += w < warp ? t : 0;
+          seg += t;
+        }
+        const unsigned long long lb = carry + wbase + incl - mine;  // before chunk i0
+        if (v0 > 0 && lb <= target && lb + v0 > target) {
+          sChunk = i0;
+          sPre = lb;
+        } else if (v1 > 0 && lb + v0 <= target && lb + mine > target) {
+          sChunk = i0 + 1;
+          sPre = lb + v0;
+        }
+        if (mine > 0) atomicMax(&sLastPos, v1 > 0 ? i0 + 1 : i0);
+        __syncthreads();
+        if (sChunk >= 0) break;
+        carry += seg;
+        __syncthreads();  // sWarpTot is rewritten next
+      }
+      if (sChunk < 0 && tid == 0) {  // not reached while u < 1: the last positive chunk
+        const int c = sLastPos < 0 ? 0 : sLastPos;
+        sChunk = c;
+        sPre = sZ - __ldcg(chunks + c);
+      }
+      __syncthreads();
+      break;
+    }
     // The residual vanished numerically: draw from p_j instead (this CTA
     // recomputes every chunk and item sum; a rare path).
     qrow = nullptr;
@@ -453,7 +437,13 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
       }
       __threadfence();
     }
+    __syncthreads();
   }
+  if (tid == 0 && sChunk < 0) {  // Z stayed 0 after the retry (not reached): chunk 0
+    sChunk = 0;
+    sPre = 0;
+  }
+  __syncthreads();
   if (warp == 0) {
     const int c = sChunk;
     float wv[8];
