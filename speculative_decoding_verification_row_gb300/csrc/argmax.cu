@@ -3,14 +3,27 @@
 // tree (TensorRT-LLM deployment page, "Eagle-2" section: paths
 // [batch, max_decoding_tokens, max_path_len]).
 //
-// One CTA per (request, row, unit) streams its slice of a target row once and
-// keeps the first position of its largest stored value (compared exactly as
-// fp32, lowest index on ties).  The request's last CTA merges the units of all
-// rows, then either scans the chain (greedy) or walks every path of the tree,
-// one path per thread, and keeps the longest accepted path.
+// Pass 1, argmax_kernel: one CTA per (request, row, unit) streams its slice
+// of a target row once and keeps the first position of its largest stored
+// value (compared exactly as fp32, lowest index on ties); it publishes the
+// pair as one 64-bit word, never 0 (no fence, no counter).  Pass 2,
+// argmax_finish_kernel, a programmatic dependent: one CTA per request waits
+// for its words, merges the units of all rows, then either scans the chain
+// (greedy) or walks every path of the tree, one path per thread, and keeps
+// the longest accepted path.
 #include "kernels.cuh"
 
 namespace sv {
+
+// A unit's (value, index) as one word: value bits low, index + 1 high, so a
+// written word is never 0 and 0 means "not yet written".
+__device__ __forceinline__ unsigned long long arg_pack(float v, int i) {
+  return ((unsigned long long)(unsigned)(i + 1) << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ void arg_unpack(unsigned long long w, float& v, int& i) {
+  v = __uint_as_float((uint32_t)w);
+  i = (int)(uint32_t)(w >> 32) - 1;
+}
 
 // (value, index) order: larger value first, then lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -49,24 +62,42 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
   __shared__ int sAcc[kWarps], sPath[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) sBad = 0;
+  unsigned long long* words = reinterpret_cast<unsigned long long*>(a.ws.part) +
+                              (size_t)b * a.R * a.nsplit;
+  // Wait for every unit of the request.  Pass 1 was scheduled in full before
+  // this grid, so each wait ends; the bound turns a broken invariant into an
+  // error instead of a hang.
+  for (int i = threadIdx.x; i < a.R * a.nsplit; i += kThreads) {
+    if (ld_relaxed_u64(words + i)) continue;
+    const long long t0 = clock64();
+    while (!ld_relaxed_u64(words + i)) {
+      if (clock64() - t0 > kWaitCycles) {
+        set_status(a.ws.status, SPEC_ETIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncthreads();
   for (int r = warp; r < a.R; r += kWarps) {
     float v = -INFINITY;
     int i = INT_MAX;
-    const float2* pr = a.ws.part + ((size_t)b * a.R + r) * a.nsplit;
+    const unsigned long long* pr = words + (size_t)r * a.nsplit;
     for (int u = lane; u < a.nsplit; u += 32) {
-      const float2 p = __ldcg(pr + u);
-      if (better(p.x, __float_as_int(p.y), v, i)) {
-        v = p.x;
-        i = __float_as_int(p.y);
+      float pv;
+      int pi;
+      arg_unpack(ld_relaxed_u64(pr + u), pv, pi);
+      if (better(pv, pi, v, i)) {
+        v = pv;
+        i = pi;
       }
     }
     warp_argmax(v, i);
     if (lane == 0) sArg[r] = i;
   }
   __syncthreads();
-  // Every call leaves the workspace zero: clear this request's partials.
-  float2* pz = a.ws.part + (size_t)b * a.R * a.nsplit;
-  for (int i = threadIdx.x; i < a.R * a.nsplit; i += kThreads) pz[i] = make_float2(0.f, 0.f);
+  // Every call leaves the workspace zero: clear this request's words.
+  for (int i = threadIdx.x; i < a.R * a.nsplit; i += kThreads) words[i] = 0;
 
   if (!a.tree) {  // ---------------------------------------------- greedy chain
     const int k = a.k;
@@ -157,7 +188,8 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4) argmax_kernel(const ArgmaxArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) argmax_kernel(const ArgmaxArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;");
   using IO = Io<DT, VEC>;
   const int per_req = a.R * a.nsplit;
   const int b = blockIdx.x / per_req;
@@ -221,17 +253,41 @@ __global__ void __launch_bounds__(kThreads, 4) argmax_kernel(const ArgmaxArgs a)
     best = lane < kWarps ? sv_[lane] : -INFINITY;
     idx = lane < kWarps ? si_[lane] : INT_MAX;
     warp_argmax(best, idx);
-    if (lane == 0) a.ws.part[blockIdx.x] = make_float2(best, __int_as_float(idx));
+    if (lane == 0)
+      st_relaxed_u64(reinterpret_cast<unsigned long long*>(a.ws.part) + blockIdx.x,
+                     arg_pack(best, idx));
   }
-  if (!last_arrival(&a.ws.sync[b].tick1, per_req)) return;
-  argmax_epilogue(a, b);
+}
+
+// One CTA per request (grid-stride).
+__global__ void __launch_bounds__(kThreads) argmax_finish_kernel(const ArgmaxArgs a) {
+  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+    argmax_epilogue(a, b);
+    __syncthreads();  // shared state of this request is no longer read
+  }
+  // Completion of this grid then implies completion of pass 1, which stream
+  // order relies on (nothing above waits for the whole of pass 1).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int DT, bool VEC>
 cudaError_t launch_argmax_t(const ArgmaxArgs& a, cudaStream_t st) {
   const long g = (long)a.B * a.R * a.nsplit;
   argmax_kernel<DT, VEC><<<(unsigned)g, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // Pass 2 may be scheduled once every pass-1 CTA has started.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B < 1024 ? a.B : 1024));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, argmax_finish_kernel, a);
 }
 
 cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st) {
