@@ -56,54 +56,81 @@ __device__ void argmax_fail(const ArgmaxArgs& a, int b) {
   }
 }
 
+// Order-preserving key of a (value, index) pair: larger value, then lower
+// index, compares larger as an unsigned integer.  -0 is taken as +0, as the
+// float comparison does.
+__device__ __forceinline__ unsigned long long arg_key(float v, int i) {
+  uint32_t bits = v == 0.f ? 0u : __float_as_uint(v);
+  bits = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+  return ((unsigned long long)bits << 32) | (uint32_t)~(uint32_t)i;
+}
+__device__ __forceinline__ int key_index(unsigned long long key) { return (int)~(uint32_t)key; }
+
+// Largest tree a finish CTA stages in shared memory (paths of larger trees
+// are read from global memory).
+constexpr int kPathStage = 4096;
+
 __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
-  __shared__ int sArg[SPEC_MAX_TREE_NODES];
+  __shared__ unsigned long long sKey[SPEC_MAX_TREE_NODES];  // per row: best (value, index)
+  __shared__ int sTok[SPEC_MAX_TREE_NODES];                 // tree tokens / draft tokens
+  __shared__ int sPaths[kPathStage];
   __shared__ int sBad;
   __shared__ int sAcc[kWarps], sPath[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int R = a.R, ns = a.nsplit;
+  // Inputs first (they do not depend on pass 1).
+  const int nt = a.tree ? R : a.k;
+  const int32_t* tsrc = a.tree ? a.tree_tokens + (size_t)b * R : a.draft_tokens + (size_t)b * a.k;
+  const int32_t* pb = a.tree ? a.paths + (size_t)b * a.P * a.L : nullptr;
+  const bool staged = a.tree && a.P * a.L <= kPathStage;
+  for (int i = threadIdx.x; i < nt; i += kThreads) sTok[i] = tsrc[i];
+  if (staged)
+    for (int i = threadIdx.x; i < a.P * a.L; i += kThreads) sPaths[i] = pb[i];
+  for (int i = threadIdx.x; i < R; i += kThreads) sKey[i] = 0;
   if (threadIdx.x == 0) sBad = 0;
-  unsigned long long* words = reinterpret_cast<unsigned long long*>(a.ws.part) +
-                              (size_t)b * a.R * a.nsplit;
-  // Wait for every unit of the request.  Pass 1 was scheduled in full before
-  // this grid, so each wait ends; the bound turns a broken invariant into an
-  // error instead of a hang.
-  for (int i = threadIdx.x; i < a.R * a.nsplit; i += kThreads) {
-    if (ld_relaxed_u64(words + i)) continue;
-    const long long t0 = clock64();
-    while (!ld_relaxed_u64(words + i)) {
-      if (clock64() - t0 > kWaitCycles) {
-        set_status(a.ws.status, SPEC_ETIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-  }
   __syncthreads();
-  for (int r = warp; r < a.R; r += kWarps) {
-    float v = -INFINITY;
-    int i = INT_MAX;
-    const unsigned long long* pr = words + (size_t)r * a.nsplit;
-    for (int u = lane; u < a.nsplit; u += 32) {
-      float pv;
-      int pi;
-      arg_unpack(ld_relaxed_u64(pr + u), pv, pi);
-      if (better(pv, pi, v, i)) {
-        v = pv;
-        i = pi;
-      }
+  // Every unit word of the request, four loads in flight per thread, folded
+  // into its row's key.  Pass 1 was scheduled in full before this grid, so
+  // each wait ends; the bound turns a broken invariant into an error instead
+  // of a hang.
+  unsigned long long* words = reinterpret_cast<unsigned long long*>(a.ws.part) +
+                              (size_t)b * R * ns;
+  for (int i0 = threadIdx.x; i0 < R * ns; i0 += 4 * kThreads) {
+    unsigned long long w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * kThreads;
+      w[q] = i < R * ns ? ld_relaxed_u64(words + i) : 0;
     }
-    warp_argmax(v, i);
-    if (lane == 0) sArg[r] = i;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * kThreads;
+      if (i >= R * ns) continue;
+      if (!w[q]) {
+        const long long t0 = clock64();
+        while (!(w[q] = ld_relaxed_u64(words + i))) {
+          if (clock64() - t0 > kWaitCycles) {
+            set_status(a.ws.status, SPEC_ETIMEOUT);
+            w[q] = arg_pack(-INFINITY, 0);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      float v;
+      int x;
+      arg_unpack(w[q], v, x);
+      atomicMax(&sKey[i / ns], arg_key(v, x));
+    }
   }
   __syncthreads();
   // Every call leaves the workspace zero: clear this request's words.
-  for (int i = threadIdx.x; i < a.R * a.nsplit; i += kThreads) words[i] = 0;
+  for (int i = threadIdx.x; i < R * ns; i += kThreads) words[i] = 0;
 
   if (!a.tree) {  // ---------------------------------------------- greedy chain
     const int k = a.k;
-    const int32_t* d = a.draft_tokens + (size_t)b * k;
     for (int i = threadIdx.x; i < k; i += kThreads)
-      if (d[i] < 0 || d[i] >= a.V) sBad = 1;
+      if (sTok[i] < 0 || sTok[i] >= a.V) sBad = 1;
     __syncthreads();
     if (sBad) {
       argmax_fail(a, b);
@@ -111,9 +138,9 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
     }
     if (threadIdx.x == 0) {
       int j = 0;
-      while (j < k && sArg[j] == d[j]) ++j;
+      while (j < k && key_index(sKey[j]) == sTok[j]) ++j;
       int32_t* out = a.out_tokens + (size_t)b * (k + 1);
-      for (int i = 0; i <= k; ++i) out[i] = i < j ? d[i] : (i == j ? sArg[j] : -1);
+      for (int i = 0; i <= k; ++i) out[i] = i < j ? sTok[i] : (i == j ? key_index(sKey[j]) : -1);
       a.out_n[b] = j;
       if (a.seq_lens) a.seq_lens[b] += j + 1;
     }
@@ -121,13 +148,12 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
   }
 
   // --------------------------------------------------------------- tree
-  const int N = a.R, P = a.P, L = a.L;
-  const int32_t* tok = a.tree_tokens + (size_t)b * N;
-  const int32_t* pb = a.paths + (size_t)b * P * L;
+  const int N = R, P = a.P, L = a.L;
+  const int32_t* paths = staged ? sPaths : pb;
   for (int n = threadIdx.x; n < N; n += kThreads)
-    if (tok[n] < 0 || tok[n] >= a.V) sBad = 1;
+    if (sTok[n] < 0 || sTok[n] >= a.V) sBad = 1;
   for (int e = threadIdx.x; e < P * L; e += kThreads) {
-    const int32_t nd = pb[e];
+    const int32_t nd = paths[e];
     if (nd < -1 || nd >= N || (e % L == 0 && nd > 0)) sBad = 1;
   }
   __syncthreads();
@@ -139,12 +165,12 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
   // lowest index among equally long paths.
   int best_acc = -1, best_p = INT_MAX;
   for (int p = threadIdx.x; p < P; p += kThreads) {
-    const int32_t* path = pb + (size_t)p * L;
+    const int32_t* path = paths + (size_t)p * L;
     if (path[0] < 0) continue;
     int acc = 0;
     for (int j = 1; j < L; ++j) {
       const int32_t node = path[j];
-      if (node < 0 || tok[node] != sArg[path[j - 1]]) break;
+      if (node < 0 || sTok[node] != key_index(sKey[path[j - 1]])) break;
       ++acc;
     }
     if (acc > best_acc) {
@@ -174,10 +200,11 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
       }
     const bool none = best_acc < 0;
     const int n = none ? 0 : best_acc;
-    const int32_t* path = none ? nullptr : pb + (size_t)best_p * L;
+    const int32_t* path = none ? nullptr : paths + (size_t)best_p * L;
     const int last = none ? 0 : path[n];
     int32_t* out = a.out_tokens + (size_t)b * L;
-    for (int j = 0; j < L; ++j) out[j] = j < n ? tok[path[j + 1]] : (j == n ? sArg[last] : -1);
+    for (int j = 0; j < L; ++j)
+      out[j] = j < n ? sTok[path[j + 1]] : (j == n ? key_index(sKey[last]) : -1);
     if (a.out_nodes)
       for (int j = 0; j < L; ++j)
         a.out_nodes[(size_t)b * L + j] = j <= n ? (none ? 0 : path[j]) : -1;
