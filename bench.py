@@ -215,7 +215,7 @@ def run_ours(args, rank, world, local):
             call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
                               ptr(c["uniforms"]), ctypes.c_float(w["temperature"]), B, k, V,
                               ptr(out_tok), ptr(out_n), None, ptr(seq), ptr(buf), buf.numel(), sh))
-    launches_per_step = 1 if (tree or greedy) else 2
+    launches_per_step = 2  # pass 1 and its programmatic-dependent finish/draw grid
 
     for i in range(args.warmup):
         rc = fn(*call_args[i & 1])
@@ -340,8 +340,8 @@ def run_ours(args, rank, world, local):
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
             "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
-                       "greedy": "spec_verify_greedy call (argmax_kernel)",
-                       "tree": "spec_verify_tree call (argmax_kernel)"}[kernel_key],
+                       "greedy": "spec_verify_greedy call (argmax_kernel + argmax_finish_kernel)",
+                       "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)"}[kernel_key],
             "algorithmic_bytes_per_call": algo_bytes,
         },
         "e2e": {"value": world * pos * args.e2e_steps / te, "unit": "positions/s",
