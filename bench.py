@@ -39,7 +39,7 @@ CSRC = os.path.join(ROOT, "speculative_decoding_verification_row_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -143,6 +143,28 @@ def recorded_traffic(key: str):
     return rec.get("dram_bytes_per_call")
 
 
+def reduce_max(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself on one process)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, positions_per_rank: int, ms_step_max: float) -> float:
+    """Whole-job verified positions per second: every rank verifies its own
+    batch each step (weak scaling), and a step lasts as long as the slowest
+    rank's."""
+    return world * positions_per_rank / (ms_step_max * 1e-3)
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch."""
+    return seed + 1000 * rank
+
+
 def positions_per_call(w, greedy):
     return w["B"] * (w["L"] - 1) if w["kind"] == "tree" else w["B"] * w["k"]
 
@@ -165,7 +187,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    w = workloads.make(args.config, seed=args.seed + 1000 * rank)
+    w = workloads.make(args.config, seed=rank_seed(args.seed, rank))
     tree = w["kind"] == "tree"
     greedy = args.greedy and not tree
     lib = sv.lib()
@@ -242,12 +264,7 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     clocks.stop()
     assert bad == 0
-    ms_total = start.elapsed_time(end)
-    if dist:
-        tt = torch.tensor([ms_total], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-    ms_step = ms_total / args.steps
+    ms_step = reduce_max(start.elapsed_time(end), dist, device) / args.steps
 
     # End to end through the public binding: pinned host inputs copied in and
     # results read back inside every step.
@@ -292,13 +309,11 @@ def run_ours(args, rank, world, local):
         for _ in range(args.e2e_steps):
             e2e_step()
         te = time.perf_counter() - te0
-    if dist and args.e2e_steps > 0:
-        tt = torch.tensor([te], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        te = float(tt.item())
+    if args.e2e_steps > 0:
+        te = reduce_max(te, dist, device)
 
     pos = positions_per_call(w, greedy)
-    value = world * pos / (ms_step * 1e-3)
+    value = job_throughput(world, pos, ms_step)
     algo_bytes = workloads.algorithmic_bytes(w, greedy=greedy or tree)
     achieved = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
@@ -344,7 +359,7 @@ def run_ours(args, rank, world, local):
                        "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)"}[kernel_key],
             "algorithmic_bytes_per_call": algo_bytes,
         },
-        "e2e": {"value": world * pos * args.e2e_steps / te, "unit": "positions/s",
+        "e2e": {"value": job_throughput(world, pos, 1e3 * te / args.e2e_steps), "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps} if args.e2e_steps > 0 else None,
         "gpu_launches": launches_per_step * args.steps,
