@@ -51,6 +51,10 @@ def parse(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["verify", "relocate"], default="verify",
+                    help="relocate: time the accepted-KV relocation after a tree verify instead")
+    ap.add_argument("--kv-row-bytes", type=int, default=131072,
+                    help="relocate: bytes of one token's KV row (32 layers x K,V x 8 heads x 128 x bf16)")
     return ap.parse_args(argv)
 
 
@@ -425,10 +429,64 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def run_relocate(args, rank, world, local):
+    """Accepted-KV relocation after the tree verify of a tree workload: a paged
+    pool of --kv-row-bytes rows, 32 tokens per block, block tables shuffled."""
+    import torch
+    import oracle
+    import speculative_decoding_verification_row_gb300 as sv
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    name = args.config if workloads.CONFIGS[args.config]["kind"] == "tree" else "tree_b16_n60_l4_v151936_bf16"
+    w = workloads.make(name, seed=rank_seed(args.seed, rank))
+    o = oracle.verify(w)                       # accepted nodes of this batch (host side, once)
+    B, N, L, tpb = w["B"], w["N"], w["L"], 32
+    rng = np.random.default_rng(args.seed)
+    base = rng.integers(512, 4096, size=B).astype(np.int32)
+    max_blocks = (4096 + N + tpb - 1) // tpb + 1
+    bt = rng.permutation(B * max_blocks).astype(np.int32).reshape(B, max_blocks)
+    rows = B * max_blocks * tpb
+    pool = torch.empty((rows, args.kv_row_bytes // 2), dtype=torch.bfloat16, device=device)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)  # noqa: E731
+    bt_d, base_d, nodes_d, n_d = d(bt), d(base), d(o["accepted_nodes"]), d(o["num_accepted"])
+    moved = sum(int(np.sum(o["accepted_nodes"][b, 1:o["num_accepted"][b] + 1] != np.arange(1, o["num_accepted"][b] + 1)))
+                for b in range(B) if o["num_accepted"][b] > 0)
+    algo = 2 * moved * args.kv_row_bytes      # read + write of every moved row
+    sv.relocate_accepted_kv(pool, bt_d, base_d, nodes_d, n_d, tpb)  # argument checks once
+    lib = sv.lib()
+    P = ctypes.c_void_p
+    stream = torch.cuda.current_stream(device)
+    call = (P(pool.data_ptr()), ctypes.c_size_t(args.kv_row_bytes), tpb, B * max_blocks, P(bt_d.data_ptr()),
+            max_blocks, P(base_d.data_ptr()), P(nodes_d.data_ptr()), P(n_d.data_ptr()), B, L,
+            P(stream.cuda_stream))
+    for _ in range(args.warmup):
+        assert lib.spec_relocate_accepted_kv(*call) == 0
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        lib.spec_relocate_accepted_kv(*call)
+    end.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * start.elapsed_time(end) / args.steps
+    peak, src = peak_hbm()
+    if rank == 0:
+        print(json.dumps({
+            "op": "relocate_accepted_kv", "workload": name, "B": B, "L": L, "tokens_per_block": tpb,
+            "kv_row_bytes": args.kv_row_bytes, "rows_moved": moved, "us_per_call": us,
+            "algorithmic_bytes_per_call": algo, "achieved_gbs": algo / (us * 1e-6) / 1e9,
+            "frac_of_peak": algo / (us * 1e-6) / 1e9 / peak, "peak_gbs": peak, "peak_source": src,
+            "steps": args.steps, "warmup": args.warmup,
+        }), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.op == "relocate":
+        run_relocate(args, rank, world, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

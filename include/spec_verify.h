@@ -166,6 +166,37 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *tree_t
 int spec_rollback_lengths(const int32_t *old_lens, const int32_t *num_accepted, int k, int B,
                           int32_t *new_lens, int32_t *rewind_lens, spec_stream_t stream);
 
+/* Accepted-KV relocation after a tree verify (TensorRT-LLM walkthrough, the
+ * "moving to the right place" step before update_resources,
+ * _update_kv_cache_draft_token_location): the KV rows of the accepted nodes,
+ * written in tree order during the draft step, are gathered into consecutive
+ * logical positions right after the committed prefix.  As on that page the
+ * cache is paged.
+ *   kv_pool        [num_blocks * tokens_per_block, row_bytes] device memory,
+ *                  16-byte aligned; one row per token (one layer's K and V
+ *                  of every KV head, or however the caller lays a token out).
+ *                  row_bytes must be a multiple of 16.
+ *   block_tables   [B, max_blocks] int32: request b's logical position t is
+ *                  pool row block_tables[b][t / tokens_per_block] *
+ *                  tokens_per_block + t % tokens_per_block.  Blocks holding
+ *                  the window must not be shared between requests.
+ *   base_lens      [B] int32: logical position of tree node 0 (the committed
+ *                  length before the verify window).
+ *   accepted_nodes [B, L] int32 and num_accepted [B]: spec_verify_tree's
+ *                  outputs (root, then the n accepted nodes; -1 padded).
+ * For j = 1..n, row base + accepted_nodes[b][j] moves to row base + j; rows
+ * past base + n are left as they are (the rollback makes them invisible).
+ * A request is left untouched when n <= 0 or n >= L (failed closed), or when
+ * its path does not start at node 0 with strictly increasing nodes, or a row
+ * it would read or write is unmapped (a block id outside [0, num_blocks) or
+ * a position past max_blocks * tokens_per_block); no status is recorded.
+ * Returns SPEC_EINVAL for null pointers, sizes outside the limits or a
+ * misaligned pool. */
+int spec_relocate_accepted_kv(void *kv_pool, size_t row_bytes, int tokens_per_block,
+                              int num_blocks, const int32_t *block_tables, int max_blocks,
+                              const int32_t *base_lens, const int32_t *accepted_nodes,
+                              const int32_t *num_accepted, int B, int L, spec_stream_t stream);
+
 /* Chain verify without a caller-provided workspace, for callers that cannot
  * allocate device memory (code whose allocator forbids allocations while a
  * step runs, or host code that owns no CUDA allocator).  The pages have no

@@ -194,6 +194,49 @@ def rollback(old_lens, num_accepted, k: int, lib=None) -> dict:
     return dict(new_lens=new, rewind_lens=rew, rc=rc)
 
 
+def relocate_kv(pool, block_tables, base_lens, accepted_nodes, num_accepted,
+                tokens_per_block: int):
+    """Accepted-KV relocation (TensorRT-LLM walkthrough, the "moving to the
+    right place" step, _update_kv_cache_draft_token_location): returns a copy
+    of ``pool`` [rows, ...] in which, for every request b with 0 < n < L whose
+    path starts at node 0 with strictly increasing nodes, all rows mapped, the
+    row at logical position base + j becomes the ORIGINAL row at base +
+    accepted_nodes[b, j] for j = 1..n.  Logical position t of request b is pool
+    row block_tables[b, t // tpb] * tpb + t % tpb."""
+    pool = np.asarray(pool)
+    bt = np.asarray(block_tables)
+    base = np.asarray(base_lens)
+    nodes = np.asarray(accepted_nodes)
+    nacc = np.asarray(num_accepted)
+    tpb = int(tokens_per_block)
+    nblocks = pool.shape[0] // tpb
+    out = pool.copy()
+
+    def row(b, t):
+        if t < 0 or t >= bt.shape[1] * tpb:
+            return None
+        blk = int(bt[b, t // tpb])
+        if blk < 0 or blk >= nblocks:
+            return None
+        return blk * tpb + t % tpb
+
+    L = nodes.shape[1]
+    for b in range(bt.shape[0]):
+        n = int(nacc[b])
+        if n <= 0 or n >= L or nodes[b, 0] != 0:
+            continue
+        path = [int(x) for x in nodes[b, :n + 1]]
+        if any(path[j] <= path[j - 1] for j in range(1, n + 1)):
+            continue
+        src = [row(b, int(base[b]) + path[j]) for j in range(n + 1)]
+        dst = [row(b, int(base[b]) + j) for j in range(n + 1)]
+        if any(r is None for r in src + dst):
+            continue
+        for j in range(1, n + 1):
+            out[dst[j]] = pool[src[j]]
+    return out
+
+
 def verify(w: dict, greedy: bool = False, lib=None) -> dict:
     """Run the oracle on a workload dict from ``workloads.make``."""
     if w["kind"] == "tree":

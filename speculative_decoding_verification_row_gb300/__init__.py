@@ -37,7 +37,8 @@ SPEC_MAX_PATH_LEN = 64
 # Every entry point the header declares.
 SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_greedy", "spec_verify_tree", "spec_rollback_lengths",
-           "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc")
+           "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc",
+           "spec_relocate_accepted_kv")
 SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
@@ -61,10 +62,12 @@ def _bind(lib):
     lib.spec_rollback_lengths.argtypes = [P, P, I, I, P, P, P]
     lib.spec_verify_chain_noalloc.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P]
     lib.spec_last_error.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int)]
+    lib.spec_relocate_accepted_kv.argtypes = [P, S, I, I, P, I, P, P, P, I, I, P]
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
-              "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc"):
+              "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc",
+              "spec_relocate_accepted_kv"):
         getattr(lib, f).restype = I
     return lib
 
@@ -298,6 +301,33 @@ def rollback_lengths(old_lens, num_accepted, k: int, *, new_lens=None, rewind_le
     if rc != SPEC_OK:
         raise SpecError("spec_rollback_lengths", rc)
     return new, rew
+
+
+def relocate_accepted_kv(kv_pool, block_tables, base_lens, accepted_nodes, num_accepted,
+                         tokens_per_block: int, *, stream=None):
+    """Gather the accepted tree nodes' KV rows to consecutive positions after
+    each request's prefix, in place.  kv_pool: [num_blocks * tokens_per_block,
+    ...] (any dtype; a token's row is its trailing dims), block_tables
+    [B, max_blocks] int32, base_lens [B], accepted_nodes [B, L], num_accepted [B]."""
+    if not isinstance(kv_pool, torch.Tensor) or not kv_pool.is_cuda or not kv_pool.is_contiguous():
+        raise ValueError("kv_pool must be a contiguous CUDA tensor")
+    rows = kv_pool.shape[0]
+    if rows % tokens_per_block:
+        raise ValueError("kv_pool rows must be num_blocks * tokens_per_block")
+    row_bytes = kv_pool.numel() * kv_pool.element_size() // max(rows, 1)
+    bt = _dev(block_tables, "block_tables", torch.int32)
+    B = bt.shape[0]
+    base = _dev(base_lens, "base_lens", torch.int32, (B,))
+    nodes = _dev(accepted_nodes, "accepted_nodes", torch.int32)
+    n = _dev(num_accepted, "num_accepted", torch.int32, (B,))
+    sh, _ = _stream_handle(stream, kv_pool.device)
+    rc = lib().spec_relocate_accepted_kv(_ptr(kv_pool), ctypes.c_size_t(row_bytes),
+                                         int(tokens_per_block), rows // tokens_per_block, _ptr(bt),
+                                         bt.shape[1], _ptr(base), _ptr(nodes), _ptr(n), B,
+                                         nodes.shape[1], sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_relocate_accepted_kv", rc)
+    return kv_pool
 
 
 def last_error(workspace: Workspace, stream=None) -> int:

@@ -110,3 +110,25 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises((ValueError, RuntimeError)):
         sv.verify_chain(t, t[:, :3], torch.zeros(2, 3, dtype=torch.int32),
                         torch.zeros(2, 4), 1.0)
+
+
+def test_relocate_rejects_bad_arguments_before_launch():
+    import ctypes
+    lib = sv.lib()
+    P = ctypes.c_void_p
+    fake = P(16 * 1024)  # never dereferenced: every check below fails on the host
+    z = P(16 * 2048)
+    args = dict(pool=fake, row_bytes=64, tpb=16, nblocks=4, bt=z, max_blocks=2, base=z, nodes=z, n=z, B=2, L=4)
+
+    def call(**over):
+        a = dict(args, **over)
+        return lib.spec_relocate_accepted_kv(a["pool"], ctypes.c_size_t(a["row_bytes"]), a["tpb"], a["nblocks"],
+                                             a["bt"], a["max_blocks"], a["base"], a["nodes"], a["n"],
+                                             a["B"], a["L"], None)
+    assert call(row_bytes=24) == sv.SPEC_EINVAL          # not a multiple of 16
+    assert call(row_bytes=0) == sv.SPEC_EINVAL
+    assert call(pool=P(16 * 1024 + 8)) == sv.SPEC_EINVAL  # misaligned pool
+    assert call(pool=None) == sv.SPEC_EINVAL
+    assert call(B=0) == sv.SPEC_EINVAL
+    assert call(L=65) == sv.SPEC_EINVAL
+    assert call(tpb=0) == sv.SPEC_EINVAL
