@@ -51,6 +51,8 @@ def parse(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--philox", action="store_true",
+                    help="chain: draw each request's uniforms in the kernel from a (seed, offset) Philox state")
     ap.add_argument("--op", choices=["verify", "relocate"], default="verify",
                     help="relocate: time the accepted-KV relocation after a tree verify instead")
     ap.add_argument("--kv-row-bytes", type=int, default=131072,
@@ -213,6 +215,8 @@ def run_ours(args, rank, world, local):
             if not greedy:
                 c["draft"] = dev_logits(w["draft"], w["dtype"], device)
                 c["uniforms"] = torch.from_numpy(w["uniforms"]).to(device)
+                c["seeds"] = torch.full((w["B"],), 1234, dtype=torch.int64, device=device)
+                c["offsets"] = torch.arange(w["B"], dtype=torch.int64, device=device) * 4096
         copies.append(c)
     seq = i32(w["seq_lens"])
     k = w["L"] - 1 if tree else w["k"]
@@ -236,6 +240,12 @@ def run_ours(args, rank, world, local):
             fn = lib.spec_verify_greedy
             call_args.append((ptr(c["target"]), code, ptr(c["tokens"]), B, k, V, ptr(out_tok),
                               ptr(out_n), ptr(seq), ptr(buf), buf.numel(), sh))
+        elif args.philox:
+            fn = lib.spec_verify_chain_philox
+            call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
+                              ptr(c["seeds"]), ptr(c["offsets"]), ctypes.c_float(w["temperature"]),
+                              B, k, V, ptr(out_tok), ptr(out_n), None, ptr(seq), ptr(buf),
+                              buf.numel(), sh))
         else:
             fn = lib.spec_verify_chain
             call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
@@ -347,7 +357,7 @@ def run_ours(args, rank, world, local):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": args.config + ("/greedy" if greedy else ""),
+            "workload": args.config + ("/greedy" if greedy else "") + ("/philox" if args.philox and not (tree or greedy) else ""),
             "B": B, "k": k, "V": V, "logits": w["dtype"],
             "temperature": None if (tree or greedy) else w["temperature"],
             "requests_per_step": B * world,

@@ -120,6 +120,31 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
                       int32_t *seq_lens,
                       void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
+/* Chain verify with each request's uniforms drawn inside the kernel from a
+ * per-request Philox state (TensorRT-LLM walkthrough, rejection-sampling
+ * section: chain_speculative_sampling takes a seed and an offset per request,
+ * the offset keeping each request's stream apart so that the seed can stay
+ * constant).  Arguments and results are those of spec_verify_chain, with
+ *   seeds    [B] uint64: Philox4x32-10 key (low word first);
+ *   offsets  [B] uint64: counter, advanced by the caller between steps;
+ * in place of uniforms.  Uniform i of request b (i = 0..k; i < k are the
+ * accept tests, i = k drives the final draw) is word i % 4 of
+ * Philox4x32-10(counter = (low word of offset, high word of offset, i / 4, 0),
+ * key = seed) (Salmon et al., SC'11), shifted right by 8 and scaled by 2^-24.
+ * The pages fix the state, not this mapping: it is this library's reading. */
+int spec_verify_chain_philox(const void *target_logits, const void *draft_logits, int dtype,
+                             const int32_t *draft_tokens, const uint64_t *seeds,
+                             const uint64_t *offsets, float temperature, int B, int k, int V,
+                             int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                             int32_t *seq_lens, void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
+
+/* The uniforms spec_verify_chain_philox draws: out[b, i] for i = 0..n-1
+ * (n <= SPEC_MAX_DRAFT + 1), from the same per-request Philox streams, so a
+ * caller can log or replay a step's randomness. */
+int spec_philox_uniforms(const uint64_t *seeds, const uint64_t *offsets, int B, int n,
+                         float *out, spec_stream_t stream);
+
 /* Greedy chain verify.
  *   target_logits [B, k+1, V], draft_tokens [B, k] in [0, V).
  * g_i = argmax_t target[b,i,t] on the stored values, lowest id on ties;

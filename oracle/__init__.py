@@ -55,8 +55,12 @@ def _bind(lib):
     lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P]
     lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.oracle_rollback.argtypes = [P, P, I, I, P, P]
+    lib.oracle_philox4x32_10.argtypes = [P, P, P]
+    lib.oracle_philox4x32_10.restype = None
+    lib.oracle_philox_uniforms.argtypes = [P, P, I, I, P]
     for f in ("oracle_softmax", "oracle_inverse_cdf", "oracle_argmax", "oracle_verify_chain",
-              "oracle_verify_greedy", "oracle_verify_tree", "oracle_rollback"):
+              "oracle_verify_greedy", "oracle_verify_tree", "oracle_rollback",
+              "oracle_philox_uniforms"):
         getattr(lib, f).restype = I
     return lib
 
@@ -234,6 +238,31 @@ def relocate_kv(pool, block_tables, base_lens, accepted_nodes, num_accepted,
             continue
         for j in range(1, n + 1):
             out[dst[j]] = pool[src[j]]
+    return out
+
+
+def philox4x32_10(ctr, key, lib=None) -> np.ndarray:
+    """One Philox4x32-10 block (Salmon et al., SC'11): 4 counter words, 2 key words -> 4 words."""
+    lib = lib or load()
+    c = _c(np.asarray(ctr, dtype=np.uint32), np.uint32)
+    k = _c(np.asarray(key, dtype=np.uint32), np.uint32)
+    out = np.empty(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def philox_uniforms(seeds, offsets, n: int, lib=None) -> np.ndarray:
+    """[B, n] float32 uniforms of each request's (seed, offset) Philox stream
+    (TensorRT-LLM walkthrough, rejection-sampling section: one Philox state
+    per request)."""
+    lib = lib or load()
+    s = _c(np.asarray(seeds, dtype=np.uint64), np.uint64)
+    o = _c(np.asarray(offsets, dtype=np.uint64), np.uint64)
+    B = s.shape[0]
+    out = np.empty((B, n), dtype=np.float32)
+    rc = lib.oracle_philox_uniforms(_ptr(s), _ptr(o), B, int(n), _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_philox_uniforms rc={rc}")
     return out
 
 

@@ -30,6 +30,13 @@
  *   - rollback lengths .............. TensorRT-LLM walkthrough, update_requests
  *                                     and rewind_cache sections (rewind =
  *                                     verified - accepted; cursor truncation).
+ *   - per-request uniforms .......... TensorRT-LLM walkthrough, rejection-
+ *                                     sampling section (a Philox state of
+ *                                     seed and offset per request); the
+ *                                     generator is Philox4x32-10 as defined by
+ *                                     Salmon, Moraes, Dror and Shaw, "Parallel
+ *                                     random numbers: as easy as 1, 2, 3"
+ *                                     (SC'11).
  *
  * Readings taken where the pages are silent:
  *   target row i and draft row i both describe token x_i; row k is the bonus
@@ -409,4 +416,57 @@ int oracle_rollback(const int32_t *old_lens, const int32_t *num_accepted, int k,
             rewind_lens[b] = k - n;
     }
     return rc;
+}
+
+/* Philox4x32-10 (Salmon et al., SC'11): ten rounds on a 128-bit counter
+ * (c0..c3) under a 64-bit key (k0, k1).  A round multiplies c0 by 0xD2511F53
+ * and c2 by 0xCD9E8D57 into 64-bit products, and the new counter is
+ * (hi(c2*M1) ^ c1 ^ k0, lo(c2*M1), hi(c0*M0) ^ c3 ^ k1, lo(c0*M0)).  The key is
+ * bumped by the Weyl constants (0x9E3779B9, 0xBB67AE85) between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* The uniforms of request b, i = 0..n-1 (this library's reading of the
+ * pages' per-request (seed, offset) state): Philox4x32-10 with key = seed_b
+ * (low word first) and counter = (low and high word of offset_b, i / 4, 0);
+ * uniform i = (word i % 4 >> 8) * 2^-24, in [0, 1). */
+int oracle_philox_uniforms(const uint64_t *seeds, const uint64_t *offsets, int B, int n,
+                           float *out)
+{
+    if (!seeds || !offsets || !out || B < 1 || n < 1)
+        return ORC_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        const uint32_t key[2] = {(uint32_t)seeds[b], (uint32_t)(seeds[b] >> 32)};
+        for (int i = 0; i < n; ++i) {
+            const uint32_t ctr[4] = {(uint32_t)offsets[b], (uint32_t)(offsets[b] >> 32),
+                                     (uint32_t)(i / 4), 0u};
+            uint32_t r[4];
+            oracle_philox4x32_10(ctr, key, r);
+            out[(size_t)b * n + i] = (float)((double)(r[i % 4] >> 8) * (1.0 / 16777216.0));
+        }
+    }
+    return ORC_OK;
 }

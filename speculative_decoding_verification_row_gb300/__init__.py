@@ -38,7 +38,7 @@ SPEC_MAX_PATH_LEN = 64
 SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_greedy", "spec_verify_tree", "spec_rollback_lengths",
            "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc",
-           "spec_relocate_accepted_kv")
+           "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms")
 SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
@@ -63,11 +63,13 @@ def _bind(lib):
     lib.spec_verify_chain_noalloc.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P]
     lib.spec_last_error.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int)]
     lib.spec_relocate_accepted_kv.argtypes = [P, S, I, I, P, I, P, P, P, I, I, P]
+    lib.spec_verify_chain_philox.argtypes = [P, P, I, P, P, P, ctypes.c_float, I, I, I, P, P, P, P, P, S, P]
+    lib.spec_philox_uniforms.argtypes = [P, P, I, I, P, P]
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
               "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc",
-              "spec_relocate_accepted_kv"):
+              "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms"):
         getattr(lib, f).restype = I
     return lib
 
@@ -167,10 +169,13 @@ def default_workspace(device, stream_handle) -> Workspace:
 # ---------------------------------------------------------------- calls
 def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
                  out_tokens=None, out_num_accepted=None, out_probs=None, want_probs=False,
-                 seq_lens=None, workspace: Workspace | None = None, stream=None):
+                 seq_lens=None, workspace: Workspace | None = None, stream=None,
+                 seeds=None, offsets=None):
     """Chain rejection-sampling verify; returns (tokens [B,k+1], num_accepted [B], probs [B,k,2] or None).
 
-    seq_lens (int32 [B], optional) is advanced in place by n_acc + 1."""
+    seq_lens (int32 [B], optional) is advanced in place by n_acc + 1.  With
+    uniforms=None, seeds and offsets (int64 [B]) select each request's Philox
+    stream and the uniforms are drawn inside the kernel."""
     t = _dev(target_logits, "target_logits")
     if t.dim() != 3:
         raise ValueError("target_logits must be [B, k+1, V]")
@@ -179,7 +184,11 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
     code = _logit_code(t, "target_logits")
     d = _dev(draft_logits, "draft_logits", t.dtype, (B, k, V))
     x = _dev(draft_tokens, "draft_tokens", torch.int32, (B, k))
-    u = _dev(uniforms, "uniforms", torch.float32, (B, k + 1))
+    if uniforms is not None:
+        u = _dev(uniforms, "uniforms", torch.float32, (B, k + 1))
+    else:
+        sd = _dev(seeds, "seeds", torch.int64, (B,))
+        of = _dev(offsets, "offsets", torch.int64, (B,))
     dev = t.device
     tok = _out(out_tokens, "out_tokens", (B, k + 1), torch.int32, dev)
     n = _out(out_num_accepted, "out_num_accepted", (B,), torch.int32, dev)
@@ -191,11 +200,18 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
     sh, _ = _stream_handle(stream, dev)
     ws = workspace or default_workspace(dev, sh)
     buf = ws.ensure(B, 2 * k + 1, V, sh)
-    rc = lib().spec_verify_chain(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
-                                 B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens),
-                                 _ptr(buf), buf.numel(), sh)
+    if uniforms is not None:
+        rc = lib().spec_verify_chain(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
+                                     B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens),
+                                     _ptr(buf), buf.numel(), sh)
+        name = "spec_verify_chain"
+    else:
+        rc = lib().spec_verify_chain_philox(_ptr(t), _ptr(d), code, _ptr(x), _ptr(sd), _ptr(of),
+                                            float(temperature), B, k, V, _ptr(tok), _ptr(n),
+                                            _ptr(probs), _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
+        name = "spec_verify_chain_philox"
     if rc != SPEC_OK:
-        raise SpecError("spec_verify_chain", rc)
+        raise SpecError(name, rc)
     return tok, n, probs
 
 
@@ -328,6 +344,20 @@ def relocate_accepted_kv(kv_pool, block_tables, base_lens, accepted_nodes, num_a
     if rc != SPEC_OK:
         raise SpecError("spec_relocate_accepted_kv", rc)
     return kv_pool
+
+
+def philox_uniforms(seeds, offsets, n: int, *, stream=None):
+    """[B, n] float32: the uniforms verify_chain draws for each request's
+    (seed, offset) Philox stream when called without uniforms."""
+    sd = _dev(seeds, "seeds", torch.int64)
+    B = sd.shape[0]
+    of = _dev(offsets, "offsets", torch.int64, (B,))
+    out = torch.empty((B, n), dtype=torch.float32, device=sd.device)
+    sh, _ = _stream_handle(stream, sd.device)
+    rc = lib().spec_philox_uniforms(_ptr(sd), _ptr(of), B, int(n), _ptr(out), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_philox_uniforms", rc)
+    return out
 
 
 def last_error(workspace: Workspace, stream=None) -> int:

@@ -73,13 +73,19 @@ int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t s
   return SPEC_OK;
 }
 
-int spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype,
-                      const int32_t* draft_tokens, const float* uniforms, float temperature,
-                      int B, int k, int V, int32_t* out_tokens, int32_t* out_num_accepted,
-                      float* out_probs, int32_t* seq_lens, void* workspace,
-                      size_t workspace_bytes, spec_stream_t stream) {
-  if (!target_logits || !draft_logits || !draft_tokens || !uniforms || !out_tokens ||
-      !out_num_accepted)
+}  // extern "C"
+
+namespace {
+
+// Chain verify with explicit uniforms, or (uniforms == nullptr) with each
+// request's uniforms drawn in the kernel from its Philox (seed, offset).
+int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
+               const int32_t* draft_tokens, const float* uniforms, const uint64_t* seeds,
+               const uint64_t* offsets, float temperature, int B, int k, int V,
+               int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
+               int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  if (!target_logits || !draft_logits || !draft_tokens || (!uniforms && (!seeds || !offsets)) ||
+      !out_tokens || !out_num_accepted)
     return SPEC_EINVAL;
   if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || k < 1 ||
       k > SPEC_MAX_DRAFT || V < 2)
@@ -94,13 +100,13 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
   a.nsplit2 = num_items(V);
-  // The chain kernel's work queue counts units in 32 bits (plus one ticket
-  // per CTA past the end).
-  if ((long)B * (R * (long)a.nsplit + a.nsplit2) > INT_MAX / 2) return SPEC_EINVAL;
+  if ((long)B * (R * (long)a.nsplit + a.nsplit2) > INT_MAX) return SPEC_EINVAL;  // grid sizes
   a.target = static_cast<const char*>(target_logits);
   a.draft = static_cast<const char*>(draft_logits);
   a.tokens = draft_tokens;
   a.uniforms = uniforms;
+  a.seeds = reinterpret_cast<const unsigned long long*>(seeds);
+  a.offsets = reinterpret_cast<const unsigned long long*>(offsets);
   a.B = B;
   a.k = k;
   a.V = V;
@@ -111,6 +117,54 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   a.ws = ws_views(workspace, WsLayout(B, R, V));
   return launch_chain(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
                                                                           : SPEC_ECUDA;
+}
+
+__global__ void philox_uniforms_kernel(const unsigned long long* seeds,
+                                       const unsigned long long* offsets, int B, int n,
+                                       float* out) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long)B * n) return;
+  const int b = (int)(i / n);
+  out[i] = philox_uniform(seeds[b], offsets[b], (int)(i - (long)b * n));
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_philox_uniforms(const uint64_t* seeds, const uint64_t* offsets, int B, int n,
+                         float* out, spec_stream_t stream) {
+  if (!seeds || !offsets || !out || B < 1 || B > SPEC_MAX_BATCH || n < 1 ||
+      n > SPEC_MAX_DRAFT + 1)
+    return SPEC_EINVAL;
+  const long total = (long)B * n;
+  philox_uniforms_kernel<<<(unsigned)((total + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const unsigned long long*>(seeds),
+      reinterpret_cast<const unsigned long long*>(offsets), B, n, out);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype,
+                      const int32_t* draft_tokens, const float* uniforms, float temperature,
+                      int B, int k, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                      float* out_probs, int32_t* seq_lens, void* workspace,
+                      size_t workspace_bytes, spec_stream_t stream) {
+  if (!uniforms) return SPEC_EINVAL;
+  return chain_impl(target_logits, draft_logits, dtype, draft_tokens, uniforms, nullptr, nullptr,
+                    temperature, B, k, V, out_tokens, out_num_accepted, out_probs, seq_lens,
+                    workspace, workspace_bytes, stream);
+}
+
+int spec_verify_chain_philox(const void* target_logits, const void* draft_logits, int dtype,
+                             const int32_t* draft_tokens, const uint64_t* seeds,
+                             const uint64_t* offsets, float temperature, int B, int k, int V,
+                             int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
+                             int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream) {
+  if (!seeds || !offsets) return SPEC_EINVAL;
+  return chain_impl(target_logits, draft_logits, dtype, draft_tokens, nullptr, seeds, offsets,
+                    temperature, B, k, V, out_tokens, out_num_accepted, out_probs, seq_lens,
+                    workspace, workspace_bytes, stream);
 }
 
 int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens, int B,

@@ -511,7 +511,9 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
       xq = load_logit<DT>(a.draft + ((size_t)b * k + tid) * row_bytes, x);
     }
   }
-  if (tid <= k) sU[tid] = a.uniforms[(size_t)b * (k + 1) + tid];
+  if (tid <= k)
+    sU[tid] = a.uniforms ? a.uniforms[(size_t)b * (k + 1) + tid]
+                         : philox_uniform(a.seeds[b], a.offsets[b], tid);
   if (tid == 0) sBad = 0;
   // Merge the slice statistics of every row of the request, in a fixed
   // order, as they arrive: warp w takes rows w, w+8, ...; it issues the loads

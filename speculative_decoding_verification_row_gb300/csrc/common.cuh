@@ -270,6 +270,38 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds; a round takes the 64-bit products
+// c0 * 0xD2511F53 and c2 * 0xCD9E8D57 and forms (hi2 ^ c1 ^ k0, lo2,
+// hi0 ^ c3 ^ k1, lo0); the key advances by (0x9E3779B9, 0xBB67AE85) between
+// rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo2 = 0xCD9E8D57u * c.z, hi2 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi2 ^ c.y ^ k0, lo2, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Uniform i of a request's Philox stream: key = seed, counter = (offset,
+// i / 4, 0); word i % 4, top 24 bits, scaled to [0, 1).
+__device__ __forceinline__ float philox_uniform(unsigned long long seed, unsigned long long offset,
+                                                int i) {
+  const uint4 r = philox4x32_10(make_uint4((uint32_t)offset, (uint32_t)(offset >> 32),
+                                           (uint32_t)(i / 4), 0u),
+                                (uint32_t)seed, (uint32_t)(seed >> 32));
+  const int w = i % 4;
+  const uint32_t x = w == 0 ? r.x : w == 1 ? r.y : w == 2 ? r.z : r.w;
+  return (float)(x >> 8) * (1.0f / 16777216.0f);
+}
+
 // Upper bound of every device-side wait (about one second at 2 GHz).  A wait
 // that runs out sets SPEC_ETIMEOUT instead of spinning forever.
 constexpr long long kWaitCycles = 2000000000LL;

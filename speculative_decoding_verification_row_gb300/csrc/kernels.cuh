@@ -9,7 +9,9 @@ struct ChainArgs {
   const char* target;
   const char* draft;
   const int32_t* tokens;
-  const float* uniforms;
+  const float* uniforms;                      // [B, k+1], or null: Philox per request
+  const unsigned long long* seeds;            // [B] Philox keys (when uniforms is null)
+  const unsigned long long* offsets;          // [B] Philox counters (when uniforms is null)
   float c_hi, c_lo;  // log2(e)/T split as hi + lo
   int B, k, V;
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
