@@ -51,8 +51,9 @@ def _bind(lib):
     lib.oracle_softmax.argtypes = [P, I, ctypes.c_double, I, P]
     lib.oracle_inverse_cdf.argtypes = [P, I, ctypes.c_double, ctypes.c_double, P]
     lib.oracle_argmax.argtypes = [P, I, I]
-    lib.oracle_verify_chain.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P]
-    lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P]
+    lib.oracle_verify_chain.argtypes = [P, P, I, P, P, P, ctypes.c_float, I, I, I, P, P, P, P]
+    lib.oracle_verify_greedy.argtypes = [P, I, P, P, I, I, I, P, P]
+    lib.oracle_rollback_paged.argtypes = [P, P, P, I, P, I, I, P, P, P]
     lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.oracle_rollback.argtypes = [P, P, I, I, P, P]
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
@@ -60,7 +61,7 @@ def _bind(lib):
     lib.oracle_philox_uniforms.argtypes = [P, P, I, I, P]
     for f in ("oracle_softmax", "oracle_inverse_cdf", "oracle_argmax", "oracle_verify_chain",
               "oracle_verify_greedy", "oracle_verify_tree", "oracle_rollback",
-              "oracle_philox_uniforms"):
+              "oracle_philox_uniforms", "oracle_rollback_paged"):
         getattr(lib, f).restype = I
     return lib
 
@@ -118,13 +119,14 @@ def argmax(x, dtype: str = "f32", lib=None) -> int:
 
 
 def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, dtype: str = "f32",
-                 lib=None) -> dict:
+                 lib=None, draft_lens=None) -> dict:
     """Chain rejection-sampling verify (vLLM anatomy page, "Speculative Decoding").
 
     target [B,k+1,V], draft [B,k,V] (fp32 values or raw bf16 bits),
     draft_tokens int [B,k], uniforms float32 [B,k+1].  Returns a dict with
     tokens [B,k+1], num_accepted [B], probs [B,k,2] (p_i(x_i), q_i(x_i)),
-    flags [B,k+1] and the return code.
+    flags [B,k+1] and the return code.  draft_lens (int [B], optional): each
+    request's real draft length k_b <= k (ragged verify).
     """
     lib = lib or load()
     target = _logits(target, dtype)
@@ -139,16 +141,17 @@ def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, dtyp
     n_acc = np.empty(B, dtype=np.int32)
     probs = np.empty((B, k, 2), dtype=np.float64)
     flags = np.empty((B, k + 1), dtype=np.int32)
+    lens = None if draft_lens is None else _c(draft_lens, np.int32)
     rc = lib.oracle_verify_chain(_ptr(target), _ptr(draft), DTYPE_CODE[dtype], _ptr(x), _ptr(r),
-                                 float(temperature), B, k, V, _ptr(tokens), _ptr(n_acc),
-                                 _ptr(probs), _ptr(flags))
+                                 None if lens is None else _ptr(lens), float(temperature), B, k, V,
+                                 _ptr(tokens), _ptr(n_acc), _ptr(probs), _ptr(flags))
     if rc not in (OK, EBADINDEX):
         raise ValueError(f"oracle_verify_chain rc={rc}")
     return dict(tokens=tokens, num_accepted=n_acc, probs=probs, flags=flags, rc=rc)
 
 
-def verify_greedy(target, draft_tokens, dtype: str = "f32", lib=None) -> dict:
-    """Greedy chain verify (Kestrel article, section 3.3)."""
+def verify_greedy(target, draft_tokens, dtype: str = "f32", lib=None, draft_lens=None) -> dict:
+    """Greedy chain verify (Kestrel article, section 3.3); draft_lens as for verify_chain."""
     lib = lib or load()
     target = _logits(target, dtype)
     B, k1, V = target.shape
@@ -157,7 +160,9 @@ def verify_greedy(target, draft_tokens, dtype: str = "f32", lib=None) -> dict:
     assert d.shape == (B, k)
     tokens = np.empty((B, k + 1), dtype=np.int32)
     n_acc = np.empty(B, dtype=np.int32)
-    rc = lib.oracle_verify_greedy(_ptr(target), DTYPE_CODE[dtype], _ptr(d), B, k, V,
+    lens = None if draft_lens is None else _c(draft_lens, np.int32)
+    rc = lib.oracle_verify_greedy(_ptr(target), DTYPE_CODE[dtype], _ptr(d),
+                                  None if lens is None else _ptr(lens), B, k, V,
                                   _ptr(tokens), _ptr(n_acc))
     if rc not in (OK, EBADINDEX):
         raise ValueError(f"oracle_verify_greedy rc={rc}")
@@ -241,6 +246,27 @@ def relocate_kv(pool, block_tables, base_lens, accepted_nodes, num_accepted,
     return out
 
 
+def rollback_paged(old_lens, num_accepted, k: int, tokens_per_block: int, draft_lens=None,
+                   blocks_held=None, lib=None) -> dict:
+    """Rollback with ragged draft lengths and paged block accounting
+    (TensorRT-LLM walkthrough, update_requests and rewind_cache)."""
+    lib = lib or load()
+    old = _c(old_lens, np.int32)
+    n = _c(num_accepted, np.int32)
+    B = old.shape[0]
+    lens = None if draft_lens is None else _c(draft_lens, np.int32)
+    held = None if blocks_held is None else _c(blocks_held, np.int32)
+    new = np.empty(B, dtype=np.int32)
+    rew = np.empty(B, dtype=np.int32)
+    free = np.empty(B, dtype=np.int32)
+    rc = lib.oracle_rollback_paged(_ptr(old), _ptr(n), None if lens is None else _ptr(lens), int(k),
+                                   None if held is None else _ptr(held), int(tokens_per_block), B,
+                                   _ptr(new), _ptr(rew), _ptr(free))
+    if rc not in (OK, EBADINDEX):
+        raise ValueError(f"oracle_rollback_paged rc={rc}")
+    return dict(new_lens=new, rewind_lens=rew, free_blocks=free, rc=rc)
+
+
 def philox4x32_10(ctr, key, lib=None) -> np.ndarray:
     """One Philox4x32-10 block (Salmon et al., SC'11): 4 counter words, 2 key words -> 4 words."""
     lib = lib or load()
@@ -271,6 +297,7 @@ def verify(w: dict, greedy: bool = False, lib=None) -> dict:
     if w["kind"] == "tree":
         return verify_tree(w["target"], w["tree_tokens"], w["paths"], w["dtype"], lib=lib)
     if greedy:
-        return verify_greedy(w["target"], w["draft_tokens"], w["dtype"], lib=lib)
+        return verify_greedy(w["target"], w["draft_tokens"], w["dtype"], lib=lib,
+                             draft_lens=w.get("draft_lens"))
     return verify_chain(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
-                        w["temperature"], w["dtype"], lib=lib)
+                        w["temperature"], w["dtype"], lib=lib, draft_lens=w.get("draft_lens"))

@@ -161,10 +161,17 @@ static void fail_closed_row(int32_t *row, int width, int32_t *n_acc)
     *n_acc = -1;
 }
 
-/* Chain rejection-sampling verify for B requests with k drafts each.
+/* Chain rejection-sampling verify for B requests with up to k drafts each.
  *   target:  [B, k+1, V] logits (row k is the bonus row)
  *   draft:   [B, k, V] logits
  *   draft_tokens [B, k], uniforms [B, k+1] (column k drives the final sample)
+ *   draft_lens [B] (nullable; NULL = k for every request): request b has
+ *     k_b <= k real drafts in a buffer padded to k (TensorRT-LLM walkthrough,
+ *     pad_draft_tokens_for_cuda_graph and the ragged verify_lens).  It is
+ *     verified as a chain of k_b: accept tests on positions 0..k_b-1, column
+ *     k_b of the uniforms drives the final sample, row k_b of the target is
+ *     its bonus row; padded positions are neither read nor checked, and
+ *     their probabilities are NaN.  A length outside [0, k] fails closed.
  *   out_tokens [B, k+1]: accepted drafts, then the corrected/bonus token, -1 pad
  *   out_num_accepted [B]: n_acc in [0, k]; -1 for a request whose draft token
  *     lies outside [0, V) (its row is all -1 and the call returns EBADINDEX)
@@ -173,7 +180,7 @@ static void fail_closed_row(int32_t *row, int width, int32_t *n_acc)
  *     (positions 0..n_acc), and at column k when the final sample is one. */
 int oracle_verify_chain(const void *target, const void *draft, int dtype,
                         const int32_t *draft_tokens, const float *uniforms,
-                        float temperature, int B, int k, int V,
+                        const int32_t *draft_lens, float temperature, int B, int k, int V,
                         int32_t *out_tokens, int32_t *out_num_accepted,
                         double *out_probs, int32_t *out_flags)
 {
@@ -202,8 +209,9 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype,
         if (flags)
             for (int i = 0; i <= k; ++i)
                 flags[i] = 0;
-        int bad = 0;
-        for (int i = 0; i < k; ++i)
+        const int kb = draft_lens ? draft_lens[b] : k;
+        int bad = kb < 0 || kb > k;
+        for (int i = 0; !bad && i < kb; ++i)
             if (x[i] < 0 || x[i] >= V)
                 bad = 1;
         if (bad) {
@@ -214,8 +222,11 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype,
             rc = ORC_EBADINDEX;
             continue;
         }
+        if (out_probs)
+            for (int i = kb; i < k; ++i)
+                out_probs[((size_t)b * k + i) * 2 + 0] = out_probs[((size_t)b * k + i) * 2 + 1] = NAN;
         /* p_i(x_i) and q_i(x_i) for every draft position. */
-        for (int i = 0; i < k; ++i) {
+        for (int i = 0; i < kb; ++i) {
             oracle_softmax(tb + (size_t)i * V * es, dtype, T, V, p);
             oracle_softmax(db + (size_t)i * V * es, dtype, T, V, q);
             double pi = p[x[i]], qi = q[x[i]];
@@ -226,8 +237,8 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype,
             ratio[i] = qi > 0.0 ? pi / qi : INFINITY;
         }
         /* Left to right: accept x_i while r_i < p_i(x_i) / q_i(x_i). */
-        int j = k;
-        for (int i = 0; i < k; ++i) {
+        int j = kb;
+        for (int i = 0; i < kb; ++i) {
             if (flags && fabs((double)r[i] - ratio[i]) < ACCEPT_TIE)
                 flags[i] = 1;
             if (!((double)r[i] < ratio[i])) {
@@ -235,9 +246,10 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype,
                 break;
             }
         }
-        /* Final token: residual max(0, p_j - q_j) after a rejection, else p_k. */
+        /* Final token: residual max(0, p_j - q_j) after a rejection, else the
+         * bonus row p_{k_b}. */
         oracle_softmax(tb + (size_t)j * V * es, dtype, T, V, p);
-        if (j < k) {
+        if (j < kb) {
             oracle_softmax(db + (size_t)j * V * es, dtype, T, V, q);
             for (int t = 0; t < V; ++t)
                 w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0;
@@ -245,9 +257,9 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype,
             memcpy(w, p, sizeof(double) * (size_t)V);
         }
         int32_t tie = 0;
-        int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);
+        int tok = oracle_inverse_cdf(w, V, (double)r[kb], SAMPLE_TIE, &tie);
         if (tok < 0) /* residual mass vanished numerically: fall back to p_j */
-            tok = oracle_inverse_cdf(p, V, (double)r[k], SAMPLE_TIE, &tie);
+            tok = oracle_inverse_cdf(p, V, (double)r[kb], SAMPLE_TIE, &tie);
         if (flags)
             flags[k] = tie;
         for (int i = 0; i < j; ++i)
@@ -262,9 +274,12 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype,
 }
 
 /* Greedy chain verify: g_i = argmax target[b,i,:]; n_acc = the longest prefix
- * with g_i == d_i; output d_0..d_{n_acc-1}, g_{n_acc}, -1 pad. */
+ * with g_i == d_i; output d_0..d_{n_acc-1}, g_{n_acc}, -1 pad.  draft_lens
+ * (nullable) as for the chain: request b has k_b real drafts; a length
+ * outside [0, k] fails closed. */
 int oracle_verify_greedy(const void *target, int dtype, const int32_t *draft_tokens,
-                         int B, int k, int V, int32_t *out_tokens, int32_t *out_num_accepted)
+                         const int32_t *draft_lens, int B, int k, int V, int32_t *out_tokens,
+                         int32_t *out_num_accepted)
 {
     if (!target || !draft_tokens || !out_tokens || !out_num_accepted || B < 1 || k < 1 || V < 2 ||
         (dtype != ORC_F32 && dtype != ORC_BF16))
@@ -275,8 +290,9 @@ int oracle_verify_greedy(const void *target, int dtype, const int32_t *draft_tok
         const char *tb = (const char *)target + (size_t)b * (size_t)(k + 1) * (size_t)V * es;
         const int32_t *d = draft_tokens + (size_t)b * k;
         int32_t *out = out_tokens + (size_t)b * (k + 1);
-        int bad = 0;
-        for (int i = 0; i < k; ++i)
+        const int kb = draft_lens ? draft_lens[b] : k;
+        int bad = kb < 0 || kb > k;
+        for (int i = 0; !bad && i < kb; ++i)
             if (d[i] < 0 || d[i] >= V)
                 bad = 1;
         if (bad) {
@@ -285,7 +301,7 @@ int oracle_verify_greedy(const void *target, int dtype, const int32_t *draft_tok
             continue;
         }
         int j = 0;
-        while (j < k && oracle_argmax(tb + (size_t)j * V * es, dtype, V) == d[j])
+        while (j < kb && oracle_argmax(tb + (size_t)j * V * es, dtype, V) == d[j])
             ++j;
         for (int i = 0; i < j; ++i)
             out[i] = d[i];
@@ -469,4 +485,46 @@ int oracle_philox_uniforms(const uint64_t *seeds, const uint64_t *offsets, int B
         }
     }
     return ORC_OK;
+}
+
+/* Paged rollback (TensorRT-LLM walkthrough, rewind_cache: the logical length
+ * shrinks, the block count needed is recomputed from tokens_per_block and
+ * only the whole surplus blocks are returned, nothing is zeroed; the vLLM
+ * learning book's free_extra_blocks_for_request keeps ceil(tokens /
+ * block_size) blocks likewise).  Per request: k_b = draft_lens[b] (or k when
+ * NULL); new_len = old + n + 1, rewind = k_b - n, and, when blocks_held is
+ * given, free_blocks = max(0, blocks_held - ceil(new_len / tokens_per_block)).
+ * An entry with k_b outside [0, k] or n outside [0, k_b] keeps its length
+ * (rewind 0, free 0) and the call returns EBADINDEX. */
+int oracle_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
+                          const int32_t *draft_lens, int k, const int32_t *blocks_held,
+                          int tokens_per_block, int B, int32_t *new_lens, int32_t *rewind_lens,
+                          int32_t *free_blocks)
+{
+    if (!old_lens || !num_accepted || !new_lens || B < 1 || k < 0 || tokens_per_block < 1)
+        return ORC_EINVAL;
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const int32_t kb = draft_lens ? draft_lens[b] : k;
+        const int32_t n = num_accepted[b];
+        if (kb < 0 || kb > k || n < 0 || n > kb) {
+            new_lens[b] = old_lens[b];
+            if (rewind_lens)
+                rewind_lens[b] = 0;
+            if (free_blocks)
+                free_blocks[b] = 0;
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        const long long len = (long long)old_lens[b] + n + 1;
+        new_lens[b] = (int32_t)len;
+        if (rewind_lens)
+            rewind_lens[b] = kb - n;
+        if (free_blocks) {
+            const long long need = (len + tokens_per_block - 1) / tokens_per_block;
+            const long long spare = blocks_held ? (long long)blocks_held[b] - need : 0;
+            free_blocks[b] = spare > 0 ? (int32_t)spare : 0;
+        }
+    }
+    return rc;
 }
