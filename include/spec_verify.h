@@ -139,6 +139,73 @@ int spec_verify_chain_philox(const void *target_logits, const void *draft_logits
                              int32_t *seq_lens, void *workspace, size_t workspace_bytes,
                              spec_stream_t stream);
 
+/* Parameters of spec_verify_chain_ex: those of spec_verify_chain and
+ * spec_verify_chain_philox in one struct, plus ragged draft lengths.  Set
+ * size = sizeof(spec_chain_params); fields a later version adds go at the
+ * end.
+ *   draft_lens [B] int32 or NULL: request b has k_b <= k real drafts in the
+ *     buffers padded to k (TensorRT-LLM walkthrough: the real draft count is
+ *     kept apart from the padded buffer, pad_draft_tokens_for_cuda_graph; the
+ *     verified window is per request, verify_lens).  It is verified as a chain
+ *     of k_b: accept tests on positions 0..k_b-1, the final draw uses uniform
+ *     column (or Philox index) k_b and target row k_b is its bonus row.  Rows
+ *     past k_b are not read (pass 1 skips them) and their draft tokens are not
+ *     checked; out_probs there is NaN.  A length outside [0, k] fails the
+ *     request closed (SPEC_EBADINDEX in the status word).
+ *   uniforms or (seeds, offsets): exactly as in the two calls above; when
+ *     uniforms is NULL both seeds and offsets are required. */
+typedef struct spec_chain_params {
+    size_t size;
+    const void *target_logits;  /* [B, k+1, V] */
+    const void *draft_logits;   /* [B, k, V] */
+    int dtype;
+    const int32_t *draft_tokens; /* [B, k] */
+    const int32_t *draft_lens;   /* [B] or NULL */
+    const float *uniforms;       /* [B, k+1] or NULL */
+    const uint64_t *seeds;       /* [B] when uniforms is NULL */
+    const uint64_t *offsets;     /* [B] when uniforms is NULL */
+    float temperature;
+    int B, k, V;
+    int32_t *out_tokens;         /* [B, k+1] */
+    int32_t *out_num_accepted;   /* [B] */
+    float *out_probs;            /* [B, k, 2] or NULL */
+    int32_t *seq_lens;           /* [B] or NULL */
+} spec_chain_params;
+int spec_verify_chain_ex(const spec_chain_params *params, void *workspace,
+                         size_t workspace_bytes, spec_stream_t stream);
+
+/* Parameters of spec_verify_greedy_ex: spec_verify_greedy's plus ragged
+ * draft lengths (as in spec_chain_params: a request with k_b drafts is
+ * greedy-verified over positions 0..k_b-1 and its bonus token is the argmax
+ * of target row k_b; rows past k_b are not read). */
+typedef struct spec_greedy_params {
+    size_t size;
+    const void *target_logits;   /* [B, k+1, V] */
+    int dtype;
+    const int32_t *draft_tokens; /* [B, k] */
+    const int32_t *draft_lens;   /* [B] or NULL */
+    int B, k, V;
+    int32_t *out_tokens;         /* [B, k+1] */
+    int32_t *out_num_accepted;   /* [B] */
+    int32_t *seq_lens;           /* [B] or NULL */
+} spec_greedy_params;
+int spec_verify_greedy_ex(const spec_greedy_params *params, void *workspace,
+                          size_t workspace_bytes, spec_stream_t stream);
+
+/* Rollback with ragged draft lengths and paged block accounting
+ * (TensorRT-LLM walkthrough: update_requests sets rewind = verified_len -
+ * accepted; rewind_cache recomputes the blocks needed from tokens_per_block
+ * and returns only whole surplus blocks, clearing nothing).
+ *   k_b = draft_lens[b] (or k when NULL); new_lens = old_lens + n + 1;
+ *   rewind_lens (nullable) = k_b - n; free_blocks (nullable) = max(0,
+ *   blocks_held[b] - ceil(new_len / tokens_per_block)), 0 when blocks_held is
+ *   NULL.  new_lens may alias old_lens.  An entry with k_b outside [0, k] or
+ *   n outside [0, k_b] keeps its length (rewind 0, free 0). */
+int spec_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
+                        const int32_t *draft_lens, int k, const int32_t *blocks_held,
+                        int tokens_per_block, int B, int32_t *new_lens, int32_t *rewind_lens,
+                        int32_t *free_blocks, spec_stream_t stream);
+
 /* The uniforms spec_verify_chain_philox draws: out[b, i] for i = 0..n-1
  * (n <= SPEC_MAX_DRAFT + 1), from the same per-request Philox streams, so a
  * caller can log or replay a step's randomness. */

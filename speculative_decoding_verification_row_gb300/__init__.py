@@ -38,8 +38,30 @@ SPEC_MAX_PATH_LEN = 64
 SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_greedy", "spec_verify_tree", "spec_rollback_lengths",
            "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc",
-           "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms")
+           "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
+           "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged")
 SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+class ChainParams(ctypes.Structure):
+    """spec_chain_params (include/spec_verify.h), field for field."""
+    _fields_ = [("size", ctypes.c_size_t), ("target_logits", ctypes.c_void_p),
+                ("draft_logits", ctypes.c_void_p), ("dtype", ctypes.c_int),
+                ("draft_tokens", ctypes.c_void_p), ("draft_lens", ctypes.c_void_p),
+                ("uniforms", ctypes.c_void_p), ("seeds", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("temperature", ctypes.c_float),
+                ("B", ctypes.c_int), ("k", ctypes.c_int), ("V", ctypes.c_int),
+                ("out_tokens", ctypes.c_void_p), ("out_num_accepted", ctypes.c_void_p),
+                ("out_probs", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p)]
+
+
+class GreedyParams(ctypes.Structure):
+    """spec_greedy_params (include/spec_verify.h), field for field."""
+    _fields_ = [("size", ctypes.c_size_t), ("target_logits", ctypes.c_void_p),
+                ("dtype", ctypes.c_int), ("draft_tokens", ctypes.c_void_p),
+                ("draft_lens", ctypes.c_void_p), ("B", ctypes.c_int), ("k", ctypes.c_int),
+                ("V", ctypes.c_int), ("out_tokens", ctypes.c_void_p),
+                ("out_num_accepted", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p)]
+
 
 _lock = threading.Lock()
 _lib = None
@@ -65,11 +87,15 @@ def _bind(lib):
     lib.spec_relocate_accepted_kv.argtypes = [P, S, I, I, P, I, P, P, P, I, I, P]
     lib.spec_verify_chain_philox.argtypes = [P, P, I, P, P, P, ctypes.c_float, I, I, I, P, P, P, P, P, S, P]
     lib.spec_philox_uniforms.argtypes = [P, P, I, I, P, P]
+    lib.spec_verify_chain_ex.argtypes = [ctypes.POINTER(ChainParams), P, S, P]
+    lib.spec_verify_greedy_ex.argtypes = [ctypes.POINTER(GreedyParams), P, S, P]
+    lib.spec_rollback_paged.argtypes = [P, P, P, I, P, I, I, P, P, P, P]
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
               "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc",
-              "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms"):
+              "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
+              "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged"):
         getattr(lib, f).restype = I
     return lib
 
@@ -170,12 +196,13 @@ def default_workspace(device, stream_handle) -> Workspace:
 def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
                  out_tokens=None, out_num_accepted=None, out_probs=None, want_probs=False,
                  seq_lens=None, workspace: Workspace | None = None, stream=None,
-                 seeds=None, offsets=None):
+                 seeds=None, offsets=None, draft_lens=None):
     """Chain rejection-sampling verify; returns (tokens [B,k+1], num_accepted [B], probs [B,k,2] or None).
 
     seq_lens (int32 [B], optional) is advanced in place by n_acc + 1.  With
     uniforms=None, seeds and offsets (int64 [B]) select each request's Philox
-    stream and the uniforms are drawn inside the kernel."""
+    stream and the uniforms are drawn inside the kernel.  draft_lens (int32
+    [B], optional): each request's real draft length (ragged verify)."""
     t = _dev(target_logits, "target_logits")
     if t.dim() != 3:
         raise ValueError("target_logits must be [B, k+1, V]")
@@ -200,7 +227,16 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
     sh, _ = _stream_handle(stream, dev)
     ws = workspace or default_workspace(dev, sh)
     buf = ws.ensure(B, 2 * k + 1, V, sh)
-    if uniforms is not None:
+    if draft_lens is not None:
+        lens = _dev(draft_lens, "draft_lens", torch.int32, (B,))
+        prm = ChainParams(ctypes.sizeof(ChainParams), _ptr(t), _ptr(d), code, _ptr(x), _ptr(lens),
+                          _ptr(u) if uniforms is not None else None,
+                          None if uniforms is not None else _ptr(sd),
+                          None if uniforms is not None else _ptr(of), float(temperature), B, k, V,
+                          _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens))
+        rc = lib().spec_verify_chain_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
+        name = "spec_verify_chain_ex"
+    elif uniforms is not None:
         rc = lib().spec_verify_chain(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
                                      B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens),
                                      _ptr(buf), buf.numel(), sh)
@@ -248,8 +284,10 @@ def verify_chain_noalloc(target_logits, draft_logits, draft_tokens, uniforms, te
 
 
 def verify_greedy(target_logits, draft_tokens, *, out_tokens=None, out_num_accepted=None,
-                  seq_lens=None, workspace: Workspace | None = None, stream=None):
-    """Greedy chain verify; returns (tokens [B,k+1], num_accepted [B])."""
+                  seq_lens=None, workspace: Workspace | None = None, stream=None,
+                  draft_lens=None):
+    """Greedy chain verify; returns (tokens [B,k+1], num_accepted [B]).
+    draft_lens (int32 [B], optional): each request's real draft length."""
     t = _dev(target_logits, "target_logits")
     if t.dim() != 3:
         raise ValueError("target_logits must be [B, k+1, V]")
@@ -265,8 +303,14 @@ def verify_greedy(target_logits, draft_tokens, *, out_tokens=None, out_num_accep
     sh, _ = _stream_handle(stream, dev)
     ws = workspace or default_workspace(dev, sh)
     buf = ws.ensure(B, k + 1, V, sh)
-    rc = lib().spec_verify_greedy(_ptr(t), code, _ptr(x), B, k, V, _ptr(tok), _ptr(n),
-                                  _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
+    if draft_lens is not None:
+        lens = _dev(draft_lens, "draft_lens", torch.int32, (B,))
+        prm = GreedyParams(ctypes.sizeof(GreedyParams), _ptr(t), code, _ptr(x), _ptr(lens), B, k, V,
+                           _ptr(tok), _ptr(n), _ptr(seq_lens))
+        rc = lib().spec_verify_greedy_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
+    else:
+        rc = lib().spec_verify_greedy(_ptr(t), code, _ptr(x), B, k, V, _ptr(tok), _ptr(n),
+                                      _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_verify_greedy", rc)
     return tok, n
@@ -344,6 +388,27 @@ def relocate_accepted_kv(kv_pool, block_tables, base_lens, accepted_nodes, num_a
     if rc != SPEC_OK:
         raise SpecError("spec_relocate_accepted_kv", rc)
     return kv_pool
+
+
+def rollback_paged(old_lens, num_accepted, k: int, tokens_per_block: int, *, draft_lens=None,
+                   blocks_held=None, new_lens=None, rewind_lens=None, free_blocks=None,
+                   stream=None):
+    """Rollback with ragged draft lengths and paged block accounting; returns
+    (new_lens [B], rewind_lens [B], free_blocks [B])."""
+    o = _dev(old_lens, "old_lens", torch.int32)
+    B = o.shape[0]
+    n = _dev(num_accepted, "num_accepted", torch.int32, (B,))
+    lens = None if draft_lens is None else _dev(draft_lens, "draft_lens", torch.int32, (B,))
+    held = None if blocks_held is None else _dev(blocks_held, "blocks_held", torch.int32, (B,))
+    new = _out(new_lens, "new_lens", (B,), torch.int32, o.device)
+    rew = _out(rewind_lens, "rewind_lens", (B,), torch.int32, o.device)
+    fre = _out(free_blocks, "free_blocks", (B,), torch.int32, o.device)
+    sh, _ = _stream_handle(stream, o.device)
+    rc = lib().spec_rollback_paged(_ptr(o), _ptr(n), _ptr(lens), int(k), _ptr(held),
+                                   int(tokens_per_block), B, _ptr(new), _ptr(rew), _ptr(fre), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_rollback_paged", rc)
+    return new, rew, fre
 
 
 def philox_uniforms(seeds, offsets, n: int, *, stream=None):

@@ -57,6 +57,31 @@ __global__ void rollback_kernel(const int32_t* old_lens, const int32_t* n_acc, i
   if (rewind_lens) rewind_lens[b] = k - n;
 }
 
+// Rollback with ragged draft lengths and paged block accounting: rewind =
+// k_b - n, and the blocks past ceil(new_len / tokens_per_block) are free.
+__global__ void rollback_paged_kernel(const int32_t* old_lens, const int32_t* n_acc,
+                                      const int32_t* draft_lens, int k,
+                                      const int32_t* blocks_held, int tpb, int B,
+                                      int32_t* new_lens, int32_t* rewind_lens,
+                                      int32_t* free_blocks) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int32_t kb = draft_lens ? draft_lens[b] : k, n = n_acc[b], old = old_lens[b];
+  if (kb < 0 || kb > k || n < 0 || n > kb) {
+    new_lens[b] = old;
+    if (rewind_lens) rewind_lens[b] = 0;
+    if (free_blocks) free_blocks[b] = 0;
+    return;
+  }
+  const long long len = (long long)old + n + 1;
+  new_lens[b] = (int32_t)len;
+  if (rewind_lens) rewind_lens[b] = kb - n;
+  if (free_blocks) {
+    const long long spare = blocks_held ? blocks_held[b] - (len + tpb - 1) / tpb : 0;
+    free_blocks[b] = spare > 0 ? (int32_t)spare : 0;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -81,7 +106,8 @@ namespace {
 // request's uniforms drawn in the kernel from its Philox (seed, offset).
 int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
                const int32_t* draft_tokens, const float* uniforms, const uint64_t* seeds,
-               const uint64_t* offsets, float temperature, int B, int k, int V,
+               const uint64_t* offsets, const int32_t* draft_lens, float temperature, int B,
+               int k, int V,
                int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
                int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream) {
   if (!target_logits || !draft_logits || !draft_tokens || (!uniforms && (!seeds || !offsets)) ||
@@ -107,6 +133,7 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
   a.uniforms = uniforms;
   a.seeds = reinterpret_cast<const unsigned long long*>(seeds);
   a.offsets = reinterpret_cast<const unsigned long long*>(offsets);
+  a.draft_lens = draft_lens;
   a.B = B;
   a.k = k;
   a.V = V;
@@ -151,8 +178,8 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
                       size_t workspace_bytes, spec_stream_t stream) {
   if (!uniforms) return SPEC_EINVAL;
   return chain_impl(target_logits, draft_logits, dtype, draft_tokens, uniforms, nullptr, nullptr,
-                    temperature, B, k, V, out_tokens, out_num_accepted, out_probs, seq_lens,
-                    workspace, workspace_bytes, stream);
+                    nullptr, temperature, B, k, V, out_tokens, out_num_accepted, out_probs,
+                    seq_lens, workspace, workspace_bytes, stream);
 }
 
 int spec_verify_chain_philox(const void* target_logits, const void* draft_logits, int dtype,
@@ -163,14 +190,18 @@ int spec_verify_chain_philox(const void* target_logits, const void* draft_logits
                              spec_stream_t stream) {
   if (!seeds || !offsets) return SPEC_EINVAL;
   return chain_impl(target_logits, draft_logits, dtype, draft_tokens, nullptr, seeds, offsets,
-                    temperature, B, k, V, out_tokens, out_num_accepted, out_probs, seq_lens,
-                    workspace, workspace_bytes, stream);
+                    nullptr, temperature, B, k, V, out_tokens, out_num_accepted, out_probs,
+                    seq_lens, workspace, workspace_bytes, stream);
 }
 
-int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens, int B,
-                       int k, int V, int32_t* out_tokens, int32_t* out_num_accepted,
-                       int32_t* seq_lens, void* workspace, size_t workspace_bytes,
-                       spec_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int greedy_impl(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                const int32_t* draft_lens, int B, int k, int V, int32_t* out_tokens,
+                int32_t* out_num_accepted, int32_t* seq_lens, void* workspace,
+                size_t workspace_bytes, spec_stream_t stream) {
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
   if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || k < 1 ||
       k > SPEC_MAX_DRAFT || V < 2)
@@ -187,6 +218,7 @@ int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draf
   a.V = V;
   a.tree = 0;
   a.draft_tokens = draft_tokens;
+  a.draft_lens = draft_lens;
   a.k = k;
   a.out_tokens = out_tokens;
   a.out_n = out_num_accepted;
@@ -194,6 +226,48 @@ int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draf
   a.ws = ws_views(workspace, WsLayout(B, R, V));
   return launch_argmax(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
                                                                            : SPEC_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens, int B,
+                       int k, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                       int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                       spec_stream_t stream) {
+  return greedy_impl(target_logits, dtype, draft_tokens, nullptr, B, k, V, out_tokens,
+                     out_num_accepted, seq_lens, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_greedy_ex(const spec_greedy_params* p, void* workspace, size_t workspace_bytes,
+                          spec_stream_t stream) {
+  if (!p || p->size < sizeof(spec_greedy_params)) return SPEC_EINVAL;
+  return greedy_impl(p->target_logits, p->dtype, p->draft_tokens, p->draft_lens, p->B, p->k,
+                     p->V, p->out_tokens, p->out_num_accepted, p->seq_lens, workspace,
+                     workspace_bytes, stream);
+}
+
+int spec_verify_chain_ex(const spec_chain_params* p, void* workspace, size_t workspace_bytes,
+                         spec_stream_t stream) {
+  if (!p || p->size < sizeof(spec_chain_params)) return SPEC_EINVAL;
+  return chain_impl(p->target_logits, p->draft_logits, p->dtype, p->draft_tokens, p->uniforms,
+                    p->seeds, p->offsets, p->draft_lens, p->temperature, p->B, p->k, p->V,
+                    p->out_tokens, p->out_num_accepted, p->out_probs, p->seq_lens, workspace,
+                    workspace_bytes, stream);
+}
+
+int spec_rollback_paged(const int32_t* old_lens, const int32_t* num_accepted,
+                        const int32_t* draft_lens, int k, const int32_t* blocks_held,
+                        int tokens_per_block, int B, int32_t* new_lens, int32_t* rewind_lens,
+                        int32_t* free_blocks, spec_stream_t stream) {
+  if (!old_lens || !num_accepted || !new_lens || B < 1 || B > SPEC_MAX_BATCH || k < 0 ||
+      tokens_per_block < 1)
+    return SPEC_EINVAL;
+  rollback_paged_kernel<<<ceil_div(B, 256), 256, 0, (cudaStream_t)stream>>>(
+      old_lens, num_accepted, draft_lens, k, blocks_held, tokens_per_block, B, new_lens,
+      rewind_lens, free_blocks);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 int spec_verify_tree(const void* target_logits, int dtype, const int32_t* tree_tokens,

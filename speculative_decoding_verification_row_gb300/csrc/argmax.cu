@@ -78,6 +78,12 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
   __shared__ int sAcc[kWarps], sPath[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = a.R, ns = a.nsplit;
+  // Ragged greedy: kb <= k real drafts, rows 0..kb; a length outside [0, k]
+  // fails closed.
+  const int kraw = !a.tree && a.draft_lens ? a.draft_lens[b] : a.k;
+  const bool bad_len = !a.tree && (kraw < 0 || kraw > a.k);
+  const int kb = bad_len ? 0 : kraw;
+  const int rows = a.tree ? R : (bad_len ? 0 : kb + 1);
   // Inputs first (they do not depend on pass 1).
   const int nt = a.tree ? R : a.k;
   const int32_t* tsrc = a.tree ? a.tree_tokens + (size_t)b * R : a.draft_tokens + (size_t)b * a.k;
@@ -95,17 +101,17 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
   // of a hang.
   unsigned long long* words = reinterpret_cast<unsigned long long*>(a.ws.part) +
                               (size_t)b * R * ns;
-  for (int i0 = threadIdx.x; i0 < R * ns; i0 += 4 * kThreads) {
+  for (int i0 = threadIdx.x; i0 < rows * ns; i0 += 4 * kThreads) {
     unsigned long long w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = i0 + q * kThreads;
-      w[q] = i < R * ns ? ld_relaxed_u64(words + i) : 0;
+      w[q] = i < rows * ns ? ld_relaxed_u64(words + i) : 0;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = i0 + q * kThreads;
-      if (i >= R * ns) continue;
+      if (i >= rows * ns) continue;
       if (!w[q]) {
         const long long t0 = clock64();
         while (!(w[q] = ld_relaxed_u64(words + i))) {
@@ -129,7 +135,8 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
 
   if (!a.tree) {  // ---------------------------------------------- greedy chain
     const int k = a.k;
-    for (int i = threadIdx.x; i < k; i += kThreads)
+    if (threadIdx.x == 0 && bad_len) sBad = 1;
+    for (int i = threadIdx.x; i < kb; i += kThreads)
       if (sTok[i] < 0 || sTok[i] >= a.V) sBad = 1;
     __syncthreads();
     if (sBad) {
@@ -138,7 +145,7 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
     }
     if (threadIdx.x == 0) {
       int j = 0;
-      while (j < k && key_index(sKey[j]) == sTok[j]) ++j;
+      while (j < kb && key_index(sKey[j]) == sTok[j]) ++j;
       int32_t* out = a.out_tokens + (size_t)b * (k + 1);
       for (int i = 0; i <= k; ++i) out[i] = i < j ? sTok[i] : (i == j ? key_index(sKey[j]) : -1);
       a.out_n[b] = j;
@@ -223,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, 5) argmax_kernel(const ArgmaxArgs a)
   const int rem = blockIdx.x - b * per_req;
   const int r = rem / a.nsplit;
   const int s = rem - r * a.nsplit;
+  if (!a.tree && a.draft_lens) {  // ragged greedy: rows past the draft length are not verified
+    const int kb = a.draft_lens[b];
+    if (kb < 0 || kb > a.k || r > kb) return;
+  }
   const char* row = a.target + ((size_t)b * a.R + r) * (size_t)a.V * IO::ES;
   const int vbeg = s * a.vps;
   const int vend = min(a.nvec, vbeg + a.vps);

@@ -120,6 +120,10 @@ __global__ void __launch_bounds__(kThreads, 6) chain_rowstats_kernel(const Chain
   const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
   int b, r;
   slice_row(a, rr, b, r);
+  if (a.draft_lens) {  // ragged: rows past the request's draft length are not verified
+    const int kb = a.draft_lens[b];
+    if (kb < 0 || kb > a.k || (r <= a.k ? r > kb : r - a.k - 1 >= kb)) return;
+  }
   const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
   const int vbeg = s * a.vps;
   const int vend = min(a.nvec, vbeg + a.vps);
@@ -500,10 +504,15 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   const int k = a.k, R = 2 * k + 1;
   const size_t row_bytes = (size_t)a.V * ES;
 
+  // Ragged verify: this request has kb <= k real drafts; rows past them were
+  // not streamed and are not read.  A length outside [0, k] fails closed.
+  const int kraw = a.draft_lens ? a.draft_lens[b] : k;
+  const bool bad_len = kraw < 0 || kraw > k;
+  const int kb = bad_len ? 0 : kraw;
   // Gather the logits of x_i (inputs only, so before the wait on pass 1).
   float xp = 0.f, xq = 0.f;
-  bool bad = false;
-  if (tid < k) {
+  bool bad = bad_len;
+  if (tid < kb) {
     const int x = a.tokens[(size_t)b * k + tid];
     bad = x < 0 || x >= a.V;
     if (!bad) {
@@ -514,14 +523,17 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   if (tid <= k)
     sU[tid] = a.uniforms ? a.uniforms[(size_t)b * (k + 1) + tid]
                          : philox_uniform(a.seeds[b], a.offsets[b], tid);
-  if (tid == 0) sBad = 0;
+  if (tid == 0) sBad = bad_len;
+  // Rows this request verifies: target rows 0..kb, draft rows 0..kb-1.
+  auto used = [&](int r) { return r <= k ? r <= kb : r - k - 1 < kb; };
+  const int rows = bad_len ? 0 : R;
   // Merge the slice statistics of every row of the request, in a fixed
   // order, as they arrive: warp w takes rows w, w+8, ...; it issues the loads
   // of four rows' words before using any (waiting only for words still 0),
   // takes each row max with shuffles, then adds S_s * 2^(c(m_s - M)) with one
   // exp per slice (no chain of exps).
   const unsigned long long* sb = a.ws.stats + (size_t)b * R * a.nsplit;
-  for (int r0 = warp; r0 < R; r0 += 4 * kWarps) {
+  for (int r0 = warp; r0 < rows; r0 += 4 * kWarps) {
     unsigned long long v[4][2];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -529,7 +541,8 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int u = lane + 32 * h;
-        v[q][h] = (r < R && u < a.nsplit) ? ld_relaxed_u64(sb + (size_t)r * a.nsplit + u) : kNoStats;
+        v[q][h] = (r < R && used(r) && u < a.nsplit) ? ld_relaxed_u64(sb + (size_t)r * a.nsplit + u)
+                                                     : kNoStats;
       }
     }
 #pragma unroll
@@ -541,7 +554,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int r = r0 + q * kWarps;
-      if (r >= R) continue;  // the same for the whole warp
+      if (r >= R || !used(r)) continue;  // the same for the whole warp
       const unsigned long long* pr = sb + (size_t)r * a.nsplit;
       const float2 e0 = stats_unpack(v[q][0]), e1 = stats_unpack(v[q][1]);
       float m = fmaxf(e0.x, e1.x);
@@ -566,7 +579,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
     }
   }
   __syncthreads();
-  if (tid < k) {
+  if (tid < kb) {
     if (bad) {
       sBad = 1;
     } else {
@@ -581,14 +594,14 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
     for (int h = 0; h < 2; ++h) {
       const int i = lane + 32 * h;
       bool rj = false;
-      if (i < k) {
+      if (i < kb) {
         const float ratio = sQ[i] > 0.f ? sP[i] / sQ[i] : INFINITY;
         rj = !(sU[i] < ratio);
       }
       rej[h] = __ballot_sync(0xffffffffu, rj);
     }
     if (lane == 0)
-      sJ = sBad ? -1 : rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : k;
+      sJ = sBad ? -1 : rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : kb;
   }
   __syncthreads();
   const int j = sJ;
@@ -598,7 +611,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   if (j >= 0) {
     prow = a.target + ((size_t)b * (k + 1) + j) * row_bytes;
     mp = sM[j];
-    if (j < k) {
+    if (j < kb) {
       qrow = a.draft + ((size_t)b * k + j) * row_bytes;
       mq = sM[k + 1 + j];
       lam = sS[j] / sS[k + 1 + j];
@@ -643,11 +656,11 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
     }
     return;
   }
-  if (a.out_probs && tid < k) {
-    a.out_probs[((size_t)b * k + tid) * 2] = sP[tid];
-    a.out_probs[((size_t)b * k + tid) * 2 + 1] = sQ[tid];
+  if (a.out_probs && tid < k) {  // padded positions are not verified: NaN
+    a.out_probs[((size_t)b * k + tid) * 2] = tid < kb ? sP[tid] : NAN;
+    a.out_probs[((size_t)b * k + tid) * 2 + 1] = tid < kb ? sQ[tid] : NAN;
   }
-  const double u = (double)sU[k];
+  const double u = (double)sU[kb];
   const int tok = draw_token<DT, VEC>(a, b, prow, qrow, mp, mq, lam, u);
   for (int i = tid; i <= k; i += kThreads)
     out[i] = i < j ? a.tokens[(size_t)b * k + i] : (i == j ? tok : -1);

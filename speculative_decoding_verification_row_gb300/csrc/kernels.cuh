@@ -12,6 +12,7 @@ struct ChainArgs {
   const float* uniforms;                      // [B, k+1], or null: Philox per request
   const unsigned long long* seeds;            // [B] Philox keys (when uniforms is null)
   const unsigned long long* offsets;          // [B] Philox counters (when uniforms is null)
+  const int32_t* draft_lens;                  // [B] real draft lengths (ragged), or null: k
   float c_hi, c_lo;  // log2(e)/T split as hi + lo
   int B, k, V;
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
@@ -29,6 +30,7 @@ struct ArgmaxArgs {
   int nvec, nsplit, vps;
   int tree;                    // 0: greedy chain, 1: tree
   const int32_t* draft_tokens; // greedy: [B, k]
+  const int32_t* draft_lens;   // greedy: [B] real draft lengths (ragged), or null: k
   int k;
   const int32_t* tree_tokens;  // tree: [B, N]
   const int32_t* paths;        // tree: [B, P, L]

@@ -132,3 +132,30 @@ def test_relocate_rejects_bad_arguments_before_launch():
     assert call(B=0) == sv.SPEC_EINVAL
     assert call(L=65) == sv.SPEC_EINVAL
     assert call(tpb=0) == sv.SPEC_EINVAL
+
+
+def test_param_structs_match_the_header(tmp_path):
+    # The binding's ctypes mirrors of spec_chain_params / spec_greedy_params
+    # must have the header's size and field offsets.
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    fields = {"spec_chain_params": sv.ChainParams, "spec_greedy_params": sv.GreedyParams}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "spec_verify.h"', "int main(void) {"]
+    for cname, py in fields.items():
+        lines.append(f'  printf("%zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'  printf("%zu\\n", offsetof({cname}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    want = []
+    for py in fields.values():
+        want.append(ctypes.sizeof(py))
+        want += [getattr(py, f).offset for f, _ in py._fields_]
+    assert got == want

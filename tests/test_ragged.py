@@ -107,3 +107,115 @@ def test_paged_rollback_closed_forms():
     a = oracle.rollback(old, n, 7)
     b = oracle.rollback_paged(old, n, 7, tokens_per_block=16)
     assert np.array_equal(a["new_lens"], b["new_lens"]) and np.array_equal(a["rewind_lens"], b["rewind_lens"])
+
+
+# ------------------------------------------------------------------ GPU parity
+def _ragged_workload(name, seed, **over):
+    w = workloads.make(name, seed=seed, **over)
+    rng = np.random.default_rng(seed)
+    k = w["k"]
+    lens = rng.integers(0, k + 1, size=w["B"]).astype(np.int32)
+    lens[0], lens[-1] = 0, k
+    x = w["draft_tokens"].copy()
+    for b in range(w["B"]):
+        x[b, lens[b]:] = -3 if b % 2 else w["V"] + 11   # padding outside [0, V): never checked
+    w["draft_tokens"] = x
+    w["draft_lens"] = lens
+    return w
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("philox", [False, True])
+@pytest.mark.parametrize("name,over", [("chain_b64_k7_v128256_bf16", dict(B=24, V=30000)),
+                                       ("chain_b8_k4_v32000_f32", dict(V=9000)),
+                                       ("chain_b256_k3_v129280_bf16", dict(B=40, V=20000))])
+def test_chain_ragged_matches_oracle(name, over, philox):
+    import speculative_decoding_verification_row_gb300 as sv
+    from test_gpu_parity import check_chain, to_dev, i32
+    w = _ragged_workload(name, 31, **over)
+    B, k = w["B"], w["k"]
+    kw = {}
+    if philox:
+        seeds = np.full(B, 77, dtype=np.int64)
+        offsets = np.arange(B, dtype=np.int64) * 1000 + 5
+        w["uniforms"] = oracle.philox_uniforms(seeds.view(np.uint64), offsets.view(np.uint64), k + 1)
+        kw = dict(seeds=torch.from_numpy(seeds).cuda(), offsets=torch.from_numpy(offsets).cuda())
+        u = None
+    else:
+        u = torch.from_numpy(w["uniforms"]).cuda()
+    seq = i32(w["seq_lens"])
+    tok, n, probs = sv.verify_chain(to_dev(w["target"], w["dtype"]), to_dev(w["draft"], w["dtype"]),
+                                    i32(w["draft_tokens"]), u, w["temperature"], want_probs=True,
+                                    seq_lens=seq, draft_lens=i32(w["draft_lens"]), **kw)
+    torch.cuda.synchronize()
+    o = oracle.verify(w)
+    assert o["rc"] == oracle.OK                      # padding tokens are never checked
+    g = dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(), probs=probs.cpu().numpy(),
+             seq_lens=seq.cpu().numpy())
+    pad = np.isnan(o["probs"])
+    assert np.array_equal(np.isnan(g["probs"]), pad)  # padded positions are NaN on both sides
+    g["probs"][pad] = 0.0
+    o = dict(o, probs=np.where(pad, 0.0, o["probs"]))
+    check_chain(w, g, o, f"ragged {name}{' philox' if philox else ''}")
+
+
+@pytest.mark.gpu
+def test_chain_ragged_bad_length_fails_closed():
+    import speculative_decoding_verification_row_gb300 as sv
+    from test_gpu_parity import to_dev, i32
+    w = _ragged_workload("chain_b64_k7_v128256_bf16", 5, B=6, V=5000)
+    w["draft_lens"][2] = 9                            # > k
+    w["draft_lens"][4] = -1
+    ws = sv.Workspace()
+    tok, n, _ = sv.verify_chain(to_dev(w["target"], w["dtype"]), to_dev(w["draft"], w["dtype"]),
+                                i32(w["draft_tokens"]), torch.from_numpy(w["uniforms"]).cuda(),
+                                w["temperature"], draft_lens=i32(w["draft_lens"]), workspace=ws)
+    torch.cuda.synchronize()
+    o = oracle.verify(w)
+    assert np.array_equal(n.cpu().numpy(), o["num_accepted"])
+    assert np.array_equal(tok.cpu().numpy()[[2, 4]], o["tokens"][[2, 4]])
+    assert n.cpu().numpy()[2] == -1 and n.cpu().numpy()[4] == -1
+    assert sv.last_error(ws) == sv.SPEC_EBADINDEX
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,over", [("chain_b8_k4_v32000_f32", {}),
+                                       ("chain_b64_k7_v128256_bf16", dict(B=16, V=40000))])
+def test_greedy_ragged_matches_oracle(name, over):
+    import speculative_decoding_verification_row_gb300 as sv
+    from test_gpu_parity import to_dev, i32
+    w = _ragged_workload(name, 8, **over)
+    # let some requests accept: copy the target argmax into the draft
+    for b in range(w["B"]):
+        for i in range(w["draft_lens"][b]):
+            if (b + i) % 3:
+                w["draft_tokens"][b, i] = oracle.argmax(w["target"][b, i], w["dtype"])
+    seq = i32(w["seq_lens"])
+    tok, n = sv.verify_greedy(to_dev(w["target"], w["dtype"]), i32(w["draft_tokens"]), seq_lens=seq,
+                              draft_lens=i32(w["draft_lens"]))
+    torch.cuda.synchronize()
+    o = oracle.verify(w, greedy=True)
+    assert np.array_equal(n.cpu().numpy(), o["num_accepted"])
+    assert np.array_equal(tok.cpu().numpy(), o["tokens"])
+    assert (o["num_accepted"] > 0).sum() >= 3
+    want_seq = oracle.rollback(w["seq_lens"], o["num_accepted"], w["k"])["new_lens"]
+    assert np.array_equal(seq.cpu().numpy(), want_seq)
+
+
+@pytest.mark.gpu
+def test_rollback_paged_matches_oracle():
+    import speculative_decoding_verification_row_gb300 as sv
+    rng = np.random.default_rng(12)
+    B, k, tpb = 3000, 7, 16
+    lens = rng.integers(-1, k + 2, size=B).astype(np.int32)
+    n = np.array([rng.integers(-1, max(int(l), 0) + 2) for l in lens], dtype=np.int32)
+    old = rng.integers(0, 5000, size=B).astype(np.int32)
+    held = ((old + k + 1 + tpb - 1) // tpb + rng.integers(0, 3, size=B)).astype(np.int32)
+    want = oracle.rollback_paged(old, n, k, tpb, draft_lens=lens, blocks_held=held)
+    d = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
+    new, rew, fre = sv.rollback_paged(d(old), d(n), k, tpb, draft_lens=d(lens), blocks_held=d(held))
+    torch.cuda.synchronize()
+    assert np.array_equal(new.cpu().numpy(), want["new_lens"])
+    assert np.array_equal(rew.cpu().numpy(), want["rewind_lens"])
+    assert np.array_equal(fre.cpu().numpy(), want["free_blocks"])
+    assert (want["free_blocks"] > 0).any() and (want["rc"] == oracle.EBADINDEX)
