@@ -6,9 +6,10 @@
 // at most kThreads * kVecPerThread vectors (32 KB of bf16/fp32).  One CTA
 // reads one unit with every thread issuing all of its (up to 8) 128-bit loads
 // before using any, so 32 KB per CTA are in flight.  CTAs are numbered
-// request-major, so the units of one request are dispatched together and
-// the per-request epilogue (run by the request's last CTA, found with an
-// atomic ticket; nothing ever waits) overlaps with other requests' streaming.
+// request-major, so the units of one request are dispatched together.  A
+// streaming CTA publishes its unit's result as one nonzero 64-bit word and
+// exits (no fence, no counter); a second grid, launched as a programmatic
+// dependent, polls each request's words and finishes the request.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -39,9 +40,8 @@ __host__ __device__ inline int num_items(int V) { return ceil_div(num_chunks(V),
 // Per-request synchronisation words, 64 bytes apart so that the CTAs of
 // different requests rarely share a line.
 struct ReqSync {
-  int tick1;  // argmax: units of the request that have finished
   int tick2;  // chain: draw items of the request that have finished
-  int pad[14];
+  int pad[15];
 };
 static_assert(sizeof(ReqSync) == 64, "ReqSync layout");
 
@@ -74,20 +74,16 @@ struct WsLayout {
 
 struct Ws {  // typed views of one call's workspace
   int* status;                 // first word of the 256-byte status block
-  unsigned* ticket;            // chain: next unit of the work queue (status block + 64)
-  unsigned* exits;             // chain: CTAs that have left the queue (status block + 128)
   ReqSync* sync;
   unsigned long long* stats;   // chain: packed (M, S) of each row slice, 0 = not yet written
-  float2* part;
+  float2* part;                // argmax: each unit's packed (max, index + 1)
   unsigned long long* chunks;  // draw-weight sum of each 256-token chunk, in 2^-32 units
   unsigned long long* items;   // sum of each draw item's chunks, in 2^-32 units
 };
 
 inline Ws ws_views(void* base, const WsLayout& l) {
   char* p = static_cast<char*>(base);
-  return Ws{reinterpret_cast<int*>(p + l.status),
-            reinterpret_cast<unsigned*>(p + l.status + 64),
-            reinterpret_cast<unsigned*>(p + l.status + 128), reinterpret_cast<ReqSync*>(p + l.sync),
+  return Ws{reinterpret_cast<int*>(p + l.status), reinterpret_cast<ReqSync*>(p + l.sync),
             reinterpret_cast<unsigned long long*>(p + l.stats),
             reinterpret_cast<float2*>(p + l.part),
             reinterpret_cast<unsigned long long*>(p + l.chunks),
@@ -189,20 +185,6 @@ struct Io {
   }
 };
 
-// ---------------------------------------------------------------- (max, sum-exp) merge
-// Merge two partial softmax statistics (m, s) with s = sum 2^(c (x - m)).
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2, float c_hi,
-                                          float c_lo) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) {
-    m = M;
-    s = 0.f;
-    return;
-  }
-  s = s * ex2(scaled(m - M, c_hi, c_lo)) + s2 * ex2(scaled(m2 - M, c_hi, c_lo));
-  m = M;
-}
-
 // ---------------------------------------------------------------- packed fp32 pairs
 // Blackwell executes add/mul/fma on fp32 pairs as one instruction.
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
@@ -226,48 +208,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       : "=f"(r.x), "=f"(r.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
-}
-
-// ---------------------------------------------------------------- mbarrier / bulk copy
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-// Make barrier initialisation visible to the async (bulk copy) proxy.
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::
-                   : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
-// 16) that reports its bytes to `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
 }
 
 // ---------------------------------------------------------------- Philox
@@ -306,30 +246,6 @@ __device__ __forceinline__ float philox_uniform(unsigned long long seed, unsigne
 // that runs out sets SPEC_ETIMEOUT instead of spinning forever.
 constexpr long long kWaitCycles = 2000000000LL;
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
-  return true;
-}
-
-__device__ __forceinline__ int ld_volatile(const int* p) {
-  return *reinterpret_cast<const volatile int*>(p);
-}
-// Device-scope atomic add with release semantics: this thread's earlier writes
-// (and those ordered before it by a CTA barrier) are visible before the add.
-__device__ __forceinline__ int atom_add_release(int* p, int v) {
-  int old;
-  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ void red_add_release(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 // Device-scope relaxed 64-bit accesses (single-copy atomic, no fence).
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -339,52 +255,7 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Barrier of the 256 compute threads (kThreads).  In a block of exactly
-// kThreads threads it is the same as __syncthreads(); in the persistent
-// kernel it leaves the producer warp out.
-__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
 // Record the first data-dependent error of a call.
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
-
-// Ticket for a CTA whose only global write to publish was made by thread 0:
-// thread 0 fences, counts itself in and learns whether it arrived last.
-__device__ __forceinline__ bool last_arrival_t0(int* counter, int expected) {
-  __shared__ int s_last0;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int t = atomicAdd(counter, 1);
-    s_last0 = (t == expected - 1);
-    if (s_last0) {
-      *counter = 0;
-      __threadfence();
-    }
-  }
-  csync();
-  return s_last0 != 0;
-}
-
-// Ticket of the threadfence-reduction pattern: returns true in exactly one CTA
-// of the `expected` CTAs that call it for the same counter (the last to
-// arrive), which then resets the counter for the next call.  No CTA waits.
-__device__ __forceinline__ bool last_arrival(int* counter, int expected) {
-  __shared__ int s_last;
-  __threadfence();  // this thread's global writes are visible device-wide
-  csync();
-  if (threadIdx.x == 0) {
-    const int t = atomicAdd(counter, 1);
-    s_last = (t == expected - 1);
-    if (s_last) *counter = 0;
-  }
-  csync();
-  if (s_last) __threadfence();  // order the epilogue's reads after the ticket
-  return s_last != 0;
-}
 
 }  // namespace sv
