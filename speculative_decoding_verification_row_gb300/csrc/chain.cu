@@ -14,7 +14,8 @@
 //
 // Pass 2, chain_draw_kernel: launched as a programmatic dependent of pass 1
 // (scheduled once every pass-1 CTA has started), one wave of CTAs taking
-// draw items (64 chunks of 256 tokens of one request) in grid-stride order.
+// draw items (64 or more chunks of 256 tokens of one request, sized so that
+// the items of the call fit in one wave where possible) in grid-stride order.
 // For each item a CTA gathers x_i's logits, merges its request's slice
 // statistics as their words arrive (no grid-wide wait: most requests are
 // complete when the grid starts, the rest finish during pass 1's last wave)
@@ -707,13 +708,22 @@ cudaError_t draw_grid(int* grid) {
 }
 
 template <int DT, bool VEC>
-cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t st) {
+cudaError_t launch_chain_t(const ChainArgs& args, cudaStream_t st) {
+  int slots = 0;
+  cudaError_t e = draw_grid<DT, VEC>(&slots);
+  if (e != cudaSuccess) return e;
+  // Draw item size: 64 chunks, doubled until every item fits in one wave of
+  // draw CTAs.  Each item pays the merge and accept-scan latency once, so
+  // with many requests fewer, larger items finish sooner; with few, smaller
+  // items spread each request over more SMs.
+  ChainArgs a = args;
+  while ((long)a.B * a.nsplit2 > slots && a.cpc < a.nchunks) {
+    a.cpc *= 2;
+    a.nsplit2 = ceil_div(a.nchunks, a.cpc);
+  }
   const long g1 = (long)a.B * (2 * a.k + 1) * a.nsplit;
   chain_rowstats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  int slots = 0;
-  e = draw_grid<DT, VEC>(&slots);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long items = (long)a.B * a.nsplit2;
   // Pass 2 may be scheduled once every pass-1 CTA has started; each draw

@@ -26,7 +26,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerThread = 8;    // vectors a thread holds in registers
 constexpr int kUnitVecs = kThreads * kVecPerThread;
 constexpr int kChunk = 256;         // elements per inverse-CDF chunk (32 lanes x 8)
-constexpr int kChunksPerCta = 64;   // chunks of one draw item (8 per warp)
+constexpr int kChunksPerCta = 64;   // chunks of one draw item, at least (the launch may double it)
 
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -34,7 +34,6 @@ __host__ __device__ inline int ceil_div(long a, long b) { return (int)((a + b - 
 // Units per row for the worst case (one element per vector).
 __host__ __device__ inline int max_splits(int V) { return ceil_div(V, kUnitVecs); }
 __host__ __device__ inline int num_chunks(int V) { return ceil_div(V, kChunk); }
-static_assert(kChunksPerCta <= 64, "the draw search scans an item's chunks two per lane");
 __host__ __device__ inline int num_items(int V) { return ceil_div(num_chunks(V), kChunksPerCta); }
 
 // Per-request synchronisation words, 64 bytes apart so that the CTAs of
