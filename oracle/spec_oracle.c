@@ -30,6 +30,10 @@
  *   - rollback lengths .............. TensorRT-LLM walkthrough, update_requests
  *                                     and rewind_cache sections (rewind =
  *                                     verified - accepted; cursor truncation).
+ *   - top-k / top-p filtering ....... TensorRT-LLM walkthrough, rejection-
+ *                                     sampling section (the target must be
+ *                                     filtered exactly as the draft was:
+ *                                     same temperature, top-k, top-p).
  *   - per-request uniforms .......... TensorRT-LLM walkthrough, rejection-
  *                                     sampling section (a Philox state of
  *                                     seed and offset per request); the
@@ -526,5 +530,172 @@ int oracle_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
             free_blocks[b] = spare > 0 ? (int32_t)spare : 0;
         }
     }
+    return rc;
+}
+
+/* One row's filtered distribution (TensorRT-LLM walkthrough, rejection-
+ * sampling section: target and draft are filtered alike).  This library's
+ * reading: the kept set is the top_k tokens ordered by (logit descending,
+ * index ascending); when top_p < 1, only the shortest prefix of that order
+ * whose probability under softmax(z) restricted to the top_k reaches top_p is
+ * kept.  p[t] = exp(z_t - z_max) / sum over the kept set, 0 elsewhere.
+ * *near_tie is set when the top-p cut lies within 1e-6 of top_p.
+ * top_k <= 0 means no filtering (plain softmax). */
+typedef struct {
+    double x;
+    int t;
+} orc_item;
+
+static int orc_item_order(const void *a, const void *b)
+{
+    const orc_item *u = (const orc_item *)a, *v = (const orc_item *)b;
+    if (u->x > v->x)
+        return -1;
+    if (u->x < v->x)
+        return 1;
+    return u->t < v->t ? -1 : (u->t > v->t);
+}
+
+int oracle_filtered_softmax(const void *x, int dtype, double temperature, int V, int top_k,
+                            double top_p, double *p, int32_t *near_tie)
+{
+    if (near_tie)
+        *near_tie = 0;
+    if (top_k <= 0)
+        return oracle_softmax(x, dtype, temperature, V, p);
+    if (!x || !p || V < 1 || !(temperature > 0.0) || !(top_p > 0.0) || top_p > 1.0)
+        return ORC_EINVAL;
+    orc_item *it = malloc(sizeof(orc_item) * (size_t)V);
+    if (!it)
+        return ORC_ENOMEM;
+    for (int t = 0; t < V; ++t) {
+        it[t].x = logit_at(x, dtype, (size_t)t);
+        it[t].t = t;
+    }
+    qsort(it, (size_t)V, sizeof(orc_item), orc_item_order);
+    const int kk = top_k < V ? top_k : V;
+    const double zmax = it[0].x / temperature;
+    double sk = 0.0;
+    for (int i = 0; i < kk; ++i)
+        sk += exp(it[i].x / temperature - zmax);
+    int m = kk;
+    if (top_p < 1.0) {
+        double cum = 0.0;
+        for (int i = 0; i < kk; ++i) {
+            const double pi = exp(it[i].x / temperature - zmax) / sk;
+            const double before = cum;
+            cum += pi;
+            if (cum >= top_p) {
+                m = i + 1;
+                if (near_tie)
+                    *near_tie = fabs(cum - top_p) < 1e-6 || fabs(before - top_p) < 1e-6;
+                break;
+            }
+        }
+    }
+    for (int t = 0; t < V; ++t)
+        p[t] = 0.0;
+    double sm = 0.0;
+    for (int i = 0; i < m; ++i)
+        sm += exp(it[i].x / temperature - zmax);
+    for (int i = 0; i < m; ++i)
+        p[it[i].t] = exp(it[i].x / temperature - zmax) / sm;
+    free(it);
+    return ORC_OK;
+}
+
+/* Chain verify on filtered distributions: oracle_verify_chain with every
+ * target and draft row passed through oracle_filtered_softmax(top_k, top_p)
+ * before the accept tests and the final sample.  A near tie of a top-p cut in
+ * a row that decides position i (its target or draft row) flags column i; one
+ * in the rows of the final sample flags column k. */
+int oracle_verify_chain_filtered(const void *target, const void *draft, int dtype,
+                                 const int32_t *draft_tokens, const float *uniforms,
+                                 float temperature, int top_k, double top_p, int B, int k, int V,
+                                 int32_t *out_tokens, int32_t *out_num_accepted,
+                                 double *out_probs, int32_t *out_flags)
+{
+    if (!target || !draft || !draft_tokens || !uniforms || !out_tokens || !out_num_accepted ||
+        B < 1 || k < 1 || V < 2 || top_k < 1 || !(temperature > 0.0f) || !isfinite(temperature) ||
+        (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_EINVAL;
+    const double T = (double)temperature;
+    double *p = malloc(sizeof(double) * (size_t)V);
+    double *q = malloc(sizeof(double) * (size_t)V);
+    double *w = malloc(sizeof(double) * (size_t)V);
+    double *ratio = malloc(sizeof(double) * (size_t)k);
+    int32_t *rowtie = malloc(sizeof(int32_t) * (size_t)k);
+    if (!p || !q || !w || !ratio || !rowtie) {
+        free(p), free(q), free(w), free(ratio), free(rowtie);
+        return ORC_ENOMEM;
+    }
+    const size_t es = dtype == ORC_F32 ? 4 : 2;
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)b * (size_t)(k + 1) * (size_t)V * es;
+        const char *db = (const char *)draft + (size_t)b * (size_t)k * (size_t)V * es;
+        const int32_t *x = draft_tokens + (size_t)b * k;
+        const float *r = uniforms + (size_t)b * (k + 1);
+        int32_t *out = out_tokens + (size_t)b * (k + 1);
+        int32_t *flags = out_flags ? out_flags + (size_t)b * (k + 1) : NULL;
+        if (flags)
+            for (int i = 0; i <= k; ++i)
+                flags[i] = 0;
+        int bad = 0;
+        for (int i = 0; i < k; ++i)
+            if (x[i] < 0 || x[i] >= V)
+                bad = 1;
+        if (bad) {
+            fail_closed_row(out, k + 1, &out_num_accepted[b]);
+            if (out_probs)
+                for (int i = 0; i < 2 * k; ++i)
+                    out_probs[(size_t)b * 2 * k + i] = NAN;
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        for (int i = 0; i < k; ++i) {
+            int32_t tp = 0, tq = 0;
+            oracle_filtered_softmax(tb + (size_t)i * V * es, dtype, T, V, top_k, top_p, p, &tp);
+            oracle_filtered_softmax(db + (size_t)i * V * es, dtype, T, V, top_k, top_p, q, &tq);
+            const double pi = p[x[i]], qi = q[x[i]];
+            if (out_probs) {
+                out_probs[((size_t)b * k + i) * 2 + 0] = pi;
+                out_probs[((size_t)b * k + i) * 2 + 1] = qi;
+            }
+            ratio[i] = qi > 0.0 ? pi / qi : INFINITY;
+            rowtie[i] = tp || tq;
+        }
+        int j = k;
+        for (int i = 0; i < k; ++i) {
+            if (flags && (fabs((double)r[i] - ratio[i]) < ACCEPT_TIE || rowtie[i]))
+                flags[i] = 1;
+            if (!((double)r[i] < ratio[i])) {
+                j = i;
+                break;
+            }
+        }
+        int32_t tp = 0, tq = 0;
+        oracle_filtered_softmax(tb + (size_t)j * V * es, dtype, T, V, top_k, top_p, p, &tp);
+        if (j < k) {
+            oracle_filtered_softmax(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, q, &tq);
+            for (int t = 0; t < V; ++t)
+                w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0;
+        } else {
+            memcpy(w, p, sizeof(double) * (size_t)V);
+        }
+        int32_t tie = 0;
+        int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);
+        if (tok < 0)
+            tok = oracle_inverse_cdf(p, V, (double)r[k], SAMPLE_TIE, &tie);
+        if (flags)
+            flags[k] = tie || tp || tq;
+        for (int i = 0; i < j; ++i)
+            out[i] = x[i];
+        out[j] = tok;
+        for (int i = j + 1; i <= k; ++i)
+            out[i] = -1;
+        out_num_accepted[b] = j;
+    }
+    free(p), free(q), free(w), free(ratio), free(rowtie);
     return rc;
 }
