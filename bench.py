@@ -53,6 +53,9 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--philox", action="store_true",
                     help="chain: draw each request's uniforms in the kernel from a (seed, offset) Philox state")
+    ap.add_argument("--top-k", type=int, default=0,
+                    help="stochastic chain on top-k / top-p filtered rows (0: unfiltered)")
+    ap.add_argument("--top-p", type=float, default=1.0)
     ap.add_argument("--op", choices=["verify", "relocate"], default="verify",
                     help="relocate: time the accepted-KV relocation after a tree verify instead")
     ap.add_argument("--kv-row-bytes", type=int, default=131072,
@@ -196,6 +199,10 @@ def run_ours(args, rank, world, local):
     w = workloads.make(args.config, seed=rank_seed(args.seed, rank))
     tree = w["kind"] == "tree"
     greedy = args.greedy and not tree
+    filtered = args.top_k > 0 and not (tree or greedy)
+    if filtered:
+        # The draft argmax is in every kept set (top_k >= 1, top_p > 0).
+        w["draft_tokens"] = filtered_draft_tokens(w)
     lib = sv.lib()
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -222,7 +229,8 @@ def run_ours(args, rank, world, local):
     k = w["L"] - 1 if tree else w["k"]
     rows = w["N"] if tree else (k + 1 if greedy else 2 * k + 1)
     ws = sv.Workspace(device)
-    buf = ws.ensure(B, rows, V, sh)
+    buf = ws.ensure(B, rows, V, sh,
+                    lib.spec_workspace_size_filtered(B, k, V, args.top_k) if filtered else None)
     out_tok = torch.empty((B, w["L"] if tree else k + 1), dtype=torch.int32, device=device)
     out_n = torch.empty(B, dtype=torch.int32, device=device)
     P = ctypes.c_void_p
@@ -240,6 +248,15 @@ def run_ours(args, rank, world, local):
             fn = lib.spec_verify_greedy
             call_args.append((ptr(c["target"]), code, ptr(c["tokens"]), B, k, V, ptr(out_tok),
                               ptr(out_n), ptr(seq), ptr(buf), buf.numel(), sh))
+        elif filtered:
+            fn = lib.spec_verify_chain_ex
+            prm = sv.ChainParams(ctypes.sizeof(sv.ChainParams), ptr(c["target"]), ptr(c["draft"]), code,
+                                 ptr(c["tokens"]), None, None if args.philox else ptr(c["uniforms"]),
+                                 ptr(c["seeds"]) if args.philox else None,
+                                 ptr(c["offsets"]) if args.philox else None, w["temperature"], B, k, V,
+                                 ptr(out_tok), ptr(out_n), None, ptr(seq), args.top_k, args.top_p)
+            c["params"] = prm
+            call_args.append((ctypes.byref(prm), ptr(buf), buf.numel(), sh))
         elif args.philox:
             fn = lib.spec_verify_chain_philox
             call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
@@ -307,7 +324,8 @@ def run_ours(args, rank, world, local):
         else:
             tk, nn, _ = sv.verify_chain(lg(dev_in["target"]), lg(dev_in["draft"]), dev_in["draft_tokens"],
                                         dev_in["uniforms"], w["temperature"], seq_lens=dev_in["seq_lens"],
-                                        workspace=ws)
+                                        workspace=ws, top_k=args.top_k if filtered else 0,
+                                        top_p=args.top_p if filtered else 1.0)
         res_tok.copy_(tk, non_blocking=True)
         res_n.copy_(nn, non_blocking=True)
         res_seq.copy_(dev_in["seq_lens"], non_blocking=True)
@@ -331,13 +349,14 @@ def run_ours(args, rank, world, local):
     algo_bytes = workloads.algorithmic_bytes(w, greedy=greedy or tree)
     achieved = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
-    kernel_key = "tree" if tree else ("greedy" if greedy else "chain")
+    kernel_key = "tree" if tree else ("greedy" if greedy else ("filtered" if filtered else "chain"))
     traffic = recorded_traffic(f"{args.config}/{kernel_key}")
     stats = sv.acceptance_stats(n_first, k)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, greedy, args.cpu_seconds)
+        cpu = cpu_baseline(w, greedy, args.cpu_seconds,
+                           (args.top_k, args.top_p) if filtered else None)
 
     if dist:
         dist.destroy_process_group()
@@ -357,7 +376,8 @@ def run_ours(args, rank, world, local):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": args.config + ("/greedy" if greedy else "") + ("/philox" if args.philox and not (tree or greedy) else ""),
+            "workload": args.config + ("/greedy" if greedy else "") + ("/philox" if args.philox and not (tree or greedy) else "")
+                        + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""),
             "B": B, "k": k, "V": V, "logits": w["dtype"],
             "temperature": None if (tree or greedy) else w["temperature"],
             "requests_per_step": B * world,
@@ -369,6 +389,7 @@ def run_ours(args, rank, world, local):
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
             "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
+                       "filtered": "spec_verify_chain_ex call (filter_topk_kernel + filter_finish_kernel)",
                        "greedy": "spec_verify_greedy call (argmax_kernel + argmax_finish_kernel)",
                        "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)"}[kernel_key],
             "algorithmic_bytes_per_call": algo_bytes,
@@ -385,11 +406,23 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, greedy, seconds):
+def filtered_draft_tokens(w):
+    """Draft tokens of a filtered run: each draft row's argmax (lowest index
+    on ties), which every top-k / top-p kept set contains."""
+    d = w["draft"]
+    x = workloads.bf16_bits_to_f32(d) if w["dtype"] == workloads.BF16 else d
+    return np.argmax(x, axis=-1).astype(np.int32)
+
+
+def cpu_baseline(w, greedy, seconds, filt=None):
     import oracle
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.verify(w, greedy=greedy)
+        if filt:
+            oracle.verify_chain_filtered(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
+                                         w["temperature"], filt[0], float(np.float32(filt[1])), w["dtype"])
+        else:
+            oracle.verify(w, greedy=greedy)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -410,11 +443,18 @@ def run_reference(args, rank, world):
     w = workloads.make(args.config, seed=args.seed)
     tree = w["kind"] == "tree"
     greedy = args.greedy and not tree
+    filtered = args.top_k > 0 and not (tree or greedy)
+    if filtered:
+        w["draft_tokens"] = filtered_draft_tokens(w)
 
     def one(b):
         sub = {key: (v[b:b + 1] if isinstance(v, np.ndarray) and v.shape[:1] == (w["B"],) else v)
                for key, v in w.items()}
         sub["B"] = 1
+        if filtered:
+            return oracle.verify_chain_filtered(sub["target"], sub["draft"], sub["draft_tokens"],
+                                                sub["uniforms"], sub["temperature"], args.top_k,
+                                                float(np.float32(args.top_p)), sub["dtype"])
         return oracle.verify(sub, greedy=greedy)
 
     for i in range(args.warmup):
@@ -431,7 +471,9 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.config + ("/greedy" if greedy else ""), "B": w["B"],
+        "config": {"workload": args.config + ("/greedy" if greedy else "")
+                               + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""),
+                   "B": w["B"],
                    "k": per, "V": w["V"], "logits": w["dtype"]},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
                          "sample": "one request per step, cycling through the batch"},

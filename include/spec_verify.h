@@ -79,6 +79,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 #define SPEC_MAX_DRAFT 64
 /* Largest batch B of any call. */
 #define SPEC_MAX_BATCH 8192
+/* Largest top_k of the filtered chain verify (spec_chain_params.top_k). */
+#define SPEC_MAX_TOPK 256
 #define SPEC_MAX_TREE_NODES 1024
 #define SPEC_MAX_PATH_LEN 64
 
@@ -88,6 +90,13 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
  * larger.  Every workspace starts with a fixed 512 KB block of per-request
  * sync lines (SPEC_MAX_BATCH of them). */
 size_t spec_workspace_size(int B, int rows_per_request, int V);
+
+/* Bytes of scratch of a filtered chain verify (spec_chain_params with
+ * top_k > 0) of B requests, k drafts, width V: the chain's, plus room for
+ * every row slice's top_k candidates and 2k probabilities per request.  An
+ * upper bound for any dtype and row alignment.  Returns 0 for invalid sizes
+ * (top_k outside [1, SPEC_MAX_TOPK] included). */
+size_t spec_workspace_size_filtered(int B, int k, int V, int top_k);
 
 /* Zero a workspace (asynchronously, on `stream`).  Call once after allocating
  * it; every verify call leaves it ready for the next. */
@@ -140,9 +149,11 @@ int spec_verify_chain_philox(const void *target_logits, const void *draft_logits
                              spec_stream_t stream);
 
 /* Parameters of spec_verify_chain_ex: those of spec_verify_chain and
- * spec_verify_chain_philox in one struct, plus ragged draft lengths.  Set
- * size = sizeof(spec_chain_params); fields a later version adds go at the
- * end.
+ * spec_verify_chain_philox in one struct, plus ragged draft lengths and
+ * top-k / top-p filtering.  Set size = sizeof(spec_chain_params); fields a
+ * later version adds go at the end, and a smaller size (an earlier version
+ * of the struct, ending at seq_lens) leaves the added fields at their
+ * defaults (no filtering).
  *   draft_lens [B] int32 or NULL: request b has k_b <= k real drafts in the
  *     buffers padded to k (TensorRT-LLM walkthrough: the real draft count is
  *     kept apart from the padded buffer, pad_draft_tokens_for_cuda_graph; the
@@ -170,6 +181,23 @@ typedef struct spec_chain_params {
     int32_t *out_num_accepted;   /* [B] */
     float *out_probs;            /* [B, k, 2] or NULL */
     int32_t *seq_lens;           /* [B] or NULL */
+    /* Symmetric filtering (TensorRT-LLM walkthrough, rejection-sampling
+     * section: target and draft are filtered by the same backend and
+     * parameters, or the accept test is silently wrong).  top_k = 0: none.
+     * top_k in [1, SPEC_MAX_TOPK]: every target and draft row keeps its
+     * top_k tokens by (logit descending, token ascending), then the shortest
+     * prefix of them whose softmax mass (over those top_k, at temperature T)
+     * reaches top_p (top_p = 1: all top_k); p and q are the softmax over the
+     * kept set, and the chain verify above runs on them (the final draw
+     * takes u * Z over the kept tokens in token order).  out_probs holds the
+     * filtered p and q.  Logits of -inf are never kept (their weight is 0);
+     * logits must not be NaN or +inf.  top_p in (0, 1]; top_p < 1 needs
+     * top_k > 0 (top-p over the whole vocabulary is not supported).  The
+     * workspace must hold spec_workspace_size_filtered(B, k, V, top_k)
+     * bytes; top_k times the row's 32 KB slices may not exceed 8192 (with
+     * 16-byte aligned rows: top_k <= 256 up to V = 262144 bf16). */
+    int top_k;
+    float top_p;
 } spec_chain_params;
 int spec_verify_chain_ex(const spec_chain_params *params, void *workspace,
                          size_t workspace_bytes, spec_stream_t stream);

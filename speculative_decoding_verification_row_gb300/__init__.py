@@ -33,13 +33,15 @@ SPEC_MAX_DRAFT = 64
 SPEC_MAX_BATCH = 8192
 SPEC_MAX_TREE_NODES = 1024
 SPEC_MAX_PATH_LEN = 64
+SPEC_MAX_TOPK = 256
 
 # Every entry point the header declares.
 SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_greedy", "spec_verify_tree", "spec_rollback_lengths",
            "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc",
            "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
-           "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged")
+           "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged",
+           "spec_workspace_size_filtered")
 SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 class ChainParams(ctypes.Structure):
@@ -51,7 +53,8 @@ class ChainParams(ctypes.Structure):
                 ("offsets", ctypes.c_void_p), ("temperature", ctypes.c_float),
                 ("B", ctypes.c_int), ("k", ctypes.c_int), ("V", ctypes.c_int),
                 ("out_tokens", ctypes.c_void_p), ("out_num_accepted", ctypes.c_void_p),
-                ("out_probs", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p)]
+                ("out_probs", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("top_k", ctypes.c_int), ("top_p", ctypes.c_float)]
 
 
 class GreedyParams(ctypes.Structure):
@@ -78,6 +81,8 @@ def _bind(lib):
     lib.spec_workspace_size.argtypes = [I, I, I]
     lib.spec_workspace_size.restype = S
     lib.spec_workspace_init.argtypes = [P, S, P]
+    lib.spec_workspace_size_filtered.argtypes = [I, I, I, I]
+    lib.spec_workspace_size_filtered.restype = S
     lib.spec_verify_chain.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P, S, P]
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
     lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P, P, P, S, P]
@@ -95,7 +100,8 @@ def _bind(lib):
     for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
               "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc",
               "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
-              "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged"):
+              "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged",
+           "spec_workspace_size_filtered"):
         getattr(lib, f).restype = I
     return lib
 
@@ -165,8 +171,10 @@ class Workspace:
         self.device = torch.device(device if device is not None else "cuda")
         self.buf = None
 
-    def ensure(self, B: int, rows: int, V: int, stream_handle) -> torch.Tensor:
-        need = lib().spec_workspace_size(B, rows, V)
+    def ensure(self, B: int, rows: int, V: int, stream_handle, need: int | None = None) -> torch.Tensor:
+        """Grow to spec_workspace_size(B, rows, V) bytes, or to `need` bytes."""
+        if need is None:
+            need = lib().spec_workspace_size(B, rows, V)
         if need == 0:
             raise SpecError("spec_workspace_size", SPEC_EINVAL)
         if self.buf is None or self.buf.numel() < need:
@@ -196,13 +204,15 @@ def default_workspace(device, stream_handle) -> Workspace:
 def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
                  out_tokens=None, out_num_accepted=None, out_probs=None, want_probs=False,
                  seq_lens=None, workspace: Workspace | None = None, stream=None,
-                 seeds=None, offsets=None, draft_lens=None):
+                 seeds=None, offsets=None, draft_lens=None, top_k: int = 0, top_p: float = 1.0):
     """Chain rejection-sampling verify; returns (tokens [B,k+1], num_accepted [B], probs [B,k,2] or None).
 
     seq_lens (int32 [B], optional) is advanced in place by n_acc + 1.  With
     uniforms=None, seeds and offsets (int64 [B]) select each request's Philox
     stream and the uniforms are drawn inside the kernel.  draft_lens (int32
-    [B], optional): each request's real draft length (ragged verify)."""
+    [B], optional): each request's real draft length (ragged verify).
+    top_k > 0 (with top_p in (0, 1]): verify on the top-k / top-p filtered
+    target and draft distributions (spec_chain_params.top_k / top_p)."""
     t = _dev(target_logits, "target_logits")
     if t.dim() != 3:
         raise ValueError("target_logits must be [B, k+1, V]")
@@ -226,14 +236,17 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
         _dev(seq_lens, "seq_lens", torch.int32, (B,))
     sh, _ = _stream_handle(stream, dev)
     ws = workspace or default_workspace(dev, sh)
-    buf = ws.ensure(B, 2 * k + 1, V, sh)
-    if draft_lens is not None:
-        lens = _dev(draft_lens, "draft_lens", torch.int32, (B,))
+    filtered = top_k != 0 or top_p != 1.0
+    need = lib().spec_workspace_size_filtered(B, k, V, int(top_k)) if top_k > 0 else None
+    buf = ws.ensure(B, 2 * k + 1, V, sh, need)
+    if draft_lens is not None or filtered:
+        lens = None if draft_lens is None else _dev(draft_lens, "draft_lens", torch.int32, (B,))
         prm = ChainParams(ctypes.sizeof(ChainParams), _ptr(t), _ptr(d), code, _ptr(x), _ptr(lens),
                           _ptr(u) if uniforms is not None else None,
                           None if uniforms is not None else _ptr(sd),
                           None if uniforms is not None else _ptr(of), float(temperature), B, k, V,
-                          _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens))
+                          _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens), int(top_k),
+                          float(top_p))
         rc = lib().spec_verify_chain_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
         name = "spec_verify_chain_ex"
     elif uniforms is not None:

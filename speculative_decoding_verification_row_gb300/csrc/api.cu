@@ -2,6 +2,7 @@
 // dispatch.  Every computation of the verification row runs in the kernels of
 // chain.cu and argmax.cu; this file only checks arguments and launches.
 #include <float.h>
+#include <stddef.h>
 #include <math.h>
 
 #include "kernels.cuh"
@@ -91,6 +92,13 @@ size_t spec_workspace_size(int B, int rows_per_request, int V) {
   return WsLayout(B, rows_per_request, V).total;
 }
 
+size_t spec_workspace_size_filtered(int B, int k, int V, int top_k) {
+  if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2 || top_k < 1 ||
+      top_k > SPEC_MAX_TOPK)
+    return 0;
+  return FilterLayout(B, k, V, max_splits(V), top_k).total;
+}
+
 int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream) {
   if (!workspace || workspace_bytes == 0) return SPEC_EINVAL;
   if (cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) != cudaSuccess)
@@ -109,7 +117,8 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
                const uint64_t* offsets, const int32_t* draft_lens, float temperature, int B,
                int k, int V,
                int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
-               int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+               int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream,
+               int top_k = 0, float top_p = 1.f) {
   if (!target_logits || !draft_logits || !draft_tokens || (!uniforms && (!seeds || !offsets)) ||
       !out_tokens || !out_num_accepted)
     return SPEC_EINVAL;
@@ -119,10 +128,17 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
   ChainArgs a{};
   if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
   const int R = 2 * k + 1;
+  if (top_k < 0 || top_k > SPEC_MAX_TOPK || !(top_p > 0.f) || !(top_p <= 1.f) ||
+      (top_k == 0 && top_p < 1.f))
+    return SPEC_EINVAL;
   if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
   const bool vec = aligned16(target_logits) && aligned16(draft_logits) &&
                    ((size_t)V * esize(dtype)) % 16 == 0;
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
+  if (top_k > 0) {
+    if ((long)a.nsplit * top_k > 8192) return SPEC_EINVAL;  // one row's lists in shared memory
+    if (workspace_bytes < FilterLayout(B, k, V, a.nsplit, top_k).total) return SPEC_EWORKSPACE;
+  }
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
   a.nsplit2 = num_items(V);
@@ -142,6 +158,15 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
   a.out_probs = out_probs;
   a.seq_lens = seq_lens;
   a.ws = ws_views(workspace, WsLayout(B, R, V));
+  if (top_k > 0) {
+    const FilterLayout fl(B, k, V, a.nsplit, top_k);
+    a.ws.cand = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + fl.cand);
+    a.ws.pq = reinterpret_cast<float*>(static_cast<char*>(workspace) + fl.pq);
+    a.top_k = top_k;
+    a.top_p = top_p;
+    return launch_filtered(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
+                                                                               : SPEC_ECUDA;
+  }
   return launch_chain(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
                                                                           : SPEC_ECUDA;
 }
@@ -250,11 +275,15 @@ int spec_verify_greedy_ex(const spec_greedy_params* p, void* workspace, size_t w
 
 int spec_verify_chain_ex(const spec_chain_params* p, void* workspace, size_t workspace_bytes,
                          spec_stream_t stream) {
-  if (!p || p->size < sizeof(spec_chain_params)) return SPEC_EINVAL;
+  // An earlier version of the struct ends at seq_lens (no filtering fields).
+  const size_t v1 = offsetof(spec_chain_params, seq_lens) + sizeof(p->seq_lens);
+  if (!p || p->size < v1) return SPEC_EINVAL;
+  const bool has_filter = p->size >= offsetof(spec_chain_params, top_p) + sizeof(p->top_p);
   return chain_impl(p->target_logits, p->draft_logits, p->dtype, p->draft_tokens, p->uniforms,
                     p->seeds, p->offsets, p->draft_lens, p->temperature, p->B, p->k, p->V,
                     p->out_tokens, p->out_num_accepted, p->out_probs, p->seq_lens, workspace,
-                    workspace_bytes, stream);
+                    workspace_bytes, stream, has_filter ? p->top_k : 0,
+                    has_filter ? p->top_p : 1.f);
 }
 
 int spec_rollback_paged(const int32_t* old_lens, const int32_t* num_accepted,

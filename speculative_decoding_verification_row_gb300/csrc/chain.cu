@@ -40,11 +40,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ const char* row_ptr(const ChainArgs& a, int b, int r, size_t row_bytes) {
-  return r <= a.k ? a.target + ((size_t)b * (a.k + 1) + r) * row_bytes
-                  : a.draft + ((size_t)b * a.k + (r - a.k - 1)) * row_bytes;
-}
-
 // Sum of 2^(c (x - M)) over one vector, as a pair of partial sums.
 template <int DT, bool VEC>
 __device__ __forceinline__ float2 vec_expsum(const uint32_t (&w)[Io<DT, VEC>::NW], float2 nm,
@@ -85,21 +80,8 @@ __device__ __forceinline__ unsigned long long stats_pack(float M, float S) {
 __device__ __forceinline__ float2 stats_unpack(unsigned long long v) {
   return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
 }
-// Poll a slice's word until pass 1 has written it.  Pass 1 was scheduled in
-// full before the draw grid, so the wait ends; the bound only turns a broken
-// invariant into an error instead of a hang.
-__device__ __noinline__ unsigned long long wait_stats(const unsigned long long* p, int* status) {
-  unsigned long long v = ld_relaxed_u64(p);
-  const long long t0 = clock64();
-  while (!v) {
-    if (clock64() - t0 > kWaitCycles) {
-      set_status(status, SPEC_ETIMEOUT);
-      return kNoStats;
-    }
-    __nanosleep(64);
-    v = ld_relaxed_u64(p);
-  }
-  return v;
+__device__ __forceinline__ unsigned long long wait_stats(const unsigned long long* p, int* status) {
+  return wait_word(p, status, kNoStats);
 }
 
 // ------------------------------------------------------------------ pass 1
@@ -239,17 +221,6 @@ __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow
       wv[i] = ep;
     }
   }
-}
-
-// A non-negative weight sum (below 2^32) as an integer number of 2^-32,
-// rounded to nearest even, with 32-bit conversions only (64-bit ones run on
-// the FP64 pipe, which is narrow on this GPU).  x = h + f with h = trunc(x)
-// and f = x - h exact; f * 2^32 < 2^32 - 255 is exact too, so rounding it
-// rounds x * 2^32, and the tie parity is that of the low word.
-__device__ __forceinline__ unsigned long long to_fixed(float x) {
-  const unsigned h = __float2uint_rz(x);
-  const unsigned l = __float2uint_rn((x - (float)h) * 4294967296.0f);
-  return ((unsigned long long)h << 32) + l;
 }
 
 // Warp-wide inclusive prefix sum of 64-bit values.

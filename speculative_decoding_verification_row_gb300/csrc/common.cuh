@@ -78,6 +78,22 @@ struct Ws {  // typed views of one call's workspace
   float2* part;                // argmax: each unit's packed (max, index + 1)
   unsigned long long* chunks;  // draw-weight sum of each 256-token chunk, in 2^-32 units
   unsigned long long* items;   // sum of each draw item's chunks, in 2^-32 units
+  unsigned long long* cand;    // filtered: each slice's top-k keys, then each row's kept list
+  float* pq;                   // filtered: p_i(x_i) and q_i(x_i) of each request
+};
+
+// The filtered chain path appends two regions to the chain layout: per
+// slice, its top-k candidate keys (the words of a row's first slice later
+// hold the row's kept list), and per request 2k draft-token probabilities.
+// `nsplit` is the slices per row of the call (max_splits(V) at most).
+struct FilterLayout {
+  size_t cand, pq, total;
+  __host__ __device__ FilterLayout(int B, int k, int V, int nsplit, int top_k) {
+    size_t off = WsLayout(B, 2 * k + 1, V).total;
+    cand = off; off += align256(sizeof(unsigned long long) * (size_t)B * (2 * k + 1) * nsplit * top_k);
+    pq = off; off += align256(sizeof(float) * (size_t)B * 2 * k);
+    total = off;
+  }
 };
 
 inline Ws ws_views(void* base, const WsLayout& l) {
@@ -86,7 +102,7 @@ inline Ws ws_views(void* base, const WsLayout& l) {
             reinterpret_cast<unsigned long long*>(p + l.stats),
             reinterpret_cast<float2*>(p + l.part),
             reinterpret_cast<unsigned long long*>(p + l.chunks),
-            reinterpret_cast<unsigned long long*>(p + l.items)};
+            reinterpret_cast<unsigned long long*>(p + l.items), nullptr, nullptr};
 }
 
 // ---------------------------------------------------------------- loads
@@ -209,6 +225,17 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return r;
 }
 
+// A non-negative weight sum (below 2^32) as an integer number of 2^-32,
+// rounded to nearest even, with 32-bit conversions only (64-bit ones run on
+// the FP64 pipe, which is narrow on this GPU).  x = h + f with h = trunc(x)
+// and f = x - h exact; f * 2^32 < 2^32 - 255 is exact too, so rounding it
+// rounds x * 2^32, and the tie parity is that of the low word.
+__device__ __forceinline__ unsigned long long to_fixed(float x) {
+  const unsigned h = __float2uint_rz(x);
+  const unsigned l = __float2uint_rn((x - (float)h) * 4294967296.0f);
+  return ((unsigned long long)h << 32) + l;
+}
+
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3", SC'11): ten rounds; a round takes the 64-bit products
@@ -256,5 +283,24 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 }
 // Record the first data-dependent error of a call.
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Poll a word until a producer grid has written it (written words are never
+// 0).  The producer was scheduled in full before the polling grid, so the
+// wait ends; the bound only turns a broken invariant into SPEC_ETIMEOUT and
+// `on_timeout` instead of a hang.
+static __device__ __noinline__ unsigned long long wait_word(const unsigned long long* p, int* status,
+                                                     unsigned long long on_timeout) {
+  unsigned long long v = ld_relaxed_u64(p);
+  const long long t0 = clock64();
+  while (!v) {
+    if (clock64() - t0 > kWaitCycles) {
+      set_status(status, SPEC_ETIMEOUT);
+      return on_timeout;
+    }
+    __nanosleep(64);
+    v = ld_relaxed_u64(p);
+  }
+  return v;
+}
 
 }  // namespace sv

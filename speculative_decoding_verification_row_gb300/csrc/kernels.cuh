@@ -17,6 +17,8 @@ struct ChainArgs {
   int B, k, V;
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
   int nchunks, cpc, nsplit2;   // draw: chunks per row, per item, items per request
+  int top_k;                   // filtered verify: tokens kept per row (0: no filtering)
+  float top_p;                 // filtered verify: nucleus mass, in (0, 1]
   int32_t* out_tokens;
   int32_t* out_n;
   float* out_probs;
@@ -43,9 +45,24 @@ struct ArgmaxArgs {
   Ws ws;
 };
 
+// Logit row r of request b in chain order: r <= k is target row r, r > k
+// is draft row r-k-1.
+__device__ __forceinline__ const char* row_ptr(const ChainArgs& a, int b, int r, size_t row_bytes) {
+  return r <= a.k ? a.target + ((size_t)b * (a.k + 1) + r) * row_bytes
+                  : a.draft + ((size_t)b * a.k + (r - a.k - 1)) * row_bytes;
+}
+
+// Whether row r of a request with the given draft length is verified: target
+// rows 0..kb, draft rows 0..kb-1 (a length outside [0, k] verifies nothing).
+__device__ __forceinline__ bool row_used(int k, int kb, int r) {
+  if (kb < 0 || kb > k) return false;
+  return r <= k ? r <= kb : r - k - 1 < kb;
+}
+
 // Enqueue the two chain passes (pass 2 as a programmatic dependent launch) /
 // the argmax pass on `st`.
 cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
+cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
 cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st);
 
 }  // namespace sv
