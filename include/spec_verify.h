@@ -92,10 +92,10 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 size_t spec_workspace_size(int B, int rows_per_request, int V);
 
 /* Bytes of scratch of a filtered chain verify (spec_chain_params with
- * top_k > 0) of B requests, k drafts, width V: the chain's, plus room for
- * every row slice's top_k candidates and 2k probabilities per request.  An
- * upper bound for any dtype and row alignment.  Returns 0 for invalid sizes
- * (top_k outside [1, SPEC_MAX_TOPK] included). */
+ * top_k > 0) of B requests, k drafts, width V: the chain's, plus each row's
+ * kept list (top_k words), 2k probabilities per request and two bytes per
+ * 2048 logits of each row.  Returns 0 for
+ * invalid sizes (top_k outside [1, SPEC_MAX_TOPK] included). */
 size_t spec_workspace_size_filtered(int B, int k, int V, int top_k);
 
 /* Zero a workspace (asynchronously, on `stream`).  Call once after allocating
@@ -194,8 +194,7 @@ typedef struct spec_chain_params {
      * logits must not be NaN or +inf.  top_p in (0, 1]; top_p < 1 needs
      * top_k > 0 (top-p over the whole vocabulary is not supported).  The
      * workspace must hold spec_workspace_size_filtered(B, k, V, top_k)
-     * bytes; top_k times the row's 32 KB slices may not exceed 8192 (with
-     * 16-byte aligned rows: top_k <= 256 up to V = 262144 bf16). */
+     * bytes. */
     int top_k;
     float top_p;
 } spec_chain_params;

@@ -96,7 +96,7 @@ size_t spec_workspace_size_filtered(int B, int k, int V, int top_k) {
   if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2 || top_k < 1 ||
       top_k > SPEC_MAX_TOPK)
     return 0;
-  return FilterLayout(B, k, V, max_splits(V), top_k).total;
+  return FilterLayout(B, k, V, top_k).total;
 }
 
 int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream) {
@@ -135,10 +135,7 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
   const bool vec = aligned16(target_logits) && aligned16(draft_logits) &&
                    ((size_t)V * esize(dtype)) % 16 == 0;
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
-  if (top_k > 0) {
-    if ((long)a.nsplit * top_k > 8192) return SPEC_EINVAL;  // one row's lists in shared memory
-    if (workspace_bytes < FilterLayout(B, k, V, a.nsplit, top_k).total) return SPEC_EWORKSPACE;
-  }
+  if (top_k > 0 && workspace_bytes < FilterLayout(B, k, V, top_k).total) return SPEC_EWORKSPACE;
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
   a.nsplit2 = num_items(V);
@@ -159,9 +156,10 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
   a.seq_lens = seq_lens;
   a.ws = ws_views(workspace, WsLayout(B, R, V));
   if (top_k > 0) {
-    const FilterLayout fl(B, k, V, a.nsplit, top_k);
+    const FilterLayout fl(B, k, V, top_k);
     a.ws.cand = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + fl.cand);
     a.ws.pq = reinterpret_cast<float*>(static_cast<char*>(workspace) + fl.pq);
+    a.ws.codes = reinterpret_cast<unsigned short*>(static_cast<char*>(workspace) + fl.codes);
     a.top_k = top_k;
     a.top_p = top_p;
     return launch_filtered(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK

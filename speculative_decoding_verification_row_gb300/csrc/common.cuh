@@ -78,20 +78,22 @@ struct Ws {  // typed views of one call's workspace
   float2* part;                // argmax: each unit's packed (max, index + 1)
   unsigned long long* chunks;  // draw-weight sum of each 256-token chunk, in 2^-32 units
   unsigned long long* items;   // sum of each draw item's chunks, in 2^-32 units
-  unsigned long long* cand;    // filtered: each slice's top-k keys, then each row's kept list
+  unsigned long long* cand;    // filtered: each row's kept list
   float* pq;                   // filtered: p_i(x_i) and q_i(x_i) of each request
+  unsigned short* codes;       // filtered: each slice thread's largest-logit prefix
 };
 
-// The filtered chain path appends two regions to the chain layout: per
-// slice, its top-k candidate keys (the words of a row's first slice later
-// hold the row's kept list), and per request 2k draft-token probabilities.
-// `nsplit` is the slices per row of the call (max_splits(V) at most).
+// The filtered chain path appends three regions to the chain layout: per
+// row, its kept list (top_k words); per request 2k draft-token
+// probabilities; per slice thread (worst case of max_splits(V) slices per
+// row), the 16-bit prefix of its largest logit.
 struct FilterLayout {
-  size_t cand, pq, total;
-  __host__ __device__ FilterLayout(int B, int k, int V, int nsplit, int top_k) {
+  size_t cand, pq, codes, total;
+  __host__ __device__ FilterLayout(int B, int k, int V, int top_k) {
     size_t off = WsLayout(B, 2 * k + 1, V).total;
-    cand = off; off += align256(sizeof(unsigned long long) * (size_t)B * (2 * k + 1) * nsplit * top_k);
+    cand = off; off += align256(sizeof(unsigned long long) * (size_t)B * (2 * k + 1) * top_k);
     pq = off; off += align256(sizeof(float) * (size_t)B * 2 * k);
+    codes = off; off += align256(sizeof(unsigned short) * (size_t)B * (2 * k + 1) * max_splits(V) * kThreads);
     total = off;
   }
 };
@@ -102,7 +104,7 @@ inline Ws ws_views(void* base, const WsLayout& l) {
             reinterpret_cast<unsigned long long*>(p + l.stats),
             reinterpret_cast<float2*>(p + l.part),
             reinterpret_cast<unsigned long long*>(p + l.chunks),
-            reinterpret_cast<unsigned long long*>(p + l.items), nullptr, nullptr};
+            reinterpret_cast<unsigned long long*>(p + l.items), nullptr, nullptr, nullptr};
 }
 
 // ---------------------------------------------------------------- loads

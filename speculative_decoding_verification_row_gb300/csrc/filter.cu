@@ -10,33 +10,25 @@
 // at the first rejection j and draw from max(0, p_j - q_j) normalised, or
 // from p_k when all k are accepted.
 //
-// Since p_j is zero outside target row j's kept set, the final draw has at
-// most top_k candidate tokens, so after one streaming pass nothing re-reads a
-// logit row.
-//
-// Pass 1, filter_topk_kernel: one CTA per 32 KB slice of a row (request-major
-// order, as the unfiltered pass 1).  It publishes the slice's top_k keys,
-// sorted, as nonzero 64-bit words.  A key is (order-preserving bits of the
-// logit) << 32 | (2^32 - 1 - token): larger key = larger logit, then lower
-// token.  Logits of -inf are never kept: their weight is exactly 0, so they
-// change no probability, no top-p prefix and no draw.
-//   Selection: each thread's largest logit; a bisection over the 256 thread
-//   maxima (one block-wide count per bit) finds tau, the top_k-th largest of
-//   them.  At least top_k elements are >= tau, so the slice's top_k all are:
-//   the vectors holding an element >= tau (about top_k of 2048) are copied
-//   to shared memory, their elements >= tau become keys, and a bitonic sort
-//   orders them.  When those do not fit (many equal logits), an exact
-//   bisection over the elements' values, then over the tied tokens' indices,
-//   selects exactly the top_k.
-// Pass 2, filter_finish_kernel: a programmatic dependent of pass 1; one CTA
-// item per (request, row).  It polls the row's slice lists, merges them by
-// rank (a key's rank is its position in its own list plus the keys above it
-// in each other list, found by binary search), applies the softmax and the
-// top-p cut to the top_k, and writes the row's kept list (token, probability)
-// and, for the rows that test a draft token, that token's probability.  The
-// request's last row item (atomic ticket) runs the accept scan and draws the
-// final token by inverse CDF over the kept tokens of target row j in token
-// order, with exact 64-bit fixed-point prefix sums.
+// Two passes; every logit is read once from HBM, plus about K 128-byte lines
+// per row.  A logit's key is (order-preserving bits of the logit) << 32 |
+// (2^32 - 1 - token): larger key = larger logit, then lower token, so the
+// kept set's order is the key order.  Logits of -inf are never kept: their
+// weight is exactly 0, so they change no probability, no top-p prefix and no
+// draw.
+//   filter_max_kernel streams the rows like the unfiltered pass 1 and keeps
+//   only one 16-bit code per 128 contiguous bytes (the prefix of its largest
+//   logit's key).
+//   filter_pick_kernel, one CTA per row, takes a code threshold that at
+//   least K codes reach, re-reads only the 128-byte groups at or above it,
+//   ranks their candidates and publishes the row's kept list (token,
+//   probability) and the probability of the draft token the row tests; the
+//   request's last row CTA (acquire-release ticket) runs the accept scan and
+//   draws the final token by inverse CDF over the kept tokens of target row
+//   j in token order (p_j is zero elsewhere), with exact 64-bit fixed-point
+//   prefix sums.
+//   filter_row_kernel (rows too wide for one CTA's codes) streams each row
+//   through one CTA with a running candidate threshold instead.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -44,10 +36,6 @@
 namespace sv {
 
 namespace {
-
-constexpr unsigned long long kNone = 1;  // an empty slot: below every real key
-constexpr int kQCap = 512;               // candidate vectors one slice CTA holds
-constexpr int kCCap = 1024;              // candidate keys one slice CTA sorts
 
 // Order-preserving map of a float (not NaN) to 32 bits, -0 taken as +0.
 __device__ __forceinline__ uint32_t ord32(float x) {
@@ -68,484 +56,789 @@ __device__ __forceinline__ int key_token(unsigned long long key) {
   return (int)(0xffffffffu - (uint32_t)key);
 }
 
-// Block-wide sum of one int per thread (all threads call; every thread gets it).
-__device__ __forceinline__ int block_sum(int v, int* scratch) {
-  const int w = __reduce_add_sync(0xffffffffu, (unsigned)v);
-  __syncthreads();  // earlier readers of *scratch are done
-  if (threadIdx.x == 0) *scratch = 0;
+// ------------------------------------------------------------------ per-row CTAs
+// filter_row_kernel: one CTA of kRowThreads per logit row (target or draft).
+// The row streams through registers in chunks of kRowThreads * kRowVecs
+// 16-byte vectors, the next chunk loading while one is filtered.  Candidates
+// are the logits whose key is >= kappa, a running threshold: at least K keys
+// >= kappa are always held (or every finite logit seen, when fewer), so the
+// row's top K are all candidates.  kappa starts from the first chunk's
+// vector maxima and rises only when the candidate buffer would overflow (its
+// keys are then cut to their exact top K).  After the last chunk the held
+// keys are ranked; the top K get the softmax and the top-p cut.
+constexpr int kRowThreads = 128;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowVecs = 4;                              // vectors per thread per chunk
+constexpr int kChunkVecs = kRowThreads * kRowVecs;
+constexpr int kBufCap = 1536;                            // candidate keys a row CTA holds
+constexpr int kRankMax = 512;                            // final ranking without a cut first
+constexpr int kRowCtasPerSm = 7;                         // 1064 rows resident on 152 SMs
+
+struct RowSmem {
+  unsigned long long buf[kBufCap + 2];   // held candidate keys (and a zero pad)
+  unsigned long long top[SPEC_MAX_TOPK]; // the top K, sorted (cut / final ranking)
+  unsigned long long kappa;              // candidates: key >= kappa
+  int n;                                 // keys held
+  int wsum[kRowWarps];                   // per-warp counts (scans)
+  int red;                               // the drawn token (finish)
+  uint32_t tcode;                        // threshold codes (warp minimum)
+  float warp_f[kRowWarps];
+  int m;                                 // top-p: kept entries
+  float sm;                              // top-p: mass of the kept entries
+  int last;                              // this CTA finishes the request
+};
+
+// Block-wide sum of one int per thread over a kRowThreads CTA.
+__device__ __forceinline__ int row_block_sum(int v, RowSmem& S) {
+  const int w = (int)__reduce_add_sync(0xffffffffu, (unsigned)v);
+  __syncthreads();  // earlier readers of S.wsum are done
+  if ((threadIdx.x & 31) == 0) S.wsum[threadIdx.x >> 5] = w;
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) atomicAdd(scratch, w);
-  __syncthreads();
-  return *scratch;
+  int t = 0;
+#pragma unroll
+  for (int q = 0; q < kRowWarps; ++q) t += S.wsum[q];
+  return t;
 }
 
-// Bitonic sort of n 64-bit keys in shared memory, descending (ascending when
-// ASC), padded with `pad` to a power of two; returns the padded length.
-template <bool ASC>
-__device__ int bitonic_sort(unsigned long long* keys, int n, unsigned long long pad) {
-  int P = 1;
-  while (P < n) P <<= 1;
-  for (int i = n + threadIdx.x; i < P; i += blockDim.x) keys[i] = pad;
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
-        const bool first_half_down = ((lo & size) == 0) != ASC;  // this block's direction
-        const unsigned long long x = keys[lo], y = keys[hi];
-        if ((x < y) == first_half_down) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  return P;
-}
-
-// Number of keys above `key` in a descending list of n keys.
-__device__ __forceinline__ int count_above(const unsigned long long* list, int n,
-                                           unsigned long long key) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (list[mid] > key) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// Inclusive prefix sum across the block (fp32 or u64); *total gets the sum.
-template <typename T>
-__device__ __forceinline__ T block_incl_scan(T v, T* warp_tot, T* total) {
+// Exclusive block scan of one int per thread; *total gets the sum.
+__device__ __forceinline__ int row_block_scan(int v, RowSmem& S, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const T o = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += o;
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
   }
-  __syncthreads();  // earlier readers of warp_tot are done
-  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();  // earlier readers of S.wsum are done
+  if (lane == 31) S.wsum[warp] = incl;
   __syncthreads();
-  T base = T(0), all = T(0);
+  int before = 0, all = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const T t = warp_tot[w];
-    if (w < warp) base += t;
+  for (int q = 0; q < kRowWarps; ++q) {
+    const int t = S.wsum[q];
+    before += q < warp ? t : 0;
     all += t;
   }
   *total = all;
-  return base + v;
+  return before + incl - v;
 }
 
-__device__ __forceinline__ void slice_row(const ChainArgs& a, int rr, int& b, int& r) {
-  const int R = 2 * a.k + 1;
-  b = rr / R;
-  r = rr - b * R;
+// Rank the n held keys (unique): each key's rank is the number of keys above
+// it; the top min(n, K) land in S.top in descending order.
+__device__ void rank_held(RowSmem& S, int n, int K) {
+  const int T = n <= kRowThreads / 4 ? 4 : n <= kRowThreads / 2 ? 2 : 1;
+  const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(S.buf);
+  if (threadIdx.x == 0) S.buf[n] = 0;  // pads the last pair (0 is below every key)
+  __syncthreads();
+  for (int c0 = 0; c0 < n; c0 += kRowThreads / T) {
+    const int ci = c0 + (int)threadIdx.x / T, part = (int)threadIdx.x % T;
+    const unsigned long long key = ci < n ? S.buf[ci] : ~0ull;
+    const int chunk = (((n + T - 1) / T) + 1) & ~1;
+    const int q0 = part * chunk, q1 = min(n, q0 + chunk);
+    int rank = 0;
+#pragma unroll 4
+    for (int q = q0; q < q1; q += 2) {
+      const ulonglong2 kv = kp[q >> 1];
+      rank += (kv.x > key ? 1 : 0) + (kv.y > key ? 1 : 0);
+    }
+    for (int o = 1; o < T; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (ci < n && part == 0 && rank < K) S.top[rank] = key;
+  }
+  __syncthreads();
 }
 
-// ------------------------------------------------------------------ pass 1
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4) filter_topk_kernel(const ChainArgs a) {
-  asm volatile("griddepcontrol.launch_dependents;");
-  using IO = Io<DT, VEC>;
-  constexpr int EPV = IO::EPV, NW = IO::NW;
-  // bf16 logits widened to fp32 differ only in their top 16 bits.
-  constexpr int LOBIT = DT == SPEC_BF16 ? 16 : 0;
-  __shared__ uint32_t sVec[kQCap][NW];
-  __shared__ int sVecIdx[kQCap];
-  __shared__ unsigned long long sKey[kCCap];
-  __shared__ int sNV, sNC, sCnt;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int K = a.top_k;
-  const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
-  int b, r;
-  slice_row(a, rr, b, r);
-  if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
-  const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
-  const int vbeg = s * a.vps;
-  const int vend = min(a.nvec, vbeg + a.vps);
+// Cut the held keys to their exact top K and raise kappa to the K-th key
+// (n > K): the K-th largest key by bisection on its 64 bits (block-wide
+// counts), then the K keys >= it move to the front of the buffer.
+__device__ __noinline__ void cut_held(RowSmem& S, int K) {
+  const int n = S.n;
+  unsigned long long kth = 0;
+  for (int bit = 63; bit >= 0; --bit) {
+    const unsigned long long c = kth | (1ull << bit);
+    int cnt = 0;
+    for (int i = threadIdx.x; i < n; i += kRowThreads) cnt += S.buf[i] >= c ? 1 : 0;
+    if (row_block_sum(cnt, S) >= K) kth = c;
+  }
+  // exactly K keys are >= kth (keys are unique): gather them in S.top at
+  // scanned offsets, then back to the front of the buffer
+  int mine = 0;
+  for (int i = threadIdx.x; i < n; i += kRowThreads) mine += S.buf[i] >= kth ? 1 : 0;
+  int total;
+  int off = row_block_scan(mine, S, &total);
+  for (int i = threadIdx.x; i < n; i += kRowThreads)
+    if (S.buf[i] >= kth) S.top[off++] = S.buf[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < total; i += kRowThreads) S.buf[i] = S.top[i];
+  if (threadIdx.x == 0) {
+    S.n = total;
+    S.kappa = kth;
+  }
+  __syncthreads();
+}
 
-  uint32_t w[kVecPerThread][NW];
-#pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int v = vbeg + tid + u * kThreads;
-    if (v < vend) IO::load(row, v, w[u]);
+// Raise kappa cheaply (n held keys, n > 4K): warp w takes keys w, w + 4, ...
+// and finds the cw-th largest 16-bit prefix of their order bits (cw =
+// ceil(K / 4), bisection between its least and largest); the least of the
+// four, as a key prefix, keeps at least K keys.  The keys below it go.
+__device__ __noinline__ void raise_held(RowSmem& S, int K) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = S.n;
+  const int cw = (K + kRowWarps - 1) / kRowWarps;
+  uint32_t lo = ~0u, hi = 0;
+  for (int i = warp + kRowWarps * lane; i < n; i += kRowThreads) {
+    const uint32_t p = (uint32_t)(S.buf[i] >> 48);
+    lo = min(lo, p);
+    hi = max(hi, p);
   }
-  float vm[kVecPerThread];
-  float m = -INFINITY;
-#pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    vm[u] = vbeg + tid + u * kThreads < vend ? IO::vmax(w[u]) : -INFINITY;
-    m = fmaxf(m, vm[u]);
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  while (lo < hi) {  // every key of the share is >= lo, and the share holds >= cw keys
+    const uint32_t mid = (lo + hi + 1) >> 1;
+    unsigned c = 0;
+    for (int i = warp + kRowWarps * lane; i < n; i += kRowThreads)
+      c += (uint32_t)(S.buf[i] >> 48) >= mid ? 1u : 0u;
+    if ((int)__reduce_add_sync(0xffffffffu, c) >= cw) lo = mid;
+    else hi = mid - 1;
   }
+  if (lane == 0) atomicMin(&S.tcode, lo);
+  __syncthreads();
+  const unsigned long long kap = (unsigned long long)S.tcode << 48;
+  int mine = 0;
+  for (int i = tid; i < n; i += kRowThreads) mine += S.buf[i] >= kap ? 1 : 0;
+  int total;
+  int off = row_block_scan(mine, S, &total);
+  // Gather the survivors in order into S.top-sized pieces is not possible
+  // (they may be more than SPEC_MAX_TOPK), so move them within the buffer:
+  // every key is read before any is written.
+  unsigned long long keep[kBufCap / kRowThreads];
+#pragma unroll
+  for (int q = 0; q < kBufCap / kRowThreads; ++q) {
+    const int i = tid + q * kRowThreads;
+    keep[q] = i < n ? S.buf[i] : 0ull;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kBufCap / kRowThreads; ++q)
+    if (keep[q] >= kap && keep[q] != 0ull) S.buf[off++] = keep[q];
   if (tid == 0) {
-    sNV = 0;
-    sNC = 0;
+    S.n = total;
+    if (kap > S.kappa) S.kappa = kap;
+    S.tcode = ~0u;
   }
-  // tau = the K-th largest thread maximum (0: fewer than K threads hold a
-  // finite logit, and every finite logit is a candidate).
-  const uint32_t mo = m > -INFINITY ? ord32(m) : 0u;
-  uint32_t t = 0;
-  for (int bit = 31; bit >= LOBIT; --bit) {
-    const uint32_t c = t | (1u << bit);
-    if (__syncthreads_count(mo >= c) >= K) t = c;
-  }
-  if (LOBIT && t && !(t & 0x80000000u)) t |= 0xffffu;  // the bf16 value's own code
-  const float tau = t ? unord32(t) : -INFINITY;
+  __syncthreads();
+}
 
-  // Copy every vector holding a candidate (x >= tau, x > -inf) to shared memory.
+// Exclusive block scan of one float per thread (kRowThreads CTA).
+__device__ __forceinline__ float row_block_scan_f(float v, RowSmem& S, float* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  __syncthreads();
+  if (lane == 31) S.warp_f[warp] = incl;
+  __syncthreads();
+  float before = 0.f, all = 0.f;
+#pragma unroll
+  for (int q = 0; q < kRowWarps; ++q) {
+    const float t = S.warp_f[q];
+    before += q < warp ? t : 0.f;
+    all += t;
+  }
+  *total = all;
+  return before + incl - v;
+}
+
+__device__ __forceinline__ unsigned long long* row_words_of(const ChainArgs& a, int b, int r) {
+  return a.ws.cand + ((size_t)b * (2 * a.k + 1) + r) * (size_t)a.top_k;
+}
+
+__device__ void finish_request(RowSmem& S, const ChainArgs& a, int b);
+
+// Chunk c of a row into registers (thread t: vectors c * kChunkVecs + t +
+// u * kRowThreads).
+template <int DT, bool VEC>
+__device__ __forceinline__ void load_chunk(const char* row, int c, int nvec,
+                                           uint32_t (&X)[kRowVecs][Io<DT, VEC>::NW]) {
+#pragma unroll
+  for (int u = 0; u < kRowVecs; ++u) {
+    const int v = c * kChunkVecs + (int)threadIdx.x + u * kRowThreads;
+    if (v < nvec) Io<DT, VEC>::load(row, v, X[u]);
+  }
+}
+
+// The candidates among the logits of vector v (register form w): logits
+// x > -inf with key >= kap; emit(key) for each, in order.
+template <int DT, bool VEC, typename F>
+__device__ __forceinline__ void vec_candidates(int v, const uint32_t (&w)[Io<DT, VEC>::NW],
+                                               unsigned long long kap, F emit) {
+  constexpr int EPV = Io<DT, VEC>::EPV;
+  float e[EPV];
+  Io<DT, VEC>::unpack(w, e);
+#pragma unroll
+  for (int q = 0; q < EPV; ++q)
+    if (e[q] > -INFINITY) {
+      const unsigned long long key = make_key(e[q], (long)v * EPV + q);
+      if (key >= kap) emit(key);
+    }
+}
+
+// Append the candidates of this thread's vectors vidx[u] (register form
+// X[u], maxima vm[u]; cnt candidates in all) to the held keys.
+template <int DT, bool VEC, int NV>
+__device__ __forceinline__ void append_chunk(RowSmem& S, int K, const int (&vidx)[NV],
+                                             const uint32_t (&X)[NV][Io<DT, VEC>::NW],
+                                             const float (&vm)[NV], int cnt) {
+  const int tid = threadIdx.x;
+  unsigned long long kap = S.kappa;
+  float kv = kap ? key_value(kap) : -INFINITY;
+  int total;
+  int off = row_block_scan(cnt, S, &total);
+  if (S.n + total <= kBufCap) {  // all of the chunk's candidates fit
+    unsigned long long* dst = S.buf + S.n + off;
+#pragma unroll
+    for (int u = 0; u < NV; ++u)
+      if (vm[u] >= kv && vm[u] > -INFINITY)
+        vec_candidates<DT, VEC>(vidx[u], X[u], kap, [&](unsigned long long key) { *dst++ = key; });
+    __syncthreads();
+    if (tid == 0) S.n += total;
+    __syncthreads();
+    if (S.n > max(4 * K, 256)) raise_held(S, K);
+    return;
+  }
+  // Vector by vector, cutting the held keys to the top K first when the
+  // vector's candidates (at most kRowThreads * EPV) would not fit.
+#pragma unroll
+  for (int u = 0; u < NV; ++u) {
+    const int v = vidx[u];
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      kap = S.kappa;
+      kv = kap ? key_value(kap) : -INFINITY;
+      int cu = 0;
+      if (vm[u] >= kv && vm[u] > -INFINITY)
+        vec_candidates<DT, VEC>(v, X[u], kap, [&](unsigned long long) { ++cu; });
+      off = row_block_scan(cu, S, &total);
+      if (S.n + total > kBufCap && attempt == 0) {  // then S.n > kBufCap - kRowThreads * 8 > K
+        cut_held(S, K);
+        continue;
+      }
+      unsigned long long* dst = S.buf + S.n + off;
+      if (vm[u] >= kv && vm[u] > -INFINITY)
+        vec_candidates<DT, VEC>(v, X[u], kap, [&](unsigned long long key) { *dst++ = key; });
+      __syncthreads();
+      if (tid == 0) S.n += total;
+      __syncthreads();
+      break;
+    }
+  }
+}
+
+// Filter chunk c (in registers): its candidates join the held keys.  The
+// first chunk also sets kappa0: each warp's cw-th largest vector maximum
+// (16-bit prefix of the order bits, bisection between the warp's least and
+// largest), the least over the warps, so at least K logits are >= it.  0:
+// some warp has fewer than cw finite vectors (every finite logit counts).
+template <int DT, bool VEC>
+__device__ __forceinline__ void filter_chunk(RowSmem& S, int K, int c, int nvec,
+                                             const uint32_t (&X)[kRowVecs][Io<DT, VEC>::NW]) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  float vm[kRowVecs];
+  int vidx[kRowVecs];
+#pragma unroll
+  for (int u = 0; u < kRowVecs; ++u) {
+    vidx[u] = c * kChunkVecs + tid + u * kRowThreads;
+    vm[u] = vidx[u] < nvec ? Io<DT, VEC>::vmax(X[u]) : -INFINITY;
+  }
+  if (c == 0) {
+    const int cw = (K + kRowWarps - 1) / kRowWarps;
+    uint32_t mo[kRowVecs], lo = ~0u, hi = 0;
+#pragma unroll
+    for (int u = 0; u < kRowVecs; ++u) {
+      mo[u] = vm[u] > -INFINITY ? ord32(vm[u]) >> 16 : 0u;
+      lo = min(lo, mo[u]);
+      hi = max(hi, mo[u]);
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    while (lo < hi) {  // all 128 of the warp's maxima are >= lo, and cw <= 64
+      const uint32_t mid = (lo + hi + 1) >> 1;
+      unsigned n = 0;
+#pragma unroll
+      for (int u = 0; u < kRowVecs; ++u) n += mo[u] >= mid ? 1u : 0u;
+      if ((int)__reduce_add_sync(0xffffffffu, n) >= cw) lo = mid;
+      else hi = mid - 1;
+    }
+    if (lane == 0) atomicMin(&S.tcode, lo << 16);
+    __syncthreads();
+    if (tid == 0) {
+      S.kappa = (unsigned long long)S.tcode << 32;
+      S.tcode = ~0u;  // for raise_held
+    }
+    __syncthreads();
+  }
+  const unsigned long long kap = S.kappa;
+  const float kv = kap ? key_value(kap) : -INFINITY;
+  int cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kRowVecs; ++u)
+    if (vm[u] >= kv && vm[u] > -INFINITY)
+      vec_candidates<DT, VEC>(vidx[u], X[u], kap, [&](unsigned long long) { ++cnt; });
+  if (__syncthreads_or(cnt > 0)) append_chunk<DT, VEC, kRowVecs>(S, K, vidx, X, vm, cnt);
+}
+
+// The row's candidates are held: rank them, softmax and top-p cut over the
+// top K, and publish the kept list (token, probability) and the probability
+// of the draft token this row tests.
+__device__ __forceinline__ void publish_row(RowSmem& S, const ChainArgs& a, int b, int r, int kb) {
+  const int tid = threadIdx.x;
+  const int K = a.top_k, k = a.k;
+  int n = S.n;
+  if (n > kRankMax) {
+    cut_held(S, K);
+    n = S.n;
+  }
+  rank_held(S, n, K);
+  const int kk = min(n, K);  // real keys in S.top
+
+  // Softmax over the top K at temperature T, then the top-p cut; thread t
+  // holds entries 2t and 2t + 1 (K <= 2 * kRowThreads).
+  const float xmax = kk > 0 ? key_value(S.top[0]) : 0.f;
+  float e[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int i = 2 * tid + q;
+    e[q] = i < kk ? ex2(scaled(key_value(S.top[i]) - xmax, a.c_hi, a.c_lo)) : 0.f;
+  }
+  float sk;
+  const float before = row_block_scan_f(e[0] + e[1], S, &sk);
+  const float incl[2] = {before + e[0], before + e[0] + e[1]};
+  if (tid == 0) S.m = K;
+  __syncthreads();
+  if (a.top_p < 1.f) {
+#pragma unroll
+    for (int q = 1; q >= 0; --q)
+      if (e[q] > 0.f && incl[q] / sk >= a.top_p) atomicMin(&S.m, 2 * tid + q + 1);
+  }
+  __syncthreads();
+  const int m = S.m;  // kept: the first m entries (zero weights past kk)
+  if (2 * tid == m - 1) S.sm = incl[0];
+  if (2 * tid + 1 == m - 1) S.sm = incl[1];
+  __syncthreads();
+  const float sm = S.sm;
+  unsigned long long* rw = row_words_of(a, b, r);
+  const int pos_x = r <= k ? r : r - k - 1;  // the draft token this row tests
+  const int x = pos_x < kb ? a.tokens[(size_t)b * k + pos_x] : -1;
+  float* pq = a.ws.pq + (size_t)b * 2 * k;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int i = 2 * tid + q;
+    if (i < K) {
+      const bool kept = i < kk && i < m && e[q] > 0.f;
+      const float prob = kept ? e[q] / sm : 0.f;
+      const int t = kept ? key_token(S.top[i]) : -1;
+      rw[i] = kept ? ((unsigned long long)(t + 1) << 32) | __float_as_uint(prob) : 0ull;
+      if (kept && t == x) pq[(r <= k ? 0 : k) + pos_x] = prob;
+    }
+  }
+}
+
+// The request's ticket (acquire-release: the row's published words before
+// it, the other rows' after it); the last of its row CTAs finishes it.
+__device__ __forceinline__ void row_done(RowSmem& S, const ChainArgs& a, int b) {
+  const int R = 2 * a.k + 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(t)
+                 : "l"(&a.ws.sync[b].tick2)
+                 : "memory");
+    S.last = t == R - 1;
+    if (S.last) a.ws.sync[b].tick2 = 0;
+  }
+  __syncthreads();
+  if (S.last) finish_request(S, a, b);
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) filter_row_kernel(const __grid_constant__ ChainArgs a) {
+  using IO = Io<DT, VEC>;
+  constexpr int NW = IO::NW;
+  __shared__ RowSmem S;
+  const int tid = threadIdx.x;
+  const int K = a.top_k, k = a.k, R = 2 * k + 1;
+  const int b = blockIdx.x / R, r = blockIdx.x - b * R;
+  const int kraw = a.draft_lens ? a.draft_lens[b] : k;
+  const int kb = (kraw < 0 || kraw > k) ? 0 : kraw;
+
+  if (row_used(k, kraw, r)) {
+    const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
+    const int nvec = a.nvec;
+    const int nch = ceil_div(nvec, kChunkVecs);
+    if (tid == 0) {
+      S.n = 0;
+      S.kappa = 0;
+      S.tcode = ~0u;
+    }
+    uint32_t X0[kRowVecs][NW], X1[kRowVecs][NW];
+    load_chunk<DT, VEC>(row, 0, nvec, X0);
+    if (nch > 1) load_chunk<DT, VEC>(row, 1, nvec, X1);
+    __syncthreads();
+    for (int c = 0; c < nch; c += 2) {  // chunk c + 2 loads while c + 1 is filtered
+      filter_chunk<DT, VEC>(S, K, c, nvec, X0);
+      if (c + 2 < nch) load_chunk<DT, VEC>(row, c + 2, nvec, X0);
+      if (c + 1 < nch) {
+        filter_chunk<DT, VEC>(S, K, c + 1, nvec, X1);
+        if (c + 3 < nch) load_chunk<DT, VEC>(row, c + 3, nvec, X1);
+      }
+    }
+    __syncthreads();
+    publish_row(S, a, b, r, kb);
+  }
+  row_done(S, a, b);
+}
+
+// ------------------------------------------------------------------ rows with 16-byte vectors
+// Pass 1, filter_max_kernel: one CTA per 32 KB slice of a row (request-major
+// order), each thread's 8 vectors read once with 128-bit loads.  For each
+// group of 8 contiguous vectors (128 bytes) it writes only the 16-bit prefix
+// of the order bits of the group's largest logit (0: no finite logit), so
+// the pass has the streaming shape of the unfiltered pass 1 without its
+// exponentials.
+// Pass 2, filter_pick_kernel: one CTA per row.  tau: a prefix that at
+// least K of the row's group prefixes reach (per-warp bisection); at least
+// K logits are >= tau (those groups' maxima), so the row's top K all lie in
+// the groups whose prefix is >= tau (somewhat more than K of them).  Only
+// those groups are read again (one 128-byte line each); their logits with
+// key >= tau << 48 are the candidates.
+constexpr int kSegSlices = 8;                     // slices per selection segment
+constexpr int kPickVecs = 6;                      // vectors a pick thread reads per round
+constexpr int kPickCtasPerSm = 7;                 // 1064 rows resident on 152 SMs
+constexpr int kSegPairs = kSegSlices * kThreads;  // (slice, group) pairs per segment
+constexpr int kMaxCodes = 16384;                  // thread prefixes a pick CTA holds
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs a) {
+  using IO = Io<DT, VEC>;
+  const int tid = threadIdx.x;
+  const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
+  const int R = 2 * a.k + 1;
+  const int b = rr / R, r = rr - b * R;
+  if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
+  const int vbeg = s * a.vps;
+  // this thread's vectors vbeg + tid + u * kThreads, u < nv
+  const int nv = min(kVecPerThread, max(0, min(a.nvec - vbeg, a.vps) - tid + kThreads - 1) / kThreads);
+  const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES) + (size_t)(vbeg + tid) * (VEC ? 16 : IO::ES);
+  uint32_t w[kVecPerThread][IO::NW];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u)
+    if (u < nv) IO::load(row, u * kThreads, w[u]);
+  // Group g of the slice = its vectors 8g .. 8g + 7 (128 contiguous bytes),
+  // held by lanes 8 (g mod 4) .. + 7 of warp (g / 4) mod 8 for u = g / 32:
+  // each lane's vector maximum, then the maximum over its eight lanes.
+  unsigned short* out = a.ws.codes + (size_t)blockIdx.x * kThreads;
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
-    const int v = vbeg + tid + u * kThreads;
-    const bool hit = v < vend && vm[u] >= tau && vm[u] > -INFINITY;
-    const unsigned bal = __ballot_sync(0xffffffffu, hit);
-    if (bal) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&sNV, __popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      const int slot = base + __popc(bal & ((1u << lane) - 1u));
-      if (hit && slot < kQCap) {
+    float m = u < nv ? IO::vmax(w[u]) : -INFINITY;
 #pragma unroll
-        for (int q = 0; q < NW; ++q) sVec[slot][q] = w[u][q];
-        sVecIdx[slot] = v;
+    for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 7) == 0)
+      out[tid / 8 + u * (kThreads / 8)] = (unsigned short)(m > -INFINITY ? ord32(m) >> 16 : 0u);
+  }
+}
+
+// A threshold t with at least K of the n codes >= t (0 excluded; 0 when a
+// warp holds fewer than cw nonzero codes): warp w takes codes w*32 + lane +
+// 128 j and finds its cw-th largest (cw = ceil(K / 4); bisection between its
+// least and largest nonzero code, ballot counts); t is the least of the four
+// (no shared-memory atomics: the codes of a row cluster on few values).
+__device__ uint32_t code_threshold(const unsigned short* codes, int n, int K, RowSmem& S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cw = (K + kRowWarps - 1) / kRowWarps;
+  constexpr int kReg = kSegPairs / kRowThreads;  // codes per lane held in registers
+  uint32_t c[kReg];
+  const bool in_regs = n <= kSegPairs;
+  uint32_t lo = ~0u, hi = 0;
+  int nz = 0;
+  if (in_regs) {
+#pragma unroll
+    for (int q = 0; q < kReg; ++q) {
+      const int i = warp * 32 + lane + q * kRowThreads;
+      c[q] = i < n ? codes[i] : 0u;
+      if (c[q]) {
+        lo = min(lo, c[q]);
+        hi = max(hi, c[q]);
+        ++nz;
+      }
+    }
+  } else {
+    for (int i = warp * 32 + lane; i < n; i += kRowThreads) {
+      const uint32_t v = codes[i];
+      if (v) {
+        lo = min(lo, v);
+        hi = max(hi, v);
+        ++nz;
       }
     }
   }
-  __syncthreads();
-  const int nv = sNV;
-  if (nv <= kQCap) {
-    for (int i = tid; i < nv; i += kThreads) {
-      uint32_t ww[NW];
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  nz = (int)__reduce_add_sync(0xffffffffu, (unsigned)nz);
+  uint32_t t = 0;
+  if (nz >= cw) {
+    while (lo < hi) {  // the warp's nz >= cw codes are all >= lo
+      const uint32_t mid = (lo + hi + 1) >> 1;
+      unsigned m = 0;
+      if (in_regs) {
 #pragma unroll
-      for (int q = 0; q < NW; ++q) ww[q] = sVec[i][q];
-      float e[EPV];
-      IO::unpack(ww, e);
-      const long t0 = (long)sVecIdx[i] * EPV;
-#pragma unroll
-      for (int q = 0; q < EPV; ++q)
-        if (e[q] >= tau && e[q] > -INFINITY) {
-          const int slot = atomicAdd(&sNC, 1);
-          if (slot < kCCap) sKey[slot] = make_key(e[q], t0 + q);
-        }
+        for (int q = 0; q < kReg; ++q) m += c[q] >= mid ? 1u : 0u;
+      } else {
+        for (int i = warp * 32 + lane; i < n; i += kRowThreads) m += codes[i] >= mid ? 1u : 0u;
+      }
+      if ((int)__reduce_add_sync(0xffffffffu, m) >= cw) lo = mid;
+      else hi = mid - 1;
     }
+    t = lo;
   }
+  if (threadIdx.x == 0) S.tcode = ~0u;
   __syncthreads();
-  int nc = sNC;
-  if (nv > kQCap || nc > kCCap) {
-    // Exact selection (many equal logits).  First the K-th largest finite
-    // value tv (bisection on its order bits), then, if the logits equal to tv
-    // are too many to sort, the highest token index among them that is kept.
-    auto count_if = [&](auto pred) {
-      int c = 0;
-#pragma unroll
-      for (int u = 0; u < kVecPerThread; ++u) {
-        const int v = vbeg + tid + u * kThreads;
-        if (v < vend) {
-          float e[EPV];
-          IO::unpack(w[u], e);
-#pragma unroll
-          for (int q = 0; q < EPV; ++q) c += pred(e[q], (long)v * EPV + q) ? 1 : 0;
+  if (lane == 0) atomicMin(&S.tcode, t);
+  __syncthreads();
+  t = S.tcode;
+  __syncthreads();  // S.tcode is rewritten next
+  return t;
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kernel(
+    const __grid_constant__ ChainArgs a) {
+  using IO = Io<DT, VEC>;
+  constexpr int NW = IO::NW;
+  __shared__ RowSmem S;
+  __shared__ unsigned short pairs[kSegPairs];  // (slice - segment start) << 8 | group
+  extern __shared__ unsigned short codes[];    // the row's thread prefixes
+  const int tid = threadIdx.x;
+  const int K = a.top_k, k = a.k, R = 2 * k + 1, ns = a.nsplit;
+  const int b = blockIdx.x / R, r = blockIdx.x - b * R;
+  const int kraw = a.draft_lens ? a.draft_lens[b] : k;
+  const int kb = (kraw < 0 || kraw > k) ? 0 : kraw;
+
+  if (row_used(k, kraw, r)) {
+    const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
+    const int n = ns * kThreads;
+    uint4* g = reinterpret_cast<uint4*>(a.ws.codes + (size_t)blockIdx.x * n);
+    for (int i = tid; i < n / 8; i += kRowThreads) {  // eight codes per 16-byte load
+      reinterpret_cast<uint4*>(codes)[i] = __ldcg(g + i);
+      g[i] = make_uint4(0, 0, 0, 0);  // every call leaves the workspace zero
+    }
+    if (tid == 0) S.n = 0;
+    __syncthreads();
+    const uint32_t tau = code_threshold(codes, n, K, S);
+    if (tid == 0) {
+      S.kappa = (unsigned long long)tau << 48;
+      S.tcode = ~0u;  // for raise_held
+    }
+    __syncthreads();
+    // The groups whose prefix is >= tau, a segment of slices at a time;
+    // their vectors, kPickVecs per CTA thread per round.
+    for (int s0 = 0; s0 < ns; s0 += kSegSlices) {
+      const int s1 = min(ns, s0 + kSegSlices);
+      int mine = 0;
+      for (int s = s0; s < s1; ++s)
+        for (int t = tid; t < kThreads; t += kRowThreads) {
+          const uint32_t c = codes[s * kThreads + t];
+          mine += (c != 0 && c >= tau) ? 1 : 0;
         }
-      }
-      return block_sum(c, &sCnt);
-    };
-    const int finite = count_if([](float x, long) { return x > -INFINITY; });
-    float tv = -INFINITY;
-    if (finite > K) {
-      uint32_t o = 0;
-      for (int bit = 31; bit >= LOBIT; --bit) {
-        const uint32_t c = o | (1u << bit);
-        if (count_if([&](float x, long) { return x > -INFINITY && ord32(x) >= c; }) >= K) o = c;
-      }
-      if (LOBIT && !(o & 0x80000000u)) o |= 0xffffu;  // the bf16 value's own code
-      tv = unord32(o);
-    }
-    const int above = count_if([&](float x, long) { return x > -INFINITY && x > tv; });
-    const int ties = count_if([&](float x, long) { return x > -INFINITY && x == tv; });
-    long tmax = LONG_MAX;  // tied tokens above this index are not kept
-    if (above + ties > kCCap) {
-      const int need = K - above;  // 1 <= need <= ties
-      long lo = (long)vbeg * EPV, hi = (long)vend * EPV - 1;
-      while (lo < hi) {  // smallest index with `need` ties at or below it
-        const long mid = lo + (hi - lo) / 2;
-        if (count_if([&](float x, long tt) { return x > -INFINITY && x == tv && tt <= mid; }) >= need)
-          hi = mid;
-        else
-          lo = mid + 1;
-      }
-      tmax = lo;
-    }
-    __syncthreads();
-    if (tid == 0) sNC = 0;
-    __syncthreads();
+      int npairs;
+      int off = row_block_scan(mine, S, &npairs);
+      for (int s = s0; s < s1; ++s)
+        for (int t = tid; t < kThreads; t += kRowThreads) {
+          const uint32_t c = codes[s * kThreads + t];
+          if (c != 0 && c >= tau) pairs[off++] = (unsigned short)(((s - s0) << 8) | t);
+        }
+      __syncthreads();
+      const int items = npairs * kVecPerThread;  // (pair, vector) items
+      for (int i0 = 0; i0 < items; i0 += kRowThreads * kPickVecs) {
+        uint32_t X[kPickVecs][NW];
+        int vidx[kPickVecs];
+        float vm[kPickVecs];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int v = vbeg + tid + u * kThreads;
-      if (v < vend) {
-        float e[EPV];
-        IO::unpack(w[u], e);
-#pragma unroll
-        for (int q = 0; q < EPV; ++q) {
-          const long tt = (long)v * EPV + q;
-          if (e[q] > -INFINITY && (e[q] > tv || (e[q] == tv && tt <= tmax))) {
-            const int slot = atomicAdd(&sNC, 1);
-            if (slot < kCCap) sKey[slot] = make_key(e[q], tt);
+        for (int u = 0; u < kPickVecs; ++u) {
+          const int i = i0 + tid + u * kRowThreads;
+          vidx[u] = -1;
+          if (i < items) {
+            const int p = pairs[i / kVecPerThread], uu = i % kVecPerThread;
+            const int s = s0 + (p >> 8), g = p & 0xff;
+            const int vbeg = s * a.vps, nvs = min(a.nvec, vbeg + a.vps) - vbeg;
+            if (8 * g + uu < nvs) {
+              vidx[u] = vbeg + 8 * g + uu;
+              IO::load(row, vidx[u], X[u]);
+            }
           }
         }
+#pragma unroll
+        for (int u = 0; u < kPickVecs; ++u) vm[u] = vidx[u] >= 0 ? IO::vmax(X[u]) : -INFINITY;
+        const unsigned long long kap = S.kappa;
+        const float kv = kap ? key_value(kap) : -INFINITY;
+        int cnt = 0;
+#pragma unroll
+        for (int u = 0; u < kPickVecs; ++u)
+          if (vm[u] >= kv && vm[u] > -INFINITY)
+            vec_candidates<DT, VEC>(vidx[u], X[u], kap, [&](unsigned long long) { ++cnt; });
+        if (__syncthreads_or(cnt > 0)) append_chunk<DT, VEC, kPickVecs>(S, K, vidx, X, vm, cnt);
       }
+      __syncthreads();  // pairs is rewritten by the next segment
     }
     __syncthreads();
-    nc = min(sNC, kCCap);
+    publish_row(S, a, b, r, kb);
   }
-  bitonic_sort<false>(sKey, nc, 0ull);
-  unsigned long long* out =
-      a.ws.cand + (((size_t)b * (2 * a.k + 1) + r) * a.nsplit + s) * (size_t)K;
-  for (int i = tid; i < K; i += kThreads) st_relaxed_u64(out + i, i < nc ? sKey[i] : kNone);
+  row_done(S, a, b);
 }
 
-// ------------------------------------------------------------------ pass 2
-// One (request, row) item: merge, filter, publish; the request's last item
-// finishes the request.
-__device__ void filter_row_item(const ChainArgs& a, int b, int r, unsigned long long* sL) {
-  __shared__ unsigned long long sTop[kThreads];
-  __shared__ float sWarpF[kWarps];
-  __shared__ unsigned long long sWarpU[kWarps];
-  __shared__ float sP[SPEC_MAX_DRAFT], sQ[SPEC_MAX_DRAFT], sU[SPEC_MAX_DRAFT + 1];
-  __shared__ int sM, sJ, sLast, sTok;
-  __shared__ float sSm;
+// The request's last row CTA finishes it: accept scan, final draw, outputs,
+// cleanup (thread t: position t of the scan; entries t and t + kRowThreads
+// of target row j's kept list).
+__device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int b) {
   const int tid = threadIdx.x;
-  const int k = a.k, R = 2 * k + 1, K = a.top_k, ns = a.nsplit;
+  const int k = a.k, R = 2 * k + 1, K = a.top_k;
   const int kraw = a.draft_lens ? a.draft_lens[b] : k;
   const bool bad_len = kraw < 0 || kraw > k;
   const int kb = bad_len ? 0 : kraw;
-  auto row_words = [&](int rr) {
-    return a.ws.cand + ((size_t)b * R + rr) * (size_t)ns * K;
-  };
   float* pq = a.ws.pq + (size_t)b * 2 * k;
-
-  if (row_used(k, kraw, r)) {
-    unsigned long long* rw = row_words(r);
-    const int n = ns * K;
-    for (int i = tid; i < n; i += kThreads) {
-      unsigned long long v = ld_relaxed_u64(rw + i);
-      if (!v) v = wait_word(rw + i, a.ws.status, kNone);
-      sL[i] = v;
-    }
-    if (tid < K) sTop[tid] = kNone;
-    if (tid == 0) sM = K;
-    __syncthreads();
-    // Global rank of each key: its place in its own (descending) list plus
-    // the keys above it in every other list (keys are unique).
-    for (int i = tid; i < n; i += kThreads) {
-      const unsigned long long key = sL[i];
-      if (key == kNone) continue;
-      const int sl = i / K;
-      int rank = i - sl * K;
-      for (int s2 = 0; s2 < ns && rank < K; ++s2)
-        if (s2 != sl) rank += count_above(sL + (size_t)s2 * K, K, key);
-      if (rank < K) sTop[rank] = key;
-    }
-    __syncthreads();
-    for (int i = K + tid; i < n; i += kThreads) rw[i] = 0;  // the first K words get the kept list
-
-    // Softmax over the top K (temperature T), then the top-p cut.
-    const unsigned long long key = tid < K ? sTop[tid] : kNone;
-    const bool real = key != kNone;
-    const float xmax = sTop[0] != kNone ? key_value(sTop[0]) : 0.f;
-    const float e = real ? ex2(scaled(key_value(key) - xmax, a.c_hi, a.c_lo)) : 0.f;
-    float sk;
-    const float incl = block_incl_scan(e, sWarpF, &sk);
-    if (a.top_p < 1.f && real && incl / sk >= a.top_p) atomicMin(&sM, tid + 1);
-    __syncthreads();
-    const int m = sM;  // kept: the first m (ranks past the real keys carry no weight)
-    if (tid == m - 1) sSm = incl;
-    __syncthreads();
-    const float prob = (real && tid < m) ? e / sSm : 0.f;
-    const int tok = real ? key_token(key) : -1;
-    if (tid < K)
-      rw[tid] = (real && tid < m)
-                    ? ((unsigned long long)(tok + 1) << 32) | __float_as_uint(prob)
-                    : 0ull;
-    // The probability of the draft token this row tests.
-    const int pos = r <= k ? r : r - k - 1;
-    if (pos < kb && tok >= 0 && tid < m) {
-      const int x = a.tokens[(size_t)b * k + pos];
-      if (x == tok) pq[(r <= k ? 0 : k) + pos] = prob;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int t = atomicAdd(&a.ws.sync[b].tick2, 1);
-    sLast = t == R - 1;
-    if (sLast) {
-      a.ws.sync[b].tick2 = 0;
-      __threadfence();
-    }
-  }
-  __syncthreads();
-  if (!sLast) return;
-
-  // ---------------------------------------------------------- finish
+  float P = 0.f, Q = 0.f, U = 0.f;
   bool bad = bad_len;
   if (tid < kb) {
     const int x = a.tokens[(size_t)b * k + tid];
     bad = x < 0 || x >= a.V;
-    sP[tid] = __ldcg(pq + tid);
-    sQ[tid] = __ldcg(pq + k + tid);
+    P = __ldcg(pq + tid);
+    Q = __ldcg(pq + k + tid);
   }
   if (tid <= k)
-    sU[tid] = a.uniforms ? a.uniforms[(size_t)b * (k + 1) + tid]
-                         : philox_uniform(a.seeds[b], a.offsets[b], tid);
-  const int any_bad = __syncthreads_or(bad);
-  if (tid < 32) {  // accept scan: r_i < p_i(x_i) / q_i(x_i), q == 0 accepts
-    unsigned rej[2];
+    U = a.uniforms ? a.uniforms[(size_t)b * (k + 1) + tid]
+                   : philox_uniform(a.seeds[b], a.offsets[b], tid);
+  if (tid == 0) S.m = kb;
+  if (tid == kb) S.sm = U;  // the final draw's uniform
+  const bool any_bad = __syncthreads_or(bad);
+  // accept x_i iff r_i < p_i(x_i) / q_i(x_i) (q = 0 accepts); j = the first rejection
+  const float ratio = Q > 0.f ? P / Q : INFINITY;
+  if (tid < kb && !(U < ratio)) atomicMin(&S.m, tid);
+  __syncthreads();
+  const int j = any_bad ? -1 : S.m;
+  const double u = (double)S.sm;
+  int32_t* out = a.out_tokens + (size_t)b * (k + 1);
+  unsigned long long* F = S.top;                   // draw weights
+  int* T = reinterpret_cast<int*>(S.buf + K);      // kept tokens of target row j
+  if (j >= 0) {
+    // Target row j's kept tokens, p and the weight max(0, p - q_j) (bonus
+    // row: p) in exact fixed point (scaled by 2^31, each < 2^32); draft row
+    // j's kept list in S.buf.
+    if (j < kb)
+      for (int i = tid; i < K; i += kRowThreads) S.buf[i] = __ldcg(row_words_of(a, b, k + 1 + j) + i);
+    int tk[2];
+    float p[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int i = tid + 32 * h;
-      bool rj = false;
-      if (i < kb) {
-        const float ratio = sQ[i] > 0.f ? sP[i] / sQ[i] : INFINITY;
-        rj = !(sU[i] < ratio);
-      }
-      rej[h] = __ballot_sync(0xffffffffu, rj);
+      const int i = tid + h * kRowThreads;
+      const unsigned long long w = i < K ? __ldcg(row_words_of(a, b, j) + i) : 0ull;
+      tk[h] = w ? (int)(w >> 32) - 1 : INT_MAX;
+      p[h] = w ? __uint_as_float((uint32_t)w) : 0.f;
     }
-    if (tid == 0) sJ = any_bad ? -1 : rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : kb;
-  }
-  __syncthreads();
-  const int j = sJ;
-  int32_t* out = a.out_tokens + (size_t)b * (k + 1);
-  if (j >= 0) {
-    // Kept tokens of target row j in token order, with p and the weight
-    // max(0, p - q_j) (bonus row: p).
-    const unsigned long long* pw = row_words(j);
-    unsigned long long* sQW = sL;  // draft row j's kept list
-    if (j < kb)
-      for (int i = tid; i < K; i += kThreads) sQW[i] = __ldcg(row_words(k + 1 + j) + i);
-    const unsigned long long word = tid < K ? __ldcg(pw + tid) : 0ull;
-    sTop[tid] = word ? word - (1ull << 32) : ~0ull;  // (token << 32 | p bits), ascending sort
     __syncthreads();
-    bitonic_sort<true>(sTop, kThreads, ~0ull);
-    const unsigned long long ent = sTop[tid];
-    const bool kept = ent != ~0ull;
-    const int tok = kept ? (int)(ent >> 32) : -1;
-    const float p = kept ? __uint_as_float((uint32_t)ent) : 0.f;
-    float q = 0.f;
-    if (kept && j < kb)
-      for (int i = 0; i < K; ++i) {
-        const unsigned long long qe = sQW[i];
-        if ((int)(qe >> 32) == tok + 1) {
-          q = __uint_as_float((uint32_t)qe);
-          break;
+    unsigned long long f[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float qv = 0.f;
+      if (tk[h] != INT_MAX && j < kb)
+        for (int i = 0; i < K; ++i) {
+          const unsigned long long e = S.buf[i];
+          if ((int)(e >> 32) == tk[h] + 1) {
+            qv = __uint_as_float((uint32_t)e);
+            break;
+          }
+        }
+      f[h] = tk[h] != INT_MAX ? to_fixed(fmaxf(p[h] - qv, 0.f) * 2147483648.0f) : 0ull;
+    }
+    // Inverse CDF in token order without sorting: an entry's prefix is the
+    // sum of the weights of the kept tokens below it.
+    unsigned long long pre[2] = {0, 0}, Z = 0;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = tid + h * kRowThreads;
+        if (i < K) {
+          F[i] = f[h];
+          T[i] = tk[h];
         }
       }
-    // Exact prefix sums of the weights scaled by 2^31 (each < 2^32).
-    const float wres = fmaxf(p - q, 0.f);
-    unsigned long long Z;
-    unsigned long long f = to_fixed(wres * 2147483648.0f);
-    unsigned long long incl = block_incl_scan(f, sWarpU, &Z);
-    if (Z == 0) {  // the residual vanished numerically: draw from p_j
-      f = to_fixed(p * 2147483648.0f);
-      incl = block_incl_scan(f, sWarpU, &Z);
+      __syncthreads();
+      pre[0] = pre[1] = 0;
+      Z = 0;
+      if (tid < K) {  // entries >= K carry nothing
+        for (int i = 0; i < K; ++i) {
+          const unsigned long long fi = F[i];
+          const int ti = T[i];
+          Z += fi;
+          pre[0] += ti < tk[0] ? fi : 0ull;
+          pre[1] += ti < tk[1] ? fi : 0ull;
+        }
+      }
+      if (tid == 0) S.kappa = Z;  // the same total in every thread that summed
+      __syncthreads();
+      Z = S.kappa;
+      __syncthreads();
+      if (Z != 0) break;
+      // The residual vanished numerically: draw from p_j.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) f[h] = tk[h] != INT_MAX ? to_fixed(p[h] * 2147483648.0f) : 0ull;
     }
-    if (tid == 0) sTok = 0;  // no kept token at all (a row without a finite logit)
-    __syncthreads();
-    const double u = (double)sU[kb];
     const unsigned long long target = (unsigned long long)(u * (double)Z);  // < Z
-    if (f > 0 && incl > target && incl - f <= target) sTok = tok;
+    if (tid == 0) S.red = 0;  // no kept token at all (a row without a finite logit)
     __syncthreads();
-    const int drawn = sTok;
-    for (int i = tid; i <= k; i += kThreads)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (f[h] > 0 && pre[h] <= target && pre[h] + f[h] > target) S.red = tk[h];
+    __syncthreads();
+    const int drawn = S.red;
+    for (int i = tid; i <= k; i += kRowThreads)
       out[i] = i < j ? a.tokens[(size_t)b * k + i] : (i == j ? drawn : -1);
     if (a.out_probs && tid < k) {  // padded positions are not verified: NaN
-      a.out_probs[((size_t)b * k + tid) * 2] = tid < kb ? sP[tid] : NAN;
-      a.out_probs[((size_t)b * k + tid) * 2 + 1] = tid < kb ? sQ[tid] : NAN;
+      a.out_probs[((size_t)b * k + tid) * 2] = tid < kb ? P : NAN;
+      a.out_probs[((size_t)b * k + tid) * 2 + 1] = tid < kb ? Q : NAN;
     }
     if (tid == 0) {
       a.out_n[b] = j;
       if (a.seq_lens) a.seq_lens[b] += j + 1;
     }
   } else {  // a draft token or the draft length was invalid: fail closed
-    for (int i = tid; i <= k; i += kThreads) out[i] = -1;
+    for (int i = tid; i <= k; i += kRowThreads) out[i] = -1;
     if (a.out_probs)
-      for (int i = tid; i < 2 * k; i += kThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
+      for (int i = tid; i < 2 * k; i += kRowThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
     if (tid == 0) {
       a.out_n[b] = -1;
       set_status(a.ws.status, SPEC_EBADINDEX);
     }
   }
   // Every call leaves the workspace zero: the kept lists and probabilities.
-  __syncthreads();
-  for (int i = tid; i < R * K; i += kThreads)
-    if (row_used(k, kraw, i / K)) row_words(i / K)[i - (i / K) * K] = 0;
-  for (int i = tid; i < 2 * k; i += kThreads) pq[i] = 0.f;
-}
-
-__global__ void __launch_bounds__(kThreads) filter_finish_kernel(const ChainArgs a) {
-  extern __shared__ unsigned long long sL[];  // nsplit * top_k keys of one row
-  const int R = 2 * a.k + 1;
-  const int items = a.B * R;
-  for (int h = blockIdx.x; h < items; h += gridDim.x) {
-    const int b = h / R;
-    filter_row_item(a, b, h - b * R, sL);
-    __syncthreads();
-  }
-  // Completion of this grid then implies completion of pass 1.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// CTAs of the finish grid that fit on the device at once for `smem` bytes
-// of dynamic shared memory (the last query is cached).
-cudaError_t finish_grid(size_t smem, int* grid) {
-  static std::mutex mu;
-  static int cdev = -1, cgrid = 0;
-  static size_t csmem = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev != cdev || smem != csmem) {
-    e = cudaFuncSetAttribute(filter_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, filter_finish_kernel, kThreads,
-                                                      smem);
-    if (e != cudaSuccess) return e;
-    cdev = dev;
-    csmem = smem;
-    cgrid = sms * (per_sm > 0 ? per_sm : 1);
-  }
-  *grid = cgrid;
-  return cudaSuccess;
+  for (int i = tid; i < R * K; i += kRowThreads)
+    if (row_used(k, kraw, i / K)) row_words_of(a, b, i / K)[i - (i / K) * K] = 0;
+  for (int i = tid; i < 2 * k; i += kRowThreads) pq[i] = 0.f;
 }
 
 template <int DT, bool VEC>
 cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(unsigned long long) * (size_t)a.nsplit * a.top_k;
-  int slots = 0;
-  cudaError_t e = finish_grid(smem, &slots);
-  if (e != cudaSuccess) return e;
-  const long g1 = (long)a.B * (2 * a.k + 1) * a.nsplit;
-  filter_topk_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long items = (long)a.B * (2 * a.k + 1);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(items < slots ? items : slots));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, filter_finish_kernel, a);
+  const long rows = (long)a.B * (2 * a.k + 1);
+  if ((long)a.nsplit * kThreads <= kMaxCodes) {
+    filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    filter_pick_kernel<DT, VEC><<<(unsigned)rows, kRowThreads,
+                                  sizeof(unsigned short) * a.nsplit * kThreads, st>>>(a);
+  } else {  // a row too wide for one CTA's prefixes: stream it through one CTA
+    filter_row_kernel<DT, VEC><<<(unsigned)rows, kRowThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
