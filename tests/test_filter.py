@@ -160,6 +160,24 @@ def test_cuda_filtered_misaligned_and_arbitrary_tokens(dtype):
 
 
 @pytest.mark.gpu
+def test_cuda_filtered_wide_unaligned_rows():
+    # V = 140001 fp32 with unaligned rows: 69 slices of 2048 logits, more
+    # group codes than one CTA holds, so each row streams through one CTA
+    # with a running candidate threshold (and the heavy-tie case with it).
+    from test_gpu_parity import check_chain
+    w = workloads.make("chain_b1_k4_v1024_f32", seed=39, B=3, k=2, V=140001)
+    w["draft_tokens"] = _filtered_tokens(w, 40, 0.9, 39)
+    g = _run_filtered(w, 40, 0.9, misalign=True)
+    check_chain(w, g, _oracle_filtered(w, 40, 0.9), "filtered wide unaligned rows")
+    rng = np.random.default_rng(39)
+    w["target"] = rng.integers(0, 2, size=w["target"].shape).astype(np.float32)
+    w["draft"] = (w["target"][:, :2] + rng.integers(0, 2, size=w["draft"].shape)).astype(np.float32)
+    w["draft_tokens"] = _filtered_tokens(w, 40, 0.935, 39)
+    g = _run_filtered(w, 40, 0.935, misalign=True)
+    check_chain(w, g, _oracle_filtered(w, 40, 0.935), "filtered wide unaligned rows, ties")
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("levels", [3, 1])
 def test_cuda_filtered_ties(levels):
     # Logits on a few levels: thousands of equal values per slice force the
