@@ -389,7 +389,7 @@ def run_ours(args, rank, world, local):
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
             "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
-                       "filtered": "spec_verify_chain_ex call (filter_topk_kernel + filter_finish_kernel)",
+                       "filtered": "spec_verify_chain_ex call (filter_max_kernel + filter_pick_kernel)",
                        "greedy": "spec_verify_greedy call (argmax_kernel + argmax_finish_kernel)",
                        "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)"}[kernel_key],
             "algorithmic_bytes_per_call": algo_bytes,
