@@ -293,3 +293,37 @@ def test_cuda_filtered_full_size_sampled():
                seq_lens=w["seq_lens"][sel])
     gs = {key: g[key][sel] for key in g}
     check_chain(sub, gs, _oracle_filtered(sub, 50, 0.9), "filtered full size (sampled)")
+
+
+def test_filtered_softmax_properties():
+    # Against numpy's own ordering and exponential on random rows (with
+    # repeated values): the kept set is the top_k by (logit desc, index asc)
+    # cut to the shortest prefix reaching top_p; the kept sets nest as top_p
+    # grows; p is the softmax of x / T restricted to the kept set.
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        V = int(rng.integers(2, 60))
+        x = rng.integers(-4, 5, size=V).astype(np.float32) * 0.5
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        K = int(rng.integers(1, V + 3))
+        order = np.lexsort((np.arange(V), -x.astype(np.float64)))[: min(K, V)]
+        prev = None
+        for top_p in (0.3, 0.6, 0.9, 1.0):
+            p, tie = oracle.filtered_softmax(x, T, K, float(np.float32(top_p)))
+            kept = np.flatnonzero(p > 0)
+            m = kept.size
+            assert set(kept) == set(order[:m])          # a prefix of the order
+            w = np.exp(x[order].astype(np.float64) / np.float64(np.float32(T)) -
+                       x[order[0]] / np.float64(np.float32(T)))
+            cum = np.cumsum(w / w.sum())
+            if top_p < 1.0 and not tie:
+                assert cum[m - 1] >= np.float32(top_p) - 1e-12
+                assert m == 1 or cum[m - 2] < np.float32(top_p) + 1e-12
+            else:
+                assert top_p < 1.0 or m == min(K, V)
+            ref = np.zeros(V)
+            ref[order[:m]] = w[:m] / w[:m].sum()
+            assert np.allclose(p, ref, rtol=1e-12, atol=1e-15)
+            if prev is not None:
+                assert set(prev) <= set(kept)
+            prev = kept
