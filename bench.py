@@ -350,7 +350,8 @@ def run_ours(args, rank, world, local):
     achieved = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
     kernel_key = "tree" if tree else ("greedy" if greedy else ("filtered" if filtered else "chain"))
-    traffic = recorded_traffic(f"{args.config}/{kernel_key}")
+    traffic = recorded_traffic(f"{args.config}/{kernel_key}"
+                               + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""))
     stats = sv.acceptance_stats(n_first, k)
 
     cpu = None
