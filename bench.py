@@ -132,9 +132,10 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def csrc_digest() -> str:
+def csrc_digest(files=None) -> str:
+    """sha256 of the named csrc files (all of csrc/ when None)."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in sorted(files) if files else sorted(os.listdir(CSRC)):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()
@@ -147,7 +148,7 @@ def recorded_traffic(key: str):
             rec = json.load(f).get(key)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("csrc_sha256") != csrc_digest():
+    if not rec or rec.get("csrc_sha256") != csrc_digest(rec.get("files")):
         return None
     return rec.get("dram_bytes_per_call")
 

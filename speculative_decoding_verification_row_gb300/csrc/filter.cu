@@ -519,9 +519,24 @@ constexpr int kPickCtasPerSm = 7;                 // 1064 rows resident on 152 S
 constexpr int kSegPairs = kSegSlices * kThreads;  // (slice, group) pairs per segment
 constexpr int kMaxCodes = 16384;                  // thread prefixes a pick CTA holds
 
+__device__ __forceinline__ uint4 ld_volatile_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.volatile.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+// Whether every 16-bit half of the eight codes is nonzero.
+__device__ __forceinline__ bool all_halves_set(const uint4& v) {
+  return __vcmpeq2(v.x, 0) == 0 && __vcmpeq2(v.y, 0) == 0 && __vcmpeq2(v.z, 0) == 0 &&
+         __vcmpeq2(v.w, 0) == 0;
+}
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs a) {
   using IO = Io<DT, VEC>;
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
   const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
   const int R = 2 * a.k + 1;
@@ -544,8 +559,13 @@ __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs
     float m = u < nv ? IO::vmax(w[u]) : -INFINITY;
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((tid & 7) == 0)
-      out[tid / 8 + u * (kThreads / 8)] = (unsigned short)(m > -INFINITY ? ord32(m) >> 16 : 0u);
+    // stored plus one: a written code is never 0 (the pick polls for it)
+    if ((tid & 7) == 0) {
+      const unsigned short c = (unsigned short)(m > -INFINITY ? (ord32(m) >> 16) + 1 : 1u);
+      asm volatile("st.relaxed.gpu.global.u16 [%0], %1;" ::"l"(out + tid / 8 + u * (kThreads / 8)),
+                   "h"(c)
+                   : "memory");
+    }
   }
 }
 
@@ -628,9 +648,27 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
   if (row_used(k, kraw, r)) {
     const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
     const int n = ns * kThreads;
+    // The row's codes as pass 1 writes them (eight per 16-byte load; a
+    // 16-bit half still 0 is not written yet: wait for it, bounded), stored
+    // back decoded (0 = no finite logit).
     uint4* g = reinterpret_cast<uint4*>(a.ws.codes + (size_t)blockIdx.x * n);
-    for (int i = tid; i < n / 8; i += kRowThreads) {  // eight codes per 16-byte load
-      reinterpret_cast<uint4*>(codes)[i] = __ldcg(g + i);
+    for (int i = tid; i < n / 8; i += kRowThreads) {
+      uint4 v = ld_volatile_v4(g + i);
+      const long long t0 = clock64();
+      while (!all_halves_set(v)) {
+        if (clock64() - t0 > kWaitCycles) {
+          set_status(a.ws.status, SPEC_ETIMEOUT);
+          break;
+        }
+        __nanosleep(256);
+        v = ld_volatile_v4(g + i);
+      }
+      // minus one per half (a half still 0 after a timeout stays 0)
+      const uint32_t m1[4] = {v.x, v.y, v.z, v.w};
+      uint32_t d[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d[q] = __vsubus2(m1[q], 0x00010001u);
+      reinterpret_cast<uint4*>(codes)[i] = make_uint4(d[0], d[1], d[2], d[3]);
       g[i] = make_uint4(0, 0, 0, 0);  // every call leaves the workspace zero
     }
     if (tid == 0) S.n = 0;
@@ -695,6 +733,8 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
     publish_row(S, a, b, r, kb);
   }
   row_done(S, a, b);
+  // Completion of this grid then implies completion of pass 1.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // The request's last row CTA finishes it: accept scan, final draw, outputs,
@@ -833,8 +873,19 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st) {
     filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    filter_pick_kernel<DT, VEC><<<(unsigned)rows, kRowThreads,
-                                  sizeof(unsigned short) * a.nsplit * kThreads, st>>>(a);
+    // The pick grid may be scheduled once every pass-1 CTA has started; each
+    // row CTA waits only for its own row's codes.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = sizeof(unsigned short) * a.nsplit * kThreads;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, filter_pick_kernel<DT, VEC>, a);
   } else {  // a row too wide for one CTA's prefixes: stream it through one CTA
     filter_row_kernel<DT, VEC><<<(unsigned)rows, kRowThreads, 0, st>>>(a);
   }
