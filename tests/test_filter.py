@@ -327,3 +327,23 @@ def test_filtered_softmax_properties():
             if prev is not None:
                 assert set(prev) <= set(kept)
             prev = kept
+
+
+@pytest.mark.gpu
+def test_cuda_filtered_b256_full_size_sampled():
+    # The 256-request, k = 3, V = 129280 bf16 workload with top_k = 20,
+    # top_p = 0.95; the oracle checks every sixteenth request.
+    from test_gpu_parity import check_chain
+    w = workloads.make("chain_b256_k3_v129280_bf16", seed=40)
+    sel = np.arange(0, w["B"], 16)
+    x = w["draft_tokens"].copy()
+    for b in sel:  # drafts from the filtered draft rows where the oracle checks
+        sub = dict(w, B=1, draft=w["draft"][b:b + 1])
+        x[b] = _filtered_tokens(sub, 20, 0.95, 40 + int(b))[0]
+    w["draft_tokens"] = x
+    g = _run_filtered(w, 20, 0.95)
+    sub = dict(w, B=sel.size, target=w["target"][sel], draft=w["draft"][sel],
+               draft_tokens=w["draft_tokens"][sel], uniforms=w["uniforms"][sel],
+               seq_lens=w["seq_lens"][sel])
+    gs = {key: g[key][sel] for key in g}
+    check_chain(sub, gs, _oracle_filtered(sub, 20, 0.95), "filtered b256 full size (sampled)")
