@@ -76,7 +76,8 @@ constexpr int kRowCtasPerSm = 7;                         // 1064 rows resident o
 
 struct RowSmem {
   unsigned long long buf[kBufCap + 2];   // held candidate keys (and a zero pad)
-  unsigned long long top[SPEC_MAX_TOPK]; // the top K, sorted (cut / final ranking)
+  alignas(16) unsigned long long top[SPEC_MAX_TOPK];  // the top K, sorted (cut / final
+                                                      // ranking); the pick's stage
   unsigned long long kappa;              // candidates: key >= kappa
   int n;                                 // keys held
   int wsum[kRowWarps];                   // per-warp counts (scans)
@@ -518,6 +519,9 @@ constexpr int kPickVecs = 6;                      // vectors a pick thread reads
 constexpr int kPickCtasPerSm = 7;                 // 1064 rows resident on 152 SMs
 constexpr int kSegPairs = kSegSlices * kThreads;  // (slice, group) pairs per segment
 constexpr int kMaxCodes = 16384;                  // thread prefixes a pick CTA holds
+constexpr int kStage = 32;                        // vectors a pick warp packs per pass
+static_assert(kRowWarps * kStage * 16 <= sizeof(unsigned long long) * SPEC_MAX_TOPK,
+              "the pick's stage lives in RowSmem::top");
 
 __device__ __forceinline__ uint4 ld_volatile_v4(const uint4* p) {
   uint4 v;
@@ -638,8 +642,9 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
   constexpr int NW = IO::NW;
   __shared__ RowSmem S;
   __shared__ unsigned short pairs[kSegPairs];  // (slice - segment start) << 8 | group
+  __shared__ int stage_idx[kRowWarps * kStage];  // vector indices of the stage
   extern __shared__ unsigned short codes[];    // the row's thread prefixes
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.top_k, k = a.k, R = 2 * k + 1, ns = a.nsplit;
   const int b = blockIdx.x / R, r = blockIdx.x - b * R;
   const int kraw = a.draft_lens ? a.draft_lens[b] : k;
@@ -718,14 +723,59 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
         }
 #pragma unroll
         for (int u = 0; u < kPickVecs; ++u) vm[u] = vidx[u] >= 0 ? IO::vmax(X[u]) : -INFINITY;
-        const unsigned long long kap = S.kappa;
-        const float kv = kap ? key_value(kap) : -INFINITY;
-        int cnt = 0;
+        // Of a selected group's eight vectors usually one reaches kappa, and
+        // its eight lanes sit side by side in a warp: filtered in place, most
+        // lanes would idle through every vector.  So the warp first packs the
+        // vectors that can hold a candidate (maximum >= kappa) into its stage,
+        // kStage at a time, and each lane then filters one of them.
+        const float kv0 = S.kappa ? key_value(S.kappa) : -INFINITY;
+        bool pass[kPickVecs];
+        int mine = 0;
 #pragma unroll
-        for (int u = 0; u < kPickVecs; ++u)
-          if (vm[u] >= kv && vm[u] > -INFINITY)
-            vec_candidates<DT, VEC>(vidx[u], X[u], kap, [&](unsigned long long) { ++cnt; });
-        if (__syncthreads_or(cnt > 0)) append_chunk<DT, VEC, kPickVecs>(S, K, vidx, X, vm, cnt);
+        for (int u = 0; u < kPickVecs; ++u) {
+          pass[u] = vidx[u] >= 0 && vm[u] >= kv0 && vm[u] > -INFINITY;
+          mine += pass[u] ? 1 : 0;
+        }
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t* stx = reinterpret_cast<uint32_t*>(S.top) + warp * kStage * NW;
+        int* sti = stage_idx + warp * kStage;
+        for (int b0 = 0; __syncthreads_or(b0 < wtot); b0 += kStage) {
+          int sl = incl - mine - b0;
+#pragma unroll
+          for (int u = 0; u < kPickVecs; ++u)
+            if (pass[u]) {
+              if (sl >= 0 && sl < kStage) {
+#pragma unroll
+                for (int w = 0; w < NW; ++w) stx[sl * NW + w] = X[u][w];
+                sti[sl] = vidx[u];
+              }
+              ++sl;
+            }
+          __syncwarp();
+          uint32_t Y[1][NW];
+          int yidx[1] = {-1};
+          float ym[1] = {-INFINITY};
+          if (b0 + lane < wtot) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) Y[0][w] = stx[lane * NW + w];
+            yidx[0] = sti[lane];
+            ym[0] = IO::vmax(Y[0]);
+          }
+          const unsigned long long kap = S.kappa;  // raised by an earlier pass, perhaps
+          const float kv = kap ? key_value(kap) : -INFINITY;
+          int cnt = 0;
+          if (ym[0] >= kv && ym[0] > -INFINITY)
+            vec_candidates<DT, VEC>(yidx[0], Y[0], kap, [&](unsigned long long) { ++cnt; });
+          // (the stage is read before this barrier and rewritten only after
+          // the next one; a cut inside may use S.top as scratch meanwhile)
+          if (__syncthreads_or(cnt > 0)) append_chunk<DT, VEC, 1>(S, K, yidx, Y, ym, cnt);
+        }
       }
       __syncthreads();  // pairs is rewritten by the next segment
     }
@@ -737,11 +787,32 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+constexpr int kHash = 2 * SPEC_MAX_TOPK;       // slots of the finisher's token table
+constexpr int kFinMaxE = SPEC_MAX_TOPK / 32;  // kept entries per lane of the draw warp
+static_assert((kHash & (kHash - 1)) == 0 && kHash / 2 + kHash / 2 + SPEC_MAX_TOPK <= kBufCap,
+              "the finisher's tables live in RowSmem::buf");
+
+// Slot of a token in the finisher's table: the top bits of a multiplicative
+// (Fibonacci) hash.
+__device__ __forceinline__ uint32_t hash_slot(uint32_t t) {
+  return (t * 2654435761u) >> (32 - 9);
+}
+static_assert(kHash == 1 << 9, "hash_slot yields 9 bits");
+
+// Exact warp-wide sum of 64-bit values whose total is below 2^64: three
+// 21/22-bit pieces summed with 32-bit reductions.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long s) {
+  const unsigned p0 = __reduce_add_sync(0xffffffffu, (unsigned)(s & 0x1fffffu));
+  const unsigned p1 = __reduce_add_sync(0xffffffffu, (unsigned)((s >> 21) & 0x1fffffu));
+  const unsigned p2 = __reduce_add_sync(0xffffffffu, (unsigned)(s >> 42));
+  return ((unsigned long long)p2 << 42) + ((unsigned long long)p1 << 21) + p0;
+}
+
 // The request's last row CTA finishes it: accept scan, final draw, outputs,
 // cleanup (thread t: position t of the scan; entries t and t + kRowThreads
 // of target row j's kept list).
 __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int b) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, R = 2 * k + 1, K = a.top_k;
   const int kraw = a.draft_lens ? a.draft_lens[b] : k;
   const bool bad_len = kraw < 0 || kraw > k;
@@ -768,77 +839,104 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
   const int j = any_bad ? -1 : S.m;
   const double u = (double)S.sm;
   int32_t* out = a.out_tokens + (size_t)b * (k + 1);
-  unsigned long long* F = S.top;                   // draw weights
-  int* T = reinterpret_cast<int*>(S.buf + K);      // kept tokens of target row j
   if (j >= 0) {
-    // Target row j's kept tokens, p and the weight max(0, p - q_j) (bonus
-    // row: p) in exact fixed point (scaled by 2^31, each < 2^32); draft row
-    // j's kept list in S.buf.
-    if (j < kb)
-      for (int i = tid; i < K; i += kRowThreads) S.buf[i] = __ldcg(row_words_of(a, b, k + 1 + j) + i);
-    int tk[2];
-    float p[2];
+    // Target row j's kept list (token, p) and, when j < kb, draft row j's:
+    // the latter goes into a hash table keyed by token (open addressing,
+    // at most SPEC_MAX_TOPK keys in kHash slots), so q_j of each target
+    // token is one or two probes.  The draw weights max(0, p - q_j) (bonus
+    // row: p) are exact 64-bit fixed point (to_fixed of a value scaled by
+    // 2^31, each < 2^32 before scaling).
+    uint32_t* hk = reinterpret_cast<uint32_t*>(S.buf);                  // token + 1; 0 = empty
+    float* hv = reinterpret_cast<float*>(S.buf + kHash / 2);            // its q
+    int* T = reinterpret_cast<int*>(S.buf + kHash);                     // kept tokens
+    float* Pj = reinterpret_cast<float*>(S.buf + kHash + SPEC_MAX_TOPK / 2);  // their p
+    unsigned long long* F = S.top;                                      // draw weights
+    unsigned long long wt[2], wd[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = tid + h * kRowThreads;
-      const unsigned long long w = i < K ? __ldcg(row_words_of(a, b, j) + i) : 0ull;
-      tk[h] = w ? (int)(w >> 32) - 1 : INT_MAX;
-      p[h] = w ? __uint_as_float((uint32_t)w) : 0.f;
+      wt[h] = i < K ? __ldcg(row_words_of(a, b, j) + i) : 0ull;
+      wd[h] = (j < kb && i < K) ? __ldcg(row_words_of(a, b, k + 1 + j) + i) : 0ull;
     }
-    __syncthreads();
-    unsigned long long f[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float qv = 0.f;
-      if (tk[h] != INT_MAX && j < kb)
-        for (int i = 0; i < K; ++i) {
-          const unsigned long long e = S.buf[i];
-          if ((int)(e >> 32) == tk[h] + 1) {
-            qv = __uint_as_float((uint32_t)e);
-            break;
-          }
-        }
-      f[h] = tk[h] != INT_MAX ? to_fixed(fmaxf(p[h] - qv, 0.f) * 2147483648.0f) : 0ull;
-    }
-    // Inverse CDF in token order without sorting: an entry's prefix is the
-    // sum of the weights of the kept tokens below it.
-    unsigned long long pre[2] = {0, 0}, Z = 0;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = tid + h * kRowThreads;
-        if (i < K) {
-          F[i] = f[h];
-          T[i] = tk[h];
-        }
-      }
-      __syncthreads();
-      pre[0] = pre[1] = 0;
-      Z = 0;
-      if (tid < K) {  // entries >= K carry nothing
-        for (int i = 0; i < K; ++i) {
-          const unsigned long long fi = F[i];
-          const int ti = T[i];
-          Z += fi;
-          pre[0] += ti < tk[0] ? fi : 0ull;
-          pre[1] += ti < tk[1] ? fi : 0ull;
-        }
-      }
-      if (tid == 0) S.kappa = Z;  // the same total in every thread that summed
-      __syncthreads();
-      Z = S.kappa;
-      __syncthreads();
-      if (Z != 0) break;
-      // The residual vanished numerically: draw from p_j.
-#pragma unroll
-      for (int h = 0; h < 2; ++h) f[h] = tk[h] != INT_MAX ? to_fixed(p[h] * 2147483648.0f) : 0ull;
-    }
-    const unsigned long long target = (unsigned long long)(u * (double)Z);  // < Z
-    if (tid == 0) S.red = 0;  // no kept token at all (a row without a finite logit)
+    for (int i = tid; i < kHash; i += kRowThreads) hk[i] = 0u;
     __syncthreads();
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      if (f[h] > 0 && pre[h] <= target && pre[h] + f[h] > target) S.red = tk[h];
+      if (wd[h]) {  // tokens of one kept list are distinct: each finds a free slot
+        const uint32_t key = (uint32_t)(wd[h] >> 32);
+        uint32_t slot = hash_slot(key - 1);
+        for (int probe = 0; probe < kHash; ++probe, slot = (slot + 1) & (kHash - 1))
+          if (atomicCAS(&hk[slot], 0u, key) == 0u) {
+            hv[slot] = __uint_as_float((uint32_t)wd[h]);
+            break;
+          }
+      }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = tid + h * kRowThreads;
+      if (i < K) {
+        const int tk = wt[h] ? (int)(wt[h] >> 32) - 1 : INT_MAX;
+        const float p = wt[h] ? __uint_as_float((uint32_t)wt[h]) : 0.f;
+        float qv = 0.f;
+        if (wt[h] && j < kb) {
+          uint32_t slot = hash_slot((uint32_t)tk);
+          for (int probe = 0; probe < kHash; ++probe, slot = (slot + 1) & (kHash - 1)) {
+            const uint32_t key = hk[slot];
+            if (key == (uint32_t)tk + 1u) {
+              qv = hv[slot];
+              break;
+            }
+            if (key == 0u) break;
+          }
+        }
+        F[i] = wt[h] ? to_fixed(fmaxf(p - qv, 0.f) * 2147483648.0f) : 0ull;
+        T[i] = tk;
+        Pj[i] = p;
+      }
+    }
+    __syncthreads();
+    // Inverse CDF in token order without sorting, in warp 0: Z = the sum of
+    // the weights, target = floor(u Z) < Z, and the drawn token is the least
+    // t whose cumulative weight over kept tokens <= t exceeds target
+    // (bisection over the token ids); that token has nonzero weight and the
+    // weights of the kept tokens below it sum to at most target.
+    if (warp == 0) {
+      unsigned long long fl[kFinMaxE], sum = 0;
+      int tl[kFinMaxE];
+#pragma unroll
+      for (int q = 0; q < kFinMaxE; ++q) {
+        const int i = q * 32 + lane;
+        fl[q] = i < K ? F[i] : 0ull;
+        tl[q] = i < K ? T[i] : INT_MAX;
+        sum += fl[q];
+      }
+      unsigned long long Z = warp_sum_u64(sum);
+      if (Z == 0) {  // the residual vanished numerically: draw from p_j
+        sum = 0;
+#pragma unroll
+        for (int q = 0; q < kFinMaxE; ++q) {
+          const int i = q * 32 + lane;
+          fl[q] = (i < K && tl[q] != INT_MAX) ? to_fixed(Pj[i] * 2147483648.0f) : 0ull;
+          sum += fl[q];
+        }
+        Z = warp_sum_u64(sum);
+      }
+      int lo = 0;  // no kept token at all (a row without a finite logit): token 0
+      if (Z != 0) {
+        const unsigned long long target = (unsigned long long)(u * (double)Z);  // < Z
+        int hi = a.V - 1;  // cumulative(hi) = Z > target
+        while (lo < hi) {
+          const int mid = lo + ((hi - lo) >> 1);
+          unsigned long long c = 0;
+#pragma unroll
+          for (int q = 0; q < kFinMaxE; ++q) c += tl[q] <= mid ? fl[q] : 0ull;
+          if (warp_sum_u64(c) > target) hi = mid;
+          else lo = mid + 1;
+        }
+      }
+      if (lane == 0) S.red = lo;
+    }
     __syncthreads();
     const int drawn = S.red;
     for (int i = tid; i <= k; i += kRowThreads)
