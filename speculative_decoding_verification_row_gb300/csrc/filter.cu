@@ -148,6 +148,66 @@ __device__ void rank_held(RowSmem& S, int n, int K) {
   __syncthreads();
 }
 
+// Sort the n held keys (unique, n <= kRowThreads * E) in descending order by
+// a bitonic network over P = kRowThreads * E slots (the slots past n hold 0,
+// below every key), thread t holding slots E t .. E t + E - 1; the top
+// min(n, K) land in S.top.  Element i of a compare-exchange at distance j in
+// merge stage kk keeps the larger of itself and i ^ j when (i & j) == 0
+// equals (i & kk) == 0.  Partners within a thread are registers, within a
+// warp shuffles, otherwise a round through S.buf.
+template <int E, int J>
+__device__ __forceinline__ void sort_local(unsigned long long (&v)[E], int base, int kk) {
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if ((e & J) == 0) {  // slot base + e is the lower of the pair
+      const unsigned long long x = v[e], y = v[e | J];
+      const bool big_first = ((base + e) & kk) == 0;
+      v[e] = (x > y) == big_first ? x : y;
+      v[e | J] = (x > y) == big_first ? y : x;
+    }
+}
+
+template <int E>
+__device__ __noinline__ void sort_held(RowSmem& S, int n, int K) {
+  constexpr int P = kRowThreads * E;
+  const int tid = threadIdx.x;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = tid * E + e < n ? S.buf[tid * E + e] : 0ull;
+  for (int kk = 2; kk <= P; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      if (j < E) {
+        if (j == 1) sort_local<E, 1>(v, tid * E, kk);
+        if constexpr (E >= 4)
+          if (j == 2) sort_local<E, 2>(v, tid * E, kk);
+      } else {
+        unsigned long long o[E];
+        if (j / E < 32) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = __shfl_xor_sync(0xffffffffu, v[e], j / E);
+        } else {
+          __syncthreads();  // earlier readers of S.buf are done
+#pragma unroll
+          for (int e = 0; e < E; ++e) S.buf[tid * E + e] = v[e];
+          __syncthreads();
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = S.buf[(tid * E + e) ^ j];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const bool keep_big = ((i & j) == 0) == ((i & kk) == 0);
+          v[e] = (v[e] > o[e]) == keep_big ? v[e] : o[e];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (tid * E + e < K) S.top[tid * E + e] = v[e];
+  __syncthreads();
+}
+
 // Cut the held keys to their exact top K and raise kappa to the K-th key
 // (n > K): the K-th largest key by bisection on its 64 bits (block-wide
 // counts), then the K keys >= it move to the front of the buffer.
@@ -400,7 +460,9 @@ __device__ __forceinline__ void publish_row(RowSmem& S, const ChainArgs& a, int 
     cut_held(S, K);
     n = S.n;
   }
-  rank_held(S, n, K);
+  if (n <= kRowThreads) rank_held(S, n, K);
+  else if (n <= 2 * kRowThreads) sort_held<2>(S, n, K);
+  else sort_held<4>(S, n, K);
   const int kk = min(n, K);  // real keys in S.top
 
   // Softmax over the top K at temperature T, then the top-p cut; thread t
@@ -520,6 +582,8 @@ constexpr int kPickCtasPerSm = 7;                 // 1064 rows resident on 152 S
 constexpr int kSegPairs = kSegSlices * kThreads;  // (slice, group) pairs per segment
 constexpr int kMaxCodes = 16384;                  // thread prefixes a pick CTA holds
 constexpr int kStage = 32;                        // vectors a pick warp packs per pass
+constexpr int kSegReads = kSegPairs / 8 / kRowThreads;  // 16-byte code reads per thread
+static_assert(kSegReads * 8 * kRowThreads == kSegPairs, "a segment's codes in 16-byte reads");
 static_assert(kRowWarps * kStage * 16 <= sizeof(unsigned long long) * SPEC_MAX_TOPK,
               "the pick's stage lives in RowSmem::top");
 
@@ -688,19 +752,34 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
     // their vectors, kPickVecs per CTA thread per round.
     for (int s0 = 0; s0 < ns; s0 += kSegSlices) {
       const int s1 = min(ns, s0 + kSegSlices);
+      // The segment's codes, eight per 16-byte read (kSegReads per thread):
+      // an 8-bit mask of those >= max(tau, 1) each; a pair is the code's
+      // index within the segment, ((s - s0) << 8) | group.
+      const int c0 = s0 * kThreads, nseg = (s1 - s0) * kThreads;
+      const uint32_t th = max(tau, 1u), th2 = th | (th << 16);
+      uint32_t mk[kSegReads];
       int mine = 0;
-      for (int s = s0; s < s1; ++s)
-        for (int t = tid; t < kThreads; t += kRowThreads) {
-          const uint32_t c = codes[s * kThreads + t];
-          mine += (c != 0 && c >= tau) ? 1 : 0;
+#pragma unroll
+      for (int h = 0; h < kSegReads; ++h) {
+        const int v = tid + h * kRowThreads;  // codes 8v .. 8v + 7 of the segment
+        mk[h] = 0;
+        if (8 * v < nseg) {
+          const uint4 x = reinterpret_cast<const uint4*>(codes + c0)[v];
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t ge = __vcmpgeu2(w[q], th2);  // 0xffff per half >= th
+            mk[h] |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * q);
+          }
         }
+        mine += __popc(mk[h]);
+      }
       int npairs;
       int off = row_block_scan(mine, S, &npairs);
-      for (int s = s0; s < s1; ++s)
-        for (int t = tid; t < kThreads; t += kRowThreads) {
-          const uint32_t c = codes[s * kThreads + t];
-          if (c != 0 && c >= tau) pairs[off++] = (unsigned short)(((s - s0) << 8) | t);
-        }
+#pragma unroll
+      for (int h = 0; h < kSegReads; ++h)
+        for (uint32_t m = mk[h]; m; m &= m - 1)
+          pairs[off++] = (unsigned short)(8 * (tid + h * kRowThreads) + __ffs(m) - 1);
       __syncthreads();
       const int items = npairs * kVecPerThread;  // (pair, vector) items
       for (int i0 = 0; i0 < items; i0 += kRowThreads * kPickVecs) {
@@ -788,9 +867,12 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
 }
 
 constexpr int kHash = 2 * SPEC_MAX_TOPK;       // slots of the finisher's token table
-constexpr int kFinMaxE = SPEC_MAX_TOPK / 32;  // kept entries per lane of the draw warp
+constexpr int kDrawBits = 9;                   // 2^9 token buckets per level of the draw search
+constexpr int kDrawBuckets = 1 << kDrawBits;
+constexpr int kDrawPerLane = kDrawBuckets / 32;
 static_assert((kHash & (kHash - 1)) == 0 && kHash / 2 + kHash / 2 + SPEC_MAX_TOPK <= kBufCap,
               "the finisher's tables live in RowSmem::buf");
+static_assert(kDrawBuckets <= kHash, "the draw's buckets reuse the token table");
 
 // Slot of a token in the finisher's table: the top bits of a multiplicative
 // (Fibonacci) hash.
@@ -820,8 +902,9 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
   float* pq = a.ws.pq + (size_t)b * 2 * k;
   float P = 0.f, Q = 0.f, U = 0.f;
   bool bad = bad_len;
+  int x = -1;  // draft token tid
   if (tid < kb) {
-    const int x = a.tokens[(size_t)b * k + tid];
+    x = a.tokens[(size_t)b * k + tid];
     bad = x < 0 || x >= a.V;
     P = __ldcg(pq + tid);
     Q = __ldcg(pq + k + tid);
@@ -898,49 +981,85 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
     __syncthreads();
     // Inverse CDF in token order without sorting, in warp 0: Z = the sum of
     // the weights, target = floor(u Z) < Z, and the drawn token is the least
-    // t whose cumulative weight over kept tokens <= t exceeds target
-    // (bisection over the token ids); that token has nonzero weight and the
-    // weights of the kept tokens below it sum to at most target.
+    // t whose cumulative weight over kept tokens <= t exceeds target; that
+    // token has nonzero weight and the weights of the kept tokens below it
+    // sum to at most target.  Search: the token range [lo, hi] is split into
+    // at most kDrawBuckets buckets of 2^sh tokens whose weights are summed
+    // exactly (64-bit shared atomics); the bucket holding target (lane-local
+    // then warp scans) becomes the range, until one token is left (two
+    // levels for V <= 2^18).  Lane l owns buckets 16 l .. 16 l + 15, stored
+    // transposed (bucket b at (b mod 16) * 32 + b / 16).
     if (warp == 0) {
-      unsigned long long fl[kFinMaxE], sum = 0;
-      int tl[kFinMaxE];
-#pragma unroll
-      for (int q = 0; q < kFinMaxE; ++q) {
-        const int i = q * 32 + lane;
-        fl[q] = i < K ? F[i] : 0ull;
-        tl[q] = i < K ? T[i] : INT_MAX;
-        sum += fl[q];
-      }
+      unsigned long long sum = 0;
+      for (int i = lane; i < K; i += 32) sum += F[i];
       unsigned long long Z = warp_sum_u64(sum);
       if (Z == 0) {  // the residual vanished numerically: draw from p_j
         sum = 0;
-#pragma unroll
-        for (int q = 0; q < kFinMaxE; ++q) {
-          const int i = q * 32 + lane;
-          fl[q] = (i < K && tl[q] != INT_MAX) ? to_fixed(Pj[i] * 2147483648.0f) : 0ull;
-          sum += fl[q];
+        for (int i = lane; i < K; i += 32) {
+          F[i] = T[i] != INT_MAX ? to_fixed(Pj[i] * 2147483648.0f) : 0ull;
+          sum += F[i];
         }
         Z = warp_sum_u64(sum);
+        __syncwarp();
       }
       int lo = 0;  // no kept token at all (a row without a finite logit): token 0
       if (Z != 0) {
-        const unsigned long long target = (unsigned long long)(u * (double)Z);  // < Z
-        int hi = a.V - 1;  // cumulative(hi) = Z > target
+        unsigned long long target = (unsigned long long)(u * (double)Z);  // < Z
+        unsigned long long* bk = S.buf;  // the token table is done with
+        int hi = a.V - 1;                // weight in [lo, hi] = Z > target
         while (lo < hi) {
-          const int mid = lo + ((hi - lo) >> 1);
-          unsigned long long c = 0;
+          // 2^sh tokens per bucket, sh the least with kDrawBuckets << sh > hi - lo
+          const int sh = max(0, 32 - __clz(hi - lo) - kDrawBits);
 #pragma unroll
-          for (int q = 0; q < kFinMaxE; ++q) c += tl[q] <= mid ? fl[q] : 0ull;
-          if (warp_sum_u64(c) > target) hi = mid;
-          else lo = mid + 1;
+          for (int q = 0; q < kDrawPerLane; ++q) bk[q * 32 + lane] = 0ull;
+          __syncwarp();
+          for (int i = lane; i < K; i += 32) {
+            const unsigned long long fi = F[i];
+            const int ti = T[i];
+            if (fi != 0ull && ti >= lo && ti <= hi) {
+              const int bb = (ti - lo) >> sh;
+              atomicAdd(&bk[(bb % kDrawPerLane) * 32 + bb / kDrawPerLane], fi);
+            }
+          }
+          __syncwarp();
+          unsigned long long own = 0;  // the lane's buckets in all
+#pragma unroll
+          for (int q = 0; q < kDrawPerLane; ++q) own += bk[q * 32 + lane];
+          unsigned long long incl = own;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+          }
+          const unsigned long long ex = incl - own;
+          const unsigned hit = __ballot_sync(0xffffffffu, ex <= target && target < incl);
+          const int src = __ffs(hit) - 1;
+          // in the lane that holds target: its bucket (the buckets wholly
+          // below target are those whose inclusive sum is <= target - ex)
+          // and the weight below it
+          int idx = 0;
+          unsigned long long below = 0, run = 0;
+#pragma unroll
+          for (int q = 0; q < kDrawPerLane; ++q) {
+            run += bk[q * 32 + lane];
+            if (run <= target - ex) {
+              ++idx;
+              below = run;
+            }
+          }
+          const int bucket = __shfl_sync(0xffffffffu, lane * kDrawPerLane + idx, src);
+          target -= __shfl_sync(0xffffffffu, ex + below, src);
+          __syncwarp();  // the buckets are cleared next
+          lo += bucket << sh;
+          hi = min(hi, lo + (1 << sh) - 1);
         }
       }
       if (lane == 0) S.red = lo;
     }
     __syncthreads();
     const int drawn = S.red;
-    for (int i = tid; i <= k; i += kRowThreads)
-      out[i] = i < j ? a.tokens[(size_t)b * k + i] : (i == j ? drawn : -1);
+    for (int i = tid; i <= k; i += kRowThreads)  // (i < j <= kb: thread i holds x_i)
+      out[i] = i < j ? (i == tid ? x : a.tokens[(size_t)b * k + i]) : (i == j ? drawn : -1);
     if (a.out_probs && tid < k) {  // padded positions are not verified: NaN
       a.out_probs[((size_t)b * k + tid) * 2] = tid < kb ? P : NAN;
       a.out_probs[((size_t)b * k + tid) * 2 + 1] = tid < kb ? Q : NAN;
@@ -959,8 +1078,11 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
     }
   }
   // Every call leaves the workspace zero: the kept lists and probabilities.
-  for (int i = tid; i < R * K; i += kRowThreads)
-    if (row_used(k, kraw, i / K)) row_words_of(a, b, i / K)[i - (i / K) * K] = 0;
+  for (int r = 0; r < R; ++r)
+    if (row_used(k, kraw, r)) {
+      unsigned long long* rw = row_words_of(a, b, r);
+      for (int i = tid; i < K; i += kRowThreads) rw[i] = 0;
+    }
   for (int i = tid; i < 2 * k; i += kRowThreads) pq[i] = 0.f;
 }
 

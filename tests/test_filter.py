@@ -133,6 +133,7 @@ FILTER_CASES = [
     ("chain_b8_k4_v32000_f32", dict(B=8), 40, 0.95),                # peaked rows, 8 slices
     ("chain_b64_k7_v128256_bf16", dict(B=6, V=70000), 64, 0.9),     # bf16, 5 slices, ragged tail
     ("chain_b64_k7_v128256_bf16", dict(B=4, V=70000), 256, 0.8),    # the largest top_k
+    ("chain_b64_k7_v128256_bf16", dict(B=4, V=70000), 150, 0.95),   # 129..256 keys held
     ("chain_b256_k3_v129280_bf16", dict(B=16, V=20000), 20, 1.0),
 ]
 
