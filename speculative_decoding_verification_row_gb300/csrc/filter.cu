@@ -580,10 +580,15 @@ constexpr int kSegSlices = 8;                     // slices per selection segmen
 constexpr int kPickVecs = 6;                      // vectors a pick thread reads per round
 constexpr int kPickCtasPerSm = 7;                 // 1064 rows resident on 152 SMs
 constexpr int kSegPairs = kSegSlices * kThreads;  // (slice, group) pairs per segment
-constexpr int kMaxCodes = 16384;                  // thread prefixes a pick CTA holds
+constexpr int kMaxCodes = 56 * kThreads;          // codes a pick CTA holds (56 slices)
 constexpr int kStage = 32;                        // vectors a pick warp packs per pass
 constexpr int kSegReads = kSegPairs / 8 / kRowThreads;  // 16-byte code reads per thread
 static_assert(kSegReads * 8 * kRowThreads == kSegPairs, "a segment's codes in 16-byte reads");
+// The pick's static shared memory plus its codes stay within the 48 KB a
+// launch may take without opting in to more.
+static_assert(sizeof(RowSmem) + sizeof(unsigned short) * kSegPairs + sizeof(int) * kRowWarps * kStage +
+                      sizeof(unsigned short) * kMaxCodes <= 48 * 1024,
+              "filter_pick_kernel's shared memory");
 static_assert(kRowWarps * kStage * 16 <= sizeof(unsigned long long) * SPEC_MAX_TOPK,
               "the pick's stage lives in RowSmem::top");
 

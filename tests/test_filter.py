@@ -134,6 +134,10 @@ FILTER_CASES = [
     ("chain_b64_k7_v128256_bf16", dict(B=6, V=70000), 64, 0.9),     # bf16, 5 slices, ragged tail
     ("chain_b64_k7_v128256_bf16", dict(B=4, V=70000), 256, 0.8),    # the largest top_k
     ("chain_b64_k7_v128256_bf16", dict(B=4, V=70000), 150, 0.95),   # 129..256 keys held
+    ("chain_b64_k7_v128256_bf16", dict(B=2, k=3, V=300000), 40, 0.9),  # 19 slices: 3 selection segments, 3-level draw
+    ("chain_b8_k4_v32000_f32", dict(B=2, V=300000), 30, 0.95),      # f32, 37 slices: 5 segments
+    ("chain_b8_k4_v32000_f32", dict(B=1, k=2, V=458752), 16, 0.9),  # 56 slices: the most codes a pick CTA holds
+    ("chain_b8_k4_v32000_f32", dict(B=1, k=2, V=480000), 16, 0.9),  # 59 slices: the per-row kernel
     ("chain_b256_k3_v129280_bf16", dict(B=16, V=20000), 20, 1.0),
 ]
 
