@@ -146,6 +146,8 @@ SMALL_CHAIN = [
     ("chain_b256_k3_v129280_bf16", dict(B=6, V=33000)),
     ("chain_b1_k4_v1024_f32", dict(B=2, k=1, V=2)),            # smallest problem
     ("chain_b1_k4_v1024_f32", dict(B=2, k=64, V=300)),         # longest draft
+    ("chain_b64_k7_v128256_bf16", dict(B=2, k=3, V=300000)),   # beyond 2^18 tokens: 19 slices
+    ("chain_b8_k4_v32000_f32", dict(B=2, k=2, V=262147)),      # beyond 2^18, element path
 ]
 
 
@@ -164,7 +166,8 @@ def test_chain_misaligned_rows(dtype_name):
 
 @pytest.mark.parametrize("name,over", [("chain_b8_k4_v32000_f32", dict(B=6, V=30011)),
                                        ("chain_b64_k7_v128256_bf16", dict(B=4, V=50000)),
-                                       ("chain_b64_k7_v128256_bf16", dict(B=2, k=1, V=2))])
+                                       ("chain_b64_k7_v128256_bf16", dict(B=2, k=1, V=2)),
+                                       ("chain_b64_k7_v128256_bf16", dict(B=2, k=3, V=300000))])
 def test_greedy_small(name, over):
     w = workloads.make(name, seed=3, **over)
     check_greedy(w, run_greedy(w), oracle.verify(w, greedy=True), f"greedy {name}{over}")
@@ -187,7 +190,8 @@ def test_greedy_ties_and_misaligned():
 
 
 @pytest.mark.parametrize("over", [dict(B=4, N=30, L=5, V=7777, level_sizes=[8, 10, 7, 4]),
-                                  dict(B=3, V=8192), dict(B=2, N=2, L=2, V=64, level_sizes=[1])])
+                                  dict(B=3, V=8192), dict(B=2, N=2, L=2, V=64, level_sizes=[1]),
+                                  dict(B=2, N=12, L=4, V=300000, level_sizes=[4, 4, 3])])
 def test_tree_small(over):
     w = workloads.make("tree_b16_n60_l4_v151936_bf16", seed=2, **over)
     check_tree(w, run_tree(w), oracle.verify(w), f"tree {over}")
