@@ -676,11 +676,37 @@ __device__ uint32_t code_threshold(const unsigned short* codes, int n, int K, Ro
       }
     }
   }
+  uint32_t t = 0;
+  bool done = false;
+  if (in_regs && cw <= 16) {
+    // The cw-th largest of the lanes' two largest codes: those are distinct
+    // codes of the warp, so at least cw codes reach it; it is below the
+    // exact cw-th largest code only when a lane holds three or more of the
+    // warp's top cw codes.  Two values per lane make the bisection cheap.
+    uint32_t m1 = 0, m2 = 0;
+#pragma unroll
+    for (int q = 0; q < kReg; ++q) {
+      m2 = max(m2, min(m1, c[q]));
+      m1 = max(m1, c[q]);
+    }
+    const int nz2 = (int)__reduce_add_sync(0xffffffffu, (m1 != 0u ? 1u : 0u) + (m2 != 0u ? 1u : 0u));
+    if (nz2 >= cw) {  // else the exact search below (e.g. a mostly masked vocabulary)
+      uint32_t l2 = __reduce_min_sync(0xffffffffu, m2 != 0u ? m2 : (m1 != 0u ? m1 : ~0u));
+      uint32_t h2 = __reduce_max_sync(0xffffffffu, m1);
+      while (l2 < h2) {  // count(>= l2) >= cw over the 2 x 32 values
+        const uint32_t mid = (l2 + h2 + 1) >> 1;
+        const unsigned m = (m1 >= mid ? 1u : 0u) + (m2 >= mid ? 1u : 0u);
+        if ((int)__reduce_add_sync(0xffffffffu, m) >= cw) l2 = mid;
+        else h2 = mid - 1;
+      }
+      t = l2;
+      done = true;
+    }
+  }
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
   nz = (int)__reduce_add_sync(0xffffffffu, (unsigned)nz);
-  uint32_t t = 0;
-  if (nz >= cw) {
+  if (!done && nz >= cw) {
     while (lo < hi) {  // the warp's nz >= cw codes are all >= lo
       const uint32_t mid = (lo + hi + 1) >> 1;
       unsigned m = 0;
