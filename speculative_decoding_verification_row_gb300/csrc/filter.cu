@@ -25,8 +25,8 @@
 //   probability) and the probability of the draft token the row tests; the
 //   request's last row CTA (acquire-release ticket) runs the accept scan and
 //   draws the final token by inverse CDF over the kept tokens of target row
-//   j in token order (p_j is zero elsewhere), with exact 64-bit fixed-point
-//   prefix sums.
+//   j in token order (p_j is zero elsewhere): exact 64-bit fixed-point
+//   weights, summed per token bucket to find the one holding u Z.
 //   filter_row_kernel (rows too wide for one CTA's codes) streams each row
 //   through one CTA with a running candidate threshold instead.
 #include <mutex>
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) filter_row_kernel(
 // the pass has the streaming shape of the unfiltered pass 1 without its
 // exponentials.
 // Pass 2, filter_pick_kernel: one CTA per row.  tau: a prefix that at
-// least K of the row's group prefixes reach (per-warp bisection); at least
+// least K of the row's group prefixes reach (per-warp bisections); at least
 // K logits are >= tau (those groups' maxima), so the row's top K all lie in
 // the groups whose prefix is >= tau (somewhat more than K of them).  Only
 // those groups are read again (one 128-byte line each); their logits with
@@ -923,7 +923,7 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long s)
 
 // The request's last row CTA finishes it: accept scan, final draw, outputs,
 // cleanup (thread t: position t of the scan; entries t and t + kRowThreads
-// of target row j's kept list).
+// of target and draft row j's kept lists; warp 0 runs the draw's search).
 __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int b) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, R = 2 * k + 1, K = a.top_k;
