@@ -29,8 +29,6 @@
 //   weights, summed per token bucket to find the one holding u Z.
 //   filter_row_kernel (rows too wide for one CTA's codes) streams each row
 //   through one CTA with a running candidate threshold instead.
-#include <mutex>
-
 #include "kernels.cuh"
 
 namespace sv {
