@@ -89,7 +89,17 @@ def pin_inverse_cdf(lib=None) -> list[str]:
 
 
 # --------------------------------------------------------------------------- exact distribution
-def enumerate_chain(target, draft, T, lib=None):
+def _topk_softmax_T(x, T, top_k):
+    """softmax(x / T) over the top_k logits (numpy's stable argsort of -x:
+    larger logit first, lower index first among equals), 0 elsewhere."""
+    x = np.asarray(x, dtype=np.float64)
+    keep = np.argsort(-x, kind="stable")[:top_k]
+    p = np.zeros(x.shape[0])
+    p[keep] = _softmax_T(x[keep], T)
+    return p
+
+
+def enumerate_chain(target, draft, T, lib=None, top_k=None):
     """Drive the oracle through every branch of the chain verify for one small problem.
 
     For every draft tuple x in [V]^k (weight prod q_i(x_i)), every stopping
@@ -97,14 +107,22 @@ def enumerate_chain(target, draft, T, lib=None):
     that take that branch: r_i = min(1,a_i)/2 accepts (weight min(1,a_i)),
     r_j = (1+a_j)/2 rejects (weight 1-a_j), and u at the midpoint of t's CDF
     interval (weight w_t/Z).  Returns (weights, expected rows, oracle result).
+    With top_k, p and q are the top-k filtered distributions of both sides and
+    the oracle's filtered verify runs.
     """
     k1, V = target.shape
     k = k1 - 1
-    p = [_softmax_T(target[i], T) for i in range(k + 1)]
-    q = [_softmax_T(draft[i], T) for i in range(k)]
+    if top_k is None:
+        p = [_softmax_T(target[i], T) for i in range(k + 1)]
+        q = [_softmax_T(draft[i], T) for i in range(k)]
+    else:
+        p = [_topk_softmax_T(target[i], T, top_k) for i in range(k + 1)]
+        q = [_topk_softmax_T(draft[i], T, top_k) for i in range(k)]
     reqs_x, reqs_r, weights, expect = [], [], [], []
     for x in itertools.product(range(V), repeat=k):
         wx = np.prod([q[i][x[i]] for i in range(k)])
+        if wx == 0:  # a draft the draft side never proposes
+            continue
         a = [p[i][x[i]] / q[i][x[i]] for i in range(k)]
         for j in range(k + 1):
             wb = wx
@@ -120,6 +138,8 @@ def enumerate_chain(target, draft, T, lib=None):
                 wts = np.maximum(p[j] - q[j], 0.0)
             else:
                 wts = p[k]
+            if wb == 0:  # an accept of weight min(1, 0): a draft outside the target's kept set
+                continue
             Z = wts.sum()
             c = np.concatenate([[0.0], np.cumsum(wts)])
             for t in range(V):
@@ -134,8 +154,12 @@ def enumerate_chain(target, draft, T, lib=None):
     Bn = len(weights)
     tgt = np.broadcast_to(target, (Bn, k + 1, V)).astype(np.float32)
     drf = np.broadcast_to(draft, (Bn, k, V)).astype(np.float32)
-    res = oracle.verify_chain(tgt, drf, np.array(reqs_x, np.int32).reshape(Bn, k),
-                              np.array(reqs_r, np.float32), T, lib=lib)
+    xs = np.array(reqs_x, np.int32).reshape(Bn, k)
+    rs = np.array(reqs_r, np.float32)
+    if top_k is None:
+        res = oracle.verify_chain(tgt, drf, xs, rs, T, lib=lib)
+    else:
+        res = oracle.verify_chain_filtered(tgt, drf, xs, rs, T, top_k, lib=lib)
     return np.array(weights), expect, res, p
 
 
@@ -375,6 +399,81 @@ def pin_worked_example(lib=None) -> list[str]:
     return errs
 
 
+# --------------------------------------------------------------------------- filtered
+def pin_filtered(lib=None) -> list[str]:
+    """Symmetric top-k / top-p filtering (TensorRT-LLM walkthrough, rejection-
+    sampling section): hand examples with closed-form values, the library
+    special cases (top_k >= V is scipy's softmax, top_k = 1 numpy's argmax),
+    identical filtered sides accept everything, and the equivalence theorem
+    on enumerated branches with both sides top-k filtered."""
+    errs = []
+    fs = lambda x, T, kk, pp=1.0: oracle.filtered_softmax(np.asarray(x, np.float32), T, kk, pp, lib=lib)[0]
+    x = [3.0, 1.0, 2.0, 2.0, 0.0]
+    e1 = np.exp(-1.0)
+    cases = [  # (T, top_k, top_p, expected p)
+        (1.0, 3, 1.0, np.array([1.0, 0.0, e1, e1, 0.0]) / (1.0 + 2.0 * e1)),
+        (1.0, 3, 0.5, np.array([1.0, 0.0, 0.0, 0.0, 0.0])),
+        # 1 / (1 + 2/e) = 0.576 reaches 0.55 alone (mass over the top 3, not the vocabulary)
+        (1.0, 3, 0.55, np.array([1.0, 0.0, 0.0, 0.0, 0.0])),
+        # two tokens; the tie at logit 2 keeps the lower index
+        (1.0, 3, 0.6, np.array([1.0, 0.0, e1, 0.0, 0.0]) / (1.0 + e1)),
+        # temperature before the cut: at T = 2 the top token has 0.452 < 0.5
+        (2.0, 3, 0.5, np.array([1.0, 0.0, np.exp(-0.5), 0.0, 0.0]) / (1.0 + np.exp(-0.5))),
+        # a cut exactly at top_p keeps the shorter prefix
+        (1.0, 2, 0.5, None),
+    ]
+    for T, kk, pp, want in cases:
+        if want is None:
+            got = fs([1.0, 1.0, 0.0], T, kk, pp)
+            want = np.array([1.0, 0.0, 0.0])
+        else:
+            got = fs(x, T, kk, pp)
+        if np.max(np.abs(got - want)) > 1e-12:
+            errs.append(f"filtered softmax T={T} top_k={kk} top_p={pp}: {got} want {want}")
+    rng = np.random.default_rng(11)
+    row = (rng.standard_normal(40) * 2).astype(np.float32)
+    if np.max(np.abs(fs(row, 0.8, 40) - _softmax_T(row, 0.8))) > 1e-12:
+        errs.append("top_k = V is not the plain softmax")
+    tie = np.array([1.0, 5.0, 5.0, 2.0], np.float32)
+    if fs(tie, 1.0, 1).tolist() != [0.0, 1.0, 0.0, 0.0] or int(np.argmax(tie)) != 1:
+        errs.append("top_k = 1 is not one-hot at the first argmax")
+    # The residual after a rejection uses the filtered draft row: p = 1/3 on
+    # tokens 0..2, the draft keeps {0, 3, 4} at 1/3 each (token 1, at 4.9, is
+    # fourth), draft token 3 (p = 0) is rejected, max(0, p - q) is 1/3 on
+    # tokens 1 and 2, and u = 0.1 draws token 1.  (Against the unfiltered
+    # draft softmax the residual would be 0.078, 0.102, 0.333 on tokens 0..2
+    # and u = 0.1 would draw token 0.)
+    tgt = np.array([[[0, 0, 0, -20, -20, -20], [0, 0, 0, 0, 0, 0]]], np.float32)
+    drf = np.array([[[5, 4.9, -20, 5, 5, -20]]], np.float32)
+    res = oracle.verify_chain_filtered(tgt, drf, np.array([[3]], np.int32),
+                                       np.array([[0.5, 0.1]], np.float32), 1.0, 3, lib=lib)
+    if res["num_accepted"][0] != 0 or res["tokens"][0].tolist() != [1, -1]:
+        errs.append(f"filtered residual example gave {res['tokens'][0]} want [1, -1]")
+    B, k, V = 16, 3, 30
+    target = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    xs = rng.integers(0, V, (B, k)).astype(np.int32)
+    r = rng.random((B, k + 1)).astype(np.float32)
+    same = oracle.verify_chain_filtered(target, target[:, :k].copy(), xs, r, 0.9, 5, 0.8, lib=lib)
+    kept = same["probs"][:, :, 1] > 0  # drafts inside the draft's kept set
+    if not np.all(same["num_accepted"][kept.all(axis=1)] == k):
+        errs.append("identically filtered sides must accept every kept draft")
+    for (k2, V2, T2, kk) in [(1, 6, 1.0, 3), (2, 5, 0.8, 2), (2, 4, 1.2, 3)]:
+        tg = (rng.standard_normal((k2 + 1, V2)) * 1.5).astype(np.float32)
+        dr = (tg[:k2] + rng.standard_normal((k2, V2)) * 0.8).astype(np.float32)
+        wts, expect, res, p = enumerate_chain(tg, dr, T2, lib=lib, top_k=kk)
+        for e, (j, rowe) in enumerate(expect):
+            if res["num_accepted"][e] != j or list(res["tokens"][e]) != rowe:
+                errs.append(f"filtered k={k2} V={V2}: branch {e} gave {res['tokens'][e]} want {rowe}")
+                break
+        n_acc, toks = res["num_accepted"], res["tokens"]
+        for i in range(k2 + 1):
+            reach = n_acc >= i
+            dist = np.array([wts[reach & (toks[:, i] == t)].sum() for t in range(V2)]) / wts[reach].sum()
+            if np.max(np.abs(dist - p[i])) > 1e-12:
+                errs.append(f"filtered k={k2} V={V2}: token {i} is not distributed as filtered p_{i}")
+    return errs
+
+
 ALL_PINS = {
     "softmax": pin_softmax,
     "inverse_cdf": pin_inverse_cdf,
@@ -384,4 +483,5 @@ ALL_PINS = {
     "tree": pin_tree,
     "rollback": pin_rollback,
     "worked_example": pin_worked_example,
+    "filtered": pin_filtered,
 }

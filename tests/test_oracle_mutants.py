@@ -31,6 +31,18 @@ MUTANTS = {
     "rollback_drops_committed_token": ("new_lens[b] = old_lens[b] + n + 1;",
                                        "new_lens[b] = old_lens[b] + n;"),
     "scan_does_not_stop": ("j = i;\n                break;", "j = i;"),
+    # symmetric filtering (TensorRT-LLM walkthrough, rejection-sampling section)
+    "filtered_tie_keeps_higher_index": ("return u->t < v->t ? -1 : (u->t > v->t);",
+                                        "return u->t > v->t ? -1 : (u->t < v->t);"),
+    "top_p_cut_strict": ("if (cum >= top_p) {", "if (cum > top_p) {"),
+    "top_p_mass_over_vocabulary": ("for (int i = 0; i < kk; ++i)\n        sk += exp(",
+                                   "for (int i = 0; i < V; ++i)\n        sk += exp("),
+    "kept_set_not_renormalised": ("p[it[i].t] = exp(it[i].x / temperature - zmax) / sm;",
+                                  "p[it[i].t] = exp(it[i].x / temperature - zmax) / sk;"),
+    "draft_side_not_filtered": ("oracle_filtered_softmax(db + (size_t)i * V * es, dtype, T, V, top_k, top_p, q, &tq);",
+                                "oracle_softmax(db + (size_t)i * V * es, dtype, T, V, q);"),
+    "residual_draft_not_filtered": ("oracle_filtered_softmax(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, q, &tq);",
+                                    "oracle_softmax(db + (size_t)j * V * es, dtype, T, V, q);"),
 }
 
 
