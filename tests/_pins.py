@@ -474,6 +474,90 @@ def pin_filtered(lib=None) -> list[str]:
     return errs
 
 
+# --------------------------------------------------------------------------- Philox, ragged, paged
+def pin_philox(lib=None) -> list[str]:
+    """Philox4x32-10 against its published known-answer vectors (Salmon et
+    al., SC'11, Random123), and the uniforms' stated counter, word and 24-bit
+    mapping on top of it."""
+    errs = []
+    kat = json.load(open(os.path.join(GOLDEN, "philox4x32_10_kat.json")))
+    h = lambda xs: [int(x, 16) for x in xs]  # noqa: E731
+    for v in kat["vectors"]:
+        if oracle.philox4x32_10(h(v["ctr"]), h(v["key"]), lib=lib).tolist() != h(v["out"]):
+            errs.append(f"Philox known answer {v['ctr']} / {v['key']}")
+    seeds = np.array([0x0123456789ABCDEF, 7], dtype=np.uint64)
+    offsets = np.array([0xFEDCBA9876543210, 0], dtype=np.uint64)
+    u = oracle.philox_uniforms(seeds, offsets, 9, lib=lib)
+    for b in range(2):
+        key = [int(seeds[b]) & 0xFFFFFFFF, int(seeds[b]) >> 32]
+        for i in range(9):
+            ctr = [int(offsets[b]) & 0xFFFFFFFF, int(offsets[b]) >> 32, i // 4, 0]
+            word = int(oracle.philox4x32_10(ctr, key, lib=lib)[i % 4])
+            if u[b, i] != np.float32((word >> 8) / 2.0**24):
+                errs.append(f"uniform {i} of stream {b} is not word {i % 4} of counter block {i // 4}")
+                return errs
+    return errs
+
+
+def pin_rollback_paged(lib=None) -> list[str]:
+    """Closed forms of the paged rollback (TensorRT-LLM walkthrough,
+    update_requests and rewind_cache: rewind k_b - n, keep ceil(len / block)
+    blocks, return the whole surplus)."""
+    errs = []
+    res = oracle.rollback_paged([10, 10, 7, 0], [2, 0, 3, 0], k=4, tokens_per_block=4,
+                                draft_lens=[3, 0, 3, 2], blocks_held=[5, 3, 2, 1], lib=lib)
+    if res["new_lens"].tolist() != [13, 11, 11, 1] or res["rewind_lens"].tolist() != [1, 0, 0, 2]:
+        errs.append(f"paged rollback lengths {res['new_lens']} / {res['rewind_lens']}")
+    if res["free_blocks"].tolist() != [1, 0, 0, 0]:  # ceil(13/4)=4 of 5; ceil(11/4)=3 of 3; 3 > 2; 1 of 1
+        errs.append(f"paged rollback free blocks {res['free_blocks']}")
+    bad = oracle.rollback_paged([5, 5], [3, 1], k=4, tokens_per_block=4, draft_lens=[2, 9],
+                                blocks_held=[9, 9], lib=lib)
+    if bad["rc"] != oracle.EBADINDEX or bad["new_lens"].tolist() != [5, 5] or bad["free_blocks"].tolist() != [0, 0]:
+        errs.append("paged rollback must refuse n > k_b and k_b > k entry by entry")
+    return errs
+
+
+def pin_ragged(lib=None) -> list[str]:
+    """Ragged draft lengths: each request equals the plain verify of its
+    truncated chain (its own k_b drafts, target rows 0..k_b, uniforms r_0..r_{k_b});
+    full lengths equal the plain call; a length outside [0, k] fails closed."""
+    errs = []
+    rng = np.random.default_rng(4)
+    B, k, V, T = 6, 5, 60, 0.9
+    target = rng.normal(0, 2, size=(B, k + 1, V)).astype(np.float32)
+    draft = (target[:, :k] + rng.normal(0, 0.6, size=(B, k, V))).astype(np.float32)
+    x = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    r = rng.random((B, k + 1), dtype=np.float32)
+    r[:, :k] *= 0.5  # longer accepted prefixes
+    lens = np.array([1, 2, 3, 0, 5, 3], np.int32)
+    got = oracle.verify_chain(target, draft, x, r, T, draft_lens=lens, lib=lib)
+    for b in range(B):
+        kb = int(lens[b])
+        if kb == 0:
+            p = _softmax_T(target[b, 0], T)
+            want_tok = int(np.searchsorted(np.cumsum(p), float(r[b, 0]) * p.sum(), side="right"))
+            if got["num_accepted"][b] != 0 or got["tokens"][b, 0] != want_tok:
+                errs.append("zero drafts must be one draw from target row 0 at r_0")
+            continue
+        rr = np.concatenate([r[b, :kb], r[b, kb:kb + 1]])[None]
+        want = oracle.verify_chain(target[b:b + 1, :kb + 1], draft[b:b + 1, :kb], x[b:b + 1, :kb], rr, T,
+                                   lib=lib)
+        if got["num_accepted"][b] != want["num_accepted"][0] or \
+                not np.array_equal(got["tokens"][b, :kb + 1], want["tokens"][0]) or \
+                np.any(got["tokens"][b, kb + 1:] != -1):
+            errs.append(f"request {b} (k_b={kb}) is not its truncated chain")
+    full = oracle.verify_chain(target, draft, x, r, T, draft_lens=np.full(B, k, np.int32), lib=lib)
+    plain = oracle.verify_chain(target, draft, x, r, T, lib=lib)
+    if not np.array_equal(full["tokens"], plain["tokens"]):
+        errs.append("full lengths must equal the plain call")
+    badl = lens.copy()
+    badl[2] = k + 1
+    bad = oracle.verify_chain(target, draft, x, r, T, draft_lens=badl, lib=lib)
+    if bad["rc"] != oracle.EBADINDEX or bad["num_accepted"][2] != -1 or np.any(bad["tokens"][2] != -1):
+        errs.append("a draft length above k must fail that request closed")
+    return errs
+
+
 ALL_PINS = {
     "softmax": pin_softmax,
     "inverse_cdf": pin_inverse_cdf,
@@ -484,4 +568,7 @@ ALL_PINS = {
     "rollback": pin_rollback,
     "worked_example": pin_worked_example,
     "filtered": pin_filtered,
+    "philox": pin_philox,
+    "rollback_paged": pin_rollback_paged,
+    "ragged": pin_ragged,
 }

@@ -43,6 +43,20 @@ MUTANTS = {
                                 "oracle_softmax(db + (size_t)i * V * es, dtype, T, V, q);"),
     "residual_draft_not_filtered": ("oracle_filtered_softmax(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, q, &tq);",
                                     "oracle_softmax(db + (size_t)j * V * es, dtype, T, V, q);"),
+    # per-request Philox uniforms (TensorRT-LLM walkthrough, rejection-sampling section)
+    "philox_nine_rounds": ("for (int round = 0; round < 10; ++round) {",
+                           "for (int round = 0; round < 9; ++round) {"),
+    "philox_key_words_swapped": ("const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;",
+                                 "const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k1;"),
+    "uniform_from_low_bits": ("(float)((double)(r[i % 4] >> 8) * (1.0 / 16777216.0))",
+                              "(float)((double)(r[i % 4] & 0xFFFFFFu) * (1.0 / 16777216.0))"),
+    "uniform_counter_words_swapped": ("(uint32_t)(i / 4), 0u};", "0u, (uint32_t)(i / 4)};"),
+    # ragged lengths and paged rollback (TensorRT-LLM walkthrough, update_requests, rewind_cache)
+    "paged_blocks_rounded_down": ("const long long need = (len + tokens_per_block - 1) / tokens_per_block;",
+                                  "const long long need = len / tokens_per_block;"),
+    "paged_rewind_from_padded_k": ("rewind_lens[b] = kb - n;", "rewind_lens[b] = k - n;"),
+    "ragged_draw_uniform_at_padded_k": ("int tok = oracle_inverse_cdf(w, V, (double)r[kb], SAMPLE_TIE, &tie);",
+                                        "int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);"),
 }
 
 
