@@ -555,6 +555,18 @@ def pin_ragged(lib=None) -> list[str]:
     bad = oracle.verify_chain(target, draft, x, r, T, draft_lens=badl, lib=lib)
     if bad["rc"] != oracle.EBADINDEX or bad["num_accepted"][2] != -1 or np.any(bad["tokens"][2] != -1):
         errs.append("a draft length above k must fail that request closed")
+    # Greedy: every draft, padding included, is numpy's argmax of its target
+    # row, so each request accepts exactly its k_b drafts and emits the argmax
+    # of row k_b; nothing past k_b is read.
+    g = np.argmax(target, axis=-1)
+    glens = np.array([0, 1, 2, 5, 4, 3], np.int32)
+    got = oracle.verify_greedy(target, g[:, :k].astype(np.int32), draft_lens=glens, lib=lib)
+    for b in range(B):
+        kb = int(glens[b])
+        want = list(g[b, :kb + 1]) + [-1] * (k - kb)
+        if got["num_accepted"][b] != kb or got["tokens"][b].tolist() != want:
+            errs.append(f"greedy request {b} (k_b={kb}) read past its length")
+            break
     return errs
 
 

@@ -57,6 +57,7 @@ MUTANTS = {
     "paged_rewind_from_padded_k": ("rewind_lens[b] = kb - n;", "rewind_lens[b] = k - n;"),
     "ragged_draw_uniform_at_padded_k": ("int tok = oracle_inverse_cdf(w, V, (double)r[kb], SAMPLE_TIE, &tie);",
                                         "int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);"),
+    "greedy_scans_padding": ("while (j < kb && oracle_argmax", "while (j < k && oracle_argmax"),
 }
 
 
