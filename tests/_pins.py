@@ -340,6 +340,17 @@ def pin_tree(lib=None) -> list[str]:
         if list(row[: n_acc + 1]) != want or np.any(row[n_acc + 1:] != -1):
             errs.append("tree output row wrong")
             break
+        # the kept path: the most accepted steps, ties to the lowest path
+        # index (numpy's first-occurrence argmax over the paths' step counts)
+        steps = []
+        for pth in paths:
+            a = 0
+            while a + 1 < L and pth[a + 1] >= 0 and ok[int(pth[a + 1])]:
+                a += 1
+            steps.append(a if pth[0] >= 0 else -1)
+        if int(res["best_path"][0]) != int(np.argmax(steps)):
+            errs.append(f"tree kept path {res['best_path'][0]}, want {int(np.argmax(steps))} (lowest index of the longest)")
+            break
     # one-chain tree == chain greedy
     B, k, V = 16, 4, 20
     target = rng.integers(-3, 4, (B, k + 1, V)).astype(np.float32)

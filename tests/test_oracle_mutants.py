@@ -58,6 +58,7 @@ MUTANTS = {
     "ragged_draw_uniform_at_padded_k": ("int tok = oracle_inverse_cdf(w, V, (double)r[kb], SAMPLE_TIE, &tie);",
                                         "int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);"),
     "greedy_scans_padding": ("while (j < kb && oracle_argmax", "while (j < k && oracle_argmax"),
+    "tree_tie_keeps_later_path": ("if (acc > best_acc) {", "if (acc >= best_acc) {"),
 }
 
 
