@@ -44,6 +44,11 @@ def pin_softmax(lib=None) -> list[str]:
         want = 1.0 / (1.0 + np.exp(-a / np.float64(np.float32(T))))
         if abs(p[0] - want) > 1e-14 or abs(p.sum() - 1.0) > 1e-15:
             errs.append(f"two-token closed form fails at a={a} T={T}")
+    # large logits: the closed form holds far beyond exp's range (the
+    # maximum is taken out before exponentiating)
+    p = oracle.softmax(np.array([1000.0, 999.0], np.float32), 1.0, lib=lib)
+    if not np.all(np.isfinite(p)) or abs(p[0] - 1.0 / (1.0 + np.exp(-1.0))) > 1e-14:
+        errs.append("softmax of [1000, 999] is not logistic(1)")
     # bf16 widening: 1.0 (0x3F80) and -2.0 (0xC000) -> logistic(3)
     p = oracle.softmax(np.array([0x3F80, 0xC000], np.uint16), 1.0, dtype="bf16", lib=lib)
     if abs(p[0] - 1.0 / (1.0 + np.exp(-3.0))) > 1e-14:

@@ -28,6 +28,9 @@ MUTANTS = {
     "temperature_multiplies": ("p[t] = logit_at(x, dtype, (size_t)t) / temperature;",
                                "p[t] = logit_at(x, dtype, (size_t)t) * temperature;"),
     "softmax_unnormalised": ("p[t] /= sum;", "p[t] /= 1.0;"),
+    "softmax_without_max_shift": ("p[t] = exp(p[t] - zmax);", "p[t] = exp(p[t]);"),
+    "bf16_widened_with_wrong_shift": ("uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;",
+                                      "uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 15;"),
     "rollback_drops_committed_token": ("new_lens[b] = old_lens[b] + n + 1;",
                                        "new_lens[b] = old_lens[b] + n;"),
     "scan_does_not_stop": ("j = i;\n                break;", "j = i;"),
