@@ -312,6 +312,17 @@ def test_workspace_shared_across_paths_and_sizes():
         check_chain(wc, run_chain(wc, workspace=ws), oracle.verify(wc), f"shared chain again {step}")
 
 
+@pytest.mark.parametrize("greedy", [False, True])
+def test_maximum_batch(greedy):
+    # SPEC_MAX_BATCH = 8192 requests (k = 2, V = 64): the largest grids and
+    # per-request workspaces the C ABI accepts.
+    w = workloads.make("chain_b1_k4_v1024_f32", seed=5, B=8192, k=2, V=64)
+    if greedy:
+        check_greedy(w, run_greedy(w), oracle.verify(w, greedy=True), "greedy, 8192 requests")
+    else:
+        check_chain(w, run_chain(w), oracle.verify(w), "chain, 8192 requests")
+
+
 # ------------------------------------------------------------------ full sizes
 FULL_CHAIN = ["chain_b1_k4_v1024_f32", "chain_b8_k4_v32000_f32", "chain_b64_k7_v128256_bf16",
               "chain_b256_k3_v129280_bf16"]
