@@ -64,24 +64,44 @@ def pin_softmax(lib=None) -> list[str]:
 
 
 # --------------------------------------------------------------------------- inverse CDF
+def _window_tie(c, target, Z, t, tol=1e-6):
+    """Whether u*Z (``target``) lies within tol*Z of C(t) or C(t-1), from
+    numpy's cumulative sums ``c``."""
+    lo = c[t - 1] if t > 0 else 0.0
+    return abs(c[t] - target) <= tol * Z or abs(lo - target) <= tol * Z
+
+
 def pin_inverse_cdf(lib=None) -> list[str]:
-    """numpy searchsorted(side='right') special case; zero weights never drawn."""
+    """numpy searchsorted(side='right') special case; zero weights never drawn;
+    the near-tie flag is set exactly when u*Z lies within 1e-6*Z of the drawn
+    token's CDF interval ends (checked on random draws and on draws placed
+    next to a boundary)."""
     errs = []
     rng = np.random.default_rng(11)
-    for trial in range(200):
+    for trial in range(400):
         V = int(rng.integers(1, 40))
         w = rng.random(V) * (rng.random(V) < 0.7)
         if w.sum() == 0:
             w[int(rng.integers(0, V))] = 0.5
-        u = float(rng.random())
-        t, tie = oracle.inverse_cdf(w, u, lib=lib)
         c = np.cumsum(w)
-        want = int(np.searchsorted(c, u * c[-1], side="right"))
-        if not tie and t != want:
+        Z = c[-1]
+        if trial % 2:  # half the draws sit within +-3e-6 of a CDF boundary
+            edge = c[int(rng.integers(0, V))] / Z
+            u = float(np.clip(edge + rng.uniform(-3e-6, 3e-6), 0.0, np.nextafter(1.0, 0.0)))
+        else:
+            u = float(rng.random())
+        t, tie = oracle.inverse_cdf(w, u, lib=lib)
+        want = int(np.searchsorted(c, u * Z, side="right"))
+        if want >= V:  # rounding past the end: the last positive weight
+            want = int(np.flatnonzero(w > 0)[-1])
+        if t != want:
             errs.append(f"searchsorted mismatch V={V} u={u}: {t} vs {want}")
             break
         if w[t] <= 0:
             errs.append("zero-weight token drawn")
+            break
+        if tie != _window_tie(c, u * Z, Z, t):
+            errs.append(f"near-tie flag {tie} wrong for u={u} (V={V})")
             break
     w = np.array([0.0, 0.0, 0.3, 0.0, 0.7, 0.0])
     if oracle.inverse_cdf(w, 0.0, lib=lib)[0] != 2:
@@ -90,6 +110,88 @@ def pin_inverse_cdf(lib=None) -> list[str]:
         errs.append("u->1 must draw the last positive-weight token")
     if oracle.inverse_cdf(np.zeros(4), 0.3, lib=lib)[0] != -1:
         errs.append("Z == 0 must return -1")
+    return errs
+
+
+def pin_near_ties(lib=None) -> list[str]:
+    """The near-tie windows (an accept test with |r - p/q| < 1e-5, a final
+    draw whose u*Z lies within 1e-6*Z of a CDF boundary), on closed-form
+    cases: a two-token chain whose p/q is a ratio of logistic functions, and
+    weights [1/4, 1/4, 1/2] whose first boundary sits at exactly Z/4.  A flag
+    must be set inside each window and clear just outside it."""
+    errs = []
+    # Final draw: boundary C(0) = Z/4 (u*Z at 0.5e-6*Z is inside, 2e-6*Z outside).
+    w = np.array([0.25, 0.25, 0.5])
+    for d, want_tok, want_tie in [(0.5e-6, 1, True), (-0.5e-6, 0, True),
+                                  (2e-6, 1, False), (-2e-6, 0, False)]:
+        t, tie = oracle.inverse_cdf(w, 0.25 + d, lib=lib)
+        if t != want_tok or tie != want_tie:
+            errs.append(f"draw at Z/4 {d:+g}*Z: token {t} flag {tie}, want {want_tok} {want_tie}")
+    # Accept test: k = 1, V = 2, T = 1; target row [a, 0], draft row [b, 0]
+    # and x_0 = 0, so p/q = logistic(a) / logistic(b).
+    a, b = np.float32(0.3), np.float32(0.9)
+    ratio = (1.0 / (1.0 + np.exp(-np.float64(a)))) / (1.0 / (1.0 + np.exp(-np.float64(b))))
+    target = np.array([[[a, 0.0], [0.5, -0.25]]], np.float32)
+    draft = np.array([[[b, 0.0]]], np.float32)
+    x = np.zeros((1, 1), np.int32)
+    for d, want_n, want_tie in [(5e-6, 0, True), (-5e-6, 1, True),
+                                (2e-5, 0, False), (-2e-5, 1, False)]:
+        r = np.array([[ratio + d, 0.3]], np.float32)
+        res = oracle.verify_chain(target, draft, x, r, 1.0, lib=lib)
+        if res["num_accepted"][0] != want_n or bool(res["flags"][0, 0]) != want_tie:
+            errs.append(f"accept test at p/q {d:+g}: n={res['num_accepted'][0]} "
+                        f"flag={res['flags'][0, 0]}, want {want_n} {want_tie}")
+    # The final draw's flag reaches the chain's column k: identical rows
+    # accept every draft, and the bonus row [0, 0, ln 4] has its first CDF
+    # boundary at 1/(2 + 4) of Z.
+    c4 = np.float32(np.log(4.0))
+    z4 = 2.0 + np.exp(np.float64(c4))
+    target = np.array([[[0.1, -0.2, 0.4], [0.0, 0.0, c4]]], np.float32)
+    x = np.zeros((1, 1), np.int32)
+    for d, want_tok, want_tie in [(0.5e-6, 1, True), (2e-6, 1, False), (-0.5e-6, 0, True),
+                                  (-2e-6, 0, False)]:
+        r = np.array([[0.5, 1.0 / z4 + d]], np.float32)
+        res = oracle.verify_chain(target, target[:, :1].copy(), x, r, 1.0, lib=lib)
+        if res["tokens"][0, 1] != want_tok or bool(res["flags"][0, 1]) != want_tie:
+            errs.append(f"bonus draw at C(0) {d:+g}*Z: token {res['tokens'][0, 1]} "
+                        f"flag {res['flags'][0, 1]}, want {want_tok} {want_tie}")
+    # Random chains whose uniforms sit near p/q and near the final draw's CDF
+    # boundaries: every flag equals the window test computed from scipy's
+    # softmax and numpy's cumulative sums; positions past the first
+    # rejection are never flagged.
+    rng = np.random.default_rng(31)
+    B, k, V, T = 300, 3, 7, 0.8
+    target = (rng.standard_normal((B, k + 1, V)) * 1.5).astype(np.float32)
+    draft = (target[:, :k] + rng.standard_normal((B, k, V)) * 0.6).astype(np.float32)
+    x = rng.integers(0, V, (B, k)).astype(np.int32)
+    r = np.empty((B, k + 1), np.float32)
+    plan = []
+    for bb in range(B):
+        p = [_softmax_T(target[bb, i], T) for i in range(k + 1)]
+        q = [_softmax_T(draft[bb, i], T) for i in range(k)]
+        ratio = [p[i][x[bb, i]] / q[i][x[bb, i]] for i in range(k)]
+        for i in range(k):
+            r[bb, i] = np.float32(min(ratio[i] + rng.uniform(-3e-5, 3e-5), 0.999))
+        j = next((i for i in range(k) if not (np.float64(r[bb, i]) < ratio[i])), k)
+        wts = np.maximum(p[j] - q[j], 0.0) if j < k else p[k]
+        c = np.cumsum(wts)
+        u = np.float32(np.clip(c[int(rng.integers(0, V))] / c[-1] + rng.uniform(-3e-6, 3e-6), 0.0,
+                               np.nextafter(np.float32(1.0), np.float32(0.0))))
+        r[bb, k] = u
+        plan.append((ratio, j, wts, c))
+    res = oracle.verify_chain(target, draft, x, r, T, lib=lib)
+    for bb in range(B):
+        ratio, j, wts, c = plan[bb]
+        if res["num_accepted"][bb] != j:
+            errs.append(f"request {bb}: n_acc {res['num_accepted'][bb]} want {j}")
+            break
+        want = [abs(np.float64(r[bb, i]) - ratio[i]) < 1e-5 if i <= min(j, k - 1) else False
+                for i in range(k)]
+        t = int(res["tokens"][bb, j])
+        want.append(_window_tie(c, np.float64(r[bb, k]) * c[-1], c[-1], t))
+        if [bool(f) for f in res["flags"][bb]] != want:
+            errs.append(f"request {bb}: flags {res['flags'][bb].tolist()} want {want}")
+            break
     return errs
 
 
@@ -589,6 +691,7 @@ def pin_ragged(lib=None) -> list[str]:
 ALL_PINS = {
     "softmax": pin_softmax,
     "inverse_cdf": pin_inverse_cdf,
+    "near_ties": pin_near_ties,
     "exact_distribution": pin_exact_distribution,
     "invariants": pin_invariants,
     "greedy": pin_greedy,

@@ -119,9 +119,10 @@ def _run_filtered(w, top_k, top_p, *, misalign=False, workspace=None, philox=Non
 
 
 def _oracle_filtered(w, top_k, top_p):
-    return oracle.verify_chain_filtered(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
-                                        w["temperature"], top_k, float(np.float32(top_p)),
-                                        w["dtype"])
+    o = oracle.verify_chain_filtered(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
+                                     w["temperature"], top_k, float(np.float32(top_p)), w["dtype"])
+    o["filter"] = (top_k, float(np.float32(top_p)))
+    return o
 
 
 FILTER_CASES = [
@@ -297,7 +298,8 @@ def test_cuda_filtered_full_size_sampled():
                draft_tokens=w["draft_tokens"][sel], uniforms=w["uniforms"][sel],
                seq_lens=w["seq_lens"][sel])
     gs = {key: g[key][sel] for key in g}
-    check_chain(sub, gs, _oracle_filtered(sub, 50, 0.9), "filtered full size (sampled)")
+    check_chain(sub, gs, _oracle_filtered(sub, 50, 0.9), "filtered full size (sampled)",
+                full_size="filtered")
 
 
 def test_filtered_softmax_properties():
@@ -351,4 +353,5 @@ def test_cuda_filtered_b256_full_size_sampled():
                draft_tokens=w["draft_tokens"][sel], uniforms=w["uniforms"][sel],
                seq_lens=w["seq_lens"][sel])
     gs = {key: g[key][sel] for key in g}
-    check_chain(sub, gs, _oracle_filtered(sub, 20, 0.95), "filtered b256 full size (sampled)")
+    check_chain(sub, gs, _oracle_filtered(sub, 20, 0.95), "filtered b256 full size (sampled)",
+                full_size="filtered b256")

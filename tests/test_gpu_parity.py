@@ -13,13 +13,11 @@ element-wise path for rows that are not 16-byte aligned), then every named
 workload at full size and seeds 0, 1, 2 in the launch configuration the
 benchmark times.
 """
-import json
-import os
-
 import numpy as np
 import pytest
 import torch
 
+import _report
 import oracle
 import workloads
 import speculative_decoding_verification_row_gb300 as sv
@@ -27,16 +25,6 @@ import speculative_decoding_verification_row_gb300 as sv
 pytestmark = pytest.mark.gpu
 
 PROB_RTOL = 1e-5
-REPORT = []
-
-
-@pytest.fixture(scope="module", autouse=True)
-def _report():
-    yield
-    path = os.environ.get("SPEC_PARITY_REPORT")
-    if path:
-        with open(path, "w") as f:
-            json.dump(REPORT, f, indent=1)
 
 
 def to_dev(arr, dtype):
@@ -70,18 +58,72 @@ def _offset_copy(t):
     return view
 
 
-def check_chain(w, g, o, label):
+# Largest fraction of requests the oracle may flag as near-ties on each
+# full-size workload (observed at seeds 0-2: 0, 0, 1.6-4.7 % and 11.7-16.8 %;
+# the last workload's residuals are nearly flat over 129k tokens, so its CDF
+# intervals are only ~8e-6 of Z wide).
+FLAG_CEILING = {"chain_b1_k4_v1024_f32": 0.0, "chain_b8_k4_v32000_f32": 0.125,
+                "chain_b64_k7_v128256_bf16": 0.10, "chain_b256_k3_v129280_bf16": 0.25}
+
+
+def draw_allowed(w, b, j, filt=None):
+    """Tokens the final draw of request b may give when the scan stops at j:
+    those whose CDF interval under the oracle's double-precision weights
+    meets u*Z +- 1e-6*Z (exactly one token when the oracle does not flag the
+    draw).  None when a filtered row of the draw has a top-p cut near-tie
+    (the kept set itself may then differ)."""
+    T, dt, k = w["temperature"], w["dtype"], w["k"]
+    if filt is None:
+        p = oracle.softmax(w["target"][b, j], T, dt)
+        q = oracle.softmax(w["draft"][b, j], T, dt) if j < k else None
+    else:
+        p, tp = oracle.filtered_softmax(w["target"][b, j], T, filt[0], filt[1], dt)
+        q, tq = (oracle.filtered_softmax(w["draft"][b, j], T, filt[0], filt[1], dt)
+                 if j < k else (None, False))
+        if tp or tq:
+            return None
+    wts = np.maximum(p - q, 0.0) if q is not None else p
+    if not wts.sum() > 0:
+        wts = p
+    c = np.cumsum(wts)
+    Z = c[-1]
+    x = float(w["uniforms"][b, k]) * Z
+    tol = oracle.SAMPLE_TIE * Z
+    ok = (wts > 0) & (c - wts <= x + tol) & (c > x - tol)
+    return set(np.flatnonzero(ok).tolist())
+
+
+def check_chain(w, g, o, label, full_size=None):
+    """Exact agreement outside flagged near-ties.  A request the CUDA path
+    resolves differently must be flagged at the decision that differs (the
+    first accept test where the counts part, or the final draw), and its
+    outputs must still be a valid outcome: the drafts up to its count, then a
+    token whose CDF interval meets the draw's 1e-6 window."""
     k, B = w["k"], w["B"]
     flags, n_o, tok_o = o["flags"], o["num_accepted"], o["tokens"]
+    filt = o.get("filter")
     flagged = mism = 0
     for b in range(B):
         tested = min(max(int(n_o[b]), 0), k - 1)
         f = bool(flags[b, : tested + 1].any() or flags[b, k])
         flagged += f
-        if g["num_accepted"][b] != n_o[b] or not np.array_equal(g["tokens"][b], tok_o[b]):
-            mism += 1
-            assert f, (f"{label}: unflagged mismatch at request {b}: gpu {g['tokens'][b]} "
-                       f"(n={g['num_accepted'][b]}) oracle {tok_o[b]} (n={n_o[b]})")
+        if g["num_accepted"][b] == n_o[b] and np.array_equal(g["tokens"][b], tok_o[b]):
+            continue
+        mism += 1
+        msg = (f"{label}: request {b}: gpu {g['tokens'][b]} (n={g['num_accepted'][b]}) "
+               f"oracle {tok_o[b]} (n={n_o[b]})")
+        assert f, "unflagged mismatch: " + msg
+        jg, jo = int(g["num_accepted"][b]), int(n_o[b])
+        assert jg >= 0 and jo >= 0, "a failed request is never a near-tie: " + msg
+        if jg != jo:
+            assert flags[b, min(jg, jo)], "the accept tests part at an unflagged position: " + msg
+            assert np.array_equal(g["tokens"][b, :jg], w["draft_tokens"][b, :jg]), msg
+        else:
+            assert flags[b, k], "the final draw differs but is not flagged: " + msg
+        assert np.all(g["tokens"][b, jg + 1:] == -1), msg
+        allowed = draw_allowed(w, b, jg, filt)
+        assert allowed is None or int(g["tokens"][b, jg]) in allowed, \
+            f"draw outside the near-tie window (allowed {sorted(allowed)}): " + msg
     ok = n_o >= 0
     po = o["probs"][ok]
     pg = g["probs"][ok].astype(np.float64)
@@ -91,9 +133,13 @@ def check_chain(w, g, o, label):
     assert rel.max(initial=0.0) <= PROB_RTOL, f"{label}: p/q relative error {rel.max()}"
     want_seq = oracle.rollback(w["seq_lens"], g["num_accepted"], k)["new_lens"]
     assert np.array_equal(g["seq_lens"], want_seq), f"{label}: seq_lens"
-    REPORT.append(dict(case=label, kind="chain", requests=B, flagged=flagged, mismatched=mism,
-                       max_prob_rel_err=float(rel.max(initial=0.0)),
-                       mean_accepted=float(np.mean(n_o[ok])) if ok.any() else 0.0))
+    if full_size in FLAG_CEILING:
+        assert flagged <= FLAG_CEILING[full_size] * B, \
+            f"{label}: {flagged} of {B} requests flagged, above the stated {FLAG_CEILING[full_size]:.0%}"
+    _report.record(case=label, kind="filtered" if filt else "chain", requests=B, flagged=flagged,
+                   mismatched=mism, max_prob_rel_err=float(rel.max(initial=0.0)),
+                   full_size=bool(full_size),
+                   mean_accepted=float(np.mean(n_o[ok])) if ok.any() else 0.0)
     return flagged, mism
 
 
@@ -112,7 +158,7 @@ def check_greedy(w, g, o, label):
     assert np.array_equal(g["num_accepted"], o["num_accepted"]), label
     want_seq = oracle.rollback(w["seq_lens"], o["num_accepted"], w["k"])["new_lens"]
     assert np.array_equal(g["seq_lens"], want_seq), label
-    REPORT.append(dict(case=label, kind="greedy", requests=w["B"], flagged=0, mismatched=0))
+    _report.record(case=label, kind="greedy", requests=w["B"], flagged=0, mismatched=0)
 
 
 def run_tree(w, misalign=False, workspace=None):
@@ -132,8 +178,8 @@ def check_tree(w, g, o, label):
         assert np.array_equal(g[key], o[key]), f"{label}: {key}\n{g[key]}\n{o[key]}"
     want_seq = oracle.rollback(w["seq_lens"], o["num_accepted"], w["N"] - 1)["new_lens"]
     assert np.array_equal(g["seq_lens"], want_seq), label
-    REPORT.append(dict(case=label, kind="tree", requests=w["B"], flagged=0, mismatched=0,
-                       mean_accepted=float(np.mean(o["num_accepted"]))))
+    _report.record(case=label, kind="tree", requests=w["B"], flagged=0, mismatched=0,
+                   mean_accepted=float(np.mean(o["num_accepted"])))
 
 
 # ------------------------------------------------------------------ small cases
@@ -332,7 +378,7 @@ FULL_CHAIN = ["chain_b1_k4_v1024_f32", "chain_b8_k4_v32000_f32", "chain_b64_k7_v
 @pytest.mark.parametrize("name", FULL_CHAIN)
 def test_chain_full(name, seed):
     w = workloads.make(name, seed=seed)
-    check_chain(w, run_chain(w), oracle.verify(w), f"{name}/s{seed}")
+    check_chain(w, run_chain(w), oracle.verify(w), f"{name}/s{seed}", full_size=name)
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])

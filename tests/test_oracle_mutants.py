@@ -62,6 +62,19 @@ MUTANTS = {
                                         "int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);"),
     "greedy_scans_padding": ("while (j < kb && oracle_argmax", "while (j < k && oracle_argmax"),
     "tree_tie_keeps_later_path": ("if (acc > best_acc) {", "if (acc >= best_acc) {"),
+    # near-tie windows (|r - p/q| < 1e-5; u*Z within 1e-6*Z of a CDF boundary)
+    "accept_window_wide": ("static const double ACCEPT_TIE = 1e-5;",
+                           "static const double ACCEPT_TIE = 1.0;"),
+    "sample_window_wide": ("static const double SAMPLE_TIE = 1e-6;",
+                           "static const double SAMPLE_TIE = 1.0;"),
+    "draw_always_flagged": ("*near_tie = (fabs(c - target) <= tol * Z) || (fabs(c_prev - target) <= tol * Z);",
+                            "*near_tie = 1;"),
+    "draw_never_flagged": ("*near_tie = (fabs(c - target) <= tol * Z) || (fabs(c_prev - target) <= tol * Z);",
+                           "*near_tie = 0;"),
+    "accept_never_flagged": ("if (flags && fabs((double)r[i] - ratio[i]) < ACCEPT_TIE)",
+                             "if (flags && fabs((double)r[i] - ratio[i]) < 0.0)"),
+    "draw_flag_one_side_only": ("*near_tie = (fabs(c - target) <= tol * Z) || (fabs(c_prev - target) <= tol * Z);",
+                                "*near_tie = (fabs(c - target) <= tol * Z);"),
 }
 
 
