@@ -45,9 +45,16 @@
  *     per row; NaN and +inf are outside the contract and are not checked.
  *   - One workspace serves one stream at a time: calls that overlap on the GPU
  *     must not share a workspace.
+ *   - The second phase of a verify waits (bounded, about one second) for
+ *     words the first phase publishes.  A wait that runs out records
+ *     SPEC_ETIMEOUT in the status word and fails the requests that depended
+ *     on it closed, as above; it cannot happen unless the GPU is broken or
+ *     another kernel starves the call.
  *   - Every call leaves its workspace ready for the next.  After a call that
  *     returned SPEC_ECUDA, or whose status word reads SPEC_ETIMEOUT, zero the
  *     workspace again with spec_workspace_init before reusing it.
+ *   - Calls run on the device that is current for the calling thread; the
+ *     arrays and the stream must belong to it.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -227,7 +234,8 @@ int spec_verify_greedy_ex(const spec_greedy_params *params, void *workspace,
  *   rewind_lens (nullable) = k_b - n; free_blocks (nullable) = max(0,
  *   blocks_held[b] - ceil(new_len / tokens_per_block)), 0 when blocks_held is
  *   NULL.  new_lens may alias old_lens.  An entry with k_b outside [0, k] or
- *   n outside [0, k_b] keeps its length (rewind 0, free 0). */
+ *   n outside [0, k_b] (a failed request reads n = -1) keeps its length; its
+ *   rewind reads -1 and its free count 0. */
 int spec_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
                         const int32_t *draft_lens, int k, const int32_t *blocks_held,
                         int tokens_per_block, int B, int32_t *new_lens, int32_t *rewind_lens,
@@ -279,9 +287,9 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *tree_t
  *   (chain: k; tree: N - 1).
  *   new_lens [B] = old_lens + n + 1 (may alias old_lens);
  *   rewind_lens [B] or NULL = k - n (rows written but not kept).
- * An entry with n outside [0, k] keeps its length (rewind 0) and sets
- * SPEC_EBADINDEX in no workspace: this call returns SPEC_OK and leaves the
- * entry unchanged. */
+ * An entry with n outside [0, k] (a failed request reads n = -1) keeps its
+ * length and its rewind reads -1, so a caller can tell it from a valid
+ * rewind (>= 0); the call itself returns SPEC_OK. */
 int spec_rollback_lengths(const int32_t *old_lens, const int32_t *num_accepted, int k, int B,
                           int32_t *new_lens, int32_t *rewind_lens, spec_stream_t stream);
 
@@ -325,14 +333,20 @@ int spec_relocate_accepted_kv(void *kv_pool, size_t row_bytes, int tokens_per_bl
  *   Scratch: a file-scope device array of SPEC_NOALLOC_SCRATCH_BYTES that
  *   every GPU loading the library holds until the process exits.  A problem
  *   whose spec_workspace_size(B, 2k+1, V) exceeds it returns SPEC_EWORKSPACE
- *   before any launch.  The first call on a device looks up the array's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture.
+ *   before any launch.
  *   Every call on a device shares the one array: calls that can overlap on the
  *   GPU (other streams, other threads) race and must be serialised by the
  *   caller.  Each call clears the array's counters and status word on
- *   `stream` before launching, so the data-dependent status is not kept: a
- *   request that fails closed shows num_accepted == -1.
+ *   `stream` before launching, so there is no status word to read: the only
+ *   data-dependent signal is a request that fails closed (num_accepted ==
+ *   -1, tokens -1, seq_len unchanged), whether for a bad draft token or for
+ *   a device wait that ran out.
+ *   The arrays must be device (or managed) memory of the current device:
+ *   the array used as scratch is the current device's.  Every argument is
+ *   checked before the array is written; a refused call (SPEC_EINVAL,
+ *   SPEC_EWORKSPACE) leaves it untouched.  Each call looks up the array's
+ *   device address (cudaGetSymbolAddress) with its device current, so no
+ *   call needs a set-up step first.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 #define SPEC_NOALLOC_SCRATCH_BYTES (4u << 20)
 int spec_verify_chain_noalloc(const void *target_logits, const void *draft_logits, int dtype,
@@ -340,6 +354,21 @@ int spec_verify_chain_noalloc(const void *target_logits, const void *draft_logit
                               float temperature, int B, int k, int V,
                               int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
                               int32_t *seq_lens, spec_stream_t stream);
+
+/* Fault injection for tests of the bounded device waits (no counterpart on
+ * the pages).  Each runs its call with the first phase left out, so that the
+ * words the second phase waits for are never written, and with every device
+ * wait bounded by wait_cycles SM clock cycles (>= 1) instead of about one
+ * second.  Arguments are those of spec_verify_chain_ex (plain or filtered;
+ * a filtered call whose rows are wider than one CTA's codes has no wait and
+ * returns SPEC_ECUDA) / spec_verify_greedy_ex.  Expected outcome: every
+ * request fails closed and the status word reads SPEC_ETIMEOUT.  The
+ * workspace may hold stale words afterwards: zero it with
+ * spec_workspace_init before its next use. */
+int spec_test_timeout_chain(const spec_chain_params *params, long long wait_cycles,
+                            void *workspace, size_t workspace_bytes, spec_stream_t stream);
+int spec_test_timeout_greedy(const spec_greedy_params *params, long long wait_cycles,
+                             void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /* Synchronise `stream`, read the workspace status word into *status_out
  * (SPEC_OK, SPEC_EBADINDEX or SPEC_ETIMEOUT) and clear it.  Returns SPEC_OK, SPEC_EINVAL or

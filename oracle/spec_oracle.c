@@ -414,8 +414,10 @@ int oracle_verify_tree(const void *target, int dtype, const int32_t *tree_tokens
 
 /* KV cursor rollback: new_len = old_len + n_acc + 1 (the last committed token
  * plus the accepted drafts stay visible), rewind = k - n_acc (rows written by
- * the verify window but not kept).  An entry with n_acc outside [0, k] is left
- * unchanged (new_len = old_len, rewind 0) and the call returns EBADINDEX. */
+ * the verify window but not kept).  An entry with n_acc outside [0, k] keeps
+ * its length (new_len = old_len), its rewind reads -1 (the Kestrel article's
+ * convention: an invalid result is reported as -1, section 3.1) and the call
+ * returns EBADINDEX. */
 int oracle_rollback(const int32_t *old_lens, const int32_t *num_accepted, int k, int B,
                     int32_t *new_lens, int32_t *rewind_lens)
 {
@@ -427,7 +429,7 @@ int oracle_rollback(const int32_t *old_lens, const int32_t *num_accepted, int k,
         if (n < 0 || n > k) {
             new_lens[b] = old_lens[b];
             if (rewind_lens)
-                rewind_lens[b] = 0;
+                rewind_lens[b] = -1;
             rc = ORC_EBADINDEX;
             continue;
         }
@@ -499,7 +501,7 @@ int oracle_philox_uniforms(const uint64_t *seeds, const uint64_t *offsets, int B
  * NULL); new_len = old + n + 1, rewind = k_b - n, and, when blocks_held is
  * given, free_blocks = max(0, blocks_held - ceil(new_len / tokens_per_block)).
  * An entry with k_b outside [0, k] or n outside [0, k_b] keeps its length
- * (rewind 0, free 0) and the call returns EBADINDEX. */
+ * (rewind -1, free 0) and the call returns EBADINDEX. */
 int oracle_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
                           const int32_t *draft_lens, int k, const int32_t *blocks_held,
                           int tokens_per_block, int B, int32_t *new_lens, int32_t *rewind_lens,
@@ -514,7 +516,7 @@ int oracle_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
         if (kb < 0 || kb > k || n < 0 || n > kb) {
             new_lens[b] = old_lens[b];
             if (rewind_lens)
-                rewind_lens[b] = 0;
+                rewind_lens[b] = -1;
             if (free_blocks)
                 free_blocks[b] = 0;
             rc = ORC_EBADINDEX;

@@ -41,7 +41,7 @@ SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc",
            "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
            "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged",
-           "spec_workspace_size_filtered")
+           "spec_workspace_size_filtered", "spec_test_timeout_chain", "spec_test_timeout_greedy")
 SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 class ChainParams(ctypes.Structure):
@@ -95,13 +95,15 @@ def _bind(lib):
     lib.spec_verify_chain_ex.argtypes = [ctypes.POINTER(ChainParams), P, S, P]
     lib.spec_verify_greedy_ex.argtypes = [ctypes.POINTER(GreedyParams), P, S, P]
     lib.spec_rollback_paged.argtypes = [P, P, P, I, P, I, I, P, P, P, P]
+    lib.spec_test_timeout_chain.argtypes = [ctypes.POINTER(ChainParams), ctypes.c_longlong, P, S, P]
+    lib.spec_test_timeout_greedy.argtypes = [ctypes.POINTER(GreedyParams), ctypes.c_longlong, P, S, P]
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     for f in ("spec_workspace_init", "spec_verify_chain", "spec_verify_greedy", "spec_verify_tree",
               "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc",
               "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
               "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged",
-           "spec_workspace_size_filtered"):
+              "spec_test_timeout_chain", "spec_test_timeout_greedy"):
         getattr(lib, f).restype = I
     return lib
 
@@ -126,6 +128,12 @@ def status_string(code: int) -> str:
 # ---------------------------------------------------------------- marshalling helpers
 def _ptr(t: torch.Tensor | None):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _on(device):
+    """The C calls run on the current device: make the arrays' device current
+    for the duration of a call."""
+    return torch.cuda.device(device)
 
 
 def _stream_handle(stream, device):
@@ -179,7 +187,8 @@ class Workspace:
             raise SpecError("spec_workspace_size", SPEC_EINVAL)
         if self.buf is None or self.buf.numel() < need:
             self.buf = torch.empty(need, dtype=torch.uint8, device=self.device)
-            rc = lib().spec_workspace_init(_ptr(self.buf), self.buf.numel(), stream_handle)
+            with _on(self.buf.device):
+                rc = lib().spec_workspace_init(_ptr(self.buf), self.buf.numel(), stream_handle)
             if rc != SPEC_OK:
                 raise SpecError("spec_workspace_init", rc)
         return self.buf
@@ -247,17 +256,20 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
                           None if uniforms is not None else _ptr(of), float(temperature), B, k, V,
                           _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens), int(top_k),
                           float(top_p))
-        rc = lib().spec_verify_chain_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
+        with _on(dev):
+            rc = lib().spec_verify_chain_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
         name = "spec_verify_chain_ex"
     elif uniforms is not None:
-        rc = lib().spec_verify_chain(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
-                                     B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens),
-                                     _ptr(buf), buf.numel(), sh)
+        with _on(dev):
+            rc = lib().spec_verify_chain(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
+                                         B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens),
+                                         _ptr(buf), buf.numel(), sh)
         name = "spec_verify_chain"
     else:
-        rc = lib().spec_verify_chain_philox(_ptr(t), _ptr(d), code, _ptr(x), _ptr(sd), _ptr(of),
-                                            float(temperature), B, k, V, _ptr(tok), _ptr(n),
-                                            _ptr(probs), _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
+        with _on(dev):
+            rc = lib().spec_verify_chain_philox(_ptr(t), _ptr(d), code, _ptr(x), _ptr(sd), _ptr(of),
+                                                float(temperature), B, k, V, _ptr(tok), _ptr(n),
+                                                _ptr(probs), _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
         name = "spec_verify_chain_philox"
     if rc != SPEC_OK:
         raise SpecError(name, rc)
@@ -289,8 +301,9 @@ def verify_chain_noalloc(target_logits, draft_logits, draft_tokens, uniforms, te
     if seq_lens is not None:
         _dev(seq_lens, "seq_lens", torch.int32, (B,))
     sh, _ = _stream_handle(stream, dev)
-    rc = lib().spec_verify_chain_noalloc(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
-                                         B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens), sh)
+    with _on(dev):
+        rc = lib().spec_verify_chain_noalloc(_ptr(t), _ptr(d), code, _ptr(x), _ptr(u), float(temperature),
+                                             B, k, V, _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_verify_chain_noalloc", rc)
     return tok, n, probs
@@ -320,10 +333,12 @@ def verify_greedy(target_logits, draft_tokens, *, out_tokens=None, out_num_accep
         lens = _dev(draft_lens, "draft_lens", torch.int32, (B,))
         prm = GreedyParams(ctypes.sizeof(GreedyParams), _ptr(t), code, _ptr(x), _ptr(lens), B, k, V,
                            _ptr(tok), _ptr(n), _ptr(seq_lens))
-        rc = lib().spec_verify_greedy_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
+        with _on(dev):
+            rc = lib().spec_verify_greedy_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
     else:
-        rc = lib().spec_verify_greedy(_ptr(t), code, _ptr(x), B, k, V, _ptr(tok), _ptr(n),
-                                      _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
+        with _on(dev):
+            rc = lib().spec_verify_greedy(_ptr(t), code, _ptr(x), B, k, V, _ptr(tok), _ptr(n),
+                                          _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_verify_greedy", rc)
     return tok, n
@@ -353,9 +368,10 @@ def verify_tree(target_logits, tree_tokens, paths, *, out_tokens=None, out_num_a
     sh, _ = _stream_handle(stream, dev)
     ws = workspace or default_workspace(dev, sh)
     buf = ws.ensure(B, N, V, sh)
-    rc = lib().spec_verify_tree(_ptr(t), code, _ptr(tt), _ptr(p), B, N, P, L, V, _ptr(tok),
-                                _ptr(n), _ptr(best), _ptr(nodes), _ptr(seq_lens), _ptr(buf),
-                                buf.numel(), sh)
+    with _on(dev):
+        rc = lib().spec_verify_tree(_ptr(t), code, _ptr(tt), _ptr(p), B, N, P, L, V, _ptr(tok),
+                                    _ptr(n), _ptr(best), _ptr(nodes), _ptr(seq_lens), _ptr(buf),
+                                    buf.numel(), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_verify_tree", rc)
     return tok, n, best, nodes
@@ -370,7 +386,8 @@ def rollback_lengths(old_lens, num_accepted, k: int, *, new_lens=None, rewind_le
     new = _out(new_lens, "new_lens", (B,), torch.int32, o.device)
     rew = _out(rewind_lens, "rewind_lens", (B,), torch.int32, o.device)
     sh, _ = _stream_handle(stream, o.device)
-    rc = lib().spec_rollback_lengths(_ptr(o), _ptr(n), int(k), B, _ptr(new), _ptr(rew), sh)
+    with _on(o.device):
+        rc = lib().spec_rollback_lengths(_ptr(o), _ptr(n), int(k), B, _ptr(new), _ptr(rew), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_rollback_lengths", rc)
     return new, rew
@@ -394,10 +411,11 @@ def relocate_accepted_kv(kv_pool, block_tables, base_lens, accepted_nodes, num_a
     nodes = _dev(accepted_nodes, "accepted_nodes", torch.int32)
     n = _dev(num_accepted, "num_accepted", torch.int32, (B,))
     sh, _ = _stream_handle(stream, kv_pool.device)
-    rc = lib().spec_relocate_accepted_kv(_ptr(kv_pool), ctypes.c_size_t(row_bytes),
-                                         int(tokens_per_block), rows // tokens_per_block, _ptr(bt),
-                                         bt.shape[1], _ptr(base), _ptr(nodes), _ptr(n), B,
-                                         nodes.shape[1], sh)
+    with _on(kv_pool.device):
+        rc = lib().spec_relocate_accepted_kv(_ptr(kv_pool), ctypes.c_size_t(row_bytes),
+                                             int(tokens_per_block), rows // tokens_per_block, _ptr(bt),
+                                             bt.shape[1], _ptr(base), _ptr(nodes), _ptr(n), B,
+                                             nodes.shape[1], sh)
     if rc != SPEC_OK:
         raise SpecError("spec_relocate_accepted_kv", rc)
     return kv_pool
@@ -417,8 +435,9 @@ def rollback_paged(old_lens, num_accepted, k: int, tokens_per_block: int, *, dra
     rew = _out(rewind_lens, "rewind_lens", (B,), torch.int32, o.device)
     fre = _out(free_blocks, "free_blocks", (B,), torch.int32, o.device)
     sh, _ = _stream_handle(stream, o.device)
-    rc = lib().spec_rollback_paged(_ptr(o), _ptr(n), _ptr(lens), int(k), _ptr(held),
-                                   int(tokens_per_block), B, _ptr(new), _ptr(rew), _ptr(fre), sh)
+    with _on(o.device):
+        rc = lib().spec_rollback_paged(_ptr(o), _ptr(n), _ptr(lens), int(k), _ptr(held),
+                                       int(tokens_per_block), B, _ptr(new), _ptr(rew), _ptr(fre), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_rollback_paged", rc)
     return new, rew, fre
@@ -432,7 +451,8 @@ def philox_uniforms(seeds, offsets, n: int, *, stream=None):
     of = _dev(offsets, "offsets", torch.int64, (B,))
     out = torch.empty((B, n), dtype=torch.float32, device=sd.device)
     sh, _ = _stream_handle(stream, sd.device)
-    rc = lib().spec_philox_uniforms(_ptr(sd), _ptr(of), B, int(n), _ptr(out), sh)
+    with _on(sd.device):
+        rc = lib().spec_philox_uniforms(_ptr(sd), _ptr(of), B, int(n), _ptr(out), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_philox_uniforms", rc)
     return out
@@ -444,7 +464,8 @@ def last_error(workspace: Workspace, stream=None) -> int:
         return SPEC_OK
     sh, _ = _stream_handle(stream, workspace.buf.device)
     out = ctypes.c_int(0)
-    rc = lib().spec_last_error(_ptr(workspace.buf), workspace.buf.numel(), sh, ctypes.byref(out))
+    with _on(workspace.buf.device):
+        rc = lib().spec_last_error(_ptr(workspace.buf), workspace.buf.numel(), sh, ctypes.byref(out))
     if rc != SPEC_OK:
         raise SpecError("spec_last_error", rc)
     return out.value

@@ -49,9 +49,9 @@ __global__ void rollback_kernel(const int32_t* old_lens, const int32_t* n_acc, i
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int32_t n = n_acc[b], old = old_lens[b];
-  if (n < 0 || n > k) {
+  if (n < 0 || n > k) {  // a failed request or a corrupt count: length kept, rewind -1
     new_lens[b] = old;
-    if (rewind_lens) rewind_lens[b] = 0;
+    if (rewind_lens) rewind_lens[b] = -1;
     return;
   }
   new_lens[b] = old + n + 1;
@@ -70,7 +70,7 @@ __global__ void rollback_paged_kernel(const int32_t* old_lens, const int32_t* n_
   const int32_t kb = draft_lens ? draft_lens[b] : k, n = n_acc[b], old = old_lens[b];
   if (kb < 0 || kb > k || n < 0 || n > kb) {
     new_lens[b] = old;
-    if (rewind_lens) rewind_lens[b] = 0;
+    if (rewind_lens) rewind_lens[b] = -1;
     if (free_blocks) free_blocks[b] = 0;
     return;
   }
@@ -108,32 +108,32 @@ int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t s
 
 }  // extern "C"
 
-namespace {
+namespace sv {
 
-// Chain verify with explicit uniforms, or (uniforms == nullptr) with each
-// request's uniforms drawn in the kernel from its Philox (seed, offset).
-int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
-               const int32_t* draft_tokens, const float* uniforms, const uint64_t* seeds,
-               const uint64_t* offsets, const int32_t* draft_lens, float temperature, int B,
-               int k, int V,
-               int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
-               int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream,
-               int top_k = 0, float top_p = 1.f) {
+// Checks the arguments of a chain verify (explicit uniforms, or with
+// uniforms == nullptr each request's Philox (seed, offset)) and fills the
+// launch arguments; launches nothing and writes nothing.
+int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* draft_logits,
+                int dtype, const int32_t* draft_tokens, const float* uniforms,
+                const uint64_t* seeds, const uint64_t* offsets, const int32_t* draft_lens,
+                float temperature, int B, int k, int V, int32_t* out_tokens,
+                int32_t* out_num_accepted, float* out_probs, int32_t* seq_lens, void* workspace,
+                size_t workspace_bytes, int top_k, float top_p) {
   if (!target_logits || !draft_logits || !draft_tokens || (!uniforms && (!seeds || !offsets)) ||
       !out_tokens || !out_num_accepted)
     return SPEC_EINVAL;
   if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || k < 1 ||
       k > SPEC_MAX_DRAFT || V < 2)
     return SPEC_EINVAL;
-  ChainArgs a{};
+  a = ChainArgs{};
   if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
   const int R = 2 * k + 1;
   if (top_k < 0 || top_k > SPEC_MAX_TOPK || !(top_p > 0.f) || !(top_p <= 1.f) ||
       (top_k == 0 && top_p < 1.f))
     return SPEC_EINVAL;
   if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
-  const bool vec = aligned16(target_logits) && aligned16(draft_logits) &&
-                   ((size_t)V * esize(dtype)) % 16 == 0;
+  vec = aligned16(target_logits) && aligned16(draft_logits) &&
+        ((size_t)V * esize(dtype)) % 16 == 0;
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
   if (top_k > 0 && workspace_bytes < FilterLayout(B, k, V, top_k).total) return SPEC_EWORKSPACE;
   a.nchunks = num_chunks(V);
@@ -154,19 +154,46 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
   a.out_n = out_num_accepted;
   a.out_probs = out_probs;
   a.seq_lens = seq_lens;
+  a.wait_cycles = kWaitCycles;
   a.ws = ws_views(workspace, WsLayout(B, R, V));
+  a.top_k = top_k;
+  a.top_p = top_p;
   if (top_k > 0) {
     const FilterLayout fl(B, k, V, top_k);
     a.ws.cand = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + fl.cand);
     a.ws.pq = reinterpret_cast<float*>(static_cast<char*>(workspace) + fl.pq);
     a.ws.codes = reinterpret_cast<unsigned short*>(static_cast<char*>(workspace) + fl.codes);
-    a.top_k = top_k;
-    a.top_p = top_p;
-    return launch_filtered(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
-                                                                               : SPEC_ECUDA;
   }
-  return launch_chain(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
-                                                                          : SPEC_ECUDA;
+  return SPEC_OK;
+}
+
+// Enqueues a chain verify set up by chain_setup.
+int chain_launch(const ChainArgs& a, int dtype, bool vec, cudaStream_t st, bool skip_pass1) {
+  const cudaError_t e = a.top_k > 0 ? launch_filtered(a, dtype, vec, st, skip_pass1)
+                                    : launch_chain(a, dtype, vec, st, skip_pass1);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+}  // namespace sv
+
+namespace {
+
+int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
+               const int32_t* draft_tokens, const float* uniforms, const uint64_t* seeds,
+               const uint64_t* offsets, const int32_t* draft_lens, float temperature, int B,
+               int k, int V, int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
+               int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream,
+               int top_k = 0, float top_p = 1.f, long long wait_cycles = kWaitCycles,
+               bool skip_pass1 = false) {
+  ChainArgs a;
+  bool vec = false;
+  if (const int rc = chain_setup(a, vec, target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                                 seeds, offsets, draft_lens, temperature, B, k, V, out_tokens,
+                                 out_num_accepted, out_probs, seq_lens, workspace, workspace_bytes,
+                                 top_k, top_p))
+    return rc;
+  a.wait_cycles = wait_cycles;
+  return chain_launch(a, dtype, vec, (cudaStream_t)stream, skip_pass1);
 }
 
 __global__ void philox_uniforms_kernel(const unsigned long long* seeds,
@@ -224,7 +251,8 @@ namespace {
 int greedy_impl(const void* target_logits, int dtype, const int32_t* draft_tokens,
                 const int32_t* draft_lens, int B, int k, int V, int32_t* out_tokens,
                 int32_t* out_num_accepted, int32_t* seq_lens, void* workspace,
-                size_t workspace_bytes, spec_stream_t stream) {
+                size_t workspace_bytes, spec_stream_t stream,
+                long long wait_cycles = kWaitCycles, bool skip_pass1 = false) {
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
   if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || k < 1 ||
       k > SPEC_MAX_DRAFT || V < 2)
@@ -246,9 +274,11 @@ int greedy_impl(const void* target_logits, int dtype, const int32_t* draft_token
   a.out_tokens = out_tokens;
   a.out_n = out_num_accepted;
   a.seq_lens = seq_lens;
+  a.wait_cycles = wait_cycles;
   a.ws = ws_views(workspace, WsLayout(B, R, V));
-  return launch_argmax(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
-                                                                           : SPEC_ECUDA;
+  return launch_argmax(a, dtype, vec, (cudaStream_t)stream, skip_pass1) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ECUDA;
 }
 
 }  // namespace
@@ -282,6 +312,26 @@ int spec_verify_chain_ex(const spec_chain_params* p, void* workspace, size_t wor
                     p->out_tokens, p->out_num_accepted, p->out_probs, p->seq_lens, workspace,
                     workspace_bytes, stream, has_filter ? p->top_k : 0,
                     has_filter ? p->top_p : 1.f);
+}
+
+int spec_test_timeout_chain(const spec_chain_params* p, long long wait_cycles, void* workspace,
+                            size_t workspace_bytes, spec_stream_t stream) {
+  const size_t v1 = offsetof(spec_chain_params, seq_lens) + sizeof(p->seq_lens);
+  if (!p || p->size < v1 || wait_cycles < 1) return SPEC_EINVAL;
+  const bool has_filter = p->size >= offsetof(spec_chain_params, top_p) + sizeof(p->top_p);
+  return chain_impl(p->target_logits, p->draft_logits, p->dtype, p->draft_tokens, p->uniforms,
+                    p->seeds, p->offsets, p->draft_lens, p->temperature, p->B, p->k, p->V,
+                    p->out_tokens, p->out_num_accepted, p->out_probs, p->seq_lens, workspace,
+                    workspace_bytes, stream, has_filter ? p->top_k : 0,
+                    has_filter ? p->top_p : 1.f, wait_cycles, true);
+}
+
+int spec_test_timeout_greedy(const spec_greedy_params* p, long long wait_cycles, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream) {
+  if (!p || p->size < sizeof(spec_greedy_params) || wait_cycles < 1) return SPEC_EINVAL;
+  return greedy_impl(p->target_logits, p->dtype, p->draft_tokens, p->draft_lens, p->B, p->k,
+                     p->V, p->out_tokens, p->out_num_accepted, p->seq_lens, workspace,
+                     workspace_bytes, stream, wait_cycles, true);
 }
 
 int spec_rollback_paged(const int32_t* old_lens, const int32_t* num_accepted,
@@ -327,6 +377,7 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* tree_t
   a.out_best = out_best_path;
   a.out_nodes = out_accepted_nodes;
   a.seq_lens = seq_lens;
+  a.wait_cycles = kWaitCycles;
   a.ws = ws_views(workspace, WsLayout(B, N, V));
   return launch_argmax(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
                                                                            : SPEC_ECUDA;

@@ -101,6 +101,7 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
   // of a hang.
   unsigned long long* words = reinterpret_cast<unsigned long long*>(a.ws.part) +
                               (size_t)b * R * ns;
+  bool to = false;  // a wait of this thread ran out
   for (int i0 = threadIdx.x; i0 < rows * ns; i0 += 4 * kThreads) {
     unsigned long long w[4];
 #pragma unroll
@@ -115,9 +116,10 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
       if (!w[q]) {
         const long long t0 = clock64();
         while (!(w[q] = ld_relaxed_u64(words + i))) {
-          if (clock64() - t0 > kWaitCycles) {
+          if (clock64() - t0 > a.wait_cycles) {
             set_status(a.ws.status, SPEC_ETIMEOUT);
             w[q] = arg_pack(-INFINITY, 0);
+            to = true;
             break;
           }
           __nanosleep(64);
@@ -129,6 +131,8 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
       atomicMax(&sKey[i / ns], arg_key(v, x));
     }
   }
+  // A unit word that never arrived: the request fails closed.
+  if (__syncthreads_or(to) && threadIdx.x == 0) sBad = 1;
   __syncthreads();
   // Every call leaves the workspace zero: clear this request's words.
   for (int i = threadIdx.x; i < R * ns; i += kThreads) words[i] = 0;
@@ -309,11 +313,13 @@ __global__ void __launch_bounds__(kThreads) argmax_finish_kernel(const ArgmaxArg
 }
 
 template <int DT, bool VEC>
-cudaError_t launch_argmax_t(const ArgmaxArgs& a, cudaStream_t st) {
+cudaError_t launch_argmax_t(const ArgmaxArgs& a, cudaStream_t st, bool skip_pass1) {
   const long g = (long)a.B * a.R * a.nsplit;
-  argmax_kernel<DT, VEC><<<(unsigned)g, kThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!skip_pass1) {
+    argmax_kernel<DT, VEC><<<(unsigned)g, kThreads, 0, st>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // Pass 2 may be scheduled once every pass-1 CTA has started.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.B < 1024 ? a.B : 1024));
@@ -328,10 +334,13 @@ cudaError_t launch_argmax_t(const ArgmaxArgs& a, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, argmax_finish_kernel, a);
 }
 
-cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st) {
+cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st,
+                          bool skip_pass1) {
   if (dtype == SPEC_BF16)
-    return vec ? launch_argmax_t<SPEC_BF16, true>(a, st) : launch_argmax_t<SPEC_BF16, false>(a, st);
-  return vec ? launch_argmax_t<SPEC_F32, true>(a, st) : launch_argmax_t<SPEC_F32, false>(a, st);
+    return vec ? launch_argmax_t<SPEC_BF16, true>(a, st, skip_pass1)
+               : launch_argmax_t<SPEC_BF16, false>(a, st, skip_pass1);
+  return vec ? launch_argmax_t<SPEC_F32, true>(a, st, skip_pass1)
+             : launch_argmax_t<SPEC_F32, false>(a, st, skip_pass1);
 }
 
 }  // namespace sv

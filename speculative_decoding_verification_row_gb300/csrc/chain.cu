@@ -80,8 +80,9 @@ __device__ __forceinline__ unsigned long long stats_pack(float M, float S) {
 __device__ __forceinline__ float2 stats_unpack(unsigned long long v) {
   return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
 }
-__device__ __forceinline__ unsigned long long wait_stats(const unsigned long long* p, int* status) {
-  return wait_word(p, status, kNoStats);
+__device__ __forceinline__ unsigned long long wait_stats(const ChainArgs& a,
+                                                         const unsigned long long* p, bool* to) {
+  return wait_word(p, a.ws.status, kNoStats, a.wait_cycles, to);
 }
 
 // ------------------------------------------------------------------ pass 1
@@ -470,7 +471,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
   __shared__ float sM[2 * SPEC_MAX_DRAFT + 1], sS[2 * SPEC_MAX_DRAFT + 1];
   __shared__ float sP[SPEC_MAX_DRAFT], sQ[SPEC_MAX_DRAFT], sU[SPEC_MAX_DRAFT + 1];
-  __shared__ int sJ, sBad, sLast;
+  __shared__ int sJ, sBad, sLast, sFailed;
   __shared__ unsigned long long sWT[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, R = 2 * k + 1;
@@ -505,6 +506,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   // takes each row max with shuffles, then adds S_s * 2^(c(m_s - M)) with one
   // exp per slice (no chain of exps).
   const unsigned long long* sb = a.ws.stats + (size_t)b * R * a.nsplit;
+  bool to = false;  // a wait of this thread ran out
   for (int r0 = warp; r0 < rows; r0 += 4 * kWarps) {
     unsigned long long v[4][2];
 #pragma unroll
@@ -522,7 +524,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         if (!v[q][h])  // only a present slice reads 0
-          v[q][h] = wait_stats(sb + (size_t)(r0 + q * kWarps) * a.nsplit + lane + 32 * h, a.ws.status);
+          v[q][h] = wait_stats(a, sb + (size_t)(r0 + q * kWarps) * a.nsplit + lane + 32 * h, &to);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int r = r0 + q * kWarps;
@@ -531,7 +533,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
       const float2 e0 = stats_unpack(v[q][0]), e1 = stats_unpack(v[q][1]);
       float m = fmaxf(e0.x, e1.x);
       for (int u = lane + 64; u < a.nsplit; u += 32)
-        m = fmaxf(m, stats_unpack(wait_stats(pr + u, a.ws.status)).x);
+        m = fmaxf(m, stats_unpack(wait_stats(a, pr + u, &to)).x);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       float sum = 0.f;
@@ -550,7 +552,13 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
       }
     }
   }
-  __syncthreads();
+  // A statistics word that never arrived: this item skips its draw work and
+  // the request fails closed (every item's flag reaches the finishing item
+  // through the ticket below).
+  if (__syncthreads_or(to) && tid == 0) {
+    sBad = 1;
+    atomicExch(&a.ws.sync[b].failed, 1);
+  }
   if (tid < kb) {
     if (bad) {
       sBad = 1;
@@ -608,6 +616,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
     if (sLast) {
       a.ws.sync[b].tick2 = 0;
       __threadfence();
+      sFailed = atomicExch(&a.ws.sync[b].failed, 0);
     }
   }
   __syncthreads();
@@ -618,7 +627,9 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   for (int i = tid; i < R * a.nsplit; i += kThreads)
     const_cast<unsigned long long*>(sb)[i] = 0;
   int32_t* out = a.out_tokens + (size_t)b * (k + 1);
-  if (j < 0) {  // a draft token was out of range: the request fails closed
+  if (j < 0 || sFailed) {  // a bad draft token or length, or a wait ran out: fail closed
+    for (int i = tid; i < a.nchunks; i += kThreads) a.ws.chunks[(size_t)b * a.nchunks + i] = 0;
+    for (int i = tid; i < a.nsplit2; i += kThreads) a.ws.items[(size_t)b * a.nsplit2 + i] = 0;
     for (int i = tid; i <= k; i += kThreads) out[i] = -1;
     if (a.out_probs)
       for (int i = tid; i < 2 * k; i += kThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
@@ -679,7 +690,7 @@ cudaError_t draw_grid(int* grid) {
 }
 
 template <int DT, bool VEC>
-cudaError_t launch_chain_t(const ChainArgs& args, cudaStream_t st) {
+cudaError_t launch_chain_t(const ChainArgs& args, cudaStream_t st, bool skip_pass1) {
   int slots = 0;
   cudaError_t e = draw_grid<DT, VEC>(&slots);
   if (e != cudaSuccess) return e;
@@ -693,9 +704,11 @@ cudaError_t launch_chain_t(const ChainArgs& args, cudaStream_t st) {
     a.nsplit2 = ceil_div(a.nchunks, a.cpc);
   }
   const long g1 = (long)a.B * (2 * a.k + 1) * a.nsplit;
-  chain_rowstats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!skip_pass1) {
+    chain_rowstats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const long items = (long)a.B * a.nsplit2;
   // Pass 2 may be scheduled once every pass-1 CTA has started; each draw
   // item waits only for its own request's slices.
@@ -714,10 +727,12 @@ cudaError_t launch_chain_t(const ChainArgs& args, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st) {
+cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st, bool skip_pass1) {
   if (dtype == SPEC_BF16)
-    return vec ? launch_chain_t<SPEC_BF16, true>(a, st) : launch_chain_t<SPEC_BF16, false>(a, st);
-  return vec ? launch_chain_t<SPEC_F32, true>(a, st) : launch_chain_t<SPEC_F32, false>(a, st);
+    return vec ? launch_chain_t<SPEC_BF16, true>(a, st, skip_pass1)
+               : launch_chain_t<SPEC_BF16, false>(a, st, skip_pass1);
+  return vec ? launch_chain_t<SPEC_F32, true>(a, st, skip_pass1)
+             : launch_chain_t<SPEC_F32, false>(a, st, skip_pass1);
 }
 
 }  // namespace sv

@@ -39,8 +39,9 @@ __host__ __device__ inline int num_items(int V) { return ceil_div(num_chunks(V),
 // Per-request synchronisation words, 64 bytes apart so that the CTAs of
 // different requests rarely share a line.
 struct ReqSync {
-  int tick2;  // chain: draw items of the request that have finished
-  int pad[15];
+  int tick2;   // chain: draw items (filtered: row CTAs) of the request that have finished
+  int failed;  // nonzero once a wait of the request's second phase ran out
+  int pad[14];
 };
 static_assert(sizeof(ReqSync) == 64, "ReqSync layout");
 
@@ -270,8 +271,9 @@ __device__ __forceinline__ float philox_uniform(unsigned long long seed, unsigne
   return (float)(x >> 8) * (1.0f / 16777216.0f);
 }
 
-// Upper bound of every device-side wait (about one second at 2 GHz).  A wait
-// that runs out sets SPEC_ETIMEOUT instead of spinning forever.
+// Default upper bound of every device-side wait (about one second at 2 GHz).
+// A wait that runs out sets SPEC_ETIMEOUT instead of spinning forever, and
+// the request whose result depended on it fails closed.
 constexpr long long kWaitCycles = 2000000000LL;
 
 // Device-scope relaxed 64-bit accesses (single-copy atomic, no fence).
@@ -288,15 +290,17 @@ __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(st
 
 // Poll a word until a producer grid has written it (written words are never
 // 0).  The producer was scheduled in full before the polling grid, so the
-// wait ends; the bound only turns a broken invariant into SPEC_ETIMEOUT and
-// `on_timeout` instead of a hang.
+// wait ends; the bound (`limit` cycles) only turns a broken invariant into
+// SPEC_ETIMEOUT, *timed_out = true and `on_timeout` instead of a hang.
 static __device__ __noinline__ unsigned long long wait_word(const unsigned long long* p, int* status,
-                                                     unsigned long long on_timeout) {
+                                                            unsigned long long on_timeout,
+                                                            long long limit, bool* timed_out) {
   unsigned long long v = ld_relaxed_u64(p);
   const long long t0 = clock64();
   while (!v) {
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_status(status, SPEC_ETIMEOUT);
+      *timed_out = true;
       return on_timeout;
     }
     __nanosleep(64);

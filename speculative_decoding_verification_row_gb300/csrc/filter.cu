@@ -85,6 +85,7 @@ struct RowSmem {
   int m;                                 // top-p: kept entries
   float sm;                              // top-p: mass of the kept entries
   int last;                              // this CTA finishes the request
+  int failed;                            // finish: a wait of the request ran out
 };
 
 // Block-wide sum of one int per thread over a kRowThreads CTA.
@@ -517,7 +518,10 @@ __device__ __forceinline__ void row_done(RowSmem& S, const ChainArgs& a, int b) 
                  : "l"(&a.ws.sync[b].tick2)
                  : "memory");
     S.last = t == R - 1;
-    if (S.last) a.ws.sync[b].tick2 = 0;
+    if (S.last) {
+      a.ws.sync[b].tick2 = 0;
+      S.failed = atomicExch(&a.ws.sync[b].failed, 0);
+    }
   }
   __syncthreads();
   if (S.last) finish_request(S, a, b);
@@ -750,12 +754,14 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
     // 16-bit half still 0 is not written yet: wait for it, bounded), stored
     // back decoded (0 = no finite logit).
     uint4* g = reinterpret_cast<uint4*>(a.ws.codes + (size_t)blockIdx.x * n);
+    bool to = false;  // a wait of this thread ran out
     for (int i = tid; i < n / 8; i += kRowThreads) {
       uint4 v = ld_volatile_v4(g + i);
       const long long t0 = clock64();
       while (!all_halves_set(v)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > a.wait_cycles) {
           set_status(a.ws.status, SPEC_ETIMEOUT);
+          to = true;
           break;
         }
         __nanosleep(256);
@@ -769,6 +775,9 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
       reinterpret_cast<uint4*>(codes)[i] = make_uint4(d[0], d[1], d[2], d[3]);
       g[i] = make_uint4(0, 0, 0, 0);  // every call leaves the workspace zero
     }
+    // A code that never arrived: the request fails closed (the flag reaches
+    // the finishing row CTA through the acquire-release ticket).
+    if (__syncthreads_or(to) && tid == 0) atomicExch(&a.ws.sync[b].failed, 1);
     if (tid == 0) S.n = 0;
     __syncthreads();
     const uint32_t tau = code_threshold(codes, n, K, S);
@@ -948,7 +957,7 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
   const float ratio = Q > 0.f ? P / Q : INFINITY;
   if (tid < kb && !(U < ratio)) atomicMin(&S.m, tid);
   __syncthreads();
-  const int j = any_bad ? -1 : S.m;
+  const int j = (any_bad || S.failed) ? -1 : S.m;
   const double u = (double)S.sm;
   int32_t* out = a.out_tokens + (size_t)b * (k + 1);
   if (j >= 0) {
@@ -1097,7 +1106,7 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
       a.out_n[b] = j;
       if (a.seq_lens) a.seq_lens[b] += j + 1;
     }
-  } else {  // a draft token or the draft length was invalid: fail closed
+  } else {  // a bad draft token or length, or a wait ran out: fail closed
     for (int i = tid; i <= k; i += kRowThreads) out[i] = -1;
     if (a.out_probs)
       for (int i = tid; i < 2 * k; i += kRowThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
@@ -1116,12 +1125,14 @@ __device__ __noinline__ void finish_request(RowSmem& S, const ChainArgs& a, int 
 }
 
 template <int DT, bool VEC>
-cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st) {
+cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st, bool skip_pass1) {
   const long rows = (long)a.B * (2 * a.k + 1);
   if ((long)a.nsplit * kThreads <= kMaxCodes) {
-    filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (!skip_pass1) {
+      filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     // The pick grid may be scheduled once every pass-1 CTA has started; each
     // row CTA waits only for its own row's codes.
     cudaLaunchConfig_t cfg = {};
@@ -1136,6 +1147,7 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st) {
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, filter_pick_kernel<DT, VEC>, a);
   } else {  // a row too wide for one CTA's prefixes: stream it through one CTA
+    if (skip_pass1) return cudaErrorNotSupported;  // one pass: no wait to run out
     filter_row_kernel<DT, VEC><<<(unsigned)rows, kRowThreads, 0, st>>>(a);
   }
   return cudaGetLastError();
@@ -1143,10 +1155,13 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_t st) {
+cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_t st,
+                            bool skip_pass1) {
   if (dtype == SPEC_BF16)
-    return vec ? launch_filtered_t<SPEC_BF16, true>(a, st) : launch_filtered_t<SPEC_BF16, false>(a, st);
-  return vec ? launch_filtered_t<SPEC_F32, true>(a, st) : launch_filtered_t<SPEC_F32, false>(a, st);
+    return vec ? launch_filtered_t<SPEC_BF16, true>(a, st, skip_pass1)
+               : launch_filtered_t<SPEC_BF16, false>(a, st, skip_pass1);
+  return vec ? launch_filtered_t<SPEC_F32, true>(a, st, skip_pass1)
+             : launch_filtered_t<SPEC_F32, false>(a, st, skip_pass1);
 }
 
 }  // namespace sv

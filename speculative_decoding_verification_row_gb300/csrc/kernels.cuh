@@ -23,6 +23,7 @@ struct ChainArgs {
   int32_t* out_n;
   float* out_probs;
   int32_t* seq_lens;
+  long long wait_cycles;       // bound of every wait of the second phase (kWaitCycles)
   Ws ws;
 };
 
@@ -42,6 +43,7 @@ struct ArgmaxArgs {
   int32_t* out_best;
   int32_t* out_nodes;
   int32_t* seq_lens;
+  long long wait_cycles;       // bound of every wait of the finish grid (kWaitCycles)
   Ws ws;
 };
 
@@ -60,9 +62,24 @@ __device__ __forceinline__ bool row_used(int k, int kb, int r) {
 }
 
 // Enqueue the two chain passes (pass 2 as a programmatic dependent launch) /
-// the argmax pass on `st`.
-cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
-cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
-cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st);
+// the argmax pass on `st`.  skip_pass1 (fault injection for tests only)
+// launches the second grid alone, so that every word it waits for stays
+// unwritten and each of its bounded waits runs out.
+cudaError_t launch_chain(const ChainArgs& a, int dtype, bool vec, cudaStream_t st,
+                         bool skip_pass1 = false);
+cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_t st,
+                            bool skip_pass1 = false);
+cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st,
+                          bool skip_pass1 = false);
+
+// Host side of a chain verify (api.cu): argument checks that fill the
+// launch arguments without writing anything, then the launch.
+int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* draft_logits,
+                int dtype, const int32_t* draft_tokens, const float* uniforms,
+                const uint64_t* seeds, const uint64_t* offsets, const int32_t* draft_lens,
+                float temperature, int B, int k, int V, int32_t* out_tokens,
+                int32_t* out_num_accepted, float* out_probs, int32_t* seq_lens, void* workspace,
+                size_t workspace_bytes, int top_k, float top_p);
+int chain_launch(const ChainArgs& a, int dtype, bool vec, cudaStream_t st, bool skip_pass1);
 
 }  // namespace sv

@@ -489,6 +489,13 @@ def pin_rollback(lib=None) -> list[str]:
     edge = oracle.rollback(np.array([10, 10], np.int32), np.array([k, 0], np.int32), k, lib=lib)
     if list(edge["rewind_lens"]) != [0, k] or list(edge["new_lens"]) != [10 + k + 1, 11]:
         errs.append("rewind boundaries wrong")
+    # a count outside [0, k] (a failed request's -1, or a corrupt k + 1)
+    # keeps the length and reads rewind -1
+    bad = oracle.rollback(np.array([10, 20, 30], np.int32), np.array([-1, k + 1, 2], np.int32), k,
+                          lib=lib)
+    if bad["rc"] != oracle.EBADINDEX or list(bad["new_lens"]) != [10, 20, 33] or \
+            list(bad["rewind_lens"]) != [-1, -1, k - 2]:
+        errs.append(f"bad rollback entries: {bad['new_lens']} / {bad['rewind_lens']}")
     return errs
 
 
@@ -630,7 +637,8 @@ def pin_rollback_paged(lib=None) -> list[str]:
         errs.append(f"paged rollback free blocks {res['free_blocks']}")
     bad = oracle.rollback_paged([5, 5], [3, 1], k=4, tokens_per_block=4, draft_lens=[2, 9],
                                 blocks_held=[9, 9], lib=lib)
-    if bad["rc"] != oracle.EBADINDEX or bad["new_lens"].tolist() != [5, 5] or bad["free_blocks"].tolist() != [0, 0]:
+    if bad["rc"] != oracle.EBADINDEX or bad["new_lens"].tolist() != [5, 5] or \
+            bad["free_blocks"].tolist() != [0, 0] or bad["rewind_lens"].tolist() != [-1, -1]:
         errs.append("paged rollback must refuse n > k_b and k_b > k entry by entry")
     return errs
 

@@ -62,6 +62,10 @@ MUTANTS = {
                                         "int tok = oracle_inverse_cdf(w, V, (double)r[k], SAMPLE_TIE, &tie);"),
     "greedy_scans_padding": ("while (j < kb && oracle_argmax", "while (j < k && oracle_argmax"),
     "tree_tie_keeps_later_path": ("if (acc > best_acc) {", "if (acc >= best_acc) {"),
+    "rollback_bad_entry_rewind_zero": ("if (n < 0 || n > k) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = -1;",
+                                       "if (n < 0 || n > k) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = 0;"),
+    "paged_bad_entry_rewind_zero": ("if (kb < 0 || kb > k || n < 0 || n > kb) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = -1;",
+                                    "if (kb < 0 || kb > k || n < 0 || n > kb) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = 0;"),
     # near-tie windows (|r - p/q| < 1e-5; u*Z within 1e-6*Z of a CDF boundary)
     "accept_window_wide": ("static const double ACCEPT_TIE = 1e-5;",
                            "static const double ACCEPT_TIE = 1.0;"),

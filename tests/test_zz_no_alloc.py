@@ -1,16 +1,19 @@
 """The allocation-free chain entry point, for callers that cannot allocate
 device memory (an allocator that forbids allocations during a step, or host
 code without a CUDA allocator).  It must give the same results as the
-workspace entry point, call after call, although every call reuses the same
-fixed device scratch array.  Collected last on purpose."""
+workspace entry point and agree with the CPU oracle, call after call,
+although every call reuses the same fixed device scratch array.  Collected
+last on purpose."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 import speculative_decoding_verification_row_gb300 as sv
+from test_gpu_parity import check_chain
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +56,33 @@ def test_noalloc_matches_workspace_entry_point(name, over):
         assert np.array_equal(s.cpu().numpy(), ref_seq), f"call {call}: seq_lens"
         rel = ((probs - ref_p).abs() / ref_p.abs().clamp_min(1e-30)).max().item()
         assert rel <= 1e-5, f"call {call}: probabilities differ by {rel}"
+        # and against the oracle itself (exact outside flagged near-ties)
+        g = dict(tokens=tok.cpu().numpy(), num_accepted=n.cpu().numpy(), probs=probs.cpu().numpy(),
+                 seq_lens=s.cpu().numpy())
+        check_chain(w, g, oracle.verify(w), f"noalloc {name} call {call}")
+
+
+def test_noalloc_refuses_host_arrays_and_leaves_its_scratch_usable():
+    # Arrays outside the current device's memory are refused (SPEC_EINVAL)
+    # before the shared scratch array is written; the next call is correct.
+    w = workloads.make("chain_b8_k4_v32000_f32", seed=25, B=3, V=3000)
+    host_tokens = np.ascontiguousarray(w["draft_tokens"], dtype=np.int32)
+    t, d = _dev(w["target"], w["dtype"]), _dev(w["draft"], w["dtype"])
+    u = torch.from_numpy(w["uniforms"]).cuda()
+    B, k, V = w["B"], w["k"], w["V"]
+    tok = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    P = lambda z: ctypes.c_void_p(z.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = sv.lib().spec_verify_chain_noalloc(P(t), P(d), 0, host_tokens.ctypes.data_as(ctypes.c_void_p), P(u),
+                                            ctypes.c_float(w["temperature"]), B, k, V, P(tok), P(n),
+                                            None, None, stream)
+    assert rc == sv.SPEC_EINVAL
+    tk, nn, pr = sv.verify_chain_noalloc(t, d, _i32(w["draft_tokens"]), u, w["temperature"], want_probs=True)
+    torch.cuda.synchronize()
+    g = dict(tokens=tk.cpu().numpy(), num_accepted=nn.cpu().numpy(), probs=pr.cpu().numpy(),
+             seq_lens=oracle.rollback(w["seq_lens"], nn.cpu().numpy(), k)["new_lens"])
+    check_chain(w, g, oracle.verify(w), "noalloc after a refused call")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
