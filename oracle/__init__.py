@@ -59,13 +59,15 @@ def _bind(lib):
                                                  I, I, I, P, P, P, P]
     lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.oracle_rollback.argtypes = [P, P, I, I, P, P]
+    lib.oracle_verify_tree_sampled.argtypes = [P, I, P, P, P, ctypes.c_float, I, I, I, I, I,
+                                               P, P, P, P, P]
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox4x32_10.restype = None
     lib.oracle_philox_uniforms.argtypes = [P, P, I, I, P]
     for f in ("oracle_softmax", "oracle_inverse_cdf", "oracle_argmax", "oracle_verify_chain",
               "oracle_verify_greedy", "oracle_verify_tree", "oracle_rollback",
               "oracle_philox_uniforms", "oracle_rollback_paged", "oracle_filtered_softmax",
-              "oracle_verify_chain_filtered"):
+              "oracle_verify_chain_filtered", "oracle_verify_tree_sampled"):
         getattr(lib, f).restype = I
     return lib
 
@@ -229,6 +231,35 @@ def verify_tree(target, tree_tokens, paths, dtype: str = "f32", lib=None) -> dic
     if rc not in (OK, EBADINDEX):
         raise ValueError(f"oracle_verify_tree rc={rc}")
     return dict(tokens=tokens, num_accepted=n_acc, best_path=best, accepted_nodes=nodes, rc=rc)
+
+
+def verify_tree_sampled(target, tree_tokens, paths, uniforms, temperature: float,
+                        dtype: str = "f32", lib=None) -> dict:
+    """Stochastic tree verify (TensorRT-LLM deployment page, tree verification
+    by rejection sampling; children are point-mass proposals): target [B,N,V],
+    tree_tokens [B,N], paths [B,P,L], uniforms float32 [B,N] (column n >= 1 is
+    node n's accept test, column 0 the final draw).  Returns tokens [B,L],
+    num_accepted [B], best_path [B], accepted_nodes [B,L], flags [B,N], rc."""
+    lib = lib or load()
+    target = _logits(target, dtype)
+    B, N, V = target.shape
+    tok = _c(tree_tokens, np.int32)
+    pth = _c(paths, np.int32)
+    _, P, L = pth.shape
+    u = _c(uniforms, np.float32)
+    assert tok.shape == (B, N) and u.shape == (B, N) and pth.shape[0] == B
+    tokens = np.empty((B, L), dtype=np.int32)
+    n_acc = np.empty(B, dtype=np.int32)
+    best = np.empty(B, dtype=np.int32)
+    nodes = np.empty((B, L), dtype=np.int32)
+    flags = np.empty((B, N), dtype=np.int32)
+    rc = lib.oracle_verify_tree_sampled(_ptr(target), DTYPE_CODE[dtype], _ptr(tok), _ptr(pth), _ptr(u),
+                                        float(temperature), B, N, P, L, V, _ptr(tokens), _ptr(n_acc),
+                                        _ptr(best), _ptr(nodes), _ptr(flags))
+    if rc not in (OK, EBADINDEX):
+        raise ValueError(f"oracle_verify_tree_sampled rc={rc}")
+    return dict(tokens=tokens, num_accepted=n_acc, best_path=best, accepted_nodes=nodes, flags=flags,
+                rc=rc)
 
 
 def rollback(old_lens, num_accepted, k: int, lib=None) -> dict:

@@ -34,6 +34,10 @@
  *                                     sampling section (the target must be
  *                                     filtered exactly as the draft was:
  *                                     same temperature, top-k, top-p).
+ *   - stochastic tree verify ........ TensorRT-LLM deployment page, "目标模型
+ *                                     验证：树注意力与批量并行" (tree tokens judged
+ *                                     by rejection sampling; children chosen by
+ *                                     top-K, "Eagle-2" section).
  *   - per-request uniforms .......... TensorRT-LLM walkthrough, rejection-
  *                                     sampling section (a Philox state of
  *                                     seed and offset per request); the
@@ -699,5 +703,177 @@ int oracle_verify_chain_filtered(const void *target, const void *draft, int dtyp
         out_num_accepted[b] = j;
     }
     free(p), free(q), free(w), free(ratio), free(rowtie);
+    return rc;
+}
+
+/* Stochastic tree verify (TensorRT-LLM deployment page, "目标模型验证：树注意力
+ * 与批量并行": the draft tree's tokens are judged against the target logits by
+ * rejection sampling; the tree itself is built by top-K selection per level,
+ * "Eagle-2 多层级树状草稿生成").  This library's reading: a node's children are
+ * chosen, not sampled, so each child c is a point-mass proposal on its token,
+ * and the rejection-sampling rule (accept with min(1, p/q), else continue
+ * from max(0, p - q) normalised; vLLM anatomy page, "Speculative Decoding")
+ * with q = that point mass becomes: accept c with probability p'(tok c), the
+ * current residual of the node's target distribution; on a rejection remove
+ * tok c from the residual (its mass max(0, p - 1) = 0) and renormalise.
+ * The emitted tokens are then distributed exactly as sampling from the
+ * target rows in turn.
+ *   target [B, N, V]: row n is the distribution after node n (node 0 = root);
+ *   tree_tokens [B, N]; paths [B, P, L] as for oracle_verify_tree;
+ *   uniforms [B, N]: uniforms[b, n] (n >= 1) is node n's accept test, used
+ *     when n is tried as a child; uniforms[b, 0] drives the final draw.
+ * Walk: the accepted prefix starts as (0).  Its candidates are the distinct
+ * nodes paths[p][d + 1] >= 0 of the used paths p whose first d + 1 entries
+ * equal the prefix (d = its depth), tried in increasing node id.  With p the
+ * softmax of the current node's row at T and R the tokens rejected so far at
+ * this node, candidate c is accepted iff u[c] < p'(tok c) = [tok c not in R]
+ * p(tok c) / (1 - sum over R of p); then c joins the prefix (at most L - 1
+ * steps).  When no candidate is accepted (or none exists) the final token is
+ * the inverse-CDF draw at u[0] from w_t = p(t) [t not in R] (from p itself if
+ * that total vanishes).  Outputs as for oracle_verify_tree; out_best_path is
+ * the lowest used path whose first n_acc + 1 entries are the accepted nodes.
+ *   out_flags [B, N] (nullable): column c = 1 when c's accept test is a near
+ *     tie, |u[c] - p'| below 1e-5 / (1 - sum over R of p) (the residual's
+ *     normaliser divides the precision of p' as well), column 0 when the
+ *     final draw is one (u*Z within 1e-6*Z of a CDF boundary).
+ * A request with a token outside [0, V), a node id outside [-1, N) or a path
+ * starting elsewhere than 0 or -1 fails closed (n_acc -1, rows all -1). */
+int oracle_verify_tree_sampled(const void *target, int dtype, const int32_t *tree_tokens,
+                               const int32_t *paths, const float *uniforms, float temperature,
+                               int B, int N, int P, int L, int V, int32_t *out_tokens,
+                               int32_t *out_num_accepted, int32_t *out_best_path,
+                               int32_t *out_accepted_nodes, int32_t *out_flags)
+{
+    if (!target || !tree_tokens || !paths || !uniforms || !out_tokens || !out_num_accepted ||
+        B < 1 || N < 1 || P < 1 || L < 2 || V < 2 || !(temperature > 0.0f) ||
+        !isfinite(temperature) || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_EINVAL;
+    const size_t es = dtype == ORC_F32 ? 4 : 2;
+    const double T = (double)temperature;
+    double *p = malloc(sizeof(double) * (size_t)V);
+    double *w = malloc(sizeof(double) * (size_t)V);
+    int *alive = malloc(sizeof(int) * (size_t)P);
+    int *cand = malloc(sizeof(int) * (size_t)P);
+    int *prefix = malloc(sizeof(int) * (size_t)L);
+    if (!p || !w || !alive || !cand || !prefix) {
+        free(p), free(w), free(alive), free(cand), free(prefix);
+        return ORC_ENOMEM;
+    }
+    int rc = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)b * (size_t)N * (size_t)V * es;
+        const int32_t *tok = tree_tokens + (size_t)b * N;
+        const int32_t *pb = paths + (size_t)b * P * L;
+        const float *u = uniforms + (size_t)b * N;
+        int32_t *out = out_tokens + (size_t)b * L;
+        int32_t *nodes = out_accepted_nodes ? out_accepted_nodes + (size_t)b * L : NULL;
+        int32_t *flags = out_flags ? out_flags + (size_t)b * N : NULL;
+        if (flags)
+            for (int n = 0; n < N; ++n)
+                flags[n] = 0;
+        int bad = 0;
+        for (int n = 0; n < N; ++n)
+            if (tok[n] < 0 || tok[n] >= V)
+                bad = 1;
+        for (int pth = 0; pth < P; ++pth) {
+            if (pb[(size_t)pth * L] != 0 && pb[(size_t)pth * L] != -1)
+                bad = 1;
+            for (int j = 0; j < L; ++j)
+                if (pb[(size_t)pth * L + j] < -1 || pb[(size_t)pth * L + j] >= N)
+                    bad = 1;
+        }
+        if (bad) {
+            fail_closed_row(out, L, &out_num_accepted[b]);
+            if (nodes)
+                for (int j = 0; j < L; ++j)
+                    nodes[j] = -1;
+            if (out_best_path)
+                out_best_path[b] = -1;
+            rc = ORC_EBADINDEX;
+            continue;
+        }
+        for (int pth = 0; pth < P; ++pth)
+            alive[pth] = pb[(size_t)pth * L] == 0;
+        prefix[0] = 0;
+        int d = 0, node = 0, final_tok = -1;
+        for (;;) {
+            oracle_softmax(tb + (size_t)node * V * es, dtype, T, V, p);
+            /* candidates: distinct next nodes of the paths still on the prefix */
+            int nc = 0;
+            if (d + 1 < L)
+                for (int pth = 0; pth < P; ++pth) {
+                    if (!alive[pth])
+                        continue;
+                    const int c = pb[(size_t)pth * L + d + 1];
+                    if (c < 0)
+                        continue;
+                    int seen = 0;
+                    for (int i = 0; i < nc; ++i)
+                        seen |= cand[i] == c;
+                    if (!seen)
+                        cand[nc++] = c;
+                }
+            for (int i = 1; i < nc; ++i) /* increasing node id */
+                for (int j2 = i; j2 > 0 && cand[j2 - 1] > cand[j2]; --j2) {
+                    const int t = cand[j2];
+                    cand[j2] = cand[j2 - 1];
+                    cand[j2 - 1] = t;
+                }
+            double removed = 0.0;
+            int next = -1;
+            for (int i = 0; i < nc; ++i) {
+                const int c = cand[i];
+                const double pc = p[tok[c]];
+                const double ratio = (1.0 - removed) > 0.0 ? pc / (1.0 - removed) : 0.0;
+                if (flags && (1.0 - removed) > 0.0 &&
+                    fabs((double)u[c] - ratio) < ACCEPT_TIE / (1.0 - removed))
+                    flags[c] = 1;
+                if ((double)u[c] < ratio) {
+                    next = c;
+                    break;
+                }
+                removed += pc;
+                p[tok[c]] = 0.0; /* the residual no longer holds tok c */
+            }
+            if (next < 0) {
+                for (int t = 0; t < V; ++t)
+                    w[t] = p[t];
+                int32_t tie = 0;
+                final_tok = oracle_inverse_cdf(w, V, (double)u[0], SAMPLE_TIE, &tie);
+                if (final_tok < 0) { /* the residual vanished: draw from the row itself */
+                    oracle_softmax(tb + (size_t)node * V * es, dtype, T, V, p);
+                    final_tok = oracle_inverse_cdf(p, V, (double)u[0], SAMPLE_TIE, &tie);
+                }
+                if (flags)
+                    flags[0] = tie;
+                break;
+            }
+            ++d;
+            prefix[d] = next;
+            node = next;
+            for (int pth = 0; pth < P; ++pth)
+                alive[pth] = alive[pth] && pb[(size_t)pth * L + d] == next;
+        }
+        int best = -1;
+        for (int pth = 0; pth < P && best < 0; ++pth) {
+            int ok = pb[(size_t)pth * L] == 0;
+            for (int j = 1; ok && j <= d; ++j)
+                ok = pb[(size_t)pth * L + j] == prefix[j];
+            if (ok)
+                best = pth;
+        }
+        for (int j = 0; j < d; ++j)
+            out[j] = tok[prefix[j + 1]];
+        out[d] = final_tok;
+        for (int j = d + 1; j < L; ++j)
+            out[j] = -1;
+        if (nodes)
+            for (int j = 0; j < L; ++j)
+                nodes[j] = j <= d ? prefix[j] : -1;
+        if (out_best_path)
+            out_best_path[b] = best;
+        out_num_accepted[b] = d;
+    }
+    free(p), free(w), free(alive), free(cand), free(prefix);
     return rc;
 }

@@ -696,6 +696,196 @@ def pin_ragged(lib=None) -> list[str]:
     return errs
 
 
+# --------------------------------------------------------------------------- stochastic tree
+def _children(paths, prefix):
+    """Distinct next nodes (increasing id) of the used paths that start with ``prefix``."""
+    d = len(prefix) - 1
+    out = set()
+    for row in paths:
+        if row[0] != 0 or d + 1 >= len(row):
+            continue
+        if list(row[: d + 1]) == list(prefix) and row[d + 1] >= 0:
+            out.add(int(row[d + 1]))
+    return sorted(out)
+
+
+def enumerate_tree_sampled(target, tokens, paths, T):
+    """Every branch of the stochastic tree walk for one small tree: for each
+    state (accepted prefix), each candidate accepted after the earlier ones
+    were rejected, or the final draw of each token with positive residual
+    weight.  Uniforms take each branch (reject: (1 + p')/2, accept: p'/2,
+    final draw: the midpoint of the token's CDF interval).  Returns
+    (weights, expected (n_acc, tokens), uniforms [n, N], reach) where reach
+    lists (branch mask of reaching node n, p_n)."""
+    N, V = target.shape
+    L = paths.shape[1]
+    p_of = [_softmax_T(target[n], T) for n in range(N)]
+    branches = []  # (weight, n_acc, tokens, uniforms, visited nodes)
+
+    def walk(prefix, weight, u, emitted):
+        node = prefix[-1]
+        p = p_of[node].copy()
+        removed = 0.0
+        for c in _children(paths, prefix):
+            pc = p[tokens[c]]
+            ratio = pc / (1.0 - removed) if 1.0 - removed > 0 else 0.0
+            if ratio > 0:
+                u2 = u.copy()
+                u2[c] = ratio / 2
+                walk(prefix + [c], weight * ratio, u2, emitted + [int(tokens[c])])
+            if ratio >= 1.0:
+                return
+            u[c] = (1.0 + ratio) / 2
+            weight *= 1.0 - ratio
+            removed += pc
+            p[tokens[c]] = 0.0
+        Z = p.sum()
+        cdf = np.concatenate([[0.0], np.cumsum(p)])
+        for t in range(V):
+            if p[t] > 0:
+                u2 = u.copy()
+                u2[0] = (cdf[t] + cdf[t + 1]) / (2 * Z)
+                toks = emitted + [t]
+                branches.append((weight * p[t] / Z, len(emitted), toks + [-1] * (L - len(toks)),
+                                 u2, list(prefix)))
+
+    walk([0], 1.0, np.full(N, 0.5), [])
+    return branches, p_of
+
+
+def _random_small_tree(rng, N, V, L):
+    parent = np.zeros(N, int)
+    depth = np.zeros(N, int)
+    for n in range(1, N):
+        cands = [m for m in range(n) if depth[m] < L - 1]
+        parent[n] = cands[int(rng.integers(0, len(cands)))]
+        depth[n] = depth[parent[n]] + 1
+    tokens = np.zeros(N, np.int32)
+    tokens[0] = int(rng.integers(0, V))
+    for n in range(1, N):
+        used = {int(tokens[m]) for m in range(1, n) if parent[m] == parent[n]}
+        free = [t for t in range(V) if t not in used]
+        tokens[n] = free[int(rng.integers(0, len(free)))]
+    return parent, tokens, _paths_from_parents(parent, L, N)
+
+
+def pin_tree_sampled(lib=None) -> list[str]:
+    """Stochastic tree verify (reading T5: chosen children are point-mass
+    proposals).  Exact enumeration of every branch on small trees: each
+    branch's outcome, and the theorem that at every reached node the next
+    emitted token is distributed as that node's target row, to 1e-12.  A
+    one-chain tree equals the chain verify with one-hot draft rows; one-hot
+    target rows equal the greedy tree verify; the near-tie windows on closed
+    forms; fail-closed inputs."""
+    errs = []
+    rng = np.random.default_rng(41)
+    for trial, (N, V, L, T) in enumerate([(4, 5, 3, 1.0), (6, 4, 4, 0.7), (7, 6, 3, 1.3), (5, 3, 5, 0.9)]):
+        parent, tokens, paths = _random_small_tree(rng, N, V, L)
+        target = (rng.standard_normal((N, V)) * 1.5).astype(np.float32)
+        # make the drafted children likely under their parent's row
+        for n in range(1, N):
+            target[parent[n], tokens[n]] += 1.0
+        branches, p_of = enumerate_tree_sampled(target, tokens, paths, T)
+        wts = np.array([b[0] for b in branches])
+        if abs(wts.sum() - 1.0) > 1e-12:
+            errs.append(f"tree {trial}: branch weights sum to {wts.sum()}")
+        n = len(branches)
+        res = oracle.verify_tree_sampled(np.broadcast_to(target, (n, N, V)).copy(),
+                                         np.broadcast_to(tokens, (n, N)).copy(),
+                                         np.broadcast_to(paths, (n,) + paths.shape).copy(),
+                                         np.array([b[3] for b in branches], np.float32), T, lib=lib)
+        for e, (_, nacc, toks, _, _) in enumerate(branches):
+            if res["num_accepted"][e] != nacc or list(res["tokens"][e]) != toks:
+                errs.append(f"tree {trial}: branch {e} gave {res['tokens'][e]} (n={res['num_accepted'][e]}), "
+                            f"want {toks} (n={nacc})")
+                break
+        # theorem: at each reached node, the next emitted token ~ p_node
+        for node in range(N):
+            reach = np.array([node in b[4] for b in branches])
+            pos = [b[4].index(node) if node in b[4] else -1 for b in branches]
+            if not reach.any():
+                continue
+            pr = wts[reach].sum()
+            dist = np.zeros(V)
+            for e in np.flatnonzero(reach):
+                dist[branches[e][2][pos[e]]] += wts[e]
+            if np.max(np.abs(dist / pr - p_of[node])) > 1e-12:
+                errs.append(f"tree {trial}: token after node {node} is not distributed as its row")
+                break
+    # one-chain tree == chain verify with one-hot draft rows (q = point mass)
+    k, V, T = 3, 9, 0.8
+    target = (rng.standard_normal((20, k + 1, V)) * 2).astype(np.float32)
+    x = rng.integers(0, V, (20, k)).astype(np.int32)
+    u = rng.random((20, k + 1)).astype(np.float32)
+    draft = np.full((20, k, V), -np.inf, np.float32)
+    for b in range(20):
+        draft[b, np.arange(k), x[b]] = 0.0
+    chain = oracle.verify_chain(target, draft, x, u, T, lib=lib)
+    toks = np.concatenate([np.zeros((20, 1), np.int32), x], axis=1)
+    paths = np.tile(np.arange(k + 1, dtype=np.int32), (20, 1, 1))
+    tu = np.concatenate([u[:, k:], u[:, :k]], axis=1)
+    tree = oracle.verify_tree_sampled(target, toks, paths, tu, T, lib=lib)
+    if not (np.array_equal(tree["tokens"], chain["tokens"]) and
+            np.array_equal(tree["num_accepted"], chain["num_accepted"])):
+        errs.append("a one-chain tree differs from the chain verify with one-hot draft rows")
+    # one-hot target rows: the stochastic walk is the greedy tree verify
+    for trial in range(30):
+        N, V, L = int(rng.integers(2, 12)), int(rng.integers(12, 20)), int(rng.integers(2, 5))
+        parent, tokens, paths = _random_small_tree(rng, N, V, L)
+        g = rng.integers(0, V, N)
+        for n in range(1, N):
+            if rng.random() < 0.6:
+                g[parent[n]] = tokens[n]
+        target = np.full((N, V), -np.inf, np.float32)
+        target[np.arange(N), g] = 1.0
+        u = rng.random((1, N)).astype(np.float32)
+        a = oracle.verify_tree_sampled(target[None], tokens[None], paths[None], u, 1.0, lib=lib)
+        gr = oracle.verify_tree(target[None], tokens[None], paths[None], lib=lib)
+        if not (np.array_equal(a["tokens"], gr["tokens"]) and
+                np.array_equal(a["accepted_nodes"], gr["accepted_nodes"])):
+            errs.append(f"one-hot rows: stochastic walk {a['tokens']} differs from greedy {gr['tokens']}")
+            break
+    # near-tie windows: root with children 1, 2 (tokens 0, 1) over V = 3,
+    # target row 0 = [a, b, 0] at T = 1; child 2's test divides by 1 - p(0)
+    a_, b_ = np.float32(0.4), np.float32(-0.3)
+    z = np.array([a_, b_, 0.0], np.float64)
+    p0 = np.exp(z) / np.exp(z).sum()
+    target = np.zeros((1, 3, 3), np.float32)
+    target[0, 0] = [a_, b_, 0.0]
+    toks = np.array([[2, 0, 1]], np.int32)
+    paths = np.array([[[0, 1], [0, 2]]], np.int32)
+    for d, want_n, want_flag in [(5e-6, 0, True), (-5e-6, 1, True), (2e-5, 0, False), (-2e-5, 1, False)]:
+        u = np.array([[0.5, p0[0] + d, 0.99]], np.float32)
+        r = oracle.verify_tree_sampled(target, toks, paths, u, 1.0, lib=lib)
+        if r["num_accepted"][0] != want_n or bool(r["flags"][0, 1]) != want_flag:
+            errs.append(f"tree accept window at p {d:+g}: n={r['num_accepted'][0]} flag={r['flags'][0, 1]}")
+    r2 = p0[1] / (1 - p0[0])
+    win = 1e-5 / (1 - p0[0])
+    # (0.8 of the scaled window is beyond the unscaled 1e-5: p(0) is about 0.46)
+    for d, want_tok, want_flag in [(0.8 * win, 2, True), (-0.8 * win, 1, True), (2 * win, 2, False),
+                                   (-2 * win, 1, False)]:
+        u = np.array([[0.5, 0.999, r2 + d]], np.float32)
+        r = oracle.verify_tree_sampled(target, toks, paths, u, 1.0, lib=lib)
+        got_n = r["num_accepted"][0]
+        if (got_n == 1) != (want_tok == 1) or bool(r["flags"][0, 2]) != want_flag:
+            errs.append(f"second child's window at {d:+g}: n={got_n} flag={r['flags'][0, 2]}")
+    # fail closed
+    target = rng.standard_normal((2, 3, 5)).astype(np.float32)
+    toks = np.array([[0, 1, 5], [0, 1, 2]], np.int32)
+    paths = np.array([[[0, 1, 2]], [[0, 3, -1]]], np.int32)
+    r = oracle.verify_tree_sampled(target, toks, paths, np.full((2, 3), 0.5, np.float32), 1.0, lib=lib)
+    if r["rc"] != oracle.EBADINDEX or list(r["num_accepted"]) != [-1, -1] or np.any(r["tokens"] != -1):
+        errs.append("bad tree tokens or node ids must fail closed")
+    # no used path: one draw from the root row at u[0], best path -1
+    paths = np.full((1, 2, 3), -1, np.int32)
+    u = np.array([[0.37, 0.1, 0.2]], np.float32)
+    r = oracle.verify_tree_sampled(target[:1], np.array([[0, 1, 2]], np.int32), paths, u, 1.0, lib=lib)
+    want, _ = oracle.inverse_cdf(_softmax_T(target[0, 0], 1.0), 0.37)
+    if r["num_accepted"][0] != 0 or r["tokens"][0, 0] != want or r["best_path"][0] != -1:
+        errs.append("a tree without used paths must draw once from the root row")
+    return errs
+
+
 ALL_PINS = {
     "softmax": pin_softmax,
     "inverse_cdf": pin_inverse_cdf,
@@ -710,4 +900,5 @@ ALL_PINS = {
     "philox": pin_philox,
     "rollback_paged": pin_rollback_paged,
     "ragged": pin_ragged,
+    "tree_sampled": pin_tree_sampled,
 }

@@ -66,6 +66,18 @@ MUTANTS = {
                                        "if (n < 0 || n > k) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = 0;"),
     "paged_bad_entry_rewind_zero": ("if (kb < 0 || kb > k || n < 0 || n > kb) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = -1;",
                                     "if (kb < 0 || kb > k || n < 0 || n > kb) {\n            new_lens[b] = old_lens[b];\n            if (rewind_lens)\n                rewind_lens[b] = 0;"),
+    # stochastic tree verify (children as point-mass proposals)
+    "tree_sampled_not_renormalised": ("const double ratio = (1.0 - removed) > 0.0 ? pc / (1.0 - removed) : 0.0;",
+                                      "const double ratio = pc;"),
+    "tree_sampled_rejected_kept": ("p[tok[c]] = 0.0; /* the residual no longer holds tok c */", ";"),
+    "tree_sampled_children_descending": ("for (int j2 = i; j2 > 0 && cand[j2 - 1] > cand[j2]; --j2) {",
+                                         "for (int j2 = i; j2 > 0 && cand[j2 - 1] < cand[j2]; --j2) {"),
+    "tree_sampled_final_uniform_of_node": ("final_tok = oracle_inverse_cdf(w, V, (double)u[0], SAMPLE_TIE, &tie);",
+                                           "final_tok = oracle_inverse_cdf(w, V, (double)u[node], SAMPLE_TIE, &tie);"),
+    "tree_sampled_tests_root_row": ("oracle_softmax(tb + (size_t)node * V * es, dtype, T, V, p);\n            /* candidates",
+                                    "oracle_softmax(tb, dtype, T, V, p);\n            /* candidates"),
+    "tree_sampled_window_unscaled": ("fabs((double)u[c] - ratio) < ACCEPT_TIE / (1.0 - removed))",
+                                     "fabs((double)u[c] - ratio) < ACCEPT_TIE)"),
     # near-tie windows (|r - p/q| < 1e-5; u*Z within 1e-6*Z of a CDF boundary)
     "accept_window_wide": ("static const double ACCEPT_TIE = 1e-5;",
                            "static const double ACCEPT_TIE = 1.0;"),

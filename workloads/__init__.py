@@ -142,13 +142,16 @@ def _tree_shape(rng, N: int, depth: int, top_k: int, level_sizes):
 
 def make_tree(*, B: int, N: int, L: int, V: int, dtype: str, seed: int, target_std: float,
               top_k: int = 8, level_sizes=None, child_noise_std: float = 1.0,
-              seq_len_range=(256, 4096), name: str = "tree") -> dict:
+              seq_len_range=(256, 4096), temperature: float = 0.5, name: str = "tree") -> dict:
     """EAGLE-style tree workload: target [B,N,V], tree_tokens [B,N], paths [B,N,L].
 
     Node 0 is the root (the last committed token); target row n is the
     distribution after node n.  The tokens of node n's c children are the top-c
     ids of target[b,n] + N(0, child_noise_std^2), so siblings are distinct.
     ``paths`` has one root-to-leaf row per leaf, -1 padded, then all-(-1) rows.
+    For the stochastic tree verify, uniforms [B,N] U[0,1) (column n >= 1:
+    node n's accept test, column 0: the final draw) are drawn last, and
+    ``temperature`` is the softmax temperature of the target rows.
     """
     depth = L - 1
     if level_sizes is None:
@@ -190,9 +193,10 @@ def make_tree(*, B: int, N: int, L: int, V: int, dtype: str, seed: int, target_s
             paths[b, pi, : len(chain)] = chain
     lo, hi = seq_len_range
     seq_lens = rng.integers(lo, hi + 1, size=B, dtype=np.int64).astype(np.int32)
+    uniforms = rng.random((B, N), dtype=np.float32)
     return dict(kind="tree", name=name, dtype=dtype, B=B, N=N, P=N, L=L, V=V,
                 target=target, tree_tokens=tree_tokens, paths=paths, parents=parents,
-                seq_lens=seq_lens)
+                seq_lens=seq_lens, uniforms=uniforms, temperature=float(temperature))
 
 
 # Named workloads (shapes and distributions of the pages' configurations).
@@ -210,10 +214,10 @@ CONFIGS = {
     "chain_b64_k7_v128256_bf16": dict(
         kind="chain", B=64, k=7, V=128256, dtype=BF16, temperature=0.7,
         target_std=2.5, draft_noise_std=0.7, zipf_max=6.0, zipf_s=1.1),
-    # tree greedy, B=16 N=60 L=4 V=151936 bf16, topK=8, depth 3
+    # tree greedy (and stochastic at T=0.25), B=16 N=60 L=4 V=151936 bf16, topK=8, depth 3
     "tree_b16_n60_l4_v151936_bf16": dict(
         kind="tree", B=16, N=60, L=4, V=151936, dtype=BF16, target_std=2.0,
-        top_k=8, level_sizes=[8, 25, 26]),
+        top_k=8, level_sizes=[8, 25, 26], temperature=0.25),
     # MTP-style chain stochastic, B=256 k=3 V=129280 bf16, 3 peaks +7.0, T=1.0
     "chain_b256_k3_v129280_bf16": dict(
         kind="chain", B=256, k=3, V=129280, dtype=BF16, temperature=1.0,
