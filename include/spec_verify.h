@@ -279,6 +279,36 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *tree_t
                      int32_t *out_accepted_nodes, int32_t *seq_lens,
                      void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
+/* Stochastic tree verify (TensorRT-LLM deployment page, "目标模型验证：树注意力
+ * 与批量并行": the tree's tokens are judged against the target logits by
+ * rejection sampling; children are chosen by top-K per level, "Eagle-2
+ * 多层级树状草稿生成").  A chosen child is a point-mass proposal on its token,
+ * so the rejection-sampling rule becomes: at each node, try its children in
+ * increasing node id; accept child c iff uniforms[b, c] < p'(token of c), the
+ * current residual of the node's softmax(row / T); on a rejection remove that
+ * token from the residual and renormalise; when no child is accepted (or the
+ * node has none, or L - 1 steps were taken) draw the final token from the
+ * residual by inverse CDF at uniforms[b, 0] (from the node's own row if the
+ * residual's mass vanished).  The emitted tokens follow the target rows.
+ *   target_logits [B, N, V], tree_tokens [B, N], paths [B, P, L]: as for
+ *                 spec_verify_tree; a node's children are the entries d + 1
+ *                 of the used paths whose first d + 1 entries are the
+ *                 accepted prefix.  P * L <= 4096.
+ *   uniforms      [B, N] float32 in [0, 1): column n >= 1 is node n's accept
+ *                 test, column 0 drives the final draw.
+ *   temperature   > 0 and finite.
+ *   Outputs as for spec_verify_tree: tokens [B, L] (accepted tokens, the
+ *   final token, -1 pad), num_accepted [B], best_path [B] (the lowest used
+ *   path holding the accepted nodes, -1 when none), accepted_nodes [B, L];
+ *   seq_lens advanced by n + 1.  Workspace: spec_workspace_size(B, N, V). */
+int spec_verify_tree_sampled(const void *target_logits, int dtype, const int32_t *tree_tokens,
+                             const int32_t *paths, const float *uniforms, float temperature,
+                             int B, int N, int P, int L, int V,
+                             int32_t *out_tokens, int32_t *out_num_accepted,
+                             int32_t *out_best_path, int32_t *out_accepted_nodes,
+                             int32_t *seq_lens, void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
+
 /* KV cursor rollback as length arithmetic only (no KV row is copied or
  * cleared; rows past the new length become invisible and are overwritten
  * later).

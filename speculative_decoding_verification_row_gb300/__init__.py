@@ -41,7 +41,8 @@ SYMBOLS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_chain",
            "spec_last_error", "spec_status_string", "spec_verify_chain_noalloc",
            "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
            "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged",
-           "spec_workspace_size_filtered", "spec_test_timeout_chain", "spec_test_timeout_greedy")
+           "spec_workspace_size_filtered", "spec_test_timeout_chain", "spec_test_timeout_greedy",
+           "spec_verify_tree_sampled")
 SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 class ChainParams(ctypes.Structure):
@@ -86,6 +87,8 @@ def _bind(lib):
     lib.spec_verify_chain.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P, S, P]
     lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
     lib.spec_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P, P, P, S, P]
+    lib.spec_verify_tree_sampled.argtypes = [P, I, P, P, P, ctypes.c_float, I, I, I, I, I, P, P, P, P, P,
+                                             P, S, P]
     lib.spec_rollback_lengths.argtypes = [P, P, I, I, P, P, P]
     lib.spec_verify_chain_noalloc.argtypes = [P, P, I, P, P, ctypes.c_float, I, I, I, P, P, P, P, P]
     lib.spec_last_error.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int)]
@@ -103,7 +106,7 @@ def _bind(lib):
               "spec_rollback_lengths", "spec_last_error", "spec_verify_chain_noalloc",
               "spec_relocate_accepted_kv", "spec_verify_chain_philox", "spec_philox_uniforms",
               "spec_verify_chain_ex", "spec_verify_greedy_ex", "spec_rollback_paged",
-              "spec_test_timeout_chain", "spec_test_timeout_greedy"):
+              "spec_test_timeout_chain", "spec_test_timeout_greedy", "spec_verify_tree_sampled"):
         getattr(lib, f).restype = I
     return lib
 
@@ -374,6 +377,44 @@ def verify_tree(target_logits, tree_tokens, paths, *, out_tokens=None, out_num_a
                                     buf.numel(), sh)
     if rc != SPEC_OK:
         raise SpecError("spec_verify_tree", rc)
+    return tok, n, best, nodes
+
+
+def verify_tree_sampled(target_logits, tree_tokens, paths, uniforms, temperature: float, *,
+                        out_tokens=None, out_num_accepted=None, out_best_path=None,
+                        out_accepted_nodes=None, seq_lens=None, workspace: Workspace | None = None,
+                        stream=None):
+    """Stochastic tree verify (chosen children as point-mass proposals);
+    uniforms float32 [B, N] (column n >= 1: node n's accept test, column 0:
+    the final draw).  Returns (tokens [B,L], num_accepted [B], best_path [B],
+    accepted_nodes [B,L])."""
+    t = _dev(target_logits, "target_logits")
+    if t.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = t.shape
+    code = _logit_code(t, "target_logits")
+    tt = _dev(tree_tokens, "tree_tokens", torch.int32, (B, N))
+    p = _dev(paths, "paths", torch.int32)
+    if p.dim() != 3 or p.shape[0] != B:
+        raise ValueError("paths must be [B, P, L]")
+    P, L = p.shape[1], p.shape[2]
+    u = _dev(uniforms, "uniforms", torch.float32, (B, N))
+    dev = t.device
+    tok = _out(out_tokens, "out_tokens", (B, L), torch.int32, dev)
+    n = _out(out_num_accepted, "out_num_accepted", (B,), torch.int32, dev)
+    best = _out(out_best_path, "out_best_path", (B,), torch.int32, dev)
+    nodes = _out(out_accepted_nodes, "out_accepted_nodes", (B, L), torch.int32, dev)
+    if seq_lens is not None:
+        _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    sh, _ = _stream_handle(stream, dev)
+    ws = workspace or default_workspace(dev, sh)
+    buf = ws.ensure(B, N, V, sh)
+    with _on(dev):
+        rc = lib().spec_verify_tree_sampled(_ptr(t), code, _ptr(tt), _ptr(p), _ptr(u), float(temperature),
+                                            B, N, P, L, V, _ptr(tok), _ptr(n), _ptr(best), _ptr(nodes),
+                                            _ptr(seq_lens), _ptr(buf), buf.numel(), sh)
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_tree_sampled", rc)
     return tok, n, best, nodes
 
 

@@ -150,6 +150,7 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
   a.B = B;
   a.k = k;
   a.V = V;
+  a.rows = R;
   a.out_tokens = out_tokens;
   a.out_n = out_num_accepted;
   a.out_probs = out_probs;
@@ -381,6 +382,48 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* tree_t
   a.ws = ws_views(workspace, WsLayout(B, N, V));
   return launch_argmax(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
                                                                            : SPEC_ECUDA;
+}
+
+int spec_verify_tree_sampled(const void* target_logits, int dtype, const int32_t* tree_tokens,
+                             const int32_t* paths, const float* uniforms, float temperature, int B,
+                             int N, int P, int L, int V, int32_t* out_tokens,
+                             int32_t* out_num_accepted, int32_t* out_best_path,
+                             int32_t* out_accepted_nodes, int32_t* seq_lens, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream) {
+  if (!target_logits || !tree_tokens || !paths || !uniforms || !out_tokens || !out_num_accepted)
+    return SPEC_EINVAL;
+  if ((dtype != SPEC_F32 && dtype != SPEC_BF16) || B < 1 || B > SPEC_MAX_BATCH || N < 1 ||
+      N > SPEC_MAX_TREE_NODES || P < 1 || L < 2 || L > SPEC_MAX_PATH_LEN || V < 2 ||
+      (long)P * L > kTreeStage)
+    return SPEC_EINVAL;
+  ChainArgs a{};
+  if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
+  if (const int rc = check_ws(workspace, workspace_bytes, B, N, V)) return rc;
+  const bool vec = aligned16(target_logits) && ((size_t)V * esize(dtype)) % 16 == 0;
+  row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
+  a.nchunks = num_chunks(V);
+  a.cpc = kChunksPerCta;
+  a.nsplit2 = num_items(V);
+  if ((long)B * ((long)N * a.nsplit + a.nsplit2) > INT_MAX) return SPEC_EINVAL;  // grid sizes
+  a.target = static_cast<const char*>(target_logits);
+  a.uniforms = uniforms;
+  a.B = B;
+  a.k = N - 1;  // pass 1 reads target rows 0..N-1
+  a.V = V;
+  a.rows = N;
+  a.tree_tokens = tree_tokens;
+  a.paths = paths;
+  a.P = P;
+  a.L = L;
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.out_best = out_best_path;
+  a.out_nodes = out_accepted_nodes;
+  a.seq_lens = seq_lens;
+  a.wait_cycles = kWaitCycles;
+  a.ws = ws_views(workspace, WsLayout(B, N, V));
+  return launch_tree_sampled(a, dtype, vec, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK
+                                                                                 : SPEC_ECUDA;
 }
 
 int spec_rollback_lengths(const int32_t* old_lens, const int32_t* num_accepted, int k, int B,

@@ -15,6 +15,7 @@ struct ChainArgs {
   const int32_t* draft_lens;                  // [B] real draft lengths (ragged), or null: k
   float c_hi, c_lo;  // log2(e)/T split as hi + lo
   int B, k, V;
+  int rows;                    // logit rows per request in pass 1 (chain: 2k + 1; tree: N)
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
   int nchunks, cpc, nsplit2;   // draw: chunks per row, per item, items per request
   int top_k;                   // filtered verify: tokens kept per row (0: no filtering)
@@ -24,6 +25,13 @@ struct ChainArgs {
   float* out_probs;
   int32_t* seq_lens;
   long long wait_cycles;       // bound of every wait of the second phase (kWaitCycles)
+  // stochastic tree verify: rows = N target rows per request (k = N - 1),
+  // uniforms [B, N]
+  const int32_t* tree_tokens;  // [B, N]
+  const int32_t* paths;        // [B, P, L]
+  int P, L;
+  int32_t* out_best;           // [B] or null
+  int32_t* out_nodes;          // [B, L] or null
   Ws ws;
 };
 
@@ -71,6 +79,11 @@ cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_
                             bool skip_pass1 = false);
 cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st,
                           bool skip_pass1 = false);
+cudaError_t launch_tree_sampled(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
+
+// Largest P * L of a stochastic tree verify (its paths and edge logits are
+// staged in shared memory).
+constexpr int kTreeStage = 4096;
 
 // Host side of a chain verify (api.cu): argument checks that fill the
 // launch arguments without writing anything, then the launch.
