@@ -55,8 +55,10 @@ def _bind(lib):
     lib.oracle_verify_greedy.argtypes = [P, I, P, P, I, I, I, P, P]
     lib.oracle_rollback_paged.argtypes = [P, P, P, I, P, I, I, P, P, P]
     lib.oracle_filtered_softmax.argtypes = [P, I, ctypes.c_double, I, I, ctypes.c_double, P, P]
+    lib.oracle_filter_row.argtypes = [P, I, ctypes.c_double, I, I, ctypes.c_double, ctypes.c_double,
+                                      P, P]
     lib.oracle_verify_chain_filtered.argtypes = [P, P, I, P, P, ctypes.c_float, I, ctypes.c_double,
-                                                 I, I, I, P, P, P, P]
+                                                 ctypes.c_double, I, I, I, P, P, P, P]
     lib.oracle_verify_tree.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.oracle_rollback.argtypes = [P, P, I, I, P, P]
     lib.oracle_verify_tree_sampled.argtypes = [P, I, P, P, P, ctypes.c_float, I, I, I, I, I,
@@ -67,7 +69,7 @@ def _bind(lib):
     for f in ("oracle_softmax", "oracle_inverse_cdf", "oracle_argmax", "oracle_verify_chain",
               "oracle_verify_greedy", "oracle_verify_tree", "oracle_rollback",
               "oracle_philox_uniforms", "oracle_rollback_paged", "oracle_filtered_softmax",
-              "oracle_verify_chain_filtered", "oracle_verify_tree_sampled"):
+              "oracle_verify_chain_filtered", "oracle_verify_tree_sampled", "oracle_filter_row"):
         getattr(lib, f).restype = I
     return lib
 
@@ -157,24 +159,25 @@ def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, dtyp
 
 
 def filtered_softmax(x, temperature: float, top_k: int, top_p: float = 1.0, dtype: str = "f32",
-                     lib=None):
+                     lib=None, min_p: float = 0.0):
     """(p, near_tie): softmax(x / T) restricted to the top_k tokens by (logit
-    descending, index ascending), then to the shortest prefix reaching top_p
-    (TensorRT-LLM walkthrough, rejection-sampling section)."""
+    descending, index ascending; top_k = 0: all), then to the shortest prefix
+    reaching top_p, then to the tokens whose probability is at least min_p
+    times the largest (TensorRT-LLM walkthrough, rejection-sampling section)."""
     lib = lib or load()
     x = _logits(x, dtype)
     p = np.empty(x.shape[-1], dtype=np.float64)
     tie = np.zeros(1, dtype=np.int32)
-    rc = lib.oracle_filtered_softmax(_ptr(x), DTYPE_CODE[dtype], float(np.float32(temperature)),
-                                     x.shape[-1], int(top_k), float(top_p), _ptr(p), _ptr(tie))
+    rc = lib.oracle_filter_row(_ptr(x), DTYPE_CODE[dtype], float(np.float32(temperature)),
+                               x.shape[-1], int(top_k), float(top_p), float(min_p), _ptr(p), _ptr(tie))
     if rc != OK:
         raise ValueError(f"oracle_filtered_softmax rc={rc}")
     return p, bool(tie[0])
 
 
 def verify_chain_filtered(target, draft, draft_tokens, uniforms, temperature: float, top_k: int,
-                          top_p: float = 1.0, dtype: str = "f32", lib=None) -> dict:
-    """verify_chain on top-k / top-p filtered target and draft rows."""
+                          top_p: float = 1.0, dtype: str = "f32", lib=None, min_p: float = 0.0) -> dict:
+    """verify_chain on top-k / top-p / min_p filtered target and draft rows."""
     lib = lib or load()
     target = _logits(target, dtype)
     draft = _logits(draft, dtype)
@@ -187,7 +190,7 @@ def verify_chain_filtered(target, draft, draft_tokens, uniforms, temperature: fl
     probs = np.empty((B, k, 2), dtype=np.float64)
     flags = np.empty((B, k + 1), dtype=np.int32)
     rc = lib.oracle_verify_chain_filtered(_ptr(target), _ptr(draft), DTYPE_CODE[dtype], _ptr(x), _ptr(r),
-                                          float(temperature), int(top_k), float(top_p), B, k, V,
+                                          float(temperature), int(top_k), float(top_p), float(min_p), B, k, V,
                                           _ptr(tokens), _ptr(n_acc), _ptr(probs), _ptr(flags))
     if rc not in (OK, EBADINDEX):
         raise ValueError(f"oracle_verify_chain_filtered rc={rc}")

@@ -540,13 +540,19 @@ int oracle_rollback_paged(const int32_t *old_lens, const int32_t *num_accepted,
 }
 
 /* One row's filtered distribution (TensorRT-LLM walkthrough, rejection-
- * sampling section: target and draft are filtered alike).  This library's
- * reading: the kept set is the top_k tokens ordered by (logit descending,
- * index ascending); when top_p < 1, only the shortest prefix of that order
- * whose probability under softmax(z) restricted to the top_k reaches top_p is
- * kept.  p[t] = exp(z_t - z_max) / sum over the kept set, 0 elsewhere.
- * *near_tie is set when the top-p cut lies within 1e-6 of top_p.
- * top_k <= 0 means no filtering (plain softmax). */
+ * sampling section: target and draft are filtered alike by temperature,
+ * top-k, top-p and min_p, named in that order).  This library's reading,
+ * applied in that order to z = x / T:
+ *   top-k  the top_k tokens ordered by (logit descending, index ascending);
+ *          top_k <= 0: every token, in that order;
+ *   top-p  when top_p < 1, only the shortest prefix of that order whose
+ *          probability under softmax(z) over the current set reaches top_p;
+ *   min_p  when min_p > 0, only the tokens of the current set whose
+ *          probability is at least min_p times the largest, that is
+ *          exp(z_t - z_max) >= min_p (the normaliser cancels);
+ * p[t] = exp(z_t - z_max) / sum over the kept set, 0 elsewhere.
+ * *near_tie is set when the top-p cut lies within 1e-6 of top_p, or a kept
+ * set token's exp(z_t - z_max) lies within 1e-6 * min_p of min_p. */
 typedef struct {
     double x;
     int t;
@@ -562,14 +568,13 @@ static int orc_item_order(const void *a, const void *b)
     return u->t < v->t ? -1 : (u->t > v->t);
 }
 
-int oracle_filtered_softmax(const void *x, int dtype, double temperature, int V, int top_k,
-                            double top_p, double *p, int32_t *near_tie)
+int oracle_filter_row(const void *x, int dtype, double temperature, int V, int top_k,
+                      double top_p, double min_p, double *p, int32_t *near_tie)
 {
     if (near_tie)
         *near_tie = 0;
-    if (top_k <= 0)
-        return oracle_softmax(x, dtype, temperature, V, p);
-    if (!x || !p || V < 1 || !(temperature > 0.0) || !(top_p > 0.0) || top_p > 1.0)
+    if (!x || !p || V < 1 || !(temperature > 0.0) || !(top_p > 0.0) || top_p > 1.0 ||
+        !(min_p >= 0.0) || min_p > 1.0)
         return ORC_EINVAL;
     orc_item *it = malloc(sizeof(orc_item) * (size_t)V);
     if (!it)
@@ -579,7 +584,7 @@ int oracle_filtered_softmax(const void *x, int dtype, double temperature, int V,
         it[t].t = t;
     }
     qsort(it, (size_t)V, sizeof(orc_item), orc_item_order);
-    const int kk = top_k < V ? top_k : V;
+    const int kk = top_k > 0 && top_k < V ? top_k : V;
     const double zmax = it[0].x / temperature;
     double sk = 0.0;
     for (int i = 0; i < kk; ++i)
@@ -593,11 +598,22 @@ int oracle_filtered_softmax(const void *x, int dtype, double temperature, int V,
             cum += pi;
             if (cum >= top_p) {
                 m = i + 1;
-                if (near_tie)
-                    *near_tie = fabs(cum - top_p) < 1e-6 || fabs(before - top_p) < 1e-6;
+                if (near_tie && (fabs(cum - top_p) < 1e-6 || fabs(before - top_p) < 1e-6))
+                    *near_tie = 1;
                 break;
             }
         }
+    }
+    if (min_p > 0.0) {
+        int m2 = 0;
+        for (int i = 0; i < m; ++i) {
+            const double ratio = exp(it[i].x / temperature - zmax);
+            if (near_tie && fabs(ratio - min_p) <= 1e-6 * min_p)
+                *near_tie = 1;
+            if (ratio >= min_p)
+                m2 = i + 1;
+        }
+        m = m2;
     }
     for (int t = 0; t < V; ++t)
         p[t] = 0.0;
@@ -610,19 +626,28 @@ int oracle_filtered_softmax(const void *x, int dtype, double temperature, int V,
     return ORC_OK;
 }
 
+/* top-k and top-p alone (min_p = 0); top_k <= 0 with top_p = 1 is the plain
+ * softmax. */
+int oracle_filtered_softmax(const void *x, int dtype, double temperature, int V, int top_k,
+                            double top_p, double *p, int32_t *near_tie)
+{
+    return oracle_filter_row(x, dtype, temperature, V, top_k, top_p, 0.0, p, near_tie);
+}
+
 /* Chain verify on filtered distributions: oracle_verify_chain with every
- * target and draft row passed through oracle_filtered_softmax(top_k, top_p)
+ * target and draft row passed through oracle_filter_row(top_k, top_p, min_p)
  * before the accept tests and the final sample.  A near tie of a top-p cut in
  * a row that decides position i (its target or draft row) flags column i; one
  * in the rows of the final sample flags column k. */
 int oracle_verify_chain_filtered(const void *target, const void *draft, int dtype,
                                  const int32_t *draft_tokens, const float *uniforms,
-                                 float temperature, int top_k, double top_p, int B, int k, int V,
+                                 float temperature, int top_k, double top_p, double min_p, int B,
+                                 int k, int V,
                                  int32_t *out_tokens, int32_t *out_num_accepted,
                                  double *out_probs, int32_t *out_flags)
 {
     if (!target || !draft || !draft_tokens || !uniforms || !out_tokens || !out_num_accepted ||
-        B < 1 || k < 1 || V < 2 || top_k < 1 || !(temperature > 0.0f) || !isfinite(temperature) ||
+        B < 1 || k < 1 || V < 2 || top_k < 0 || !(temperature > 0.0f) || !isfinite(temperature) ||
         (dtype != ORC_F32 && dtype != ORC_BF16))
         return ORC_EINVAL;
     const double T = (double)temperature;
@@ -661,8 +686,8 @@ int oracle_verify_chain_filtered(const void *target, const void *draft, int dtyp
         }
         for (int i = 0; i < k; ++i) {
             int32_t tp = 0, tq = 0;
-            oracle_filtered_softmax(tb + (size_t)i * V * es, dtype, T, V, top_k, top_p, p, &tp);
-            oracle_filtered_softmax(db + (size_t)i * V * es, dtype, T, V, top_k, top_p, q, &tq);
+            oracle_filter_row(tb + (size_t)i * V * es, dtype, T, V, top_k, top_p, min_p, p, &tp);
+            oracle_filter_row(db + (size_t)i * V * es, dtype, T, V, top_k, top_p, min_p, q, &tq);
             const double pi = p[x[i]], qi = q[x[i]];
             if (out_probs) {
                 out_probs[((size_t)b * k + i) * 2 + 0] = pi;
@@ -681,9 +706,9 @@ int oracle_verify_chain_filtered(const void *target, const void *draft, int dtyp
             }
         }
         int32_t tp = 0, tq = 0;
-        oracle_filtered_softmax(tb + (size_t)j * V * es, dtype, T, V, top_k, top_p, p, &tp);
+        oracle_filter_row(tb + (size_t)j * V * es, dtype, T, V, top_k, top_p, min_p, p, &tp);
         if (j < k) {
-            oracle_filtered_softmax(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, q, &tq);
+            oracle_filter_row(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, min_p, q, &tq);
             for (int t = 0; t < V; ++t)
                 w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0;
         } else {

@@ -206,7 +206,27 @@ def _topk_softmax_T(x, T, top_k):
     return p
 
 
-def enumerate_chain(target, draft, T, lib=None, top_k=None):
+def _filter_np(x, T, top_k=0, top_p=1.0, min_p=0.0):
+    """Reading F5/F6 written with numpy's sort and cumulative sums: the top_k
+    tokens by (logit descending, index ascending; 0 = all), then the shortest
+    prefix whose mass over that set reaches top_p, then the tokens with
+    exp(z - z_max) >= min_p; softmax of x / T over what is left."""
+    x = np.asarray(x, dtype=np.float64)
+    z = x / np.float64(np.float32(T))
+    order = np.lexsort((np.arange(x.size), -x))
+    keep = order[: x.size if top_k <= 0 else min(top_k, x.size)]
+    e = np.exp(z[keep] - z[order[0]])
+    if top_p < 1.0:
+        m = int(np.searchsorted(np.cumsum(e / e.sum()), top_p, side="left")) + 1
+        keep, e = keep[:m], e[:m]
+    if min_p > 0.0:
+        keep, e = keep[e >= min_p], e[e >= min_p]
+    p = np.zeros(x.size)
+    p[keep] = e / e.sum()
+    return p
+
+
+def enumerate_chain(target, draft, T, lib=None, top_k=None, filt=None):
     """Drive the oracle through every branch of the chain verify for one small problem.
 
     For every draft tuple x in [V]^k (weight prod q_i(x_i)), every stopping
@@ -219,7 +239,10 @@ def enumerate_chain(target, draft, T, lib=None, top_k=None):
     """
     k1, V = target.shape
     k = k1 - 1
-    if top_k is None:
+    if filt is not None:
+        p = [_filter_np(target[i], T, *filt) for i in range(k + 1)]
+        q = [_filter_np(draft[i], T, *filt) for i in range(k)]
+    elif top_k is None:
         p = [_softmax_T(target[i], T) for i in range(k + 1)]
         q = [_softmax_T(draft[i], T) for i in range(k)]
     else:
@@ -263,7 +286,9 @@ def enumerate_chain(target, draft, T, lib=None, top_k=None):
     drf = np.broadcast_to(draft, (Bn, k, V)).astype(np.float32)
     xs = np.array(reqs_x, np.int32).reshape(Bn, k)
     rs = np.array(reqs_r, np.float32)
-    if top_k is None:
+    if filt is not None:
+        res = oracle.verify_chain_filtered(tgt, drf, xs, rs, T, filt[0], filt[1], lib=lib, min_p=filt[2])
+    elif top_k is None:
         res = oracle.verify_chain(tgt, drf, xs, rs, T, lib=lib)
     else:
         res = oracle.verify_chain_filtered(tgt, drf, xs, rs, T, top_k, lib=lib)
@@ -886,6 +911,91 @@ def pin_tree_sampled(lib=None) -> list[str]:
     return errs
 
 
+def pin_filter_min_p_and_wide_top_p(lib=None) -> list[str]:
+    """min_p and top-p over the whole vocabulary (reading F6: temperature, then
+    top-k, top-p and min_p in the walkthrough's order; top_k = 0 keeps every
+    token).  Closed-form hand examples, a min_p tie kept and flagged, 300
+    random rows against numpy's sort and cumulative sums, and the equivalence
+    theorem on enumerated branches with both sides filtered by top-p and
+    min_p alone."""
+    errs = []
+    fr = lambda x, T, kk, pp, mp: oracle.filtered_softmax(np.asarray(x, np.float32), T, kk, pp, lib=lib,
+                                                          min_p=mp)
+    x = [3.0, 1.0, 2.0, 2.0, 0.0]
+    e1, e2, e3 = np.exp(-1.0), np.exp(-2.0), np.exp(-3.0)
+    cases = [  # (T, top_k, top_p, min_p, expected p)
+        # min_p = e^-1.5 keeps the logits within 1.5 of the maximum
+        (1.0, 0, 1.0, np.exp(-1.5), np.array([1.0, 0.0, e1, e1, 0.0]) / (1.0 + 2 * e1)),
+        # min_p = 1/2 keeps the maximum alone
+        (1.0, 0, 1.0, 0.5, np.array([1.0, 0.0, 0.0, 0.0, 0.0])),
+        # top-p over the whole vocabulary: p(0) = 1/(1 + e^-2 + 2e^-1 + e^-3) = 0.521 < 0.55,
+        # so token 2 joins (over the top 3 alone 0.576 would reach it)
+        (1.0, 0, 0.55, 0.0, np.array([1.0, 0.0, e1, 0.0, 0.0]) / (1.0 + e1)),
+        # min_p after top-p: top-p 0.9 keeps {0, 2, 3, 1}, min_p e^-1.2 then drops token 1
+        (1.0, 0, 0.9, np.exp(-1.2), np.array([1.0, 0.0, e1, e1, 0.0]) / (1.0 + 2 * e1)),
+        # top-k, then min_p: top_k = 2 keeps {0, 2}; min_p e^-1.5 keeps both
+        (1.0, 2, 1.0, np.exp(-1.5), np.array([1.0, 0.0, e1, 0.0, 0.0]) / (1.0 + e1)),
+        # temperature applies before min_p: at T = 2, exp((2 - 3)/2) = 0.607 >= 0.6
+        (2.0, 0, 1.0, 0.6, np.array([1.0, 0.0, np.exp(-0.5), np.exp(-0.5), 0.0]) / (1.0 + 2 * np.exp(-0.5))),
+    ]
+    for T, kk, pp, mp, want in cases:
+        got, _ = fr(x, T, kk, pp, mp)
+        if np.max(np.abs(got - want)) > 1e-12:
+            errs.append(f"filter T={T} top_k={kk} top_p={pp} min_p={mp:.4f}: {got} want {want}")
+    # a token exactly at min_p is kept, and the row is flagged as a near tie
+    got, tie = fr(x, 1.0, 0, 1.0, e1)
+    if np.max(np.abs(got - np.array([1.0, 0.0, e1, e1, 0.0]) / (1.0 + 2 * e1))) > 1e-12 or not tie:
+        errs.append(f"a token exactly at min_p must be kept and flagged: {got} {tie}")
+    # min_p decides an accept test: target row [0, 0, -0.5, -3] with min_p =
+    # e^-1 keeps tokens 0..2, p(0) = 1 / (2 + e^-0.5) = 0.3861 (unfiltered it
+    # would be 0.3693); the draft row is one-hot at token 0, so r = 0.378
+    # accepts token 0 only under the filtered target row.
+    tgt = np.array([[[0.0, 0.0, -0.5, -3.0], [0.0, -1.0, 0.5, 0.0]]], np.float32)
+    drf = np.array([[[0.0, -np.inf, -np.inf, -np.inf]]], np.float32)
+    res = oracle.verify_chain_filtered(tgt, drf, np.array([[0]], np.int32),
+                                       np.array([[0.378, 0.2]], np.float32), 1.0, 0, 1.0, lib=lib, min_p=e1)
+    if res["num_accepted"][0] != 1 or abs(res["probs"][0, 0, 0] - 1.0 / (2.0 + np.exp(-0.5))) > 1e-12:
+        errs.append(f"min_p accept example: n={res['num_accepted'][0]} p={res['probs'][0, 0, 0]}")
+    # min_p = 1 keeps the tied maxima; no filter at all is scipy's softmax
+    got, _ = fr([5.0, 1.0, 5.0, 2.0], 1.0, 0, 1.0, 1.0)
+    if got.tolist() != [0.5, 0.0, 0.5, 0.0]:
+        errs.append(f"min_p = 1 must keep the tied maxima: {got}")
+    rng = np.random.default_rng(19)
+    row = (rng.standard_normal(50) * 2).astype(np.float32)
+    if np.max(np.abs(fr(row, 0.7, 0, 1.0, 0.0)[0] - _softmax_T(row, 0.7))) > 1e-12:
+        errs.append("no filter is not the plain softmax")
+    for trial in range(300):
+        V = int(rng.integers(2, 60))
+        xr = (rng.integers(-6, 7, size=V) * 0.5).astype(np.float32)
+        T = float(rng.choice([0.5, 1.0, 1.6]))
+        kk = int(rng.choice([0, 0, 1, 3, V + 2]))
+        pp = float(np.float32(rng.choice([0.3, 0.6, 0.9, 1.0])))
+        mp = float(rng.choice([0.0, 0.01, 0.1, 0.5]))
+        got, tie = fr(xr, T, kk, pp, mp)
+        if tie:
+            continue
+        want = _filter_np(xr, T, kk, pp, mp)
+        if np.max(np.abs(got - want)) > 1e-12:
+            errs.append(f"filter row {trial} (top_k={kk}, top_p={pp}, min_p={mp}) differs from numpy")
+            break
+    for (k2, V2, T2, filt) in [(1, 6, 1.0, (0, 0.8, 0.0)), (2, 5, 0.8, (0, 1.0, 0.2)),
+                               (2, 4, 1.2, (0, 0.7, 0.1)), (2, 5, 1.0, (3, 0.9, 0.3))]:
+        tg = (rng.standard_normal((k2 + 1, V2)) * 1.5).astype(np.float32)
+        dr = (tg[:k2] + rng.standard_normal((k2, V2)) * 0.8).astype(np.float32)
+        wts, expect, res, p = enumerate_chain(tg, dr, T2, lib=lib, filt=filt)
+        for e, (j, rowe) in enumerate(expect):
+            if res["num_accepted"][e] != j or list(res["tokens"][e]) != rowe:
+                errs.append(f"filter {filt} k={k2}: branch {e} gave {res['tokens'][e]} want {rowe}")
+                break
+        n_acc, toks = res["num_accepted"], res["tokens"]
+        for i in range(k2 + 1):
+            reach = n_acc >= i
+            dist = np.array([wts[reach & (toks[:, i] == t)].sum() for t in range(V2)]) / wts[reach].sum()
+            if np.max(np.abs(dist - p[i])) > 1e-12:
+                errs.append(f"filter {filt} k={k2}: token {i} is not distributed as filtered p_{i}")
+    return errs
+
+
 ALL_PINS = {
     "softmax": pin_softmax,
     "inverse_cdf": pin_inverse_cdf,
@@ -901,4 +1011,5 @@ ALL_PINS = {
     "rollback_paged": pin_rollback_paged,
     "ragged": pin_ragged,
     "tree_sampled": pin_tree_sampled,
+    "filter_min_p_wide_top_p": pin_filter_min_p_and_wide_top_p,
 }

@@ -42,9 +42,9 @@ MUTANTS = {
                                    "for (int i = 0; i < V; ++i)\n        sk += exp("),
     "kept_set_not_renormalised": ("p[it[i].t] = exp(it[i].x / temperature - zmax) / sm;",
                                   "p[it[i].t] = exp(it[i].x / temperature - zmax) / sk;"),
-    "draft_side_not_filtered": ("oracle_filtered_softmax(db + (size_t)i * V * es, dtype, T, V, top_k, top_p, q, &tq);",
+    "draft_side_not_filtered": ("oracle_filter_row(db + (size_t)i * V * es, dtype, T, V, top_k, top_p, min_p, q, &tq);",
                                 "oracle_softmax(db + (size_t)i * V * es, dtype, T, V, q);"),
-    "residual_draft_not_filtered": ("oracle_filtered_softmax(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, q, &tq);",
+    "residual_draft_not_filtered": ("oracle_filter_row(db + (size_t)j * V * es, dtype, T, V, top_k, top_p, min_p, q, &tq);",
                                     "oracle_softmax(db + (size_t)j * V * es, dtype, T, V, q);"),
     # per-request Philox uniforms (TensorRT-LLM walkthrough, rejection-sampling section)
     "philox_nine_rounds": ("for (int round = 0; round < 10; ++round) {",
@@ -78,6 +78,14 @@ MUTANTS = {
                                     "oracle_softmax(tb, dtype, T, V, p);\n            /* candidates"),
     "tree_sampled_window_unscaled": ("fabs((double)u[c] - ratio) < ACCEPT_TIE / (1.0 - removed))",
                                      "fabs((double)u[c] - ratio) < ACCEPT_TIE)"),
+    # min_p and top-p over the whole vocabulary (reading F6)
+    "min_p_against_mass": ("const double ratio = exp(it[i].x / temperature - zmax);",
+                           "const double ratio = exp(it[i].x / temperature - zmax) / sk;"),
+    "min_p_strict": ("if (ratio >= min_p)", "if (ratio > min_p)"),
+    "no_top_k_means_no_filter": ("    qsort(it, (size_t)V, sizeof(orc_item), orc_item_order);",
+                                 "    if (top_k <= 0) {\n        free(it);\n        return oracle_softmax(x, dtype, temperature, V, p);\n    }\n    qsort(it, (size_t)V, sizeof(orc_item), orc_item_order);"),
+    "min_p_skipped_on_target_rows": ("oracle_filter_row(tb + (size_t)i * V * es, dtype, T, V, top_k, top_p, min_p, p, &tp);",
+                                     "oracle_filter_row(tb + (size_t)i * V * es, dtype, T, V, top_k, top_p, 0.0, p, &tp);"),
     # near-tie windows (|r - p/q| < 1e-5; u*Z within 1e-6*Z of a CDF boundary)
     "accept_window_wide": ("static const double ACCEPT_TIE = 1e-5;",
                            "static const double ACCEPT_TIE = 1.0;"),
