@@ -76,7 +76,9 @@ typedef enum {
     SPEC_EBADINDEX = -2,   /* a token or node id was out of range (device status) */
     SPEC_ECUDA = -3,       /* a CUDA launch or copy failed */
     SPEC_EWORKSPACE = -4,  /* workspace missing or smaller than spec_workspace_size() */
-    SPEC_ETIMEOUT = -5     /* a bounded device wait ran out (device status) */
+    SPEC_ETIMEOUT = -5,    /* a bounded device wait ran out (device status) */
+    SPEC_ELIMIT = -6       /* a top-p / min_p kept set without top-k held more than
+                              SPEC_MAX_TOPK - 1 tokens (device status) */
 } spec_status_t;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
@@ -99,10 +101,11 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 size_t spec_workspace_size(int B, int rows_per_request, int V);
 
 /* Bytes of scratch of a filtered chain verify (spec_chain_params with
- * top_k > 0) of B requests, k drafts, width V: the chain's, plus each row's
- * kept list (top_k words), 2k probabilities per request and two bytes per
- * 2048 logits of each row.  Returns 0 for
- * invalid sizes (top_k outside [1, SPEC_MAX_TOPK] included). */
+ * top_k > 0, or top_k = 0 with top_p < 1 or min_p > 0) of B requests, k
+ * drafts, width V: the chain's, plus each row's kept list (top_k words;
+ * SPEC_MAX_TOPK when top_k = 0), 2k probabilities per request and two bytes
+ * per 2048 logits of each row.  Returns 0 for invalid sizes (top_k outside
+ * [0, SPEC_MAX_TOPK] included). */
 size_t spec_workspace_size_filtered(int B, int k, int V, int top_k);
 
 /* Zero a workspace (asynchronously, on `stream`).  Call once after allocating
@@ -198,12 +201,22 @@ typedef struct spec_chain_params {
      * kept set, and the chain verify above runs on them (the final draw
      * takes u * Z over the kept tokens in token order).  out_probs holds the
      * filtered p and q.  Logits of -inf are never kept (their weight is 0);
-     * logits must not be NaN or +inf.  top_p in (0, 1]; top_p < 1 needs
-     * top_k > 0 (top-p over the whole vocabulary is not supported).  The
-     * workspace must hold spec_workspace_size_filtered(B, k, V, top_k)
-     * bytes. */
+     * logits must not be NaN or +inf.  top_p in (0, 1].  top_k = 0 with
+     * top_p < 1 (or min_p > 0) keeps every token before the top-p cut, whose
+     * mass is then over the whole vocabulary; such a kept set must end
+     * within the SPEC_MAX_TOPK largest logits of the row (at most
+     * SPEC_MAX_TOPK - 1 tokens), else the request fails closed and the
+     * status word reads SPEC_ELIMIT.  The workspace must hold
+     * spec_workspace_size_filtered(B, k, V, top_k) bytes.  Rows wider than
+     * 917504 bf16 or 458752 fp32 logits support top_k > 0 only. */
     int top_k;
     float top_p;
+    /* min_p in [0, 1] (0: off), applied after top-p (the walkthrough names
+     * temperature, top-k, top-p and min_p in that order): a token of the
+     * kept set stays when its probability is at least min_p times the
+     * largest, 2^((x - x_max) log2(e) / T) >= min_p.  A struct ending at
+     * top_p leaves it at 0. */
+    float min_p;
 } spec_chain_params;
 int spec_verify_chain_ex(const spec_chain_params *params, void *workspace,
                          size_t workspace_bytes, spec_stream_t stream);

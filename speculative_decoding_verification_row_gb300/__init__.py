@@ -28,6 +28,7 @@ from .stats import acceptance_stats, anchored_emitted  # noqa: F401  (host bookk
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
 
 SPEC_OK, SPEC_EINVAL, SPEC_EBADINDEX, SPEC_ECUDA, SPEC_EWORKSPACE, SPEC_ETIMEOUT = 0, -1, -2, -3, -4, -5
+SPEC_ELIMIT = -6
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_MAX_DRAFT = 64
 SPEC_MAX_BATCH = 8192
@@ -55,7 +56,7 @@ class ChainParams(ctypes.Structure):
                 ("B", ctypes.c_int), ("k", ctypes.c_int), ("V", ctypes.c_int),
                 ("out_tokens", ctypes.c_void_p), ("out_num_accepted", ctypes.c_void_p),
                 ("out_probs", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
-                ("top_k", ctypes.c_int), ("top_p", ctypes.c_float)]
+                ("top_k", ctypes.c_int), ("top_p", ctypes.c_float), ("min_p", ctypes.c_float)]
 
 
 class GreedyParams(ctypes.Structure):
@@ -216,15 +217,17 @@ def default_workspace(device, stream_handle) -> Workspace:
 def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
                  out_tokens=None, out_num_accepted=None, out_probs=None, want_probs=False,
                  seq_lens=None, workspace: Workspace | None = None, stream=None,
-                 seeds=None, offsets=None, draft_lens=None, top_k: int = 0, top_p: float = 1.0):
+                 seeds=None, offsets=None, draft_lens=None, top_k: int = 0, top_p: float = 1.0,
+                 min_p: float = 0.0):
     """Chain rejection-sampling verify; returns (tokens [B,k+1], num_accepted [B], probs [B,k,2] or None).
 
     seq_lens (int32 [B], optional) is advanced in place by n_acc + 1.  With
     uniforms=None, seeds and offsets (int64 [B]) select each request's Philox
     stream and the uniforms are drawn inside the kernel.  draft_lens (int32
     [B], optional): each request's real draft length (ragged verify).
-    top_k > 0 (with top_p in (0, 1]): verify on the top-k / top-p filtered
-    target and draft distributions (spec_chain_params.top_k / top_p)."""
+    top_k > 0, top_p < 1 or min_p > 0: verify on the top-k / top-p / min_p
+    filtered target and draft distributions (spec_chain_params.top_k /
+    top_p / min_p; top_k = 0 ranks no top-k set)."""
     t = _dev(target_logits, "target_logits")
     if t.dim() != 3:
         raise ValueError("target_logits must be [B, k+1, V]")
@@ -248,8 +251,8 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
         _dev(seq_lens, "seq_lens", torch.int32, (B,))
     sh, _ = _stream_handle(stream, dev)
     ws = workspace or default_workspace(dev, sh)
-    filtered = top_k != 0 or top_p != 1.0
-    need = lib().spec_workspace_size_filtered(B, k, V, int(top_k)) if top_k > 0 else None
+    filtered = top_k != 0 or top_p != 1.0 or min_p != 0.0
+    need = lib().spec_workspace_size_filtered(B, k, V, int(top_k)) if filtered else None
     buf = ws.ensure(B, 2 * k + 1, V, sh, need)
     if draft_lens is not None or filtered:
         lens = None if draft_lens is None else _dev(draft_lens, "draft_lens", torch.int32, (B,))
@@ -258,7 +261,7 @@ def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperatur
                           None if uniforms is not None else _ptr(sd),
                           None if uniforms is not None else _ptr(of), float(temperature), B, k, V,
                           _ptr(tok), _ptr(n), _ptr(probs), _ptr(seq_lens), int(top_k),
-                          float(top_p))
+                          float(top_p), float(min_p))
         with _on(dev):
             rc = lib().spec_verify_chain_ex(ctypes.byref(prm), _ptr(buf), buf.numel(), sh)
         name = "spec_verify_chain_ex"

@@ -93,10 +93,11 @@ size_t spec_workspace_size(int B, int rows_per_request, int V) {
 }
 
 size_t spec_workspace_size_filtered(int B, int k, int V, int top_k) {
-  if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2 || top_k < 1 ||
+  if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2 || top_k < 0 ||
       top_k > SPEC_MAX_TOPK)
     return 0;
-  return FilterLayout(B, k, V, top_k).total;
+  // top_k = 0 (top-p or min_p alone) ranks SPEC_MAX_TOPK candidates per row
+  return FilterLayout(B, k, V, top_k > 0 ? top_k : SPEC_MAX_TOPK).total;
 }
 
 int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream) {
@@ -118,7 +119,7 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
                 const uint64_t* seeds, const uint64_t* offsets, const int32_t* draft_lens,
                 float temperature, int B, int k, int V, int32_t* out_tokens,
                 int32_t* out_num_accepted, float* out_probs, int32_t* seq_lens, void* workspace,
-                size_t workspace_bytes, int top_k, float top_p) {
+                size_t workspace_bytes, int top_k, float top_p, float min_p) {
   if (!target_logits || !draft_logits || !draft_tokens || (!uniforms && (!seeds || !offsets)) ||
       !out_tokens || !out_num_accepted)
     return SPEC_EINVAL;
@@ -129,13 +130,16 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
   if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
   const int R = 2 * k + 1;
   if (top_k < 0 || top_k > SPEC_MAX_TOPK || !(top_p > 0.f) || !(top_p <= 1.f) ||
-      (top_k == 0 && top_p < 1.f))
+      !(min_p >= 0.f) || !(min_p <= 1.f))
     return SPEC_EINVAL;
+  // Without top-k, top-p and min_p rank SPEC_MAX_TOPK candidates per row.
+  const bool wide = top_k == 0 && (top_p < 1.f || min_p > 0.f);
+  const int kcand = wide ? SPEC_MAX_TOPK : top_k;
   if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
   vec = aligned16(target_logits) && aligned16(draft_logits) &&
         ((size_t)V * esize(dtype)) % 16 == 0;
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
-  if (top_k > 0 && workspace_bytes < FilterLayout(B, k, V, top_k).total) return SPEC_EWORKSPACE;
+  if (kcand > 0 && workspace_bytes < FilterLayout(B, k, V, kcand).total) return SPEC_EWORKSPACE;
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
   a.nsplit2 = num_items(V);
@@ -157,10 +161,12 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
   a.seq_lens = seq_lens;
   a.wait_cycles = kWaitCycles;
   a.ws = ws_views(workspace, WsLayout(B, R, V));
-  a.top_k = top_k;
+  a.top_k = kcand;
   a.top_p = top_p;
-  if (top_k > 0) {
-    const FilterLayout fl(B, k, V, top_k);
+  a.min_p = min_p;
+  a.wide = wide;
+  if (kcand > 0) {
+    const FilterLayout fl(B, k, V, kcand);
     a.ws.cand = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + fl.cand);
     a.ws.pq = reinterpret_cast<float*>(static_cast<char*>(workspace) + fl.pq);
     a.ws.codes = reinterpret_cast<unsigned short*>(static_cast<char*>(workspace) + fl.codes);
@@ -185,13 +191,13 @@ int chain_impl(const void* target_logits, const void* draft_logits, int dtype,
                int k, int V, int32_t* out_tokens, int32_t* out_num_accepted, float* out_probs,
                int32_t* seq_lens, void* workspace, size_t workspace_bytes, spec_stream_t stream,
                int top_k = 0, float top_p = 1.f, long long wait_cycles = kWaitCycles,
-               bool skip_pass1 = false) {
+               bool skip_pass1 = false, float min_p = 0.f) {
   ChainArgs a;
   bool vec = false;
   if (const int rc = chain_setup(a, vec, target_logits, draft_logits, dtype, draft_tokens, uniforms,
                                  seeds, offsets, draft_lens, temperature, B, k, V, out_tokens,
                                  out_num_accepted, out_probs, seq_lens, workspace, workspace_bytes,
-                                 top_k, top_p))
+                                 top_k, top_p, min_p))
     return rc;
   a.wait_cycles = wait_cycles;
   return chain_launch(a, dtype, vec, (cudaStream_t)stream, skip_pass1);
@@ -304,15 +310,18 @@ int spec_verify_greedy_ex(const spec_greedy_params* p, void* workspace, size_t w
 
 int spec_verify_chain_ex(const spec_chain_params* p, void* workspace, size_t workspace_bytes,
                          spec_stream_t stream) {
-  // An earlier version of the struct ends at seq_lens (no filtering fields).
+  // Earlier versions of the struct end at seq_lens (no filtering fields) or
+  // at top_p (no min_p).
   const size_t v1 = offsetof(spec_chain_params, seq_lens) + sizeof(p->seq_lens);
   if (!p || p->size < v1) return SPEC_EINVAL;
   const bool has_filter = p->size >= offsetof(spec_chain_params, top_p) + sizeof(p->top_p);
+  const bool has_min_p = p->size >= offsetof(spec_chain_params, min_p) + sizeof(p->min_p);
   return chain_impl(p->target_logits, p->draft_logits, p->dtype, p->draft_tokens, p->uniforms,
                     p->seeds, p->offsets, p->draft_lens, p->temperature, p->B, p->k, p->V,
                     p->out_tokens, p->out_num_accepted, p->out_probs, p->seq_lens, workspace,
                     workspace_bytes, stream, has_filter ? p->top_k : 0,
-                    has_filter ? p->top_p : 1.f);
+                    has_filter ? p->top_p : 1.f, kWaitCycles, false,
+                    has_min_p ? p->min_p : 0.f);
 }
 
 int spec_test_timeout_chain(const spec_chain_params* p, long long wait_cycles, void* workspace,
@@ -320,11 +329,12 @@ int spec_test_timeout_chain(const spec_chain_params* p, long long wait_cycles, v
   const size_t v1 = offsetof(spec_chain_params, seq_lens) + sizeof(p->seq_lens);
   if (!p || p->size < v1 || wait_cycles < 1) return SPEC_EINVAL;
   const bool has_filter = p->size >= offsetof(spec_chain_params, top_p) + sizeof(p->top_p);
+  const bool has_min_p = p->size >= offsetof(spec_chain_params, min_p) + sizeof(p->min_p);
   return chain_impl(p->target_logits, p->draft_logits, p->dtype, p->draft_tokens, p->uniforms,
                     p->seeds, p->offsets, p->draft_lens, p->temperature, p->B, p->k, p->V,
                     p->out_tokens, p->out_num_accepted, p->out_probs, p->seq_lens, workspace,
                     workspace_bytes, stream, has_filter ? p->top_k : 0,
-                    has_filter ? p->top_p : 1.f, wait_cycles, true);
+                    has_filter ? p->top_p : 1.f, wait_cycles, true, has_min_p ? p->min_p : 0.f);
 }
 
 int spec_test_timeout_greedy(const spec_greedy_params* p, long long wait_cycles, void* workspace,
@@ -455,6 +465,7 @@ const char* spec_status_string(int status) {
     case SPEC_ECUDA: return "CUDA error";
     case SPEC_EWORKSPACE: return "workspace missing or too small";
     case SPEC_ETIMEOUT: return "device wait timed out";
+    case SPEC_ELIMIT: return "a kept set exceeded the supported size";
     default: return "unknown status";
   }
 }

@@ -86,6 +86,7 @@ struct RowSmem {
   float sm;                              // top-p: mass of the kept entries
   int last;                              // this CTA finishes the request
   int failed;                            // finish: a wait of the request ran out
+  float rowM, rowS;                      // wide top-p: the row's softmax statistics
 };
 
 // Block-wide sum of one int per thread over a kRowThreads CTA.
@@ -476,15 +477,33 @@ __device__ __forceinline__ void publish_row(RowSmem& S, const ChainArgs& a, int 
   float sk;
   const float before = row_block_scan_f(e[0] + e[1], S, &sk);
   const float incl[2] = {before + e[0], before + e[0] + e[1]};
+  // The top-p mass: over the top K (top-k given), or over the whole
+  // vocabulary (no top-k: the row's S from pass 1, relative to its maximum).
+  const float norm = a.wide ? S.rowS * ex2(scaled(S.rowM - xmax, a.c_hi, a.c_lo)) : sk;
   if (tid == 0) S.m = K;
   __syncthreads();
   if (a.top_p < 1.f) {
 #pragma unroll
     for (int q = 1; q >= 0; --q)
-      if (e[q] > 0.f && incl[q] / sk >= a.top_p) atomicMin(&S.m, 2 * tid + q + 1);
+      if (e[q] > 0.f && incl[q] / norm >= a.top_p) atomicMin(&S.m, 2 * tid + q + 1);
+  }
+  // min_p after top-p: the entries are in decreasing order, so it keeps the
+  // prefix of those with 2^(c(x - xmax)) >= min_p.
+  if (a.min_p > 0.f) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = 2 * tid + q;
+      if (i < kk && e[q] < a.min_p) atomicMin(&S.m, i);
+    }
   }
   __syncthreads();
   const int m = S.m;  // kept: the first m entries (zero weights past kk)
+  // Without top-k the kept set must end inside the K ranked candidates: when
+  // neither filter cut them and the row holds more, the request fails closed.
+  if (a.wide && m >= K && kk >= K && tid == 0) {
+    set_status(a.ws.status, SPEC_ELIMIT);
+    atomicExch(&a.ws.sync[b].failed, 1);
+  }
   if (2 * tid == m - 1) S.sm = incl[0];
   if (2 * tid + 1 == m - 1) S.sm = incl[1];
   __syncthreads();
@@ -608,7 +627,7 @@ __device__ __forceinline__ bool all_halves_set(const uint4& v) {
          __vcmpeq2(v.w, 0) == 0;
 }
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool STATS>
 __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs a) {
   using IO = Io<DT, VEC>;
   asm volatile("griddepcontrol.launch_dependents;");
@@ -640,6 +659,48 @@ __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs
       asm volatile("st.relaxed.gpu.global.u16 [%0], %1;" ::"l"(out + tid / 8 + u * (kThreads / 8)),
                    "h"(c)
                    : "memory");
+    }
+  }
+  if constexpr (STATS) {
+    // Top-p over the whole vocabulary needs the row's softmax normaliser:
+    // this slice's (M, S) as one nonzero 64-bit word, as the chain's pass 1
+    // publishes it (each warp sums relative to its own maximum).
+    __shared__ float s_wm[kWarps], s_ws[kWarps];
+    float m = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u)
+      if (u < nv) m = fmaxf(m, IO::vmax(w[u]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float Ms = m == -INFINITY ? 0.f : m;
+    float sum = 0.f;
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u)
+      if (u < nv) {
+        float e[IO::EPV];
+        IO::unpack(w[u], e);
+#pragma unroll
+        for (int i = 0; i < IO::EPV; ++i) sum += ex2(scaled(e[i] - Ms, a.c_hi, a.c_lo));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((tid & 31) == 0) {
+      s_wm[tid >> 5] = m;
+      s_ws[tid >> 5] = sum;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float M = s_wm[0];
+#pragma unroll
+      for (int i = 1; i < kWarps; ++i) M = fmaxf(M, s_wm[i]);
+      float S = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i)
+          if (s_ws[i] > 0.f) S += s_ws[i] * ex2(scaled(s_wm[i] - M, a.c_hi, a.c_lo));
+      }
+      st_relaxed_u64(a.ws.stats + (size_t)rr * a.nsplit + s,
+                     ((unsigned long long)__float_as_uint(S) << 32) | __float_as_uint(M));
     }
   }
 }
@@ -775,8 +836,38 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
       reinterpret_cast<uint4*>(codes)[i] = make_uint4(d[0], d[1], d[2], d[3]);
       g[i] = make_uint4(0, 0, 0, 0);  // every call leaves the workspace zero
     }
-    // A code that never arrived: the request fails closed (the flag reaches
-    // the finishing row CTA through the acquire-release ticket).
+    // Wide top-p: the row's softmax statistics from pass 1's slice words
+    // (waited for like the codes), merged in a fixed order by warp 0.
+    if (a.wide && a.top_p < 1.f && warp == 0) {
+      const unsigned long long* sw = a.ws.stats + ((size_t)b * R + r) * ns;
+      unsigned long long v[2];
+      float m = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // ns <= 56 slices
+        const int u = lane + 32 * h;
+        v[h] = u < ns ? ld_relaxed_u64(sw + u) : 0xff800000ull;
+        if (u < ns && !v[h]) v[h] = wait_word(sw + u, a.ws.status, 0xff800000ull, a.wait_cycles, &to);
+        m = fmaxf(m, __uint_as_float((uint32_t)v[h]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float sM = __uint_as_float((uint32_t)v[h]), sS = __uint_as_float((uint32_t)(v[h] >> 32));
+        if (sS > 0.f && m != -INFINITY) sum += sS * ex2(scaled(sM - m, a.c_hi, a.c_lo));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) {
+        S.rowM = m;
+        S.rowS = sum;
+      }
+      for (int u = lane; u < ns; u += 32) const_cast<unsigned long long*>(sw)[u] = 0;  // left zero
+    }
+    // A code or statistics word that never arrived: the request fails closed
+    // (the flag reaches the finishing row CTA through the acquire-release
+    // ticket).
     if (__syncthreads_or(to) && tid == 0) atomicExch(&a.ws.sync[b].failed, 1);
     if (tid == 0) S.n = 0;
     __syncthreads();
@@ -1129,7 +1220,10 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st, bool skip_pas
   const long rows = (long)a.B * (2 * a.k + 1);
   if ((long)a.nsplit * kThreads <= kMaxCodes) {
     if (!skip_pass1) {
-      filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
+      if (a.wide && a.top_p < 1.f)
+        filter_max_kernel<DT, VEC, true><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
+      else
+        filter_max_kernel<DT, VEC, false><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -1147,7 +1241,7 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st, bool skip_pas
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, filter_pick_kernel<DT, VEC>, a);
   } else {  // a row too wide for one CTA's prefixes: stream it through one CTA
-    if (skip_pass1) return cudaErrorNotSupported;  // one pass: no wait to run out
+    if (skip_pass1 || a.wide) return cudaErrorNotSupported;  // one pass: no wait, no row S
     filter_row_kernel<DT, VEC><<<(unsigned)rows, kRowThreads, 0, st>>>(a);
   }
   return cudaGetLastError();

@@ -20,6 +20,9 @@ struct ChainArgs {
   int nchunks, cpc, nsplit2;   // draw: chunks per row, per item, items per request
   int top_k;                   // filtered verify: tokens kept per row (0: no filtering)
   float top_p;                 // filtered verify: nucleus mass, in (0, 1]
+  float min_p;                 // filtered verify: kept iff p >= min_p * max p (0: off)
+  int wide;                    // filtered verify without top-k: top_k holds the candidates
+                               // ranked (SPEC_MAX_TOPK), top-p mass is over the vocabulary
   int32_t* out_tokens;
   int32_t* out_n;
   float* out_probs;
@@ -92,7 +95,7 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
                 const uint64_t* seeds, const uint64_t* offsets, const int32_t* draft_lens,
                 float temperature, int B, int k, int V, int32_t* out_tokens,
                 int32_t* out_num_accepted, float* out_probs, int32_t* seq_lens, void* workspace,
-                size_t workspace_bytes, int top_k, float top_p);
+                size_t workspace_bytes, int top_k, float top_p, float min_p);
 int chain_launch(const ChainArgs& a, int dtype, bool vec, cudaStream_t st, bool skip_pass1);
 
 }  // namespace sv

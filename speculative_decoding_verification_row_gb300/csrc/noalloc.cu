@@ -57,7 +57,7 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   if (const int rc = chain_setup(a, vec, target_logits, draft_logits, dtype, draft_tokens,
                                  uniforms, nullptr, nullptr, nullptr, temperature, B, k, V,
                                  out_tokens, out_num_accepted, out_probs, seq_lens, scratch,
-                                 SPEC_NOALLOC_SCRATCH_BYTES, 0, 1.f))
+                                 SPEC_NOALLOC_SCRATCH_BYTES, 0, 1.f, 0.f))
     return rc;
   // The kernels run on the current device, whose array this is: the caller's
   // arrays must live there too.

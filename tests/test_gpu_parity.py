@@ -77,8 +77,9 @@ def draw_allowed(w, b, j, filt=None):
         p = oracle.softmax(w["target"][b, j], T, dt)
         q = oracle.softmax(w["draft"][b, j], T, dt) if j < k else None
     else:
-        p, tp = oracle.filtered_softmax(w["target"][b, j], T, filt[0], filt[1], dt)
-        q, tq = (oracle.filtered_softmax(w["draft"][b, j], T, filt[0], filt[1], dt)
+        mp = filt[2] if len(filt) > 2 else 0.0
+        p, tp = oracle.filtered_softmax(w["target"][b, j], T, filt[0], filt[1], dt, min_p=mp)
+        q, tq = (oracle.filtered_softmax(w["draft"][b, j], T, filt[0], filt[1], dt, min_p=mp)
                  if j < k else (None, False))
         if tp or tq:
             return None
