@@ -18,7 +18,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int esize(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
 
 // log2(e)/T as c_hi + c_lo with c_hi rounded down and c_lo > 0.
-bool temperature_consts(float T, float* hi, float* lo) {
+bool temperature_consts(float T, float* hi, float* lo, float* rn = nullptr) {
   if (!(T > 0.f) || !isfinite(T)) return false;
   const double c = kLog2e / (double)T;
   if (!(c < (double)FLT_MAX) || !(c > (double)FLT_MIN)) return false;
@@ -28,6 +28,7 @@ bool temperature_consts(float T, float* hi, float* lo) {
   if (!(l > 0.f)) l = FLT_MIN;
   *hi = h;
   *lo = l;
+  if (rn) *rn = (float)c;
   return true;
 }
 
@@ -127,7 +128,7 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
       k > SPEC_MAX_DRAFT || V < 2)
     return SPEC_EINVAL;
   a = ChainArgs{};
-  if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
+  if (!temperature_consts(temperature, &a.c_hi, &a.c_lo, &a.c_rn)) return SPEC_EINVAL;
   const int R = 2 * k + 1;
   if (top_k < 0 || top_k > SPEC_MAX_TOPK || !(top_p > 0.f) || !(top_p <= 1.f) ||
       !(min_p >= 0.f) || !(min_p <= 1.f))
@@ -407,7 +408,7 @@ int spec_verify_tree_sampled(const void* target_logits, int dtype, const int32_t
       (long)P * L > kTreeStage)
     return SPEC_EINVAL;
   ChainArgs a{};
-  if (!temperature_consts(temperature, &a.c_hi, &a.c_lo)) return SPEC_EINVAL;
+  if (!temperature_consts(temperature, &a.c_hi, &a.c_lo, &a.c_rn)) return SPEC_EINVAL;
   if (const int rc = check_ws(workspace, workspace_bytes, B, N, V)) return rc;
   const bool vec = aligned16(target_logits) && ((size_t)V * esize(dtype)) % 16 == 0;
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);

@@ -149,6 +149,16 @@ __device__ __forceinline__ float scaled(float d, float c_hi, float c_lo) {
   return fmaf(d, c_hi, d * c_lo);
 }
 
+// -m * c rounded to fp32 for the one-fma exponent 2^(x c + o): returns o
+// and, in *eps, its rounding error (-m c - o, exact by the product's fma),
+// so that 2^(x c - m c) = 2^(x c + o) * 2^(-eps) up to the exponent's final
+// rounding.  m = -inf is not passed (callers use 0 for an empty set).
+__device__ __forceinline__ float fma_offset(float m, float c, float* eps) {
+  const float o = -m * c;
+  *eps = fmaf(-m, c, -o);
+  return o;
+}
+
 // One stored logit widened to fp32 (exact for both dtypes).
 template <int DT>
 __device__ __forceinline__ float load_logit(const char* row, long t) {

@@ -48,11 +48,12 @@ template <int DT, bool VEC>
 __device__ __forceinline__ float2 vec_expsum(const uint32_t (&w)[Io<DT, VEC>::NW], float2 nm,
                                              float2 ch, float2 cl) {
   if constexpr (VEC && DT == SPEC_BF16) {
+    // here ch = (c, c) and nm = (-M c, -M c) rounded (see fma_offset):
+    // 2^(x c - M c) with one packed fma per pair
     float2 e[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 d = add2(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), nm);
-      const float2 y = fma2(d, ch, mul2(d, cl));
+      const float2 y = fma2(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), ch, nm);
       e[j] = make_float2(ex2(y.x), ex2(y.y));
     }
     return add2(add2(e[0], e[1]), add2(e[2], e[3]));
@@ -139,13 +140,18 @@ __global__ void __launch_bounds__(kThreads, 6) chain_rowstats_kernel(const Chain
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float Ms = m == -INFINITY ? 0.f : m;
-  const float2 nm = make_float2(-Ms, -Ms), ch = make_float2(a.c_hi, a.c_hi),
+  constexpr bool kFma = VEC && DT == SPEC_BF16;
+  float eps = 0.f;  // bf16: the rounding error of -Ms * c, restored in the sum below
+  const float nmc = kFma ? fma_offset(Ms, a.c_rn, &eps) : -Ms;
+  const float2 nm = make_float2(nmc, nmc),
+               ch = kFma ? make_float2(a.c_rn, a.c_rn) : make_float2(a.c_hi, a.c_hi),
                cl = make_float2(a.c_lo, a.c_lo);
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u)
     if (vbeg + tid + u * kThreads < vend) acc = add2(acc, vec_expsum<DT, VEC>(w[u], nm, ch, cl));
-  const float ssum = warp_sum(acc.x + acc.y);
+  float ssum = warp_sum(acc.x + acc.y);
+  if (kFma) ssum *= ex2(eps);
   if (lane == 0) {
     s_wm[warp] = m;
     s_ws[warp] = ssum;
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 6) chain_rowstats_kernel(const Chain
 template <int DT, bool VEC, bool MASK = false>
 __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow, int c, int lane,
                                               int V, float mp, float mq, float lam, float c_hi,
-                                              float c_lo, float (&wv)[8],
+                                              float c_lo, float c_rn, float (&wv)[8],
                                               TokenMask mask = TokenMask{nullptr, 0}) {
   const long t0 = (long)c * kChunk + lane * 8;
   float xp[8], xq[8];
@@ -215,14 +221,36 @@ __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow
       xq[i] = (qrow && t < V) ? load_logit<DT>(qrow, t) : -INFINITY;
     }
   }
+  if constexpr (VEC && DT == SPEC_BF16) {
+    // the one-fma exponents of chunk_sums' bf16 path, operation for operation
+    float ep_, eq_ = 0.f;
+    const float op = fma_offset(mp, c_rn, &ep_), oq = qrow ? fma_offset(mq, c_rn, &eq_) : 0.f;
+    const float lam2 = qrow ? lam * ex2(eq_ - ep_) : 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float ep = ex2(scaled(xp[i] - mp, c_hi, c_lo));
-    if (qrow) {
-      const float eq = ex2(scaled(xq[i] - mq, c_hi, c_lo));
-      wv[i] = fmaxf(fmaf(-lam, eq, ep), 0.f);
-    } else {
-      wv[i] = ep;
+    for (int j = 0; j < 4; ++j) {
+      const float2 yp = fma2(make_float2(xp[2 * j], xp[2 * j + 1]), make_float2(c_rn, c_rn), make_float2(op, op));
+      const float2 e_p = make_float2(ex2(yp.x), ex2(yp.y));
+      if (qrow) {
+        const float2 yq = fma2(make_float2(xq[2 * j], xq[2 * j + 1]), make_float2(c_rn, c_rn), make_float2(oq, oq));
+        const float2 e_q = make_float2(ex2(yq.x), ex2(yq.y));
+        const float2 w = fma2(make_float2(-lam2, -lam2), e_q, e_p);
+        wv[2 * j] = fmaxf(w.x, 0.f);
+        wv[2 * j + 1] = fmaxf(w.y, 0.f);
+      } else {
+        wv[2 * j] = e_p.x;
+        wv[2 * j + 1] = e_p.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float ep = ex2(scaled(xp[i] - mp, c_hi, c_lo));
+      if (qrow) {
+        const float eq = ex2(scaled(xq[i] - mq, c_hi, c_lo));
+        wv[i] = fmaxf(fmaf(-lam, eq, ep), 0.f);
+      } else {
+        wv[i] = ep;
+      }
     }
   }
   if constexpr (MASK) apply_mask(mask, t0, wv);
@@ -250,12 +278,10 @@ __device__ __forceinline__ void weights8_bf16(const uint32_t (&P)[4], const uint
                                               float2 ch, float2 cl, float (&wv)[8]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float2 dp = add2(make_float2(bf16_lo(P[j]), bf16_hi(P[j])), nmp);
-    const float2 yp = fma2(dp, ch, mul2(dp, cl));
+    const float2 yp = fma2(make_float2(bf16_lo(P[j]), bf16_hi(P[j])), ch, nmp);
     const float2 ep = make_float2(ex2(yp.x), ex2(yp.y));
     if (resid) {
-      const float2 dq = add2(make_float2(bf16_lo(Q[j]), bf16_hi(Q[j])), nmq);
-      const float2 yq = fma2(dq, ch, mul2(dq, cl));
+      const float2 yq = fma2(make_float2(bf16_lo(Q[j]), bf16_hi(Q[j])), ch, nmq);
       const float2 eq = make_float2(ex2(yq.x), ex2(yq.y));
       const float2 w = fma2(nlam, eq, ep);
       wv[2 * j] = fmaxf(w.x, 0.f);
@@ -282,8 +308,15 @@ __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, con
   if constexpr (VEC && DT == SPEC_BF16) {
     constexpr int GRP = 4;
     const bool resid = qrow != nullptr;
-    const float2 nmp = make_float2(-mp, -mp), nmq = make_float2(-mq, -mq),
-                 nlam = make_float2(-lam, -lam), ch = make_float2(a.c_hi, a.c_hi),
+    // 2^(x c - m c) with one packed fma per pair, the offsets -m c rounded;
+    // their rounding errors are a common factor of each side's weights, so
+    // only their difference enters, through lam (the p side's factor is
+    // common to every weight and leaves the draw unchanged)
+    float ep_, eq_ = 0.f;
+    const float op = fma_offset(mp, a.c_rn, &ep_), oq = resid ? fma_offset(mq, a.c_rn, &eq_) : 0.f;
+    const float lam2 = resid ? lam * ex2(eq_ - ep_) : 0.f;
+    const float2 nmp = make_float2(op, op), nmq = make_float2(oq, oq),
+                 nlam = make_float2(-lam2, -lam2), ch = make_float2(a.c_rn, a.c_rn),
                  cl = make_float2(a.c_lo, a.c_lo);
 #pragma unroll 1
     for (int cb = c0 + warp; cb < c1; cb += GRP * kWarps) {
@@ -315,7 +348,7 @@ __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, con
   } else {
     for (int c = c0 + warp; c < c1; c += kWarps) {
       float wv[8];
-      chunk_weights<DT, VEC, MASK>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, wv, mask);
+      chunk_weights<DT, VEC, MASK>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv, mask);
       const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
       if (lane == 0) out[c] = f;
       wtot += f;
@@ -409,7 +442,7 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
     use_mask = false;
     for (int c = warp; c < n; c += kWarps) {
       float wv[8];
-      chunk_weights<DT, VEC>(prow, nullptr, c, lane, a.V, mp, 0.f, 0.f, a.c_hi, a.c_lo, wv);
+      chunk_weights<DT, VEC>(prow, nullptr, c, lane, a.V, mp, 0.f, 0.f, a.c_hi, a.c_lo, a.c_rn, wv);
       const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
       if (lane == 0) chunks[c] = f;
     }
@@ -434,9 +467,9 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
     const int c = sChunk;
     float wv[8];
     if (use_mask)
-      chunk_weights<DT, VEC, MASK>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, wv, mask);
+      chunk_weights<DT, VEC, MASK>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv, mask);
     else
-      chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, wv);
+      chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv);
     float loc[8];
     loc[0] = wv[0];
 #pragma unroll

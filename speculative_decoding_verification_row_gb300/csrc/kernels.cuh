@@ -14,6 +14,7 @@ struct ChainArgs {
   const unsigned long long* offsets;          // [B] Philox counters (when uniforms is null)
   const int32_t* draft_lens;                  // [B] real draft lengths (ragged), or null: k
   float c_hi, c_lo;  // log2(e)/T split as hi + lo
+  float c_rn;        // log2(e)/T rounded to nearest (the bf16 one-fma exponents)
   int B, k, V;
   int rows;                    // logit rows per request in pass 1 (chain: 2k + 1; tree: N)
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
