@@ -48,6 +48,8 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--greedy", action="store_true", help="greedy chain verify instead of stochastic")
+    ap.add_argument("--sampled", action="store_true",
+                    help="tree workloads: the stochastic tree verify instead of the greedy one")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -200,6 +202,7 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=device)
     w = workloads.make(args.config, seed=rank_seed(args.seed, rank))
     tree = w["kind"] == "tree"
+    sampled = tree and args.sampled
     greedy = args.greedy and not tree
     filtered = args.top_k > 0 and not (tree or greedy)
     if filtered:
@@ -219,6 +222,7 @@ def run_ours(args, rank, world, local):
         c = {"target": dev_logits(w["target"], w["dtype"], device)}
         if tree:
             c["tree_tokens"], c["paths"] = i32(w["tree_tokens"]), i32(w["paths"])
+            c["uniforms"] = torch.from_numpy(w["uniforms"]).to(device)
         else:
             c["tokens"] = i32(w["draft_tokens"])
             if not greedy:
@@ -239,7 +243,15 @@ def run_ours(args, rank, world, local):
     ptr = lambda t: P(t.data_ptr())  # noqa: E731
     call_args = []
     for c in copies:
-        if tree:
+        if sampled:
+            best = torch.empty(B, dtype=torch.int32, device=device)
+            nodes = torch.empty((B, w["L"]), dtype=torch.int32, device=device)
+            fn = lib.spec_verify_tree_sampled
+            call_args.append((ptr(c["target"]), code, ptr(c["tree_tokens"]), ptr(c["paths"]),
+                              ptr(c["uniforms"]), ctypes.c_float(w["temperature"]), B, w["N"], w["P"],
+                              w["L"], V, ptr(out_tok), ptr(out_n), ptr(best), ptr(nodes), ptr(seq),
+                              ptr(buf), buf.numel(), sh))
+        elif tree:
             best = torch.empty(B, dtype=torch.int32, device=device)
             nodes = torch.empty((B, w["L"]), dtype=torch.int32, device=device)
             fn = lib.spec_verify_tree
@@ -320,7 +332,7 @@ def run_ours(args, rank, world, local):
     # results read back inside every step.
     host = {key: torch.from_numpy(np.ascontiguousarray(
         w[key].view(np.int16) if (w["dtype"] == workloads.BF16 and key in ("target", "draft")) else w[key])).pin_memory()
-        for key in (["target", "tree_tokens", "paths"] if tree else
+        for key in ((["target", "tree_tokens", "paths"] + (["uniforms"] if sampled else [])) if tree else
                     ["target", "draft_tokens"] + ([] if greedy else ["draft", "uniforms"]))}
     host["seq_lens"] = torch.from_numpy(w["seq_lens"].copy()).pin_memory()
     dev_in = {key: torch.empty(t.shape, dtype=t.dtype, device=device) for key, t in host.items()}
@@ -334,7 +346,11 @@ def run_ours(args, rank, world, local):
         for key, t in host.items():
             dev_in[key].copy_(t, non_blocking=True)
         lg = (lambda t: t.view(torch.bfloat16)) if w["dtype"] == workloads.BF16 else (lambda t: t)
-        if tree:
+        if sampled:
+            tk, nn, _, _ = sv.verify_tree_sampled(lg(dev_in["target"]), dev_in["tree_tokens"], dev_in["paths"],
+                                                  dev_in["uniforms"], w["temperature"],
+                                                  seq_lens=dev_in["seq_lens"], workspace=ws)
+        elif tree:
             tk, nn, _, _ = sv.verify_tree(lg(dev_in["target"]), dev_in["tree_tokens"], dev_in["paths"],
                                           seq_lens=dev_in["seq_lens"], workspace=ws)
         elif greedy:
@@ -368,7 +384,8 @@ def run_ours(args, rank, world, local):
     algo_bytes = workloads.algorithmic_bytes(w, greedy=greedy or tree)
     achieved = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
-    kernel_key = "tree" if tree else ("greedy" if greedy else ("filtered" if filtered else "chain"))
+    kernel_key = ("tree_sampled" if sampled else "tree") if tree else \
+        ("greedy" if greedy else ("filtered" if filtered else "chain"))
     traffic = recorded_traffic(f"{args.config}/{kernel_key}"
                                + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""))
     stats = sv.acceptance_stats(n_first, k)
@@ -376,7 +393,7 @@ def run_ours(args, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, greedy, args.cpu_seconds,
-                           (args.top_k, args.top_p) if filtered else None)
+                           (args.top_k, args.top_p) if filtered else None, sampled=sampled)
 
     if dist:
         dist.destroy_process_group()
@@ -398,10 +415,11 @@ def run_ours(args, rank, world, local):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": args.config + ("/greedy" if greedy else "") + ("/philox" if args.philox and not (tree or greedy) else "")
+            "workload": args.config + ("/greedy" if greedy else "") + ("/sampled" if sampled else "")
+                        + ("/philox" if args.philox and not (tree or greedy) else "")
                         + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""),
             "B": B, "k": k, "V": V, "logits": w["dtype"],
-            "temperature": None if (tree or greedy) else w["temperature"],
+            "temperature": None if ((tree and not sampled) or greedy) else w["temperature"],
             "requests_per_step": B * world,
             "l2": "inputs larger than L2: two resident copies of the logits used alternately",
             "timing": f"one CUDA event pair around the K steps on the launching stream, {PREQUEUE} untimed "
@@ -416,7 +434,8 @@ def run_ours(args, rank, world, local):
             "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
                        "filtered": "spec_verify_chain_ex call (filter_max_kernel + filter_pick_kernel)",
                        "greedy": "spec_verify_greedy call (argmax_kernel + argmax_finish_kernel)",
-                       "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)"}[kernel_key],
+                       "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)",
+                       "tree_sampled": "spec_verify_tree_sampled call (chain_rowstats_kernel + tree_draw_kernel)"}[kernel_key],
             "algorithmic_bytes_per_call": algo_bytes,
         },
         "e2e": {"value": job_throughput(world, pos, 1e3 * te / args.e2e_steps), "unit": "positions/s",
@@ -440,11 +459,14 @@ def filtered_draft_tokens(w):
     return np.argmax(x, axis=-1).astype(np.int32)
 
 
-def cpu_baseline(w, greedy, seconds, filt=None):
+def cpu_baseline(w, greedy, seconds, filt=None, sampled=False):
     import oracle
     reps, t0 = 0, time.perf_counter()
     while True:
-        if filt:
+        if sampled:
+            oracle.verify_tree_sampled(w["target"], w["tree_tokens"], w["paths"], w["uniforms"],
+                                       w["temperature"], w["dtype"])
+        elif filt:
             oracle.verify_chain_filtered(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
                                          w["temperature"], filt[0], float(np.float32(filt[1])), w["dtype"])
         else:
@@ -490,6 +512,7 @@ def run_reference(args, rank, world):
     import oracle
     w = workloads.make(args.config, seed=args.seed)
     tree = w["kind"] == "tree"
+    sampled = tree and args.sampled
     greedy = args.greedy and not tree
     filtered = args.top_k > 0 and not (tree or greedy)
     if filtered:
@@ -499,6 +522,9 @@ def run_reference(args, rank, world):
         sub = {key: (v[b:b + 1] if isinstance(v, np.ndarray) and v.shape[:1] == (w["B"],) else v)
                for key, v in w.items()}
         sub["B"] = 1
+        if sampled:
+            return oracle.verify_tree_sampled(sub["target"], sub["tree_tokens"], sub["paths"],
+                                              sub["uniforms"], sub["temperature"], sub["dtype"])
         if filtered:
             return oracle.verify_chain_filtered(sub["target"], sub["draft"], sub["draft_tokens"],
                                                 sub["uniforms"], sub["temperature"], args.top_k,
@@ -519,7 +545,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.config + ("/greedy" if greedy else "")
+        "config": {"workload": args.config + ("/greedy" if greedy else "") + ("/sampled" if sampled else "")
                                + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""),
                    "B": w["B"],
                    "k": per, "V": w["V"], "logits": w["dtype"]},
