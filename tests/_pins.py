@@ -978,6 +978,23 @@ def pin_filter_min_p_and_wide_top_p(lib=None) -> list[str]:
         if np.max(np.abs(got - want)) > 1e-12:
             errs.append(f"filter row {trial} (top_k={kk}, top_p={pp}, min_p={mp}) differs from numpy")
             break
+    # kept sets of hundreds to thousands of tokens (top_k above 256, top-p and
+    # min_p over wide rows), logits on a coarse grid so that the cuts fall
+    # inside runs of equal values
+    for trial in range(24):
+        V = int(rng.integers(300, 3000))
+        xr = (np.round(rng.standard_normal(V) * 24) / 8).astype(np.float32)
+        T = float(rng.choice([0.7, 1.0, 2.0]))
+        kk = int(rng.choice([0, 0, 257, 1000, V - 1]))
+        pp = float(np.float32(rng.choice([0.5, 0.9, 0.99, 1.0])))
+        mp = float(rng.choice([0.0, 0.0, 1e-4, 0.01]))
+        got, tie = fr(xr, T, kk, pp, mp)
+        if tie:
+            continue
+        want = _filter_np(xr, T, kk, pp, mp)
+        if np.max(np.abs(got - want)) > 1e-12 or not np.array_equal(got > 0, want > 0):
+            errs.append(f"wide filter row {trial} (V={V}, top_k={kk}, top_p={pp}, min_p={mp}) differs from numpy")
+            break
     for (k2, V2, T2, filt) in [(1, 6, 1.0, (0, 0.8, 0.0)), (2, 5, 0.8, (0, 1.0, 0.2)),
                                (2, 4, 1.2, (0, 0.7, 0.1)), (2, 5, 1.0, (3, 0.9, 0.3))]:
         tg = (rng.standard_normal((k2 + 1, V2)) * 1.5).astype(np.float32)
