@@ -57,8 +57,9 @@ def parse(argv=None):
     ap.add_argument("--philox", action="store_true",
                     help="chain: draw each request's uniforms in the kernel from a (seed, offset) Philox state")
     ap.add_argument("--top-k", type=int, default=0,
-                    help="stochastic chain on top-k / top-p filtered rows (0: unfiltered)")
+                    help="stochastic chain on top-k / top-p / min_p filtered rows (0: no top-k)")
     ap.add_argument("--top-p", type=float, default=1.0)
+    ap.add_argument("--min-p", type=float, default=0.0)
     ap.add_argument("--op", choices=["verify", "relocate"], default="verify",
                     help="relocate: time the accepted-KV relocation after a tree verify instead")
     ap.add_argument("--kv-row-bytes", type=int, default=131072,
@@ -204,7 +205,8 @@ def run_ours(args, rank, world, local):
     tree = w["kind"] == "tree"
     sampled = tree and args.sampled
     greedy = args.greedy and not tree
-    filtered = args.top_k > 0 and not (tree or greedy)
+    filtered = is_filtered(args) and not (tree or greedy)
+    wide = filtered and (args.top_k == 0 or args.top_k > sv.SPEC_MAX_TOPK)
     if filtered:
         # The draft argmax is in every kept set (top_k >= 1, top_p > 0).
         w["draft_tokens"] = filtered_draft_tokens(w)
@@ -268,7 +270,8 @@ def run_ours(args, rank, world, local):
                                  ptr(c["tokens"]), None, None if args.philox else ptr(c["uniforms"]),
                                  ptr(c["seeds"]) if args.philox else None,
                                  ptr(c["offsets"]) if args.philox else None, w["temperature"], B, k, V,
-                                 ptr(out_tok), ptr(out_n), None, ptr(seq), args.top_k, args.top_p)
+                                 ptr(out_tok), ptr(out_n), None, ptr(seq), args.top_k, args.top_p,
+                                 args.min_p)
             c["params"] = prm
             call_args.append((ctypes.byref(prm), ptr(buf), buf.numel(), sh))
         elif args.philox:
@@ -282,7 +285,9 @@ def run_ours(args, rank, world, local):
             call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
                               ptr(c["uniforms"]), ctypes.c_float(w["temperature"]), B, k, V,
                               ptr(out_tok), ptr(out_n), None, ptr(seq), ptr(buf), buf.numel(), sh))
-    launches_per_step = 2  # pass 1 and its programmatic-dependent finish/draw grid
+    # pass 1 and its programmatic-dependent finish/draw grid; the wide filter:
+    # pass 1, histogram, bins, candidates, cut, draw
+    launches_per_step = 6 if wide else 2
 
     for i in range(args.warmup):
         rc = fn(*call_args[i & 1])
@@ -360,7 +365,8 @@ def run_ours(args, rank, world, local):
             tk, nn, _ = sv.verify_chain(lg(dev_in["target"]), lg(dev_in["draft"]), dev_in["draft_tokens"],
                                         dev_in["uniforms"], w["temperature"], seq_lens=dev_in["seq_lens"],
                                         workspace=ws, top_k=args.top_k if filtered else 0,
-                                        top_p=args.top_p if filtered else 1.0)
+                                        top_p=args.top_p if filtered else 1.0,
+                                        min_p=args.min_p if filtered else 0.0)
         res_tok.copy_(tk, non_blocking=True)
         res_n.copy_(nn, non_blocking=True)
         res_seq.copy_(dev_in["seq_lens"], non_blocking=True)
@@ -385,15 +391,14 @@ def run_ours(args, rank, world, local):
     achieved = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
     kernel_key = ("tree_sampled" if sampled else "tree") if tree else \
-        ("greedy" if greedy else ("filtered" if filtered else "chain"))
-    traffic = recorded_traffic(f"{args.config}/{kernel_key}"
-                               + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""))
+        ("greedy" if greedy else (("wide" if wide else "filtered") if filtered else "chain"))
+    traffic = recorded_traffic(f"{args.config}/{kernel_key}" + (filter_tag(args) if filtered else ""))
     stats = sv.acceptance_stats(n_first, k)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, greedy, args.cpu_seconds,
-                           (args.top_k, args.top_p) if filtered else None, sampled=sampled)
+                           (args.top_k, args.top_p, args.min_p) if filtered else None, sampled=sampled)
 
     if dist:
         dist.destroy_process_group()
@@ -417,7 +422,7 @@ def run_ours(args, rank, world, local):
         "config": {
             "workload": args.config + ("/greedy" if greedy else "") + ("/sampled" if sampled else "")
                         + ("/philox" if args.philox and not (tree or greedy) else "")
-                        + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""),
+                        + (filter_tag(args) if filtered else ""),
             "B": B, "k": k, "V": V, "logits": w["dtype"],
             "temperature": None if ((tree and not sampled) or greedy) else w["temperature"],
             "requests_per_step": B * world,
@@ -433,6 +438,8 @@ def run_ours(args, rank, world, local):
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
             "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
                        "filtered": "spec_verify_chain_ex call (filter_max_kernel + filter_pick_kernel)",
+                       "wide": "spec_verify_chain_ex call (chain_rowstats_kernel + wide_hist_kernel + "
+                               "wide_bins_kernel + wide_cand_kernel + wide_cut_kernel + wide_draw_kernel)",
                        "greedy": "spec_verify_greedy call (argmax_kernel + argmax_finish_kernel)",
                        "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)",
                        "tree_sampled": "spec_verify_tree_sampled call (chain_rowstats_kernel + tree_draw_kernel)"}[kernel_key],
@@ -449,6 +456,14 @@ def run_ours(args, rank, world, local):
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
+
+
+def is_filtered(args):
+    return args.top_k > 0 or args.top_p < 1.0 or args.min_p > 0.0
+
+
+def filter_tag(args):
+    return f"/top_k={args.top_k},top_p={args.top_p:g}" + (f",min_p={args.min_p:g}" if args.min_p > 0 else "")
 
 
 def filtered_draft_tokens(w):
@@ -468,7 +483,8 @@ def cpu_baseline(w, greedy, seconds, filt=None, sampled=False):
                                        w["temperature"], w["dtype"])
         elif filt:
             oracle.verify_chain_filtered(w["target"], w["draft"], w["draft_tokens"], w["uniforms"],
-                                         w["temperature"], filt[0], float(np.float32(filt[1])), w["dtype"])
+                                         w["temperature"], filt[0], float(np.float32(filt[1])), w["dtype"],
+                                         min_p=float(np.float32(filt[2])))
         else:
             oracle.verify(w, greedy=greedy)
         reps += 1
@@ -514,7 +530,7 @@ def run_reference(args, rank, world):
     tree = w["kind"] == "tree"
     sampled = tree and args.sampled
     greedy = args.greedy and not tree
-    filtered = args.top_k > 0 and not (tree or greedy)
+    filtered = is_filtered(args) and not (tree or greedy)
     if filtered:
         w["draft_tokens"] = filtered_draft_tokens(w)
 
@@ -528,7 +544,8 @@ def run_reference(args, rank, world):
         if filtered:
             return oracle.verify_chain_filtered(sub["target"], sub["draft"], sub["draft_tokens"],
                                                 sub["uniforms"], sub["temperature"], args.top_k,
-                                                float(np.float32(args.top_p)), sub["dtype"])
+                                                float(np.float32(args.top_p)), sub["dtype"],
+                                                min_p=float(np.float32(args.min_p)))
         return oracle.verify(sub, greedy=greedy)
 
     for i in range(args.warmup):
@@ -546,7 +563,7 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.config + ("/greedy" if greedy else "") + ("/sampled" if sampled else "")
-                               + (f"/top_k={args.top_k},top_p={args.top_p:g}" if filtered else ""),
+                               + (filter_tag(args) if filtered else ""),
                    "B": w["B"],
                    "k": per, "V": w["V"], "logits": w["dtype"]},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",

@@ -77,8 +77,8 @@ typedef enum {
     SPEC_ECUDA = -3,       /* a CUDA launch or copy failed */
     SPEC_EWORKSPACE = -4,  /* workspace missing or smaller than spec_workspace_size() */
     SPEC_ETIMEOUT = -5,    /* a bounded device wait ran out (device status) */
-    SPEC_ELIMIT = -6       /* a top-p / min_p kept set without top-k held more than
-                              SPEC_MAX_TOPK - 1 tokens (device status) */
+    SPEC_ELIMIT = -6       /* a filtered row's cut search found its bins inconsistent
+                              (an internal check, not expected; device status) */
 } spec_status_t;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
@@ -88,7 +88,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 #define SPEC_MAX_DRAFT 64
 /* Largest batch B of any call. */
 #define SPEC_MAX_BATCH 8192
-/* Largest top_k of the filtered chain verify (spec_chain_params.top_k). */
+/* Largest top_k the filtered chain verify serves with explicit kept lists;
+ * a larger top_k (and top-p or min_p without top-k) takes per-row cuts. */
 #define SPEC_MAX_TOPK 256
 #define SPEC_MAX_TREE_NODES 1024
 #define SPEC_MAX_PATH_LEN 64
@@ -102,10 +103,12 @@ size_t spec_workspace_size(int B, int rows_per_request, int V);
 
 /* Bytes of scratch of a filtered chain verify (spec_chain_params with
  * top_k > 0, or top_k = 0 with top_p < 1 or min_p > 0) of B requests, k
- * drafts, width V: the chain's, plus each row's kept list (top_k words;
- * SPEC_MAX_TOPK when top_k = 0), 2k probabilities per request and two bytes
- * per 2048 logits of each row.  Returns 0 for invalid sizes (top_k outside
- * [0, SPEC_MAX_TOPK] included). */
+ * drafts, width V: the chain's, plus for 1 <= top_k <= SPEC_MAX_TOPK each
+ * row's kept list (top_k words), 2k probabilities per request and two bytes
+ * per 2048 logits of each row; for top_k = 0 or top_k > SPEC_MAX_TOPK
+ * (per-row cuts) each row's 2048-bin mass histogram and counts (24 KB), a
+ * 64-byte record and a 4096-entry candidate list (16 KB).  Returns 0 for
+ * invalid sizes (top_k < 0 included). */
 size_t spec_workspace_size_filtered(int B, int k, int V, int top_k);
 
 /* Zero a workspace (asynchronously, on `stream`).  Call once after allocating
@@ -194,21 +197,22 @@ typedef struct spec_chain_params {
     /* Symmetric filtering (TensorRT-LLM walkthrough, rejection-sampling
      * section: target and draft are filtered by the same backend and
      * parameters, or the accept test is silently wrong).  top_k = 0: none.
-     * top_k in [1, SPEC_MAX_TOPK]: every target and draft row keeps its
-     * top_k tokens by (logit descending, token ascending), then the shortest
-     * prefix of them whose softmax mass (over those top_k, at temperature T)
-     * reaches top_p (top_p = 1: all top_k); p and q are the softmax over the
-     * kept set, and the chain verify above runs on them (the final draw
-     * takes u * Z over the kept tokens in token order).  out_probs holds the
-     * filtered p and q.  Logits of -inf are never kept (their weight is 0);
-     * logits must not be NaN or +inf.  top_p in (0, 1].  top_k = 0 with
-     * top_p < 1 (or min_p > 0) keeps every token before the top-p cut, whose
-     * mass is then over the whole vocabulary; such a kept set must end
-     * within the SPEC_MAX_TOPK largest logits of the row (at most
-     * SPEC_MAX_TOPK - 1 tokens), else the request fails closed and the
-     * status word reads SPEC_ELIMIT.  The workspace must hold
-     * spec_workspace_size_filtered(B, k, V, top_k) bytes.  Rows wider than
-     * 917504 bf16 or 458752 fp32 logits support top_k > 0 only. */
+     * top_k >= 1: every target and draft row keeps its top_k tokens by
+     * (logit descending, token ascending) (top_k >= V: all), then the
+     * shortest prefix of them whose softmax mass (over those top_k, at
+     * temperature T) reaches top_p (top_p = 1: all top_k); p and q are the
+     * softmax over the kept set, and the chain verify above runs on them
+     * (the final draw takes u * Z over the kept tokens in token order).
+     * out_probs holds the filtered p and q.  Logits of -inf carry weight 0
+     * (they change no probability, no top-p prefix and no draw); logits must
+     * not be NaN or +inf.  top_p in (0, 1].  top_k = 0 with top_p < 1 keeps
+     * the shortest prefix of the whole row whose mass reaches top_p.  Kept
+     * sets of any size are exact: 1 <= top_k <= SPEC_MAX_TOPK uses explicit
+     * kept lists, top_k = 0 (with top_p < 1 or min_p > 0) and top_k >
+     * SPEC_MAX_TOPK a per-row cut found from a mass histogram and a radix
+     * selection over the tokens of the bins the cut can fall in.  The
+     * workspace must hold spec_workspace_size_filtered(B, k, V, top_k)
+     * bytes. */
     int top_k;
     float top_p;
     /* min_p in [0, 1] (0: off), applied after top-p (the walkthrough names

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["api.cu", "chain.cu", "argmax.cu", "noalloc.cu", "relocate.cu", "filter.cu",
-           "tree_sampled.cu"]
+           "tree_sampled.cu", "wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 

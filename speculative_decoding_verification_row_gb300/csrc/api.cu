@@ -94,11 +94,12 @@ size_t spec_workspace_size(int B, int rows_per_request, int V) {
 }
 
 size_t spec_workspace_size_filtered(int B, int k, int V, int top_k) {
-  if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2 || top_k < 0 ||
-      top_k > SPEC_MAX_TOPK)
+  if (B < 1 || B > SPEC_MAX_BATCH || k < 1 || k > SPEC_MAX_DRAFT || V < 2 || top_k < 0)
     return 0;
-  // top_k = 0 (top-p or min_p alone) ranks SPEC_MAX_TOPK candidates per row
-  return FilterLayout(B, k, V, top_k > 0 ? top_k : SPEC_MAX_TOPK).total;
+  // top_k = 0 (top-p or min_p alone, or no filter) and top_k above
+  // SPEC_MAX_TOPK take the per-row cuts of the wide path
+  if (top_k == 0 || top_k > SPEC_MAX_TOPK) return WideLayout(B, k, V).total;
+  return FilterLayout(B, k, V, top_k).total;
 }
 
 int spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream) {
@@ -130,17 +131,18 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
   a = ChainArgs{};
   if (!temperature_consts(temperature, &a.c_hi, &a.c_lo, &a.c_rn)) return SPEC_EINVAL;
   const int R = 2 * k + 1;
-  if (top_k < 0 || top_k > SPEC_MAX_TOPK || !(top_p > 0.f) || !(top_p <= 1.f) ||
-      !(min_p >= 0.f) || !(min_p <= 1.f))
+  if (top_k < 0 || !(top_p > 0.f) || !(top_p <= 1.f) || !(min_p >= 0.f) || !(min_p <= 1.f))
     return SPEC_EINVAL;
-  // Without top-k, top-p and min_p rank SPEC_MAX_TOPK candidates per row.
-  const bool wide = top_k == 0 && (top_p < 1.f || min_p > 0.f);
-  const int kcand = wide ? SPEC_MAX_TOPK : top_k;
+  // Kept lists for 1 <= top_k <= SPEC_MAX_TOPK; per-row cuts for kept sets
+  // of any size (top-p or min_p without top-k, or a larger top-k).
+  const bool wide = (top_k == 0 && (top_p < 1.f || min_p > 0.f)) || top_k > SPEC_MAX_TOPK;
+  const int kcand = wide ? 0 : top_k;
   if (const int rc = check_ws(workspace, workspace_bytes, B, R, V)) return rc;
   vec = aligned16(target_logits) && aligned16(draft_logits) &&
         ((size_t)V * esize(dtype)) % 16 == 0;
   row_units(V, dtype, vec, &a.nvec, &a.nsplit, &a.vps);
   if (kcand > 0 && workspace_bytes < FilterLayout(B, k, V, kcand).total) return SPEC_EWORKSPACE;
+  if (wide && workspace_bytes < WideLayout(B, k, V).total) return SPEC_EWORKSPACE;
   a.nchunks = num_chunks(V);
   a.cpc = kChunksPerCta;
   a.nsplit2 = num_items(V);
@@ -162,11 +164,18 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
   a.seq_lens = seq_lens;
   a.wait_cycles = kWaitCycles;
   a.ws = ws_views(workspace, WsLayout(B, R, V));
-  a.top_k = kcand;
+  a.top_k = wide ? top_k : kcand;
   a.top_p = top_p;
   a.min_p = min_p;
   a.wide = wide;
-  if (kcand > 0) {
+  if (wide) {
+    const WideLayout wl(B, k, V);
+    char* base = static_cast<char*>(workspace);
+    a.ws.whist = reinterpret_cast<unsigned long long*>(base + wl.hist);
+    a.ws.wcount = reinterpret_cast<unsigned*>(base + wl.count);
+    a.ws.wrow = reinterpret_cast<WideRow*>(base + wl.rec);
+    a.ws.wcand = reinterpret_cast<unsigned*>(base + wl.cand);
+  } else if (kcand > 0) {
     const FilterLayout fl(B, k, V, kcand);
     a.ws.cand = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + fl.cand);
     a.ws.pq = reinterpret_cast<float*>(static_cast<char*>(workspace) + fl.pq);
@@ -177,8 +186,10 @@ int chain_setup(ChainArgs& a, bool& vec, const void* target_logits, const void* 
 
 // Enqueues a chain verify set up by chain_setup.
 int chain_launch(const ChainArgs& a, int dtype, bool vec, cudaStream_t st, bool skip_pass1) {
-  const cudaError_t e = a.top_k > 0 ? launch_filtered(a, dtype, vec, st, skip_pass1)
-                                    : launch_chain(a, dtype, vec, st, skip_pass1);
+  if (a.wide && skip_pass1) return SPEC_EINVAL;  // the wide path waits for nothing
+  const cudaError_t e = a.wide        ? launch_wide(a, dtype, vec, st)
+                        : a.top_k > 0 ? launch_filtered(a, dtype, vec, st, skip_pass1)
+                                      : launch_chain(a, dtype, vec, st, skip_pass1);
   return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
@@ -466,7 +477,7 @@ const char* spec_status_string(int status) {
     case SPEC_ECUDA: return "CUDA error";
     case SPEC_EWORKSPACE: return "workspace missing or too small";
     case SPEC_ETIMEOUT: return "device wait timed out";
-    case SPEC_ELIMIT: return "a kept set exceeded the supported size";
+    case SPEC_ELIMIT: return "a filtered row's cut search failed an internal check";
     default: return "unknown status";
   }
 }

@@ -72,6 +72,26 @@ struct WsLayout {
   }
 };
 
+// Exact filtering of any kept-set size (top-p or min_p without top-k, top-k
+// above SPEC_MAX_TOPK): each row's mass histogram over kWideBins bins of
+// 1/kWideBinsPerLog2 of a log2 unit below the row maximum (the last bin
+// holds the rest), its candidate list (the tokens of the bins a cut can fall
+// in) and its record.
+constexpr int kWideBinsPerLog2 = 32;
+constexpr int kWideBins = 2048;
+constexpr int kWideCandCap = 4096;  // candidates listed per row; a row with more rescans itself
+struct WideRow {
+  unsigned long long zmin;  // sum of the fixed-point masses with 2^(c(x - M)) >= min_p
+  unsigned kmin_inv;        // ~ the smallest order key (ord32) among those tokens
+  unsigned ncand;           // tokens appended to the row's candidate list
+  int bk, blo, bhi;         // the top-k bin, the top-p bin range (-1: none)
+  int pad0;
+  unsigned long long kcut;  // token t is kept iff make_key(x_t, t) >= kcut
+  float M, Z;               // row maximum and kept mass (2^(c(x - M)) units)
+  int pad1[4];
+};
+static_assert(sizeof(WideRow) == 64, "WideRow layout");
+
 struct Ws {  // typed views of one call's workspace
   int* status;                 // first word of the 256-byte status block
   ReqSync* sync;
@@ -82,6 +102,10 @@ struct Ws {  // typed views of one call's workspace
   unsigned long long* cand;    // filtered: each row's kept list
   float* pq;                   // filtered: p_i(x_i) and q_i(x_i) of each request
   unsigned short* codes;       // filtered: each slice thread's largest-logit prefix
+  unsigned long long* whist;   // wide filter: per row kWideBins fixed-point masses (2^-40)
+  unsigned* wcount;            // wide filter: per row kWideBins token counts (top-k cut)
+  WideRow* wrow;               // wide filter: per row record
+  unsigned* wcand;             // wide filter: per row kWideCandCap candidate token ids
 };
 
 // The filtered chain path appends three regions to the chain layout: per
@@ -99,13 +123,28 @@ struct FilterLayout {
   }
 };
 
+// The wide filtered path appends its per-row regions to the chain layout.
+struct WideLayout {
+  size_t hist, count, rec, cand, total;
+  __host__ __device__ WideLayout(int B, int k, int V) {
+    const size_t rows = (size_t)B * (2 * k + 1);
+    size_t off = WsLayout(B, 2 * k + 1, V).total;
+    hist = off; off += align256(sizeof(unsigned long long) * rows * kWideBins);
+    count = off; off += align256(sizeof(unsigned) * rows * kWideBins);
+    rec = off; off += align256(sizeof(WideRow) * rows);
+    cand = off; off += align256(sizeof(unsigned) * rows * kWideCandCap);
+    total = off;
+  }
+};
+
 inline Ws ws_views(void* base, const WsLayout& l) {
   char* p = static_cast<char*>(base);
   return Ws{reinterpret_cast<int*>(p + l.status), reinterpret_cast<ReqSync*>(p + l.sync),
             reinterpret_cast<unsigned long long*>(p + l.stats),
             reinterpret_cast<float2*>(p + l.part),
             reinterpret_cast<unsigned long long*>(p + l.chunks),
-            reinterpret_cast<unsigned long long*>(p + l.items), nullptr, nullptr, nullptr};
+            reinterpret_cast<unsigned long long*>(p + l.items), nullptr, nullptr, nullptr,
+            nullptr, nullptr, nullptr, nullptr};
 }
 
 // ---------------------------------------------------------------- loads
@@ -157,6 +196,21 @@ __device__ __forceinline__ float fma_offset(float m, float c, float* eps) {
   const float o = -m * c;
   *eps = fmaf(-m, c, -o);
   return o;
+}
+
+// Order keys: ord32 is monotone in the logit (-0 and +0 alike);
+// make_key(x, t) orders tokens by (logit descending, token ascending) as
+// decreasing 64-bit keys.
+__device__ __forceinline__ uint32_t ord32(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+__device__ __forceinline__ unsigned long long make_key(float x, long t) {
+  return ((unsigned long long)ord32(x) << 32) | (0xffffffffu - (uint32_t)t);
 }
 
 // One stored logit widened to fp32 (exact for both dtypes).

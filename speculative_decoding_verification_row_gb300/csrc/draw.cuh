@@ -8,7 +8,8 @@
 // The draw: draw weights of 256-token chunks summed in 64-bit fixed point
 // (chunk_sums), then the request's last CTA locates u*Z among the chunk sums
 // and scans the one chunk that holds it (draw_token).  A TokenMask forces the
-// weights of a few tokens to 0 (the stochastic tree's rejected children).
+// weights of a few tokens to 0 (the stochastic tree's rejected children); a
+// CutMask reads the tokens below each row's filter cut as -inf.
 #pragma once
 
 #include "kernels.cuh"
@@ -22,6 +23,21 @@ struct TokenMask {
   const int* tok;
   int n;
 };
+
+// Filtered rows (the wide filter): token t of the target row counts only
+// when make_key(x_t, t) >= kp, of the draft row when >= kq; the others are
+// read as logit -inf on that side.
+struct CutMask {
+  unsigned long long kp, kq;
+};
+
+// A bf16 pair (tokens t, t + 1) with the halves below the cut set to -inf.
+__device__ __forceinline__ uint32_t cut_pair(uint32_t w, long t, unsigned long long k) {
+  uint32_t r = w;
+  if (make_key(__uint_as_float(w << 16), t) < k) r = (r & 0xffff0000u) | 0xff80u;
+  if (make_key(__uint_as_float(w & 0xffff0000u), t + 1) < k) r = (r & 0x0000ffffu) | 0xff800000u;
+  return r;
+}
 
 // Zeroes the weights of the masked tokens among t0 .. t0 + 7.
 __device__ __forceinline__ void apply_mask(const TokenMask& m, long t0, float (&wv)[8]) {
@@ -176,11 +192,12 @@ __global__ void __launch_bounds__(kThreads, 6) chain_rowstats_kernel(const Chain
 // The 8 draw weights of lane `lane` in chunk `c` (0 past the row's end):
 // residual: 2^(c(xp - mp)) - lam * 2^(c(xq - mq)) clamped at 0, lam = Sp/Sq
 // (that is Sp * max(0, p - q)); bonus (qrow == nullptr): 2^(c(xp - mp)).
-template <int DT, bool VEC, bool MASK = false>
+template <int DT, bool VEC, bool MASK = false, bool CUT = false>
 __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow, int c, int lane,
                                               int V, float mp, float mq, float lam, float c_hi,
                                               float c_lo, float c_rn, float (&wv)[8],
-                                              TokenMask mask = TokenMask{nullptr, 0}) {
+                                              TokenMask mask = TokenMask{nullptr, 0},
+                                              CutMask cut = CutMask{0, 0}) {
   const long t0 = (long)c * kChunk + lane * 8;
   float xp[8], xq[8];
   if constexpr (VEC) {
@@ -219,6 +236,13 @@ __device__ __forceinline__ void chunk_weights(const char* prow, const char* qrow
       const long t = t0 + i;
       xp[i] = t < V ? load_logit<DT>(prow, t) : -INFINITY;
       xq[i] = (qrow && t < V) ? load_logit<DT>(qrow, t) : -INFINITY;
+    }
+  }
+  if constexpr (CUT) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (make_key(xp[i], t0 + i) < cut.kp) xp[i] = -INFINITY;
+      if (qrow && make_key(xq[i], t0 + i) < cut.kq) xq[i] = -INFINITY;
     }
   }
   if constexpr (VEC && DT == SPEC_BF16) {
@@ -297,12 +321,13 @@ __device__ __forceinline__ void weights8_bf16(const uint32_t (&P)[4], const uint
 // Each warp issues the loads of four chunks before using any.  The weights
 // are those of chunk_weights, computed with the same operations.
 // Returns, in lane 0 of each warp, the fixed-point total of that warp's chunks.
-template <int DT, bool VEC, bool MASK = false>
+template <int DT, bool VEC, bool MASK = false, bool CUT = false>
 __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, const char* prow,
                                                          const char* qrow, int c0, int c1, float mp,
                                                          float mq, float lam,
                                                          unsigned long long* out,
-                                                         TokenMask mask = TokenMask{nullptr, 0}) {
+                                                         TokenMask mask = TokenMask{nullptr, 0},
+                                                         CutMask cut = CutMask{0, 0}) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long wtot = 0;
   if constexpr (VEC && DT == SPEC_BF16) {
@@ -337,6 +362,14 @@ __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, con
       for (int i = 0; i < GRP; ++i) {
         const int c = cb + i * kWarps;
         if (c >= c1) continue;
+        if constexpr (CUT) {
+          const long t = (long)c * kChunk + lane * 8;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            P[i][e] = cut_pair(P[i][e], t + 2 * e, cut.kp);
+            if (resid) Q[i][e] = cut_pair(Q[i][e], t + 2 * e, cut.kq);
+          }
+        }
         float wv[8];
         weights8_bf16(P[i], Q[i], resid, nmp, nmq, nlam, ch, cl, wv);
         if constexpr (MASK) apply_mask(mask, (long)c * kChunk + lane * 8, wv);
@@ -348,7 +381,8 @@ __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, con
   } else {
     for (int c = c0 + warp; c < c1; c += kWarps) {
       float wv[8];
-      chunk_weights<DT, VEC, MASK>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv, mask);
+      chunk_weights<DT, VEC, MASK, CUT>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv,
+                                        mask, cut);
       const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
       if (lane == 0) out[c] = f;
       wtot += f;
@@ -360,10 +394,10 @@ __device__ __forceinline__ unsigned long long chunk_sums(const ChainArgs& a, con
 // The request's last CTA: locate u*Z among the chunk sums (one round trip for
 // all of them), re-read and scan that chunk, return the token (all threads
 // call it; the result is valid in every thread).
-template <int DT, bool VEC, bool MASK = false>
+template <int DT, bool VEC, bool MASK = false, bool CUT = false>
 __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const char* qrow,
                           float mp, float mq, float lam, double u,
-                          TokenMask mask = TokenMask{nullptr, 0}) {
+                          TokenMask mask = TokenMask{nullptr, 0}, CutMask cut = CutMask{0, 0}) {
   __shared__ unsigned long long sTarget, sPre, sZ;
   __shared__ unsigned long long sWarpTot[kWarps];
   __shared__ int sChunk, sTok, sRetry, sLastPos;
@@ -436,13 +470,15 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
       break;
     }
     // The residual vanished numerically: draw from p_j instead (this CTA
-    // recomputes every chunk and item sum; a rare path; unmasked).
+    // recomputes every chunk and item sum; a rare path; without the token
+    // mask, with the row's filter cut).
     qrow = nullptr;
     lam = 0.f;
     use_mask = false;
     for (int c = warp; c < n; c += kWarps) {
       float wv[8];
-      chunk_weights<DT, VEC>(prow, nullptr, c, lane, a.V, mp, 0.f, 0.f, a.c_hi, a.c_lo, a.c_rn, wv);
+      chunk_weights<DT, VEC, false, CUT>(prow, nullptr, c, lane, a.V, mp, 0.f, 0.f, a.c_hi, a.c_lo, a.c_rn,
+                                         wv, TokenMask{nullptr, 0}, cut);
       const unsigned long long f = to_fixed(warp_sum(tree8(wv)));
       if (lane == 0) chunks[c] = f;
     }
@@ -467,9 +503,11 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
     const int c = sChunk;
     float wv[8];
     if (use_mask)
-      chunk_weights<DT, VEC, MASK>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv, mask);
+      chunk_weights<DT, VEC, MASK, CUT>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv,
+                                        mask, cut);
     else
-      chunk_weights<DT, VEC>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv);
+      chunk_weights<DT, VEC, false, CUT>(prow, qrow, c, lane, a.V, mp, mq, lam, a.c_hi, a.c_lo, a.c_rn, wv,
+                                         TokenMask{nullptr, 0}, cut);
     float loc[8];
     loc[0] = wv[0];
 #pragma unroll

@@ -4,7 +4,10 @@
 // accept test is silently wrong).  Every target and draft row is reduced to
 // its kept set: the top_k tokens by (logit descending, token ascending), then
 // the shortest prefix of them whose softmax mass (softmax over those top_k,
-// at temperature T) reaches top_p; p and q are the softmax over the kept set.
+// at temperature T) reaches top_p, then those with 2^(c(x - x_max)) >= min_p;
+// p and q are the softmax over the kept set.  This file serves
+// 1 <= top_k <= SPEC_MAX_TOPK with explicit kept lists; wide.cu serves
+// kept sets of any size (no top-k, or a larger one) through per-row cuts.
 // The verify itself is the plain chain rule (vLLM anatomy page, "Speculative
 // Decoding"): accept x_i iff r_i < p_i(x_i) / q_i(x_i) (q = 0 accepts), stop
 // at the first rejection j and draw from max(0, p_j - q_j) normalised, or
@@ -35,18 +38,7 @@ namespace sv {
 
 namespace {
 
-// Order-preserving map of a float (not NaN) to 32 bits, -0 taken as +0.
-__device__ __forceinline__ uint32_t ord32(float x) {
-  uint32_t u = __float_as_uint(x);
-  if (u == 0x80000000u) u = 0;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float unord32(uint32_t o) {
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
-}
-__device__ __forceinline__ unsigned long long make_key(float x, long t) {
-  return ((unsigned long long)ord32(x) << 32) | (0xffffffffu - (uint32_t)t);
-}
+// The logit and the token of a make_key key.
 __device__ __forceinline__ float key_value(unsigned long long key) {
   return unord32((uint32_t)(key >> 32));
 }
@@ -86,7 +78,6 @@ struct RowSmem {
   float sm;                              // top-p: mass of the kept entries
   int last;                              // this CTA finishes the request
   int failed;                            // finish: a wait of the request ran out
-  float rowM, rowS;                      // wide top-p: the row's softmax statistics
 };
 
 // Block-wide sum of one int per thread over a kRowThreads CTA.
@@ -477,9 +468,7 @@ __device__ __forceinline__ void publish_row(RowSmem& S, const ChainArgs& a, int 
   float sk;
   const float before = row_block_scan_f(e[0] + e[1], S, &sk);
   const float incl[2] = {before + e[0], before + e[0] + e[1]};
-  // The top-p mass: over the top K (top-k given), or over the whole
-  // vocabulary (no top-k: the row's S from pass 1, relative to its maximum).
-  const float norm = a.wide ? S.rowS * ex2(scaled(S.rowM - xmax, a.c_hi, a.c_lo)) : sk;
+  const float norm = sk;  // the top-p mass is over the top K
   if (tid == 0) S.m = K;
   __syncthreads();
   if (a.top_p < 1.f) {
@@ -498,12 +487,6 @@ __device__ __forceinline__ void publish_row(RowSmem& S, const ChainArgs& a, int 
   }
   __syncthreads();
   const int m = S.m;  // kept: the first m entries (zero weights past kk)
-  // Without top-k the kept set must end inside the K ranked candidates: when
-  // neither filter cut them and the row holds more, the request fails closed.
-  if (a.wide && m >= K && kk >= K && tid == 0) {
-    set_status(a.ws.status, SPEC_ELIMIT);
-    atomicExch(&a.ws.sync[b].failed, 1);
-  }
   if (2 * tid == m - 1) S.sm = incl[0];
   if (2 * tid + 1 == m - 1) S.sm = incl[1];
   __syncthreads();
@@ -627,7 +610,7 @@ __device__ __forceinline__ bool all_halves_set(const uint4& v) {
          __vcmpeq2(v.w, 0) == 0;
 }
 
-template <int DT, bool VEC, bool STATS>
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs a) {
   using IO = Io<DT, VEC>;
   asm volatile("griddepcontrol.launch_dependents;");
@@ -659,48 +642,6 @@ __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs
       asm volatile("st.relaxed.gpu.global.u16 [%0], %1;" ::"l"(out + tid / 8 + u * (kThreads / 8)),
                    "h"(c)
                    : "memory");
-    }
-  }
-  if constexpr (STATS) {
-    // Top-p over the whole vocabulary needs the row's softmax normaliser:
-    // this slice's (M, S) as one nonzero 64-bit word, as the chain's pass 1
-    // publishes it (each warp sums relative to its own maximum).
-    __shared__ float s_wm[kWarps], s_ws[kWarps];
-    float m = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u)
-      if (u < nv) m = fmaxf(m, IO::vmax(w[u]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float Ms = m == -INFINITY ? 0.f : m;
-    float sum = 0.f;
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u)
-      if (u < nv) {
-        float e[IO::EPV];
-        IO::unpack(w[u], e);
-#pragma unroll
-        for (int i = 0; i < IO::EPV; ++i) sum += ex2(scaled(e[i] - Ms, a.c_hi, a.c_lo));
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if ((tid & 31) == 0) {
-      s_wm[tid >> 5] = m;
-      s_ws[tid >> 5] = sum;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float M = s_wm[0];
-#pragma unroll
-      for (int i = 1; i < kWarps; ++i) M = fmaxf(M, s_wm[i]);
-      float S = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int i = 0; i < kWarps; ++i)
-          if (s_ws[i] > 0.f) S += s_ws[i] * ex2(scaled(s_wm[i] - M, a.c_hi, a.c_lo));
-      }
-      st_relaxed_u64(a.ws.stats + (size_t)rr * a.nsplit + s,
-                     ((unsigned long long)__float_as_uint(S) << 32) | __float_as_uint(M));
     }
   }
 }
@@ -835,35 +776,6 @@ __global__ void __launch_bounds__(kRowThreads, kPickCtasPerSm) filter_pick_kerne
       for (int q = 0; q < 4; ++q) d[q] = __vsubus2(m1[q], 0x00010001u);
       reinterpret_cast<uint4*>(codes)[i] = make_uint4(d[0], d[1], d[2], d[3]);
       g[i] = make_uint4(0, 0, 0, 0);  // every call leaves the workspace zero
-    }
-    // Wide top-p: the row's softmax statistics from pass 1's slice words
-    // (waited for like the codes), merged in a fixed order by warp 0.
-    if (a.wide && a.top_p < 1.f && warp == 0) {
-      const unsigned long long* sw = a.ws.stats + ((size_t)b * R + r) * ns;
-      unsigned long long v[2];
-      float m = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // ns <= 56 slices
-        const int u = lane + 32 * h;
-        v[h] = u < ns ? ld_relaxed_u64(sw + u) : 0xff800000ull;
-        if (u < ns && !v[h]) v[h] = wait_word(sw + u, a.ws.status, 0xff800000ull, a.wait_cycles, &to);
-        m = fmaxf(m, __uint_as_float((uint32_t)v[h]));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float sum = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float sM = __uint_as_float((uint32_t)v[h]), sS = __uint_as_float((uint32_t)(v[h] >> 32));
-        if (sS > 0.f && m != -INFINITY) sum += sS * ex2(scaled(sM - m, a.c_hi, a.c_lo));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) {
-        S.rowM = m;
-        S.rowS = sum;
-      }
-      for (int u = lane; u < ns; u += 32) const_cast<unsigned long long*>(sw)[u] = 0;  // left zero
     }
     // A code or statistics word that never arrived: the request fails closed
     // (the flag reaches the finishing row CTA through the acquire-release
@@ -1220,10 +1132,7 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st, bool skip_pas
   const long rows = (long)a.B * (2 * a.k + 1);
   if ((long)a.nsplit * kThreads <= kMaxCodes) {
     if (!skip_pass1) {
-      if (a.wide && a.top_p < 1.f)
-        filter_max_kernel<DT, VEC, true><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
-      else
-        filter_max_kernel<DT, VEC, false><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
+      filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -1241,7 +1150,7 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st, bool skip_pas
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, filter_pick_kernel<DT, VEC>, a);
   } else {  // a row too wide for one CTA's prefixes: stream it through one CTA
-    if (skip_pass1 || a.wide) return cudaErrorNotSupported;  // one pass: no wait, no row S
+    if (skip_pass1) return cudaErrorNotSupported;  // one pass: nothing to wait for
     filter_row_kernel<DT, VEC><<<(unsigned)rows, kRowThreads, 0, st>>>(a);
   }
   return cudaGetLastError();

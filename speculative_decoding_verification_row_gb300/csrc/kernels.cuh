@@ -19,11 +19,11 @@ struct ChainArgs {
   int rows;                    // logit rows per request in pass 1 (chain: 2k + 1; tree: N)
   int nvec, nsplit, vps;       // vectors per row, units per row, vectors per unit
   int nchunks, cpc, nsplit2;   // draw: chunks per row, per item, items per request
-  int top_k;                   // filtered verify: tokens kept per row (0: no filtering)
+  int top_k;                   // filtered verify: tokens kept per row (0: no top-k)
   float top_p;                 // filtered verify: nucleus mass, in (0, 1]
   float min_p;                 // filtered verify: kept iff p >= min_p * max p (0: off)
-  int wide;                    // filtered verify without top-k: top_k holds the candidates
-                               // ranked (SPEC_MAX_TOPK), top-p mass is over the vocabulary
+  int wide;                    // filtered verify through per-row cuts (wide.cu): no top-k
+                               // with top-p or min_p, or top_k > SPEC_MAX_TOPK
   int32_t* out_tokens;
   int32_t* out_n;
   float* out_probs;
@@ -84,6 +84,9 @@ cudaError_t launch_filtered(const ChainArgs& a, int dtype, bool vec, cudaStream_
 cudaError_t launch_argmax(const ArgmaxArgs& a, int dtype, bool vec, cudaStream_t st,
                           bool skip_pass1 = false);
 cudaError_t launch_tree_sampled(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
+// Filtered chain verify with kept sets of any size (a.wide): six
+// stream-ordered grids, nothing polls.
+cudaError_t launch_wide(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
 
 // Largest P * L of a stochastic tree verify (its paths and edge logits are
 // staged in shared memory).

@@ -1,0 +1,722 @@
+// Filtered chain verify for kept sets of any size: top-p or min_p without
+// top-k, and top-k above SPEC_MAX_TOPK (TensorRT-LLM walkthrough, rejection-
+// sampling section: target and draft rows are filtered alike by temperature,
+// top-k, top-p and min_p, in that order; vLLM anatomy page, "Speculative
+// Decoding": accept/reject and the residual draw, here on the filtered
+// rows).  filter.cu keeps explicit lists for top_k <= SPEC_MAX_TOPK.
+//
+// A kept set is a prefix of its row in (logit descending, token ascending)
+// order, possibly shortened by min_p (a cut on the logit alone), so one
+// 64-bit order key fixes it: token t is kept iff make_key(x_t, t) >= kcut.
+// Each token's mass is e_t = 2^(c (x_t - M)) (c = log2(e)/T, M the row
+// maximum), summed in 2^-40 fixed point so that every sum below is exact
+// whatever its order.  Six stream-ordered grids, each a programmatic
+// dependent that waits for its predecessor before reading (no polling):
+//   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima.
+//   2. wide_hist_kernel, one CTA per 32 KB slice: each token's mass and bin
+//      floor(32 c (M - x)) (2048 bins of 1/32 of a log2 unit, the last
+//      holding everything below) into a shared-memory histogram, then into
+//      the row's (masses; counts too when top-k cuts); the mass and the
+//      smallest logit key of the tokens with e_t >= min_p.
+//   3. wide_bins_kernel, one CTA per row: prefix sums over the bins give
+//      the bin where the top-k count is reached and the range of bins the
+//      top-p threshold can fall in (the top-k mass is known to within the
+//      top-k bin).
+//   4. wide_cand_kernel, one CTA per slice: the tokens of those bins are
+//      listed per row (most rows: tens to hundreds).
+//   5. wide_cut_kernel, one CTA per row: radix selection over the listed
+//      tokens' keys, eight bits at a time, with exact per-digit counts and
+//      masses: the top-k cut and its mass, then the first token at which
+//      the running top-p mass reaches top_p times it; min_p replaces the
+//      cut when its logit cut lies above.  Writes the row's cut, maximum and
+//      kept mass.
+//   6. wide_draw_kernel: the chain's draw items with the accept test on
+//      p'(x_i) / q'(x_i) and the residual max(0, p' - q') (or the bonus p')
+//      over the filtered rows: tokens below a row's cut read as -inf.
+// Every call leaves the histograms, candidate lists, row records and
+// statistics words zero, as the chain path does (a later call's layout may
+// place its statistics words there).
+#include <mutex>
+
+#include "draw.cuh"
+
+namespace sv {
+
+namespace {
+
+constexpr int kStage = 2048;  // listed candidates the cut kernel stages in shared memory
+
+__device__ __forceinline__ int mass_bin(float x, float M, float cR) {
+  const float f = (M - x) * cR;  // >= 0; +inf for x = -inf
+  return f < (float)kWideBins ? (int)f : kWideBins - 1;
+}
+// e = 2^(c (x - M)) <= 1 as an integer number of 2^-40.
+__device__ __forceinline__ unsigned long long mass_fix(float x, float M, float c_hi, float c_lo) {
+  return to_fixed(ex2(scaled(x - M, c_hi, c_lo)) * 256.f);
+}
+
+// The row's maximum from its slices' pass-1 words (all written by now).
+__device__ float row_max(const ChainArgs& a, int rr) {
+  __shared__ float s_m[kWarps];
+  const int tid = threadIdx.x;
+  float m = -INFINITY;
+  for (int u = tid; u < a.nsplit; u += kThreads)
+    m = fmaxf(m, stats_unpack(ld_relaxed_u64(a.ws.stats + (size_t)rr * a.nsplit + u)).x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((tid & 31) == 0) s_m[tid >> 5] = m;
+  __syncthreads();
+  float M = s_m[0];
+#pragma unroll
+  for (int i = 1; i < kWarps; ++i) M = fmaxf(M, s_m[i]);
+  __syncthreads();
+  return M == -INFINITY ? 0.f : M;
+}
+
+// Block-wide exclusive prefix sum of one value per thread (thread order);
+// *total receives the sum.
+__device__ unsigned long long block_excl_u64(unsigned long long v, unsigned long long* total) {
+  __shared__ unsigned long long s_w[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long incl = warp_incl_u64(v);
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  unsigned long long base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    base += w < warp ? s_w[w] : 0;
+    tot += s_w[w];
+  }
+  __syncthreads();
+  *total = tot;
+  return base + incl - v;
+}
+
+// The top-p threshold over a top-k mass Z: the running mass must reach
+// top_p * Z, i.e. ceil(top_p * Z) in fixed point (at least 1).
+__device__ __forceinline__ unsigned long long top_p_threshold(float top_p, unsigned long long Z) {
+  const double t = ceil((double)top_p * (double)Z);
+  return t < 1.0 ? 1ull : (unsigned long long)t;
+}
+
+// ------------------------------------------------------------------ 2
+template <int DT, bool VEC, bool COUNT>
+__global__ void __launch_bounds__(kThreads) wide_hist_kernel(const ChainArgs a) {
+  __shared__ unsigned long long hm[kWideBins];
+  __shared__ unsigned hc[COUNT ? kWideBins : 1];
+  __shared__ unsigned long long s_z[kWarps];
+  __shared__ unsigned s_k[kWarps];
+  using IO = Io<DT, VEC>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
+  int b, r;
+  slice_row(a, rr, b, r);
+  for (int i = tid; i < kWideBins; i += kThreads) {
+    hm[i] = 0;
+    if (COUNT) hc[i] = 0;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
+  const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
+  const int vbeg = s * a.vps;
+  const int vend = min(a.nvec, vbeg + a.vps);
+  uint32_t w[kVecPerThread][IO::NW];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int v = vbeg + tid + u * kThreads;
+    if (v < vend) IO::load(row, v, w[u]);
+  }
+  const float M = row_max(a, rr);  // also orders the clearing above before the adds
+  const float cR = a.c_rn * (float)kWideBinsPerLog2;
+  const bool use_min_p = a.min_p > 0.f;
+  unsigned long long zmin = 0;
+  unsigned kinv = 0;
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    if (vbeg + tid + u * kThreads >= vend) continue;
+    float x[IO::EPV];
+    IO::unpack(w[u], x);
+#pragma unroll
+    for (int i = 0; i < IO::EPV; ++i) {
+      const float e = ex2(scaled(x[i] - M, a.c_hi, a.c_lo));
+      const unsigned long long f = to_fixed(e * 256.f);
+      const int bin = mass_bin(x[i], M, cR);
+      if (f) atomicAdd(&hm[bin], f);
+      if (COUNT) atomicAdd(&hc[bin], 1u);
+      if (use_min_p && e >= a.min_p) {
+        zmin += f;
+        kinv = max(kinv, ~ord32(x[i]));
+      }
+    }
+  }
+  __syncthreads();
+  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
+  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
+  for (int i = tid; i < kWideBins; i += kThreads) {
+    if (hm[i]) atomicAdd(gh + i, hm[i]);
+    if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
+  }
+  if (use_min_p) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      zmin += __shfl_xor_sync(0xffffffffu, zmin, o);
+      kinv = max(kinv, __shfl_xor_sync(0xffffffffu, kinv, o));
+    }
+    if (lane == 0) {
+      s_z[warp] = zmin;
+      s_k[warp] = kinv;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long z = 0;
+      unsigned kk = 0;
+#pragma unroll
+      for (int i = 0; i < kWarps; ++i) {
+        z += s_z[i];
+        kk = max(kk, s_k[i]);
+      }
+      WideRow* wr = a.ws.wrow + rr;
+      if (z) atomicAdd(&wr->zmin, z);
+      if (kk) atomicMax(&wr->kmin_inv, kk);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ 3
+// Bins b of a row are held 8 per thread (thread t: 8t .. 8t + 7).
+constexpr int kBinsPerThread = kWideBins / kThreads;
+static_assert(kBinsPerThread * kThreads == kWideBins, "bins per thread");
+
+__global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) {
+  __shared__ int s_bk, s_blo, s_bhi;
+  __shared__ unsigned long long s_mb, s_mbin;
+  const int tid = threadIdx.x;
+  const int rr = blockIdx.x, b = rr / a.rows, r = rr - b * a.rows;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
+  const unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  const unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  const bool count_cut = a.top_k > 0;
+  unsigned long long m[kBinsPerThread], tm = 0, tc = 0;
+  unsigned c[kBinsPerThread];
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    m[j] = gh[j];
+    c[j] = count_cut ? gc[j] : 0u;
+    tm += m[j];
+    tc += c[j];
+  }
+  if (tid == 0) {
+    s_bk = s_blo = s_bhi = -1;
+    s_mb = 0;
+    s_mbin = 0;
+  }
+  unsigned long long Z, N;
+  const unsigned long long pm = block_excl_u64(tm, &Z);
+  const unsigned long long pc = block_excl_u64(tc, &N);
+  // top-k: the bin where the running count reaches top_k
+  if (count_cut && (unsigned long long)a.top_k < N) {
+    unsigned long long cb = pc, mb = pm;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      if (cb < (unsigned long long)a.top_k && (unsigned long long)a.top_k <= cb + c[j]) {
+        s_bk = kBinsPerThread * tid + j;
+        s_mb = mb;
+        s_mbin = m[j];
+      }
+      cb += c[j];
+      mb += m[j];
+    }
+  }
+  __syncthreads();
+  if (a.top_p < 1.f) {
+    // the top-k mass lies in [zlo, zhi]; so does the threshold's bin range
+    const unsigned long long zlo = s_bk >= 0 ? s_mb : Z, zhi = s_bk >= 0 ? s_mb + s_mbin : Z;
+    const unsigned long long tl = top_p_threshold(a.top_p, zlo), th = top_p_threshold(a.top_p, zhi);
+    unsigned long long mb = pm;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      if (mb < tl && tl <= mb + m[j]) s_blo = kBinsPerThread * tid + j;
+      if (mb < th && th <= mb + m[j]) s_bhi = kBinsPerThread * tid + j;
+      mb += m[j];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    WideRow* wr = a.ws.wrow + rr;
+    wr->bk = s_bk;
+    wr->blo = s_blo;
+    wr->bhi = s_blo >= 0 ? s_bhi : -1;
+  }
+}
+
+// ------------------------------------------------------------------ 4
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads) wide_cand_kernel(const ChainArgs a) {
+  __shared__ unsigned s_base;
+  using IO = Io<DT, VEC>;
+  const int tid = threadIdx.x;
+  const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
+  int b, r;
+  slice_row(a, rr, b, r);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
+  WideRow* wr = a.ws.wrow + rr;
+  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi;
+  if (bk < 0 && blo < 0) return;  // no cut falls inside a bin: nothing to list
+  const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
+  const int vbeg = s * a.vps;
+  const int vend = min(a.nvec, vbeg + a.vps);
+  uint32_t w[kVecPerThread][IO::NW];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int v = vbeg + tid + u * kThreads;
+    if (v < vend) IO::load(row, v, w[u]);
+  }
+  const float M = row_max(a, rr);
+  const float cR = a.c_rn * (float)kWideBinsPerLog2;
+  unsigned long long sel = 0;  // bit u * EPV + i: element i of vector u is listed
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    if (vbeg + tid + u * kThreads >= vend) continue;
+    float x[IO::EPV];
+    IO::unpack(w[u], x);
+#pragma unroll
+    for (int i = 0; i < IO::EPV; ++i) {
+      const int bin = mass_bin(x[i], M, cR);
+      if (bin == bk || (blo <= bin && bin <= bhi)) sel |= 1ull << (u * IO::EPV + i);
+    }
+  }
+  unsigned long long total;
+  const unsigned long long off = block_excl_u64((unsigned long long)__popcll(sel), &total);
+  if (total == 0) return;  // uniform
+  if (tid == 0) s_base = atomicAdd(&wr->ncand, (unsigned)total);
+  __syncthreads();
+  unsigned pos = s_base + (unsigned)off;
+  unsigned* out = a.ws.wcand + (size_t)rr * kWideCandCap;
+  while (sel) {
+    const int bit = __ffsll((long long)sel) - 1;
+    sel &= sel - 1;
+    if (pos < (unsigned)kWideCandCap) {
+      const int u = bit / IO::EPV, i = bit - u * IO::EPV;
+      out[pos] = (unsigned)((vbeg + tid + u * kThreads) * IO::EPV + i);
+    }
+    ++pos;
+  }
+}
+
+// ------------------------------------------------------------------ 5
+struct SelSmem {
+  unsigned cnt[256];
+  unsigned long long mass[256];
+  int digit;
+  unsigned long long before_w, before_m;
+};
+
+// Among the row's listed tokens i < n that satisfy pred(key, bin), in
+// decreasing key order (logit descending, token ascending), the first at
+// which the running weight (a count, or the fixed-point mass when by_mass)
+// reaches `target` (1 <= target <= their total): radix selection over the
+// 64-bit keys, eight bits at a time from the top, with the exact weight of
+// every digit.  Returns its key; *mass_incl receives the mass up to and
+// including it.
+template <class Get, class Pred>
+__device__ unsigned long long radix_select(int n, const Get& get, const Pred& pred, bool by_mass,
+                                           unsigned long long target, float M, const ChainArgs& a,
+                                           SelSmem& S, unsigned long long* mass_incl) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long prefix = 0, mbefore = 0;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kThreads) {
+      S.cnt[i] = 0;
+      S.mass[i] = 0;
+    }
+    __syncthreads();
+    const unsigned long long hi = shift == 56 ? 0ull : ~0ull << (shift + 8);
+    for (int i = tid; i < n; i += kThreads) {
+      unsigned long long K;
+      int bin;
+      get(i, K, bin);
+      if (!pred(K, bin) || ((K ^ prefix) & hi)) continue;
+      const int d = (int)(K >> shift) & 255;
+      atomicAdd(&S.cnt[d], 1u);
+      const unsigned long long f = mass_fix(unord32((uint32_t)(K >> 32)), M, a.c_hi, a.c_lo);
+      if (f) atomicAdd(&S.mass[d], f);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l: digits 255 - 8l down to 248 - 8l (decreasing keys first)
+      unsigned long long wv[8], mv[8], lw = 0, lm = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int d = 255 - 8 * lane - j;
+        mv[j] = S.mass[d];
+        wv[j] = by_mass ? mv[j] : (unsigned long long)S.cnt[d];
+        lw += wv[j];
+        lm += mv[j];
+      }
+      const unsigned long long iw = warp_incl_u64(lw), im = warp_incl_u64(lm);
+      unsigned long long bw = iw - lw, bm = im - lm;
+      if (bw < target && target <= iw) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (bw < target && target <= bw + wv[j]) {
+            S.digit = 255 - 8 * lane - j;
+            S.before_w = bw;
+            S.before_m = bm;
+          }
+          bw += wv[j];
+          bm += mv[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (unsigned long long)S.digit << shift;
+    target -= S.before_w;
+    mbefore += S.before_m;
+    __syncthreads();
+  }
+  *mass_incl = mbefore + mass_fix(unord32((uint32_t)(prefix >> 32)), M, a.c_hi, a.c_lo);
+  return prefix;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
+  __shared__ unsigned long long me[kWideBins + 1];  // mass before each bin
+  __shared__ unsigned long long sKey[kStage];
+  __shared__ unsigned short sBin[kStage];
+  __shared__ SelSmem S;
+  __shared__ unsigned long long s_cbk;
+  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
+  const int tid = threadIdx.x;
+  const int rr = blockIdx.x, b = rr / a.rows, r = rr - b * a.rows;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
+  const char* row = row_ptr(a, b, r, (size_t)a.V * ES);
+  WideRow* wr = a.ws.wrow + rr;
+  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi;
+  const unsigned ncand = wr->ncand;
+  const unsigned long long zmin = wr->zmin;
+  const unsigned kinv = wr->kmin_inv;
+  const float M = row_max(a, rr);
+  // the statistics words are consumed: every call leaves them zero
+  for (int u = tid; u < a.nsplit; u += kThreads) a.ws.stats[(size_t)rr * a.nsplit + u] = 0;
+  // Prefix masses of the bins (and the count before the top-k bin); the
+  // histogram is returned to zero.
+  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  const bool count_cut = a.top_k > 0;
+  unsigned long long m[kBinsPerThread], tm = 0, tc = 0;
+  unsigned c[kBinsPerThread];
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    m[j] = gh[j];
+    c[j] = count_cut ? gc[j] : 0u;
+    tm += m[j];
+    tc += c[j];
+  }
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    gh[j] = 0;
+    if (count_cut) gc[j] = 0;
+  }
+  unsigned long long Z, N;
+  unsigned long long mb = block_excl_u64(tm, &Z);
+  unsigned long long cb = block_excl_u64(tc, &N);
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    const int bin = kBinsPerThread * tid + j;
+    me[bin] = mb;
+    if (bin == bk) s_cbk = cb;
+    mb += m[j];
+    cb += c[j];
+  }
+  if (tid == kThreads - 1) me[kWideBins] = Z;
+  // Stage the listed tokens (or, past the list's capacity, read the row).
+  const bool listed = ncand <= (unsigned)kWideCandCap;
+  const int n = listed ? (int)ncand : a.V;
+  const bool staged = listed && n <= kStage;
+  const unsigned* cand = a.ws.wcand + (size_t)rr * kWideCandCap;
+  const float cR = a.c_rn * (float)kWideBinsPerLog2;
+  if (staged)
+    for (int i = tid; i < n; i += kThreads) {
+      const unsigned t = cand[i];
+      const float x = load_logit<DT>(row, t);
+      sKey[i] = make_key(x, t);
+      sBin[i] = (unsigned short)mass_bin(x, M, cR);
+    }
+  __syncthreads();
+  auto get = [&](int i, unsigned long long& K, int& bin) {
+    if (staged) {
+      K = sKey[i];
+      bin = sBin[i];
+    } else {
+      const unsigned t = listed ? cand[i] : (unsigned)i;
+      const float x = load_logit<DT>(row, t);
+      K = make_key(x, t);
+      bin = mass_bin(x, M, cR);
+    }
+  };
+  unsigned long long kcut = 0, kept = Z, zk = Z, kk = 0;
+  bool ok = true;
+  if (bk >= 0) {  // top-k: the (top_k - count above)-th token of bin bk
+    unsigned long long in;
+    kk = radix_select(n, get, [&](unsigned long long, int bin) { return bin == bk; }, false,
+                      (unsigned long long)a.top_k - s_cbk, M, a, S, &in);
+    kcut = kk;
+    zk = me[bk] + in;
+    kept = zk;
+  }
+  if (a.top_p < 1.f) {
+    const unsigned long long th = top_p_threshold(a.top_p, zk);
+    // the last bin whose preceding mass is below the threshold (within the top-k set)
+    int lo = 0, hi = bk >= 0 ? bk : kWideBins - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (me[mid] < th) lo = mid; else hi = mid - 1;
+    }
+    const int bp = lo;
+    ok = bp == bk || (blo <= bp && bp <= bhi);
+    if (ok) {
+      unsigned long long in;
+      const unsigned long long ktop = kk;
+      kcut = radix_select(n, get,
+                          [&](unsigned long long K, int bin) { return bin == bp && (bp != bk || K >= ktop); },
+                          true, th - me[bp], M, a, S, &in);
+      kept = me[bp] + in;
+    }
+  }
+  if (a.min_p > 0.f) {  // a cut on the logit alone, after top-p
+    const unsigned long long kmin = (unsigned long long)(~kinv) << 32;
+    if (kmin > kcut) {
+      kcut = kmin;
+      kept = zmin;
+    }
+  }
+  __syncthreads();
+  // The list is consumed (past its capacity only the first kWideCandCap
+  // entries were written): every call leaves it zero.
+  for (int i = tid; i < (int)min(ncand, (unsigned)kWideCandCap); i += kThreads)
+    const_cast<unsigned*>(cand)[i] = 0;
+  if (tid == 0) {
+    if (!ok) {  // the selection's bins disagree (not expected): the request fails closed
+      set_status(a.ws.status, SPEC_ELIMIT);
+      atomicExch(&a.ws.sync[b].failed, 1);
+    }
+    wr->kcut = kcut;
+    wr->M = M;
+    wr->Z = (float)((double)kept * 0x1p-40);
+    wr->zmin = 0;
+    wr->kmin_inv = 0;
+    wr->ncand = 0;
+  }
+}
+
+// ------------------------------------------------------------------ 6
+template <int DT, bool VEC>
+__device__ __forceinline__ void wide_draw_item(const ChainArgs& a, int b, int part) {
+  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
+  __shared__ float sP[SPEC_MAX_DRAFT], sQ[SPEC_MAX_DRAFT], sU[SPEC_MAX_DRAFT + 1];
+  __shared__ int sJ, sBad, sLast, sFailed;
+  __shared__ unsigned long long sWT[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k;
+  const size_t row_bytes = (size_t)a.V * ES;
+  const WideRow* rec = a.ws.wrow + (size_t)b * a.rows;  // target rows 0..k, then draft rows
+
+  const int kraw = a.draft_lens ? a.draft_lens[b] : k;
+  const bool bad_len = kraw < 0 || kraw > k;
+  const int kb = bad_len ? 0 : kraw;
+  if (tid == 0) sBad = bad_len;
+  if (tid <= k)
+    sU[tid] = a.uniforms ? a.uniforms[(size_t)b * (k + 1) + tid]
+                         : philox_uniform(a.seeds[b], a.offsets[b], tid);
+  __syncthreads();
+  if (tid < kb) {  // p'(x_i) and q'(x_i) on the filtered rows
+    const int x = a.tokens[(size_t)b * k + tid];
+    if (x < 0 || x >= a.V) {
+      sBad = 1;
+    } else {
+      const float xp = load_logit<DT>(a.target + ((size_t)b * (k + 1) + tid) * row_bytes, x);
+      const float xq = load_logit<DT>(a.draft + ((size_t)b * k + tid) * row_bytes, x);
+      const WideRow rp = rec[tid], rq = rec[k + 1 + tid];
+      sP[tid] = make_key(xp, x) >= rp.kcut ? ex2(scaled(xp - rp.M, a.c_hi, a.c_lo)) / rp.Z : 0.f;
+      sQ[tid] = make_key(xq, x) >= rq.kcut ? ex2(scaled(xq - rq.M, a.c_hi, a.c_lo)) / rq.Z : 0.f;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // accept scan: r_i < p'_i / q'_i, q' == 0 accepts; j = first reject
+    unsigned rej[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      bool rj = false;
+      if (i < kb) {
+        const float ratio = sQ[i] > 0.f ? sP[i] / sQ[i] : INFINITY;
+        rj = !(sU[i] < ratio);
+      }
+      rej[h] = __ballot_sync(0xffffffffu, rj);
+    }
+    if (lane == 0)
+      sJ = sBad ? -1 : rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : kb;
+  }
+  __syncthreads();
+  const int j = sJ;
+  const char* prow = nullptr;
+  const char* qrow = nullptr;
+  float mp = 0.f, mq = 0.f, lam = 0.f;
+  CutMask cut{0, 0};
+  if (j >= 0) {
+    const WideRow rp = rec[j];
+    prow = a.target + ((size_t)b * (k + 1) + j) * row_bytes;
+    mp = rp.M;
+    cut.kp = rp.kcut;
+    if (j < kb) {
+      const WideRow rq = rec[k + 1 + j];
+      qrow = a.draft + ((size_t)b * k + j) * row_bytes;
+      mq = rq.M;
+      cut.kq = rq.kcut;
+      lam = rp.Z / rq.Z;  // max(0, p' - q') = max(0, e_p - lam e_q) / Z_p
+    }
+    const int c0 = part * a.cpc, c1 = min(a.nchunks, c0 + a.cpc);
+    const unsigned long long wt = chunk_sums<DT, VEC, false, true>(
+        a, prow, qrow, c0, c1, mp, mq, lam, a.ws.chunks + (size_t)b * a.nchunks, TokenMask{nullptr, 0}, cut);
+    if (lane == 0) sWT[warp] = wt;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long t = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) t += sWT[w];
+      a.ws.items[(size_t)b * a.nsplit2 + part] = t;
+    }
+  }
+  if (lane == 0) __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(&a.ws.sync[b].tick2, 1);
+    sLast = t == a.nsplit2 - 1;
+    if (sLast) {
+      a.ws.sync[b].tick2 = 0;
+      __threadfence();
+      sFailed = atomicExch(&a.ws.sync[b].failed, 0);
+    }
+  }
+  __syncthreads();
+  if (!sLast) return;
+
+  // Every item has read the request's row records: return them to zero.
+  for (int i = tid; i < a.rows * (int)(sizeof(WideRow) / 4); i += kThreads)
+    reinterpret_cast<unsigned*>(const_cast<WideRow*>(rec))[i] = 0;
+  int32_t* out = a.out_tokens + (size_t)b * (k + 1);
+  if (j < 0 || sFailed) {  // a bad draft token or length, or a failed cut: fail closed
+    for (int i = tid; i < a.nchunks; i += kThreads) a.ws.chunks[(size_t)b * a.nchunks + i] = 0;
+    for (int i = tid; i < a.nsplit2; i += kThreads) a.ws.items[(size_t)b * a.nsplit2 + i] = 0;
+    for (int i = tid; i <= k; i += kThreads) out[i] = -1;
+    if (a.out_probs)
+      for (int i = tid; i < 2 * k; i += kThreads) a.out_probs[(size_t)b * 2 * k + i] = NAN;
+    if (tid == 0) {
+      a.out_n[b] = -1;
+      set_status(a.ws.status, j < 0 ? SPEC_EBADINDEX : SPEC_ELIMIT);
+    }
+    return;
+  }
+  if (a.out_probs && tid < k) {  // padded positions are not verified: NaN
+    a.out_probs[((size_t)b * k + tid) * 2] = tid < kb ? sP[tid] : NAN;
+    a.out_probs[((size_t)b * k + tid) * 2 + 1] = tid < kb ? sQ[tid] : NAN;
+  }
+  const double u = (double)sU[kb];
+  const int tok = draw_token<DT, VEC, false, true>(a, b, prow, qrow, mp, mq, lam, u, TokenMask{nullptr, 0}, cut);
+  for (int i = tid; i <= k; i += kThreads)
+    out[i] = i < j ? a.tokens[(size_t)b * k + i] : (i == j ? tok : -1);
+  if (tid == 0) {
+    a.out_n[b] = j;
+    if (a.seq_lens) a.seq_lens[b] += j + 1;
+  }
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) wide_draw_kernel(const ChainArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int items = a.B * a.nsplit2;
+  for (int h = blockIdx.x; h < items; h += gridDim.x) {
+    const int b = h / a.nsplit2;
+    wide_draw_item<DT, VEC>(a, b, h - b * a.nsplit2);
+    __syncthreads();
+  }
+}
+
+template <class K>
+cudaError_t launch_dep(K kernel, long grid, const ChainArgs& a, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+template <int DT, bool VEC>
+cudaError_t wide_draw_grid(int* grid) {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wide_draw_kernel<DT, VEC>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    cached[dev] = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  *grid = cached[dev];
+  return cudaSuccess;
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
+  int slots = 0;
+  cudaError_t e = wide_draw_grid<DT, VEC>(&slots);
+  if (e != cudaSuccess) return e;
+  ChainArgs a = args;
+  while ((long)a.B * a.nsplit2 > slots && a.cpc < a.nchunks) {  // as the chain's draw
+    a.cpc *= 2;
+    a.nsplit2 = ceil_div(a.nchunks, a.cpc);
+  }
+  const long rows = (long)a.B * a.rows;
+  const long slices = rows * a.nsplit;
+  const long items = (long)a.B * a.nsplit2;
+  chain_rowstats_kernel<DT, VEC><<<(unsigned)slices, kThreads, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.top_k > 0)
+    e = launch_dep(wide_hist_kernel<DT, VEC, true>, slices, a, st);
+  else
+    e = launch_dep(wide_hist_kernel<DT, VEC, false>, slices, a, st);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_dep(wide_bins_kernel, rows, a, st)) != cudaSuccess) return e;
+  if ((e = launch_dep(wide_cand_kernel<DT, VEC>, slices, a, st)) != cudaSuccess) return e;
+  if ((e = launch_dep(wide_cut_kernel<DT>, rows, a, st)) != cudaSuccess) return e;
+  return launch_dep(wide_draw_kernel<DT, VEC>, items < slots ? items : slots, a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_wide(const ChainArgs& a, int dtype, bool vec, cudaStream_t st) {
+  if (dtype == SPEC_BF16)
+    return vec ? launch_wide_t<SPEC_BF16, true>(a, st) : launch_wide_t<SPEC_BF16, false>(a, st);
+  return vec ? launch_wide_t<SPEC_F32, true>(a, st) : launch_wide_t<SPEC_F32, false>(a, st);
+}
+
+}  // namespace sv

@@ -48,6 +48,17 @@ def test_workspace_size_and_status_strings(libso):
     assert a > b > 0 and a % 256 == 0
     assert libso.spec_status_string(-2) == b"token or node id out of range"
     assert libso.spec_status_string(0) == b"ok"
+    # filtered: kept lists up to SPEC_MAX_TOPK, per-row cuts beyond (and
+    # without top-k): the chain's layout plus 24 KB of histogram, a 64-byte
+    # record and a 16 KB candidate list per row
+    f = libso.spec_workspace_size_filtered
+    f.restype = ctypes.c_size_t
+    rows = 64 * 15
+    assert f(64, 7, 128256, -1) == 0
+    wide = f(64, 7, 128256, 0)
+    assert wide == f(64, 7, 128256, 257) == f(64, 7, 128256, 100000)
+    assert wide >= a + rows * (2048 * 12 + 64 + 4096 * 4)
+    assert 0 < f(64, 7, 128256, 256) != wide
 
 
 def test_invalid_arguments_rejected_before_launch(libso):
