@@ -85,9 +85,9 @@ struct WideRow {
   unsigned kmin_inv;        // ~ the smallest order key (ord32) among those tokens
   unsigned ncand;           // tokens appended to the row's candidate list
   int bk, blo, bhi;         // the top-k bin, the top-p bin range (-1: none)
-  int pad0;
+  int b0;                   // bins >= b0 are merged into the last bin (light tokens)
   unsigned long long kcut;  // token t is kept iff make_key(x_t, t) >= kcut
-  float M, Z;               // row maximum and kept mass (2^(c(x - M)) units)
+  float M, Z;               // row maximum and (after the cut) kept mass, 2^(c(x - M)) units
   int pad1[4];
 };
 static_assert(sizeof(WideRow) == 64, "WideRow layout");

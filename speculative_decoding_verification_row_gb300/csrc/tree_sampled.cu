@@ -36,6 +36,8 @@ __device__ __forceinline__ void tree_item(const ChainArgs& a, int b, int part) {
   __shared__ short sPath[kTreeStage];
   __shared__ float sEdge[kTreeStage];  // [p * L + d]: logit of paths[p][d+1]'s token in row paths[p][d]
   __shared__ int sPrefix[SPEC_MAX_PATH_LEN];
+  __shared__ unsigned sBits[SPEC_MAX_TREE_NODES / 32];  // the walk's candidate set
+  __shared__ short sCandE[SPEC_MAX_TREE_NODES];        // a candidate's edge (index into sEdge)
   __shared__ int sLast, sFailed, sNode, sDepth, sNMask, sBest;
   __shared__ unsigned long long sWT[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -67,54 +69,32 @@ __device__ __forceinline__ void tree_item(const ChainArgs& a, int b, int part) {
   }
 
   // Merge the slice statistics of every row (all of them, also for a bad
-  // request, so that its words are written before they are cleared): warp w
-  // takes rows w, w + 8, ...; it issues the loads of four rows' words before
-  // using any, waiting only for words still 0.
+  // request, so that its words are written before they are cleared): thread
+  // r takes row r, issues the loads of all its words before using any
+  // (waiting only for words still 0), then merges them in slice order.
   const unsigned long long* sb = a.ws.stats + (size_t)b * N * a.nsplit;
   bool to = false;  // a wait of this thread ran out
-  for (int r0 = warp; r0 < N; r0 += 4 * kWarps) {
-    unsigned long long v[4][2];
+  for (int r = tid; r < N; r += kThreads) {
+    const unsigned long long* pr = sb + (size_t)r * a.nsplit;
+    float m = -INFINITY;
+    for (int u0 = 0; u0 < a.nsplit; u0 += 16) {
+      unsigned long long v[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
+      for (int q = 0; q < 16; ++q) v[q] = u0 + q < a.nsplit ? ld_relaxed_u64(pr + u0 + q) : kNoStats;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int u = lane + 32 * h;
-        v[q][h] = (r < N && u < a.nsplit) ? ld_relaxed_u64(sb + (size_t)r * a.nsplit + u) : kNoStats;
+      for (int q = 0; q < 16; ++q) {
+        if (!v[q]) v[q] = wait_stats(a, pr + u0 + q, &to);  // only a present slice reads 0
+        m = fmaxf(m, stats_unpack(v[q]).x);
       }
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (!v[q][h])  // only a present slice reads 0
-          v[q][h] = wait_stats(a, sb + (size_t)(r0 + q * kWarps) * a.nsplit + lane + 32 * h, &to);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
-      if (r >= N) continue;  // the same for the whole warp
-      const unsigned long long* pr = sb + (size_t)r * a.nsplit;
-      const float2 e0 = stats_unpack(v[q][0]), e1 = stats_unpack(v[q][1]);
-      float m = fmaxf(e0.x, e1.x);
-      for (int u = lane + 64; u < a.nsplit; u += 32)
-        m = fmaxf(m, stats_unpack(wait_stats(a, pr + u, &to)).x);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      float sum = 0.f;
-      if (m != -INFINITY) {
-        if (e0.y > 0.f) sum += e0.y * ex2(scaled(e0.x - m, a.c_hi, a.c_lo));
-        if (e1.y > 0.f) sum += e1.y * ex2(scaled(e1.x - m, a.c_hi, a.c_lo));
-        for (int u = lane + 64; u < a.nsplit; u += 32) {
-          const float2 e = stats_unpack(ld_relaxed_u64(pr + u));
-          if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - m, a.c_hi, a.c_lo));
-        }
+    float sum = 0.f;
+    if (m != -INFINITY)
+      for (int u = 0; u < a.nsplit; ++u) {
+        const float2 e = stats_unpack(ld_relaxed_u64(pr + u));  // written: seen above
+        if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - m, a.c_hi, a.c_lo));
       }
-      sum = warp_sum(sum);
-      if (lane == 0) {
-        sM[r] = m;
-        sS[r] = sum;
-      }
-    }
+    sM[r] = m;
+    sS[r] = sum;
   }
   // A statistics word that never arrived fails the request closed (the flag
   // reaches the finishing item through the ticket).
@@ -124,58 +104,88 @@ __device__ __forceinline__ void tree_item(const ChainArgs& a, int b, int part) {
 
   // The walk, in warp 0 (uniform across its lanes).  Lane l holds bit j for
   // path l + 32 j: set while the path's first d + 1 entries are the accepted
-  // prefix.  At depth d the candidates are those paths' entries d + 1, taken
-  // in increasing node id; w_c / S_rest is the residual probability of the
-  // candidate's token (S_rest: the row's S less the rejected tokens' weights).
+  // prefix.  At depth d the candidates are those paths' entries d + 1 (a
+  // bitmap over node ids gives them in increasing id), tried 32 at a time:
+  // lane i takes the i-th, with weight w_i = 2^(c(x - M)) of its edge logit
+  // (0 when an earlier candidate at this node carried the same token, which
+  // already left the residual), and S_rest before it is the row's S less the
+  // weights of the candidates before it (all rejected if it is reached); the
+  // first lane with u[c] < w_i / S_rest_i is the accepted child.
   if (warp == 0 && !skip) {
     unsigned long long alive = 0;
-    for (int j = 0; j < 64; ++j) {
+    for (int j = 0; j < (P + 31) / 32; ++j) {
       const int p = lane + 32 * j;
       if (p < P && sPath[p * L] == 0) alive |= 1ull << j;
     }
+    const int nwords = (N + 31) / 32;
     int node = 0, d = 0, nmask = 0;
     if (lane == 0) sPrefix[0] = 0;
     while (d + 1 < L) {
+      if (lane < nwords) sBits[lane] = 0u;
+      __syncwarp();
+      for (unsigned long long bits = alive; bits; bits &= bits - 1) {
+        const int p = lane + 32 * (__ffsll((long long)bits) - 1);
+        const int nx = sPath[p * L + d + 1];
+        if (nx >= 0) {
+          atomicOr(&sBits[nx >> 5], 1u << (nx & 31));
+          sCandE[nx] = (short)(p * L + d);  // any alive path: the same edge logit
+        }
+      }
+      __syncwarp();
+      const unsigned word = lane < nwords ? sBits[lane] : 0u;
+      const int cnt = __popc(word);
+      int excl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, excl, o);
+        if (lane >= o) excl += t;
+      }
+      const int total = __shfl_sync(0xffffffffu, excl, 31);
+      excl -= cnt;
       const float M = sM[node];
       float Srest = sS[node];
       nmask = 0;
-      int last = -1, next = -1;
-      for (;;) {
-        int mn = INT_MAX;
-        for (unsigned long long bits = alive; bits; bits &= bits - 1) {
-          const int p = lane + 32 * (__ffsll((long long)bits) - 1);
-          const int nx = sPath[p * L + d + 1];
-          if (nx > last && nx < mn) mn = nx;
+      int next = -1;
+      for (int base = 0; base < total; base += 32) {
+        const int idx = base + lane;
+        int wsel = 0;  // the word holding candidate idx: the last with excl <= idx
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+          const int e = __shfl_sync(0xffffffffu, excl, wsel + step);
+          if (wsel + step < nwords && e <= idx) wsel += step;
         }
-        const int c = __reduce_min_sync(0xffffffffu, mn);
-        if (c == INT_MAX) break;  // no candidate left
-        float xe = 0.f;
-        bool has = false;
-        for (unsigned long long bits = alive; bits && !has; bits &= bits - 1) {
-          const int p = lane + 32 * (__ffsll((long long)bits) - 1);
-          if (sPath[p * L + d + 1] == c) {
-            xe = sEdge[p * L + d];
-            has = true;
-          }
+        const unsigned wv = __shfl_sync(0xffffffffu, word, wsel);
+        const int rank = idx - __shfl_sync(0xffffffffu, excl, wsel);
+        const bool valid = idx < total;
+        const int c = valid ? 32 * wsel + (int)__fns(wv, 0, rank + 1) : -1;
+        const int tc = valid ? sTok[c] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, valid ? tc : -2 - lane);
+        bool gone = (same & ((1u << lane) - 1u)) != 0u;
+        for (int i = 0; i < nmask && valid && !gone; ++i) gone = sMask[i] == tc;
+        const float w = (valid && !gone) ? ex2(scaled(sEdge[sCandE[c]] - M, a.c_hi, a.c_lo)) : 0.f;
+        float before = w;  // exclusive prefix of the weights
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float t = __shfl_up_sync(0xffffffffu, before, o);
+          if (lane >= o) before += t;
         }
-        const unsigned who = __ballot_sync(0xffffffffu, has);
-        xe = __shfl_sync(0xffffffffu, xe, __ffs(who) - 1);
-        const int tc = sTok[c];
-        bool gone = false;  // its token already left the residual (a repeated sibling token)
-        for (int i = 0; i < nmask; ++i) gone |= sMask[i] == tc;
-        const float w = gone ? 0.f : ex2(scaled(xe - M, a.c_hi, a.c_lo));
-        const float ratio = Srest > 0.f ? w / Srest : 0.f;
-        if (sU[c] < ratio) {
-          next = c;
+        const float batch = __shfl_sync(0xffffffffu, before, 31);
+        before -= w;
+        const float sr = Srest - before;
+        const bool acc = valid && !gone && sr > 0.f && sU[c] < w / sr;
+        const unsigned accm = __ballot_sync(0xffffffffu, acc);
+        const int first = accm ? __ffs(accm) - 1 : 32;
+        // the rejected candidates' tokens (before the accepted one) leave the residual
+        const bool rej = valid && !gone && lane < first;
+        const unsigned rejm = __ballot_sync(0xffffffffu, rej);
+        if (rej) sMask[nmask + __popc(rejm & ((1u << lane) - 1u))] = tc;
+        nmask += __popc(rejm);
+        __syncwarp();
+        if (accm) {
+          next = __shfl_sync(0xffffffffu, c, first);
           break;
         }
-        if (!gone) {
-          Srest -= w;
-          if (lane == 0) sMask[nmask] = tc;
-          ++nmask;
-          __syncwarp();
-        }
-        last = c;
+        Srest -= batch;
       }
       if (next < 0) break;  // final draw at this node
       unsigned long long keep = 0;
@@ -301,10 +311,16 @@ cudaError_t launch_tree_sampled_t(const ChainArgs& args, cudaStream_t st) {
   int slots = 0;
   cudaError_t e = tree_slots<DT, VEC>(&slots);
   if (e != cudaSuccess) return e;
-  // Draw items of 64 chunks, doubled until the items fit in one wave.
+  // Draw items of 64 chunks, doubled until the items fit in one wave, or
+  // halved (down to 32) while twice as many still do: each item's chunk
+  // sums are then one round of loads per warp.
   ChainArgs a = args;
   while ((long)a.B * a.nsplit2 > slots && a.cpc < a.nchunks) {
     a.cpc *= 2;
+    a.nsplit2 = ceil_div(a.nchunks, a.cpc);
+  }
+  while (a.cpc > 32 && (long)a.B * ceil_div(a.nchunks, a.cpc / 2) <= slots) {
+    a.cpc /= 2;
     a.nsplit2 = ceil_div(a.nchunks, a.cpc);
   }
   const long g1 = (long)a.B * a.rows * a.nsplit;

@@ -17,7 +17,12 @@
 //      floor(32 c (M - x)) (2048 bins of 1/32 of a log2 unit, the last
 //      holding everything below) into a shared-memory histogram, then into
 //      the row's (masses; counts too when top-k cuts); the mass and the
-//      smallest logit key of the tokens with e_t >= min_p.
+//      smallest logit key of the tokens with e_t >= min_p.  Without a top-k
+//      cut only tokens above a depth D0 get their own bin: the V tokens
+//      below it weigh at most V 2^-D0 = (1 - top_p) Z / 2, so the top-p cut
+//      cannot fall among them; their mass is summed in registers into the
+//      last bin (on the headline shape D0 leaves ~13 % of the tokens to the
+//      shared-memory atomics).
 //   3. wide_bins_kernel, one CTA per row: prefix sums over the bins give
 //      the bin where the top-k count is reached and the range of bins the
 //      top-p threshold can fall in (the top-k mass is known to within the
@@ -55,13 +60,14 @@ __device__ __forceinline__ unsigned long long mass_fix(float x, float M, float c
   return to_fixed(ex2(scaled(x - M, c_hi, c_lo)) * 256.f);
 }
 
-// The row's maximum from its slices' pass-1 words (all written by now).
-__device__ float row_max(const ChainArgs& a, int rr) {
-  __shared__ float s_m[kWarps];
+// The row's maximum and softmax sum (relative to it) from its slices'
+// pass-1 words (all written by now); every CTA of the row gets the same.
+__device__ float row_stats(const ChainArgs& a, int rr, float* Z) {
+  __shared__ float s_m[kWarps], s_s[kWarps];
   const int tid = threadIdx.x;
+  const unsigned long long* sw = a.ws.stats + (size_t)rr * a.nsplit;
   float m = -INFINITY;
-  for (int u = tid; u < a.nsplit; u += kThreads)
-    m = fmaxf(m, stats_unpack(ld_relaxed_u64(a.ws.stats + (size_t)rr * a.nsplit + u)).x);
+  for (int u = tid; u < a.nsplit; u += kThreads) m = fmaxf(m, stats_unpack(ld_relaxed_u64(sw + u)).x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((tid & 31) == 0) s_m[tid >> 5] = m;
@@ -69,8 +75,26 @@ __device__ float row_max(const ChainArgs& a, int rr) {
   float M = s_m[0];
 #pragma unroll
   for (int i = 1; i < kWarps; ++i) M = fmaxf(M, s_m[i]);
+  float sum = 0.f;
+  if (M != -INFINITY)
+    for (int u = tid; u < a.nsplit; u += kThreads) {
+      const float2 e = stats_unpack(ld_relaxed_u64(sw + u));
+      if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - M, a.c_hi, a.c_lo));
+    }
+  sum = warp_sum(sum);
+  if ((tid & 31) == 0) s_s[tid >> 5] = sum;
   __syncthreads();
+  float S = 0.f;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) S += s_s[i];
+  *Z = S;
   return M == -INFINITY ? 0.f : M;
+}
+
+// A token's bin with the row's light tokens (bins >= b0) in the last bin.
+__device__ __forceinline__ int wide_bin(float x, float M, float cR, int b0) {
+  const int b = mass_bin(x, M, cR);
+  return b < b0 ? b : kWideBins - 1;
 }
 
 // Block-wide exclusive prefix sum of one value per thread (thread order);
@@ -101,7 +125,7 @@ __device__ __forceinline__ unsigned long long top_p_threshold(float top_p, unsig
 
 // ------------------------------------------------------------------ 2
 template <int DT, bool VEC, bool COUNT>
-__global__ void __launch_bounds__(kThreads) wide_hist_kernel(const ChainArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) wide_hist_kernel(const ChainArgs a) {
   __shared__ unsigned long long hm[kWideBins];
   __shared__ unsigned hc[COUNT ? kWideBins : 1];
   __shared__ unsigned long long s_z[kWarps];
@@ -127,10 +151,27 @@ __global__ void __launch_bounds__(kThreads) wide_hist_kernel(const ChainArgs a) 
     const int v = vbeg + tid + u * kThreads;
     if (v < vend) IO::load(row, v, w[u]);
   }
-  const float M = row_max(a, rr);  // also orders the clearing above before the adds
+  float Zs;
+  const float M = row_stats(a, rr, &Zs);  // also orders the clearing above before the adds
   const float cR = a.c_rn * (float)kWideBinsPerLog2;
+  // Bins from b0 on take the light tokens, summed in registers (no top-k
+  // cut: the top-p cut lies above depth D0; min_p alone needs no bins).
+  int b0 = kWideBins;
+  if (!COUNT) {
+    if (a.top_p < 1.f) {
+      const float D0 = log2f((float)a.V / ((1.f - a.top_p) * fmaxf(Zs, 1.f))) + 1.f;
+      const float fb = ceilf(D0 * (float)kWideBinsPerLog2) + 1.f;
+      b0 = fb < 1.f ? 1 : (fb >= (float)(kWideBins - 1) ? kWideBins - 1 : (int)fb);
+    } else {
+      b0 = 0;
+    }
+  }
+  if (s == 0 && tid == 0) {  // every slice of the row computes the same
+    a.ws.wrow[rr].b0 = b0;
+    a.ws.wrow[rr].M = M;
+  }
   const bool use_min_p = a.min_p > 0.f;
-  unsigned long long zmin = 0;
+  unsigned long long zmin = 0, light = 0;
   unsigned kinv = 0;
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
@@ -142,18 +183,28 @@ __global__ void __launch_bounds__(kThreads) wide_hist_kernel(const ChainArgs a) 
       const float e = ex2(scaled(x[i] - M, a.c_hi, a.c_lo));
       const unsigned long long f = to_fixed(e * 256.f);
       const int bin = mass_bin(x[i], M, cR);
-      if (f) atomicAdd(&hm[bin], f);
-      if (COUNT) atomicAdd(&hc[bin], 1u);
+      if (bin < b0) {
+        if (f) atomicAdd(&hm[bin], f);
+      } else {
+        light += f;
+      }
+      if (COUNT) atomicAdd(&hc[bin], 1u);  // b0 = kWideBins: every token has its bin
       if (use_min_p && e >= a.min_p) {
         zmin += f;
         kinv = max(kinv, ~ord32(x[i]));
       }
     }
   }
-  __syncthreads();
   unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
   unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
-  for (int i = tid; i < kWideBins; i += kThreads) {
+  if (b0 < kWideBins) {  // the light tokens' mass, into the last bin
+    unsigned long long tot;
+    block_excl_u64(light, &tot);  // (its barriers also order the adds above)
+    if (tid == 0 && tot) atomicAdd(gh + kWideBins - 1, tot);
+  } else {
+    __syncthreads();
+  }
+  for (int i = tid; i < min(b0, kWideBins); i += kThreads) {
     if (hm[i]) atomicAdd(gh + i, hm[i]);
     if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
   }
@@ -254,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) 
 
 // ------------------------------------------------------------------ 4
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) wide_cand_kernel(const ChainArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) wide_cand_kernel(const ChainArgs a) {
   __shared__ unsigned s_base;
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x;
@@ -276,7 +327,8 @@ __global__ void __launch_bounds__(kThreads) wide_cand_kernel(const ChainArgs a) 
     const int v = vbeg + tid + u * kThreads;
     if (v < vend) IO::load(row, v, w[u]);
   }
-  const float M = row_max(a, rr);
+  const float M = wr->M;
+  const int b0 = wr->b0;
   const float cR = a.c_rn * (float)kWideBinsPerLog2;
   unsigned long long sel = 0;  // bit u * EPV + i: element i of vector u is listed
 #pragma unroll
@@ -286,7 +338,7 @@ __global__ void __launch_bounds__(kThreads) wide_cand_kernel(const ChainArgs a) 
     IO::unpack(w[u], x);
 #pragma unroll
     for (int i = 0; i < IO::EPV; ++i) {
-      const int bin = mass_bin(x[i], M, cR);
+      const int bin = wide_bin(x[i], M, cR, b0);
       if (bin == bk || (blo <= bin && bin <= bhi)) sel |= 1ull << (u * IO::EPV + i);
     }
   }
@@ -402,7 +454,8 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
   const unsigned ncand = wr->ncand;
   const unsigned long long zmin = wr->zmin;
   const unsigned kinv = wr->kmin_inv;
-  const float M = row_max(a, rr);
+  const float M = wr->M;
+  const int b0 = wr->b0;
   // the statistics words are consumed: every call leaves them zero
   for (int u = tid; u < a.nsplit; u += kThreads) a.ws.stats[(size_t)rr * a.nsplit + u] = 0;
   // Prefix masses of the bins (and the count before the top-k bin); the
@@ -447,7 +500,7 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
       const unsigned t = cand[i];
       const float x = load_logit<DT>(row, t);
       sKey[i] = make_key(x, t);
-      sBin[i] = (unsigned short)mass_bin(x, M, cR);
+      sBin[i] = (unsigned short)wide_bin(x, M, cR, b0);
     }
   __syncthreads();
   auto get = [&](int i, unsigned long long& K, int& bin) {
@@ -458,7 +511,7 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
       const unsigned t = listed ? cand[i] : (unsigned)i;
       const float x = load_logit<DT>(row, t);
       K = make_key(x, t);
-      bin = mass_bin(x, M, cR);
+      bin = wide_bin(x, M, cR, b0);
     }
   };
   unsigned long long kcut = 0, kept = Z, zk = Z, kk = 0;
