@@ -75,8 +75,9 @@ struct WsLayout {
 // Exact filtering of any kept-set size (top-p or min_p without top-k, top-k
 // above SPEC_MAX_TOPK): each row's mass histogram over kWideBins bins of
 // 1/kWideBinsPerLog2 of a log2 unit below the row maximum (the last bin
-// holds the rest), its candidate list (the tokens of the bins a cut can fall
-// in) and its record.
+// holds the rest; once the bins are chosen it holds exclusive prefix sums),
+// its candidate list (the tokens of the bins a cut can fall in) and its
+// record.
 constexpr int kWideBinsPerLog2 = 32;
 constexpr int kWideBins = 2048;
 constexpr int kWideCandCap = 4096;  // candidates listed per row; a row with more rescans itself
@@ -88,7 +89,8 @@ struct WideRow {
   int b0;                   // bins >= b0 are merged into the last bin (light tokens)
   unsigned long long kcut;  // token t is kept iff make_key(x_t, t) >= kcut
   float M, Z;               // row maximum and (after the cut) kept mass, 2^(c(x - M)) units
-  int pad1[4];
+  unsigned long long ztot;  // the row's total fixed-point mass
+  int pad1[2];
 };
 static_assert(sizeof(WideRow) == 64, "WideRow layout");
 

@@ -124,9 +124,13 @@ __device__ __forceinline__ unsigned long long top_p_threshold(float top_p, unsig
 }
 
 // ------------------------------------------------------------------ 2
-template <int DT, bool VEC, bool COUNT>
-__global__ void __launch_bounds__(kThreads, 5) wide_hist_kernel(const ChainArgs a) {
-  __shared__ unsigned long long hm[kWideBins];
+// BINS = false (min_p alone): no histogram, only the min_p mass and key.
+template <int DT, bool VEC, bool COUNT, bool MINP, bool BINS>
+__global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs a) {
+  // The slice's bin masses in three 14-bit parts of the 2^-40 fixed point
+  // (32-bit shared adds; a slice holds at most 2^14 tokens, so each part's
+  // sum stays below 2^28), recombined exactly at the end.
+  __shared__ unsigned hm[3][kWideBins];
   __shared__ unsigned hc[COUNT ? kWideBins : 1];
   __shared__ unsigned long long s_z[kWarps];
   __shared__ unsigned s_k[kWarps];
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 5) wide_hist_kernel(const ChainArgs 
   int b, r;
   slice_row(a, rr, b, r);
   for (int i = tid; i < kWideBins; i += kThreads) {
-    hm[i] = 0;
+    hm[0][i] = hm[1][i] = hm[2][i] = 0u;
     if (COUNT) hc[i] = 0;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -149,7 +153,12 @@ __global__ void __launch_bounds__(kThreads, 5) wide_hist_kernel(const ChainArgs 
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
     const int v = vbeg + tid + u * kThreads;
-    if (v < vend) IO::load(row, v, w[u]);
+    if (v < vend) {
+      IO::load(row, v, w[u]);
+    } else {  // past the row: -inf (no mass; not counted, see below)
+#pragma unroll
+      for (int q = 0; q < IO::NW; ++q) w[u][q] = (VEC && DT == SPEC_BF16) ? 0xff80ff80u : 0xff800000u;
+    }
   }
   float Zs;
   const float M = row_stats(a, rr, &Zs);  // also orders the clearing above before the adds
@@ -170,45 +179,98 @@ __global__ void __launch_bounds__(kThreads, 5) wide_hist_kernel(const ChainArgs 
     a.ws.wrow[rr].b0 = b0;
     a.ws.wrow[rr].M = M;
   }
-  const bool use_min_p = a.min_p > 0.f;
-  unsigned long long zmin = 0, light = 0;
+  const float fb0 = (float)b0;
+  unsigned long long zmin = 0;
   unsigned kinv = 0;
+  float light = 0.f;  // light tokens' mass: each < 2^-D0, summed in fp32 per thread
+  // Heavy tokens of each vector (8 or 4 per lane) are packed per warp by
+  // ballot into a shared queue as (bin, mass) and added to the histogram
+  // after the vector, one per lane: a warp-wide 64-bit shared add costs
+  // about the same however few of its lanes are active, so one add per 32
+  // heavy tokens instead of one per token position.
+  // (with a top-k count cut every token is heavy: no queue, direct adds)
+  __shared__ unsigned qbin[COUNT ? 1 : kWarps][COUNT ? 1 : 32 * IO::EPV];
+  __shared__ float qe[COUNT ? 1 : kWarps][COUNT ? 1 : 32 * IO::EPV];
+  auto add_mass = [&](unsigned bin, float e) {
+    const unsigned long long f = to_fixed(e * 256.f);  // < 2^41
+    if (f) {
+      atomicAdd(&hm[0][bin], (unsigned)f & 0x3fffu);
+      atomicAdd(&hm[1][bin], (unsigned)(f >> 14) & 0x3fffu);
+      atomicAdd(&hm[2][bin], (unsigned)(f >> 28));
+    }
+  };
+  const unsigned below = (1u << lane) - 1u;
+  const float2 nM = make_float2(-M, -M), chi = make_float2(a.c_hi, a.c_hi), clo = make_float2(a.c_lo, a.c_lo),
+               ncR = make_float2(-cR, -cR);
 #pragma unroll
   for (int u = 0; u < kVecPerThread; ++u) {
-    if (vbeg + tid + u * kThreads >= vend) continue;
     float x[IO::EPV];
     IO::unpack(w[u], x);
+    int qn = 0;  // warp-uniform
 #pragma unroll
-    for (int i = 0; i < IO::EPV; ++i) {
-      const float e = ex2(scaled(x[i] - M, a.c_hi, a.c_lo));
-      const unsigned long long f = to_fixed(e * 256.f);
-      const int bin = mass_bin(x[i], M, cR);
-      if (bin < b0) {
-        if (f) atomicAdd(&hm[bin], f);
-      } else {
-        light += f;
+    for (int i = 0; i < IO::EPV; i += 2) {
+      // two tokens at a time in packed fp32x2: d = x - M, the exponent
+      // scaled(d) = d c_hi + d c_lo and the bin (M - x) cR = d (-cR), each
+      // the same rounding as the scalar operations of mass_fix / mass_bin
+      const float x1 = i + 1 < IO::EPV ? x[i + 1 < IO::EPV ? i + 1 : i] : -INFINITY;  // (EPV may be 1)
+      const float2 d = add2(make_float2(x[i], x1), nM);
+      const float2 y = fma2(d, chi, mul2(d, clo));
+      const float2 fb = mul2(d, ncR);
+      const float e2[2] = {ex2(y.x), ex2(y.y)};
+      const float fbin2[2] = {fb.x, fb.y};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (i + h >= IO::EPV) break;
+        const float e = e2[h], fbin = fbin2[h];
+        if constexpr (MINP) {
+          if (e >= a.min_p) {
+            zmin += to_fixed(e * 256.f);
+            kinv = max(kinv, ~ord32(h ? x1 : x[i]));
+          }
+        }
+        if constexpr (!BINS) {
+          // min_p alone: the cut is the smallest key with e >= min_p
+        } else if constexpr (COUNT) {  // every token of the row is counted
+          if (vbeg + tid + u * kThreads < vend) {
+            const unsigned bin = (unsigned)(int)fminf(fbin, (float)(kWideBins - 1));
+            add_mass(bin, e);
+            atomicAdd(&hc[bin], 1u);
+          }
+        } else {  // past the row: x = -inf, so fbin = +inf, light, no mass
+          const bool heavy = fbin < fb0;
+          light += heavy ? 0.f : e;
+          const unsigned hmask = __ballot_sync(0xffffffffu, heavy);
+          if (heavy) {
+            const int slot = qn + __popc(hmask & below);
+            qbin[warp][slot] = __float_as_uint(fbin);
+            qe[warp][slot] = e;
+          }
+          qn += __popc(hmask);
+        }
       }
-      if (COUNT) atomicAdd(&hc[bin], 1u);  // b0 = kWideBins: every token has its bin
-      if (use_min_p && e >= a.min_p) {
-        zmin += f;
-        kinv = max(kinv, ~ord32(x[i]));
-      }
+    }
+    if constexpr (!COUNT && BINS) {
+      __syncwarp();
+      for (int q = lane; q < qn; q += 32)
+        add_mass((unsigned)(int)__uint_as_float(qbin[warp][q]), qe[warp][q]);  // fbin < b0 <= 2047
+      __syncwarp();
     }
   }
   unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
   unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
   if (b0 < kWideBins) {  // the light tokens' mass, into the last bin
     unsigned long long tot;
-    block_excl_u64(light, &tot);  // (its barriers also order the adds above)
+    block_excl_u64(to_fixed(light * 256.f), &tot);  // (its barriers also order the adds above)
     if (tid == 0 && tot) atomicAdd(gh + kWideBins - 1, tot);
   } else {
     __syncthreads();
   }
   for (int i = tid; i < min(b0, kWideBins); i += kThreads) {
-    if (hm[i]) atomicAdd(gh + i, hm[i]);
+    const unsigned long long m = ((unsigned long long)hm[2][i] << 28) + ((unsigned long long)hm[1][i] << 14) + hm[0][i];
+    if (m) atomicAdd(gh + i, m);
     if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
   }
-  if (use_min_p) {
+  if (MINP) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       zmin += __shfl_xor_sync(0xffffffffu, zmin, o);
@@ -247,8 +309,8 @@ __global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
-  const unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins + kBinsPerThread * tid;
-  const unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins + kBinsPerThread * tid;
   const bool count_cut = a.top_k > 0;
   unsigned long long m[kBinsPerThread], tm = 0, tc = 0;
   unsigned c[kBinsPerThread];
@@ -294,18 +356,54 @@ __global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) 
       mb += m[j];
     }
   }
+  // The bins become their exclusive prefix sums (mass, and count when top-k
+  // cuts): the cut kernel reads the few it needs.
+  {
+    unsigned long long mb = pm, cb = pc;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      gh[j] = mb;
+      if (count_cut) gc[j] = (unsigned)cb;
+      mb += m[j];
+      cb += c[j];
+    }
+  }
   __syncthreads();
   if (tid == 0) {
     WideRow* wr = a.ws.wrow + rr;
     wr->bk = s_bk;
     wr->blo = s_blo;
     wr->bhi = s_blo >= 0 ? s_bhi : -1;
+    wr->ztot = Z;
   }
 }
 
 // ------------------------------------------------------------------ 4
+// The bits of this thread's tokens whose logits lie in [lo1, hi1] (or
+// [lo2, hi2] when TWO); v0 is its first vector.
+template <int DT, bool VEC, bool TWO>
+__device__ __forceinline__ unsigned long long listed_bits(const uint32_t (&w)[kVecPerThread][Io<DT, VEC>::NW],
+                                                          int v0, int vend, float lo1, float hi1, float lo2,
+                                                          float hi2) {
+  using IO = Io<DT, VEC>;
+  unsigned long long sel = 0;
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    if (v0 + u * kThreads >= vend) continue;
+    float x[IO::EPV];
+    IO::unpack(w[u], x);
+#pragma unroll
+    for (int i = 0; i < IO::EPV; ++i) {
+      bool in = x[i] >= lo1 && x[i] <= hi1;
+      if (TWO) in = in || (x[i] >= lo2 && x[i] <= hi2);
+      if (in) sel |= 1ull << (u * IO::EPV + i);
+    }
+  }
+  return sel;
+}
+
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 6) wide_cand_kernel(const ChainArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) wide_cand_kernel(const ChainArgs a) {
   __shared__ unsigned s_base;
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x;
@@ -315,9 +413,6 @@ __global__ void __launch_bounds__(kThreads, 6) wide_cand_kernel(const ChainArgs 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
-  WideRow* wr = a.ws.wrow + rr;
-  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi;
-  if (bk < 0 && blo < 0) return;  // no cut falls inside a bin: nothing to list
   const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
   const int vbeg = s * a.vps;
   const int vend = min(a.nvec, vbeg + a.vps);
@@ -327,21 +422,36 @@ __global__ void __launch_bounds__(kThreads, 6) wide_cand_kernel(const ChainArgs 
     const int v = vbeg + tid + u * kThreads;
     if (v < vend) IO::load(row, v, w[u]);
   }
+  WideRow* wr = a.ws.wrow + rr;  // read while the slice is in flight
+  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi;
+  if (bk < 0 && blo < 0) return;  // no cut falls inside a bin: nothing to list
   const float M = wr->M;
   const int b0 = wr->b0;
   const float cR = a.c_rn * (float)kWideBinsPerLog2;
-  unsigned long long sel = 0;  // bit u * EPV + i: element i of vector u is listed
-#pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    if (vbeg + tid + u * kThreads >= vend) continue;
-    float x[IO::EPV];
-    IO::unpack(w[u], x);
-#pragma unroll
-    for (int i = 0; i < IO::EPV; ++i) {
-      const int bin = wide_bin(x[i], M, cR, b0);
-      if (bin == bk || (blo <= bin && bin <= bhi)) sel |= 1ull << (u * IO::EPV + i);
-    }
-  }
+  // Bin b holds the tokens with (M - x) cR in [b, b + 1), and the last bin
+  // everything from min(b0, kWideBins - 1) on (down to -inf).  The listed
+  // bins as logit intervals [xlo, xhi], widened by a relative 1e-5 so that
+  // they hold every token of those bins whatever the rounding; the cut
+  // kernel keeps only the tokens whose bin is one it needs.
+  auto lo_of = [&](int bin) { return bin == kWideBins - 1 ? (float)min(b0, kWideBins - 1) : (float)bin; };
+  auto xhi_of = [&](float flo) {  // the largest logit of bins >= flo
+    const float t = M - flo / cR;
+    return t + 1e-5f * (fabsf(M) + fabsf(t)) + 1e-30f;
+  };
+  auto xlo_of = [&](int bin) {  // the smallest logit of bins <= bin
+    if (bin == kWideBins - 1) return -INFINITY;
+    const float t = M - (float)(bin + 1) / cR;
+    return t - 1e-5f * (fabsf(M) + fabsf(t)) - 1e-30f;
+  };
+  const float k_hi = bk >= 0 ? xhi_of(lo_of(bk)) : -INFINITY, k_lo = bk >= 0 ? xlo_of(bk) : INFINITY;
+  const float r_hi = blo >= 0 ? xhi_of(lo_of(blo)) : -INFINITY, r_lo = blo >= 0 ? xlo_of(bhi) : INFINITY;
+  // bit u * EPV + i: element i of vector u is listed (one interval in the
+  // usual cases: top-p alone or top-k alone)
+  unsigned long long sel =
+      bk >= 0 && blo >= 0
+          ? listed_bits<DT, VEC, true>(w, vbeg + tid, vend, k_lo, k_hi, r_lo, r_hi)
+          : (bk >= 0 ? listed_bits<DT, VEC, false>(w, vbeg + tid, vend, k_lo, k_hi, 0.f, 0.f)
+                     : listed_bits<DT, VEC, false>(w, vbeg + tid, vend, r_lo, r_hi, 0.f, 0.f));
   unsigned long long total;
   const unsigned long long off = block_excl_u64((unsigned long long)__popcll(sel), &total);
   if (total == 0) return;  // uniform
@@ -435,13 +545,49 @@ __device__ unsigned long long radix_select(int n, const Get& get, const Pred& pr
   return prefix;
 }
 
+// Among the staged tokens i < n that satisfy pred(key, bin), in decreasing
+// key order, the first at which the running weight (a count, or the mass
+// when by_mass) reaches `target`: every thread ranks its own tokens against
+// all n (O(n) each, one barrier), for short lists.  Returns the key; *mass_incl
+// receives the mass up to and including it.
+template <class Pred>
+__device__ unsigned long long rank_select(int n, const unsigned long long* sKey, const unsigned short* sBin,
+                                          const unsigned long long* sF, const Pred& pred, bool by_mass,
+                                          unsigned long long target, unsigned long long* mass_incl) {
+  __shared__ unsigned long long s_key, s_mass;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const unsigned long long K = sKey[i];
+    if (!pred(K, sBin[i])) continue;
+    unsigned long long bw = 0, bm = 0;
+    for (int t = 0; t < n; ++t) {
+      const unsigned long long Kt = sKey[t];
+      if (Kt > K && pred(Kt, sBin[t])) {
+        bm += sF[t];
+        bw += by_mass ? sF[t] : 1ull;
+      }
+    }
+    const unsigned long long w = by_mass ? sF[i] : 1ull;
+    if (bw < target && target <= bw + w) {
+      s_key = K;
+      s_mass = bm + sF[i];
+    }
+  }
+  __syncthreads();
+  *mass_incl = s_mass;
+  const unsigned long long K = s_key;
+  __syncthreads();
+  return K;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
-  __shared__ unsigned long long me[kWideBins + 1];  // mass before each bin
-  __shared__ unsigned long long sKey[kStage];
+  constexpr int kMeStage = 256;  // prefix sums of the top-p bin range held at once
+  __shared__ unsigned long long sKey[kStage], sF[kStage];
   __shared__ unsigned short sBin[kStage];
+  __shared__ unsigned long long sMe[kMeStage + 1];
   __shared__ SelSmem S;
-  __shared__ unsigned long long s_cbk;
+  __shared__ unsigned long long s_mek, s_cbk;
+  __shared__ int s_bp;
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
   const int tid = threadIdx.x;
   const int rr = blockIdx.x, b = rr / a.rows, r = rr - b * a.rows;
@@ -450,45 +596,19 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
   if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
   const char* row = row_ptr(a, b, r, (size_t)a.V * ES);
   WideRow* wr = a.ws.wrow + rr;
-  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi;
+  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi, b0 = wr->b0;
   const unsigned ncand = wr->ncand;
-  const unsigned long long zmin = wr->zmin;
+  const unsigned long long zmin = wr->zmin, Z = wr->ztot;
   const unsigned kinv = wr->kmin_inv;
   const float M = wr->M;
-  const int b0 = wr->b0;
-  // the statistics words are consumed: every call leaves them zero
-  for (int u = tid; u < a.nsplit; u += kThreads) a.ws.stats[(size_t)rr * a.nsplit + u] = 0;
-  // Prefix masses of the bins (and the count before the top-k bin); the
-  // histogram is returned to zero.
-  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins + kBinsPerThread * tid;
-  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins + kBinsPerThread * tid;
+  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;  // exclusive prefix sums now
+  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
   const bool count_cut = a.top_k > 0;
-  unsigned long long m[kBinsPerThread], tm = 0, tc = 0;
-  unsigned c[kBinsPerThread];
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    m[j] = gh[j];
-    c[j] = count_cut ? gc[j] : 0u;
-    tm += m[j];
-    tc += c[j];
+  auto me = [&](int bin) { return bin >= kWideBins ? Z : gh[bin]; };
+  if (tid == 0) {
+    s_mek = bk >= 0 ? me(bk) : 0;
+    s_cbk = bk >= 0 ? gc[bk] : 0;
   }
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    gh[j] = 0;
-    if (count_cut) gc[j] = 0;
-  }
-  unsigned long long Z, N;
-  unsigned long long mb = block_excl_u64(tm, &Z);
-  unsigned long long cb = block_excl_u64(tc, &N);
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    const int bin = kBinsPerThread * tid + j;
-    me[bin] = mb;
-    if (bin == bk) s_cbk = cb;
-    mb += m[j];
-    cb += c[j];
-  }
-  if (tid == kThreads - 1) me[kWideBins] = Z;
   // Stage the listed tokens (or, past the list's capacity, read the row).
   const bool listed = ncand <= (unsigned)kWideCandCap;
   const int n = listed ? (int)ncand : a.V;
@@ -501,6 +621,7 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
       const float x = load_logit<DT>(row, t);
       sKey[i] = make_key(x, t);
       sBin[i] = (unsigned short)wide_bin(x, M, cR, b0);
+      sF[i] = mass_fix(x, M, a.c_hi, a.c_lo);
     }
   __syncthreads();
   auto get = [&](int i, unsigned long long& K, int& bin) {
@@ -514,33 +635,45 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
       bin = wide_bin(x, M, cR, b0);
     }
   };
+  const bool short_list = staged && n <= 512;
   unsigned long long kcut = 0, kept = Z, zk = Z, kk = 0;
   bool ok = true;
   if (bk >= 0) {  // top-k: the (top_k - count above)-th token of bin bk
     unsigned long long in;
-    kk = radix_select(n, get, [&](unsigned long long, int bin) { return bin == bk; }, false,
-                      (unsigned long long)a.top_k - s_cbk, M, a, S, &in);
+    auto pk = [&](unsigned long long, int bin) { return bin == bk; };
+    const unsigned long long tk = (unsigned long long)a.top_k - s_cbk;
+    kk = short_list ? rank_select(n, sKey, sBin, sF, pk, false, tk, &in)
+                    : radix_select(n, get, pk, false, tk, M, a, S, &in);
     kcut = kk;
-    zk = me[bk] + in;
+    zk = s_mek + in;
     kept = zk;
   }
   if (a.top_p < 1.f) {
     const unsigned long long th = top_p_threshold(a.top_p, zk);
-    // the last bin whose preceding mass is below the threshold (within the top-k set)
-    int lo = 0, hi = bk >= 0 ? bk : kWideBins - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (me[mid] < th) lo = mid; else hi = mid - 1;
+    // the last bin (within the top-k set) whose preceding mass is below the
+    // threshold: bk, or one of blo .. bhi (their prefixes staged in pieces)
+    if (tid == 0) s_bp = -1;
+    __syncthreads();
+    const int hi = bk >= 0 ? min(bhi, bk) : bhi;
+    for (int c0 = blo; c0 <= hi; c0 += kMeStage) {
+      const int cnt = min(kMeStage, hi - c0 + 1);
+      for (int i = tid; i <= cnt; i += kThreads) sMe[i] = me(c0 + i);
+      __syncthreads();
+      for (int i = tid; i < cnt; i += kThreads)
+        if (sMe[i] < th && th <= sMe[i + 1]) s_bp = c0 + i;
+      __syncthreads();
     }
-    const int bp = lo;
-    ok = bp == bk || (blo <= bp && bp <= bhi);
+    int bp = s_bp;
+    if (bp < 0 && bk >= 0 && s_mek < th) bp = bk;  // the threshold inside the top-k bin
+    ok = bp >= 0 && (bp == bk || (blo <= bp && bp <= bhi));
     if (ok) {
       unsigned long long in;
       const unsigned long long ktop = kk;
-      kcut = radix_select(n, get,
-                          [&](unsigned long long K, int bin) { return bin == bp && (bp != bk || K >= ktop); },
-                          true, th - me[bp], M, a, S, &in);
-      kept = me[bp] + in;
+      auto pp = [&](unsigned long long K, int bin) { return bin == bp && (bp != bk || K >= ktop); };
+      const unsigned long long mbp = bp == bk ? s_mek : me(bp);
+      kcut = short_list ? rank_select(n, sKey, sBin, sF, pp, true, th - mbp, &in)
+                        : radix_select(n, get, pp, true, th - mbp, M, a, S, &in);
+      kept = mbp + in;
     }
   }
   if (a.min_p > 0.f) {  // a cut on the logit alone, after top-p
@@ -551,17 +684,22 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
     }
   }
   __syncthreads();
-  // The list is consumed (past its capacity only the first kWideCandCap
-  // entries were written): every call leaves it zero.
+  // Consumed: the list, the prefix sums and the statistics words (every
+  // call leaves them zero; past its capacity only kWideCandCap list entries
+  // were written).
   for (int i = tid; i < (int)min(ncand, (unsigned)kWideCandCap); i += kThreads)
     const_cast<unsigned*>(cand)[i] = 0;
+  for (int i = tid; i < kWideBins; i += kThreads) {
+    gh[i] = 0;
+    if (count_cut) gc[i] = 0;
+  }
+  for (int u = tid; u < a.nsplit; u += kThreads) a.ws.stats[(size_t)rr * a.nsplit + u] = 0;
   if (tid == 0) {
     if (!ok) {  // the selection's bins disagree (not expected): the request fails closed
       set_status(a.ws.status, SPEC_ELIMIT);
       atomicExch(&a.ws.sync[b].failed, 1);
     }
     wr->kcut = kcut;
-    wr->M = M;
     wr->Z = (float)((double)kept * 0x1p-40);
     wr->zmin = 0;
     wr->kmin_inv = 0;
@@ -753,10 +891,15 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
   const long items = (long)a.B * a.nsplit2;
   chain_rowstats_kernel<DT, VEC><<<(unsigned)slices, kThreads, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.top_k > 0)
-    e = launch_dep(wide_hist_kernel<DT, VEC, true>, slices, a, st);
-  else
-    e = launch_dep(wide_hist_kernel<DT, VEC, false>, slices, a, st);
+  const bool cnt = a.top_k > 0, mp = a.min_p > 0.f;
+  if (cnt)
+    e = mp ? launch_dep(wide_hist_kernel<DT, VEC, true, true, true>, slices, a, st)
+           : launch_dep(wide_hist_kernel<DT, VEC, true, false, true>, slices, a, st);
+  else if (a.top_p < 1.f)
+    e = mp ? launch_dep(wide_hist_kernel<DT, VEC, false, true, true>, slices, a, st)
+           : launch_dep(wide_hist_kernel<DT, VEC, false, false, true>, slices, a, st);
+  else  // min_p alone
+    e = launch_dep(wide_hist_kernel<DT, VEC, false, true, false>, slices, a, st);
   if (e != cudaSuccess) return e;
   if ((e = launch_dep(wide_bins_kernel, rows, a, st)) != cudaSuccess) return e;
   if ((e = launch_dep(wide_cand_kernel<DT, VEC>, slices, a, st)) != cudaSuccess) return e;
