@@ -406,9 +406,11 @@ int spec_verify_chain_noalloc(const void *target_logits, const void *draft_logit
  * the pages).  Each runs its call with the first phase left out, so that the
  * words the second phase waits for are never written, and with every device
  * wait bounded by wait_cycles SM clock cycles (>= 1) instead of about one
- * second.  Arguments are those of spec_verify_chain_ex (plain or filtered;
- * a filtered call whose rows are wider than one CTA's codes has no wait and
- * returns SPEC_ECUDA) / spec_verify_greedy_ex.  Expected outcome: every
+ * second.  Arguments are those of spec_verify_chain_ex (plain or filtered
+ * with kept lists; a filtered call whose rows are wider than one CTA's codes
+ * has no wait and returns SPEC_ECUDA, and the per-row-cut filter (top_k = 0
+ * with top_p < 1 or min_p > 0, or top_k > SPEC_MAX_TOPK) waits for nothing
+ * and returns SPEC_EINVAL) / spec_verify_greedy_ex.  Expected outcome: every
  * request fails closed and the status word reads SPEC_ETIMEOUT.  The
  * workspace may hold stale words afterwards: zero it with
  * spec_workspace_init before its next use. */
