@@ -227,6 +227,7 @@ __device__ void argmax_epilogue(const ArgmaxArgs& a, int b) {
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, 5) argmax_kernel(const ArgmaxArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // launched by launch_first
   asm volatile("griddepcontrol.launch_dependents;");
   using IO = Io<DT, VEC>;
   const int per_req = a.R * a.nsplit;
@@ -316,8 +317,7 @@ template <int DT, bool VEC>
 cudaError_t launch_argmax_t(const ArgmaxArgs& a, cudaStream_t st, bool skip_pass1) {
   const long g = (long)a.B * a.R * a.nsplit;
   if (!skip_pass1) {
-    argmax_kernel<DT, VEC><<<(unsigned)g, kThreads, 0, st>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_first(argmax_kernel<DT, VEC>, g, kThreads, st, a);
     if (e != cudaSuccess) return e;
   }
   // Pass 2 may be scheduled once every pass-1 CTA has started.

@@ -273,8 +273,7 @@ cudaError_t launch_chain_t(const ChainArgs& args, cudaStream_t st, bool skip_pas
   }
   const long g1 = (long)a.B * a.rows * a.nsplit;
   if (!skip_pass1) {
-    chain_rowstats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
-    e = cudaGetLastError();
+    e = launch_first(chain_rowstats_kernel<DT, VEC>, g1, kThreads, st, a);
     if (e != cudaSuccess) return e;
   }
   const long items = (long)a.B * a.nsplit2;

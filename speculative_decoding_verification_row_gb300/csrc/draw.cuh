@@ -117,6 +117,7 @@ __device__ __forceinline__ void slice_row(const ChainArgs& a, int rr, int& b, in
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, 6) chain_rowstats_kernel(const ChainArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // launched by launch_first
   asm volatile("griddepcontrol.launch_dependents;");
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x;

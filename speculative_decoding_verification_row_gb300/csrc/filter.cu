@@ -613,6 +613,7 @@ __device__ __forceinline__ bool all_halves_set(const uint4& v) {
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, 6) filter_max_kernel(const ChainArgs a) {
   using IO = Io<DT, VEC>;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // launched by launch_first
   asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
   const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
@@ -1132,8 +1133,7 @@ cudaError_t launch_filtered_t(const ChainArgs& a, cudaStream_t st, bool skip_pas
   const long rows = (long)a.B * (2 * a.k + 1);
   if ((long)a.nsplit * kThreads <= kMaxCodes) {
     if (!skip_pass1) {
-      filter_max_kernel<DT, VEC><<<(unsigned)(rows * a.nsplit), kThreads, 0, st>>>(a);
-      const cudaError_t e = cudaGetLastError();
+      const cudaError_t e = launch_first(filter_max_kernel<DT, VEC>, rows * a.nsplit, kThreads, st, a);
       if (e != cudaSuccess) return e;
     }
     // The pick grid may be scheduled once every pass-1 CTA has started; each

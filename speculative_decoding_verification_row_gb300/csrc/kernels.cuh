@@ -88,6 +88,26 @@ cudaError_t launch_tree_sampled(const ChainArgs& a, int dtype, bool vec, cudaStr
 // stream-ordered grids, nothing polls.
 cudaError_t launch_wide(const ChainArgs& a, int dtype, bool vec, cudaStream_t st);
 
+// Launch the first grid of a call as a programmatic dependent of whatever
+// kernel precedes it on `st`: its CTAs may be scheduled while that grid's
+// last CTAs finish, and it begins with griddepcontrol.wait, so it still runs
+// after that grid has completed and sees all of its writes (stream order is
+// kept; the next call's pass 1 no longer pays a full launch gap).
+template <class Kern, class Arg>
+cudaError_t launch_first(Kern kernel, long grid, int block, cudaStream_t st, const Arg& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 // Largest P * L of a stochastic tree verify (its paths and edge logits are
 // staged in shared memory).
 constexpr int kTreeStage = 4096;

@@ -324,8 +324,7 @@ cudaError_t launch_tree_sampled_t(const ChainArgs& args, cudaStream_t st) {
     a.nsplit2 = ceil_div(a.nchunks, a.cpc);
   }
   const long g1 = (long)a.B * a.rows * a.nsplit;
-  chain_rowstats_kernel<DT, VEC><<<(unsigned)g1, kThreads, 0, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_first(chain_rowstats_kernel<DT, VEC>, g1, kThreads, st, a);
   if (e != cudaSuccess) return e;
   const long items = (long)a.B * a.nsplit2;
   cudaLaunchConfig_t cfg = {};

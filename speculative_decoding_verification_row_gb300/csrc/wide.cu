@@ -889,8 +889,7 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
   const long rows = (long)a.B * a.rows;
   const long slices = rows * a.nsplit;
   const long items = (long)a.B * a.nsplit2;
-  chain_rowstats_kernel<DT, VEC><<<(unsigned)slices, kThreads, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_first(chain_rowstats_kernel<DT, VEC>, slices, kThreads, st, a)) != cudaSuccess) return e;
   const bool cnt = a.top_k > 0, mp = a.min_p > 0.f;
   if (cnt)
     e = mp ? launch_dep(wide_hist_kernel<DT, VEC, true, true, true>, slices, a, st)
