@@ -94,6 +94,20 @@ def test_cuda_wide_filter_leaves_the_workspace_zero(V, top_k, top_p):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("T,top_k,top_p,min_p", [(0.7, 0, 1.0, 0.999), (1.5, 0, 0.95, 0.0), (0.05, 0, 0.9, 0.0),
+                                                  (5.0, 0, 0.9, 0.0), (5.0, 3000, 0.95, 0.01)])
+def test_cuda_wide_filter_edge_parameters(T, top_k, top_p, min_p):
+    # min_p near 1 keeps the maxima only; a very low temperature (a few
+    # tokens hold the mass) and high ones (flat rows: tens of thousands of
+    # tokens kept, the tail bound deep in the row).
+    from test_gpu_parity import check_chain
+    w = workloads.make("chain_b64_k7_v128256_bf16", seed=60, B=4, V=50000)
+    w["temperature"] = T
+    w["draft_tokens"] = _filtered_tokens(w, top_k, top_p, 60, min_p)
+    g = _run_filtered(w, top_k, top_p, min_p=min_p)
+    check_chain(w, g, _oracle_filtered(w, top_k, top_p, min_p), f"wide edge T={T} {top_k} {top_p} {min_p}")
+
+
 def test_cuda_wide_filter_masked_vocab():
     # Most of each row is -inf: top_k above the finite count, and top-p over
     # the finite tokens; -inf tokens carry no mass and are never drawn.
