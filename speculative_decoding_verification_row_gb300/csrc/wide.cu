@@ -9,32 +9,38 @@
 // order, possibly shortened by min_p (a cut on the logit alone), so one
 // 64-bit order key fixes it: token t is kept iff make_key(x_t, t) >= kcut.
 // Each token's mass is e_t = 2^(c (x_t - M)) (c = log2(e)/T, M the row
-// maximum), summed in 2^-40 fixed point so that every sum below is exact
-// whatever its order.  Six stream-ordered grids, each a programmatic
-// dependent that waits for its predecessor before reading (no polling):
-//   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima.
-//   2. wide_hist_kernel, one CTA per 32 KB slice: each token's mass and bin
+// maximum).  Masses that decide a cut are summed in 2^-40 fixed point, so
+// those sums are exact whatever their order; the tail below the depth D0
+// (step 2) is summed in fp32 per thread, at most (1 - top_p) Z / 2 in all, so
+// its rounding stays far inside the oracle's 1e-6 near-tie window.  Six
+// stream-ordered grids, each a programmatic dependent that waits for its
+// predecessor before reading (no polling):
+//   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima and sums.
+//   2. wide_hist_kernel, one CTA per 32 KB slice: each token's bin
 //      floor(32 c (M - x)) (2048 bins of 1/32 of a log2 unit, the last
-//      holding everything below) into a shared-memory histogram, then into
-//      the row's (masses; counts too when top-k cuts); the mass and the
+//      holding everything below) and mass, into a shared-memory histogram
+//      (counts too when top-k cuts), then into the row's; the mass and the
 //      smallest logit key of the tokens with e_t >= min_p.  Without a top-k
 //      cut only tokens above a depth D0 get their own bin: the V tokens
 //      below it weigh at most V 2^-D0 = (1 - top_p) Z / 2, so the top-p cut
-//      cannot fall among them; their mass is summed in registers into the
-//      last bin (on the headline shape D0 leaves ~13 % of the tokens to the
-//      shared-memory atomics).
+//      cannot fall among them; their mass goes into the last bin (on the
+//      headline shape D0 leaves ~13 % of the tokens heavy; each warp queues
+//      its heavy tokens by ballot and adds them 32 at a time).  min_p alone
+//      needs no bins.
 //   3. wide_bins_kernel, one CTA per row: prefix sums over the bins give
 //      the bin where the top-k count is reached and the range of bins the
 //      top-p threshold can fall in (the top-k mass is known to within the
-//      top-k bin).
-//   4. wide_cand_kernel, one CTA per slice: the tokens of those bins are
-//      listed per row (most rows: tens to hundreds).
-//   5. wide_cut_kernel, one CTA per row: radix selection over the listed
-//      tokens' keys, eight bits at a time, with exact per-digit counts and
-//      masses: the top-k cut and its mass, then the first token at which
-//      the running top-p mass reaches top_p times it; min_p replaces the
-//      cut when its logit cut lies above.  Writes the row's cut, maximum and
-//      kept mass.
+//      top-k bin); the bins are rewritten as their exclusive prefix sums.
+//   4. wide_cand_kernel, one CTA per slice: the tokens of those bins (as
+//      logit intervals, slightly widened) are listed per row (most rows:
+//      tens to hundreds).
+//   5. wide_cut_kernel, one CTA per row: exact selection over the listed
+//      tokens' keys, with exact counts and masses (lists up to 512 ranked in
+//      one pass, longer ones radix-selected eight bits at a time, a row with
+//      more than 4096 rescanning itself): the top-k cut and its mass, then
+//      the first token at which the running top-p mass reaches top_p times
+//      it; min_p replaces the cut when its logit cut lies above.  Writes the
+//      row's cut and kept mass.
 //   6. wide_draw_kernel: the chain's draw items with the accept test on
 //      p'(x_i) / q'(x_i) and the residual max(0, p' - q') (or the bonus p')
 //      over the filtered rows: tokens below a row's cut read as -inf.
