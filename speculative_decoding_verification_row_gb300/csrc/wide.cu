@@ -791,9 +791,12 @@ __device__ __forceinline__ void wide_draw_item(const ChainArgs& a, int b, int pa
       a.ws.items[(size_t)b * a.nsplit2 + part] = t;
     }
   }
-  if (lane == 0) __threadfence();
+  // One device-scope fence by thread 0 after the barrier releases the whole
+  // CTA's sums (the fence is cumulative over the writes the barrier made
+  // visible to it) before the ticket.
   __syncthreads();
   if (tid == 0) {
+    __threadfence();
     const int t = atomicAdd(&a.ws.sync[b].tick2, 1);
     sLast = t == a.nsplit2 - 1;
     if (sLast) {
