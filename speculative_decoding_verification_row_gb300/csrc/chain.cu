@@ -68,57 +68,34 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
   // Rows this request verifies: target rows 0..kb, draft rows 0..kb-1.
   auto used = [&](int r) { return r <= k ? r <= kb : r - k - 1 < kb; };
   const int rows = bad_len ? 0 : R;
-  // Merge the slice statistics of every row of the request, in a fixed
-  // order, as they arrive: warp w takes rows w, w+8, ...; it issues the loads
-  // of four rows' words before using any (waiting only for words still 0),
-  // takes each row max with shuffles, then adds S_s * 2^(c(m_s - M)) with one
-  // exp per slice (no chain of exps).
+  // Merge the slice statistics of every row of the request as they arrive:
+  // thread r takes row r, issues the loads of its words (eight at a time)
+  // before using any, waiting only for words still 0, then adds
+  // S_s * 2^(c(m_s - M)) over its slices in slice order (one exp per slice).
   const unsigned long long* sb = a.ws.stats + (size_t)b * R * a.nsplit;
   bool to = false;  // a wait of this thread ran out
-  for (int r0 = warp; r0 < rows; r0 += 4 * kWarps) {
-    unsigned long long v[4][2];
+  for (int r = tid; r < rows; r += kThreads) {
+    if (!used(r)) continue;
+    const unsigned long long* pr = sb + (size_t)r * a.nsplit;
+    float m = -INFINITY;
+    for (int u0 = 0; u0 < a.nsplit; u0 += 8) {
+      unsigned long long v[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
+      for (int q = 0; q < 8; ++q) v[q] = u0 + q < a.nsplit ? ld_relaxed_u64(pr + u0 + q) : kNoStats;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int u = lane + 32 * h;
-        v[q][h] = (r < R && used(r) && u < a.nsplit) ? ld_relaxed_u64(sb + (size_t)r * a.nsplit + u)
-                                                     : kNoStats;
+      for (int q = 0; q < 8; ++q) {
+        if (!v[q]) v[q] = wait_stats(a, pr + u0 + q, &to);  // only a present slice reads 0
+        m = fmaxf(m, stats_unpack(v[q]).x);
       }
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (!v[q][h])  // only a present slice reads 0
-          v[q][h] = wait_stats(a, sb + (size_t)(r0 + q * kWarps) * a.nsplit + lane + 32 * h, &to);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
-      if (r >= R || !used(r)) continue;  // the same for the whole warp
-      const unsigned long long* pr = sb + (size_t)r * a.nsplit;
-      const float2 e0 = stats_unpack(v[q][0]), e1 = stats_unpack(v[q][1]);
-      float m = fmaxf(e0.x, e1.x);
-      for (int u = lane + 64; u < a.nsplit; u += 32)
-        m = fmaxf(m, stats_unpack(wait_stats(a, pr + u, &to)).x);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      float sum = 0.f;
-      if (m != -INFINITY) {
-        if (e0.y > 0.f) sum += e0.y * ex2(scaled(e0.x - m, a.c_hi, a.c_lo));
-        if (e1.y > 0.f) sum += e1.y * ex2(scaled(e1.x - m, a.c_hi, a.c_lo));
-        for (int u = lane + 64; u < a.nsplit; u += 32) {
-          const float2 e = stats_unpack(ld_relaxed_u64(pr + u));  // written: seen above
-          if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - m, a.c_hi, a.c_lo));
-        }
+    float sum = 0.f;
+    if (m != -INFINITY)
+      for (int u = 0; u < a.nsplit; ++u) {
+        const float2 e = stats_unpack(ld_relaxed_u64(pr + u));  // written: seen above
+        if (e.y > 0.f) sum += e.y * ex2(scaled(e.x - m, a.c_hi, a.c_lo));
       }
-      sum = warp_sum(sum);
-      if (lane == 0) {
-        sM[r] = m;
-        sS[r] = sum;
-      }
-    }
+    sM[r] = m;
+    sS[r] = sum;
   }
   // A statistics word that never arrived: this item skips its draw work and
   // the request fails closed (every item's flag reaches the finishing item
