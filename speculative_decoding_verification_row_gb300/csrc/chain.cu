@@ -112,7 +112,7 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
       sQ[tid] = ex2(scaled(xq - sM[k + 1 + tid], a.c_hi, a.c_lo)) / sS[k + 1 + tid];
     }
   }
-  __syncthreads();
+  if (k > 32) __syncthreads(); else __syncwarp();  // k <= 32: warp 0 wrote sP, sQ, sBad
   if (warp == 0) {  // accept scan: r_i < p_i(x_i) / q_i(x_i), q == 0 accepts; j = first reject
     unsigned rej[2];
 #pragma unroll
@@ -153,10 +153,9 @@ __device__ __forceinline__ void draw_item(const ChainArgs& a, int b, int part) {
       a.ws.items[(size_t)b * a.nsplit2 + part] = t;
     }
   }
-  // One device-scope fence by thread 0 after the barrier releases the whole
-  // CTA's sums (the fence is cumulative over the writes the barrier made
-  // visible to it) before the ticket.
-  __syncthreads();
+  // One device-scope fence by thread 0 releases the whole CTA's sums before
+  // the ticket: every chunk sum was written before the barrier above, which
+  // made it visible to thread 0, and the fence is cumulative over them.
   if (tid == 0) {
     __threadfence();
     const int t = atomicAdd(&a.ws.sync[b].tick2, 1);

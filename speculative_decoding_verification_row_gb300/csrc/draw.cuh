@@ -462,12 +462,14 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
         carry += seg;
         __syncthreads();  // sWarpTot is rewritten next
       }
-      if (sChunk < 0 && tid == 0) {  // not reached while u < 1: the last positive chunk
-        const int c = sLastPos < 0 ? 0 : sLastPos;
-        sChunk = c;
-        sPre = sZ - __ldcg(chunks + c);
+      if (sChunk < 0) {  // (uniform: read after the loop's last barrier)
+        if (tid == 0) {  // not reached while u < 1: the last positive chunk
+          const int c = sLastPos < 0 ? 0 : sLastPos;
+          sChunk = c;
+          sPre = sZ - __ldcg(chunks + c);
+        }
+        __syncthreads();
       }
-      __syncthreads();
       break;
     }
     // The residual vanished numerically: draw from p_j instead (this CTA
@@ -495,11 +497,13 @@ __device__ int draw_token(const ChainArgs& a, int b, const char* prow, const cha
     }
     __syncthreads();
   }
-  if (tid == 0 && sChunk < 0) {  // Z stayed 0 after the retry (not reached): chunk 0
-    sChunk = 0;
-    sPre = 0;
+  if (sChunk < 0) {  // (uniform) Z stayed 0 after the retry (not reached): chunk 0
+    if (tid == 0) {
+      sChunk = 0;
+      sPre = 0;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (warp == 0) {
     const int c = sChunk;
     float wv[8];

@@ -10,27 +10,34 @@
 // 64-bit order key fixes it: token t is kept iff make_key(x_t, t) >= kcut.
 // Each token's mass is e_t = 2^(c (x_t - M)) (c = log2(e)/T, M the row
 // maximum).  Masses that decide a cut are summed in 2^-40 fixed point, so
-// those sums are exact whatever their order; the tail below the depth D0
-// (step 2) is summed in fp32 per thread, at most (1 - top_p) Z / 2 in all, so
-// its rounding stays far inside the oracle's 1e-6 near-tie window.  Six
-// stream-ordered grids, each a programmatic dependent that waits for its
+// those sums are exact whatever their order; a row's total mass comes from
+// pass 1's slice sums (fp32, about 1e-7 relative, far inside the oracle's
+// 1e-6 near-tie window on the top-p cut).  Six stream-ordered grids (four for
+// min_p alone), each a programmatic dependent that waits for its
 // predecessor before reading (no polling):
 //   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima and sums.
-//   2. wide_hist_kernel, one CTA per 32 KB slice: each token's bin
-//      floor(32 c (M - x)) (2048 bins of 1/32 of a log2 unit, the last
-//      holding everything below) and mass, into a shared-memory histogram
-//      (counts too when top-k cuts), then into the row's; the mass and the
-//      smallest logit key of the tokens with e_t >= min_p.  Without a top-k
-//      cut only tokens above a depth D0 get their own bin: the V tokens
-//      below it weigh at most V 2^-D0 = (1 - top_p) Z / 2, so the top-p cut
-//      cannot fall among them; their mass goes into the last bin (on the
-//      headline shape D0 leaves ~13 % of the tokens heavy; each warp queues
-//      its heavy tokens by ballot and adds them 32 at a time).  min_p alone
+//   2. wide_hist_kernel, one CTA per 32 KB slice.  Only the heavy tokens,
+//      those above a light depth, are binned: bin floor(32 c (M - x)) (2048
+//      bins of 1/32 log2 unit), exact mass (and count when top-k cuts).  The
+//      depth comes from a sample of the slice (an eighth): where the row's
+//      tail below is estimated at half of (1 - top_p) Z, or where the count
+//      above is estimated at 3 top_k + 256; on the headline shape about 3 %
+//      of the tokens are heavy.  A 16-byte vector whose largest logit lies
+//      below the depth (and below min_p's) is passed over after one packed
+//      compare; the others are queued per warp and their tokens binned one
+//      per lane.  The same pass sums min_p's mass and key.  min_p alone
 //      needs no bins.
-//   3. wide_bins_kernel, one CTA per row: prefix sums over the bins give
-//      the bin where the top-k count is reached and the range of bins the
-//      top-p threshold can fall in (the top-k mass is known to within the
-//      top-k bin); the bins are rewritten as their exclusive prefix sums.
+//   3. wide_bins_kernel, one CTA per row: the row's total mass is pass 1's
+//      (never below the heavy tokens' exact sum: the light ones are the
+//      rest); it checks exactly that the cut lies among the bins every slice
+//      filled (the top-k count or the top-p threshold is reached above the
+//      shallowest slice depth) and otherwise rebuilds the row's histogram
+//      itself with the a-priori depth D0 = log2(V / ((1 - top_p) Z)) + 1
+//      (the V tokens below it weigh at most (1 - top_p) Z / 2) or, for
+//      top-k, every token counted.  Then prefix sums give the bin where the
+//      top-k count is reached and the range of bins the top-p threshold can
+//      fall in (the top-k mass is known to within the top-k bin); the bins
+//      are rewritten as their exclusive prefix sums.
 //   4. wide_cand_kernel, one CTA per slice: the tokens of those bins (as
 //      logit intervals, slightly widened) are listed per row (most rows:
 //      tens to hundreds).
@@ -130,14 +137,267 @@ __device__ __forceinline__ unsigned long long top_p_threshold(float top_p, unsig
 }
 
 // ------------------------------------------------------------------ 2
+constexpr int kQueue = 64;   // queued vectors a warp holds before binning them
+constexpr int kLevels = 64;  // the sample's depth levels, half a log2 unit each
+
+// The light depth that bounds the mass below it a priori: the V tokens
+// deeper than D0 = log2(V / ((1 - top_p) Z)) + 1 weigh at most V 2^-D0 =
+// (1 - top_p) Z / 2, so the top-p cut cannot fall among them (as a bin
+// index, bins of 1/32 log2 unit).
+__device__ __forceinline__ int safe_depth_bin(const ChainArgs& a, float Zs) {
+  const float D0 = log2f((float)a.V / ((1.f - a.top_p) * fmaxf(Zs, 1.f))) + 1.f;
+  const float fb = ceilf(D0 * (float)kWideBinsPerLog2) + 1.f;
+  return fb < 1.f ? 1 : (fb >= (float)(kWideBins - 1) ? kWideBins - 1 : (int)fb);
+}
+
+// t moved down by a relative 1e-5 (and 1e-5 absolute): far more than the
+// rounding of the logit-domain tests below.
+__device__ __forceinline__ float widen_down(float t, float M) {
+  return t - 1e-5f * (fabsf(M) + fabsf(t)) - 1e-5f;
+}
+
+struct HistParams {
+  float M, c_hi, c_lo, cR;  // row maximum, log2(e)/T in two parts, bins per unit of logit
+  float xthr;               // vectors whose largest logit is below xthr hold only light tokens
+  float fb1;                // a token with (M - x) cR < fb1 is heavy
+  float min_p;
+  bool all;                 // every token is heavy (counted and binned)
+};
+
+// Heavy tokens are those of bins < b1 (all of them when b1 = kWideBins);
+// xthr lies below every heavy token's logit and below every logit with
+// 2^(c (x - M)) >= min_p (MINP).
+__device__ __forceinline__ HistParams hist_params(const ChainArgs& a, float M, int b1, bool bins, bool minp) {
+  HistParams h;
+  h.M = M;
+  h.c_hi = a.c_hi;
+  h.c_lo = a.c_lo;
+  h.cR = a.c_rn * (float)kWideBinsPerLog2;
+  h.all = b1 >= kWideBins;
+  h.fb1 = (float)b1;
+  h.min_p = a.min_p;
+  float x = INFINITY;
+  if (bins) x = h.all ? -INFINITY : widen_down(M - (float)b1 / h.cR, M);
+  if (minp) x = fminf(x, widen_down(M + log2f(a.min_p) / a.c_rn, M));
+  h.xthr = x;
+  return h;
+}
+
+// Where heavy tokens go: the CTA's shared histogram (three 14-bit parts of
+// the 2^-40 fixed point in 32-bit adds; at most 2^14 tokens reach it between
+// two flushes, so each part's sum stays below 2^28) ...
+template <bool COUNT>
+struct SharedBins {
+  unsigned (*hm)[kWideBins];
+  unsigned* hc;
+  __device__ __forceinline__ void add(unsigned bin, float e) const {
+    const unsigned long long f = to_fixed(e * 256.f);  // <= 2^40
+    if (f) {
+      atomicAdd(&hm[0][bin], (unsigned)f & 0x3fffu);
+      atomicAdd(&hm[1][bin], (unsigned)(f >> 14) & 0x3fffu);
+      atomicAdd(&hm[2][bin], (unsigned)(f >> 28));
+    }
+    if (COUNT) atomicAdd(&hc[bin], 1u);
+  }
+};
+// ... or, when one CTA rebuilds a whole row, the row's global bins.
+template <bool COUNT>
+struct GlobalBins {
+  unsigned long long* gh;
+  unsigned* gc;
+  __device__ __forceinline__ void add(unsigned bin, float e) const {
+    const unsigned long long f = to_fixed(e * 256.f);
+    if (f) atomicAdd(gh + bin, f);
+    if (COUNT) atomicAdd(gc + bin, 1u);
+  }
+};
+
+// One slice, held in registers (this thread's vectors v0 + u kThreads), into
+// the bins.  A vector whose largest logit is below xthr holds only light
+// tokens and is passed over (their mass is the row's total, from pass 1,
+// less the heavy tokens').  Every other vector is queued by its warp
+// (ballot); its tokens are then tested one per lane (4 vectors of 8 bf16 per
+// step) and those at or above xthr queued again, so that the exact work --
+// a heavy token's mass (and count) into its bin, and min_p's sum and key
+// for every token with e >= min_p (MINP) -- runs 32 tokens at a time.
+// Whatever xthr is, each token's bin is what its own test gives; xthr only
+// decides how many tokens are tested one by one.
+template <int DT, bool VEC, bool MINP, bool BINS, class Sink>
+__device__ __forceinline__ void hist_slice(const Sink& sink, uint4* q, float* hq,
+                                           const uint32_t (&w)[kVecPerThread][Io<DT, VEC>::NW], int v0,
+                                           int vend, const HistParams& h, unsigned long long& zmin,
+                                           unsigned& kinv) {
+  using IO = Io<DT, VEC>;
+  constexpr int EPV = IO::EPV;
+  constexpr int VPS = 32 / EPV;  // queued vectors per warp step
+  const int lane = threadIdx.x & 31;
+  const unsigned below = (1u << lane) - 1u;
+  int hn = 0;  // tokens in hq (warp-uniform, < 32 between steps)
+  auto take = [&](int n) {  // the first n <= 32 tokens of hq, one per lane
+    __syncwarp();
+    if (lane < n) {
+      const float x = hq[lane];
+      const float e = ex2(scaled(x - h.M, h.c_hi, h.c_lo));
+      if constexpr (MINP) {
+        if (e >= h.min_p) {
+          zmin += to_fixed(e * 256.f);
+          kinv = max(kinv, ~ord32(x));
+        }
+      }
+      if constexpr (BINS) {
+        const float fbin = (h.M - x) * h.cR;
+        if (h.all || fbin < h.fb1) sink.add((unsigned)(int)fminf(fbin, (float)(kWideBins - 1)), e);
+      }
+    }
+    __syncwarp();
+  };
+  auto drain = [&](int qn) {
+    __syncwarp();
+    for (int q0 = 0; q0 < qn; q0 += VPS) {
+      const int qi = q0 + lane / EPV, el = lane % EPV;
+      float x = -INFINITY;
+      if (qi < qn) {
+        if constexpr (VEC && DT == SPEC_BF16)
+          x = __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(q + qi)[el] << 16);
+        else if constexpr (VEC)
+          x = reinterpret_cast<const float*>(q + qi)[el];
+        else
+          x = __uint_as_float(q[qi].x);  // (scalar bf16 is held in the high half)
+      }
+      // every token of a queued vector when all are heavy (-inf included)
+      const bool need = qi < qn && (h.all || x >= h.xthr);
+      const unsigned m = __ballot_sync(0xffffffffu, need);
+      if (need) hq[hn + __popc(m & below)] = x;
+      hn += __popc(m);
+      if (hn >= 32) {
+        take(32);
+        if (lane < hn - 32) hq[lane] = hq[32 + lane];
+        __syncwarp();
+        hn -= 32;
+      }
+    }
+    __syncwarp();
+  };
+  int qn = 0;  // warp-uniform
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const bool fl = v0 + u * kThreads < vend && IO::vmax(w[u]) >= h.xthr;
+    const unsigned m = __ballot_sync(0xffffffffu, fl);
+    if (fl) {
+      uint4 v;
+      v.x = w[u][0];
+      if constexpr (IO::NW == 4) {
+        v.y = w[u][1];
+        v.z = w[u][2];
+        v.w = w[u][3];
+      } else {
+        v.y = v.z = v.w = 0u;
+      }
+      q[qn + __popc(m & below)] = v;
+    }
+    qn += __popc(m);
+    if (qn > kQueue - 32) {
+      drain(qn);
+      qn = 0;
+    }
+  }
+  if (qn) drain(qn);
+  if (hn) take(hn);
+}
+
+// This slice's light depth (a bin index): from a sample of the slice, its
+// first vector per thread (an eighth of it), the shallowest depth, in half
+// log2 units, at which the row's estimated mass below stays under half of
+// (1 - top_p) Z with at least 16 sampled tokens above it (top-p: a tail
+// estimate resting on fewer tokens is not trusted), or the estimated count
+// above reaches 3 top_k + 256 (top-k); never deeper than b0.  Only a speed choice: the bins grid checks
+// exactly that the row's cut lies above the row's shallowest light depth
+// and rebuilds the row otherwise.
+template <int DT, bool VEC, bool COUNT>
+__device__ int sample_depth(const uint32_t (&w0)[Io<DT, VEC>::NW], bool valid, const ChainArgs& a, float M,
+                            float Zs, int b0, float* lm, unsigned* lc, float* zsub, unsigned* nsub, int* b1out) {
+  using IO = Io<DT, VEC>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lmax = COUNT ? kLevels : min(kLevels, b0 / 16);
+  float zs = 0.f;
+  if (valid) {
+    float x[IO::EPV];
+    IO::unpack(w0, x);
+    const float c2 = 2.f * a.c_rn;
+#pragma unroll
+    for (int i = 0; i < IO::EPV; ++i) {
+      const float dl = (M - x[i]) * c2;  // depth in half log2 units (+inf for -inf)
+      const int lv = dl < (float)lmax ? (int)dl : lmax;
+      if (lv < lmax) atomicAdd(lc + lv, 1u);
+      if (!COUNT) {
+        const float e = ex2(-0.5f * dl);
+        zs += e;
+        if (lv < lmax) atomicAdd(lm + lv, e);
+      }
+    }
+  }
+  unsigned ns = valid ? (unsigned)IO::EPV : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    zs += __shfl_xor_sync(0xffffffffu, zs, o);
+    ns += __shfl_xor_sync(0xffffffffu, ns, o);
+  }
+  if (lane == 0) {
+    if (!COUNT) atomicAdd(zsub, zs);
+    atomicAdd(nsub, ns);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const float scale = *nsub ? (float)a.V / (float)*nsub : 0.f;
+    const int j0 = 2 * lane, j1 = j0 + 1;
+    // running totals over the levels above j0 and j1 (lane order = depth
+    // order): sampled tokens, and (top-p) their mass
+    const float n0 = (float)lc[j0], n1 = (float)lc[j1];
+    const float v0 = COUNT ? 0.f : lm[j0], v1 = COUNT ? 0.f : lm[j1];
+    float ninc = n0 + n1, inc = v0 + v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, ninc, o), t2 = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) {
+        ninc += t;
+        inc += t2;
+      }
+    }
+    const float nab0 = ninc - n0 - n1, nab1 = nab0 + n0;
+    const float above0 = inc - v0 - v1, above1 = above0 + v0;
+    bool ok0, ok1;
+    if (COUNT) {  // tokens above the depth
+      const float need = 3.f * (float)a.top_k + 256.f;
+      ok0 = j0 >= 1 && scale * nab0 >= need;
+      ok1 = scale * nab1 >= need;
+    } else {  // mass below the depth
+      const float tail = 0.5f * (1.f - a.top_p) * Zs, z = *zsub;
+      ok0 = j0 >= 1 && j0 <= lmax && nab0 >= 16.f && scale * (z - above0) <= tail;
+      ok1 = j1 <= lmax && nab1 >= 16.f && scale * (z - above1) <= tail;
+    }
+    const unsigned m0 = __ballot_sync(0xffffffffu, ok0), m1 = __ballot_sync(0xffffffffu, ok1);
+    int j = kLevels;
+    if (m0) j = 2 * (__ffs(m0) - 1);
+    if (m1) j = min(j, 2 * (__ffs(m1) - 1) + 1);
+    if (lane == 0) *b1out = j < kLevels ? min(16 * j, b0) : b0;
+  }
+  __syncthreads();
+  return *b1out;
+}
+
 // BINS = false (min_p alone): no histogram, only the min_p mass and key.
+// COUNT: top-k cuts (the light tokens then need no mass unless top_k >= V).
 template <int DT, bool VEC, bool COUNT, bool MINP, bool BINS>
 __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs a) {
-  // The slice's bin masses in three 14-bit parts of the 2^-40 fixed point
-  // (32-bit shared adds; a slice holds at most 2^14 tokens, so each part's
-  // sum stays below 2^28), recombined exactly at the end.
   __shared__ unsigned hm[3][kWideBins];
   __shared__ unsigned hc[COUNT ? kWideBins : 1];
+  __shared__ uint4 sq[kWarps][kQueue];
+  __shared__ float shq[kWarps][64];
+  __shared__ float s_lm[kLevels];
+  __shared__ unsigned s_lc[kLevels];
+  __shared__ float s_zsub;
+  __shared__ unsigned s_nsub;
+  __shared__ int s_b1;
   __shared__ unsigned long long s_z[kWarps];
   __shared__ unsigned s_k[kWarps];
   using IO = Io<DT, VEC>;
@@ -145,9 +405,18 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
   int b, r;
   slice_row(a, rr, b, r);
-  for (int i = tid; i < kWideBins; i += kThreads) {
-    hm[0][i] = hm[1][i] = hm[2][i] = 0u;
-    if (COUNT) hc[i] = 0;
+  if (BINS)
+    for (int i = tid; i < kWideBins; i += kThreads) {
+      hm[0][i] = hm[1][i] = hm[2][i] = 0u;
+      if (COUNT) hc[i] = 0;
+    }
+  if (tid < kLevels) {
+    s_lm[tid] = 0.f;
+    s_lc[tid] = 0u;
+  }
+  if (tid == 0) {
+    s_zsub = 0.f;
+    s_nsub = 0u;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -161,120 +430,42 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
     const int v = vbeg + tid + u * kThreads;
     if (v < vend) {
       IO::load(row, v, w[u]);
-    } else {  // past the row: -inf (no mass; not counted, see below)
+    } else {  // past the row: -inf (no mass; never queued)
 #pragma unroll
       for (int q = 0; q < IO::NW; ++q) w[u][q] = (VEC && DT == SPEC_BF16) ? 0xff80ff80u : 0xff800000u;
     }
   }
   float Zs;
   const float M = row_stats(a, rr, &Zs);  // also orders the clearing above before the adds
-  const float cR = a.c_rn * (float)kWideBinsPerLog2;
-  // Bins from b0 on take the light tokens, summed in registers (no top-k
-  // cut: the top-p cut lies above depth D0; min_p alone needs no bins).
-  int b0 = kWideBins;
-  if (!COUNT) {
-    if (a.top_p < 1.f) {
-      const float D0 = log2f((float)a.V / ((1.f - a.top_p) * fmaxf(Zs, 1.f))) + 1.f;
-      const float fb = ceilf(D0 * (float)kWideBinsPerLog2) + 1.f;
-      b0 = fb < 1.f ? 1 : (fb >= (float)(kWideBins - 1) ? kWideBins - 1 : (int)fb);
-    } else {
-      b0 = 0;
-    }
+  const bool count_active = COUNT && a.top_k < a.V;  // (else every token is counted)
+  int b1 = kWideBins;
+  if constexpr (BINS) {
+    const int b0 = COUNT ? kWideBins : safe_depth_bin(a, Zs);
+    b1 = COUNT && !count_active
+             ? kWideBins
+             : sample_depth<DT, VEC, COUNT>(w[0], vbeg + tid < vend, a, M, Zs, b0, s_lm, s_lc, &s_zsub,
+                                            &s_nsub, &s_b1);
   }
-  if (s == 0 && tid == 0) {  // every slice of the row computes the same
-    a.ws.wrow[rr].b0 = b0;
-    a.ws.wrow[rr].M = M;
+  WideRow* wr = a.ws.wrow + rr;
+  if (tid == 0) {
+    if (s == 0) wr->M = M;                          // every slice of the row computes the same
+    if (BINS) atomicMax(&wr->b0, kWideBins + 1 - b1);  // the row's shallowest light depth, encoded
   }
-  const float fb0 = (float)b0;
+  const HistParams h = hist_params(a, M, b1, BINS, MINP);
   unsigned long long zmin = 0;
   unsigned kinv = 0;
-  float light = 0.f;  // light tokens' mass: each < 2^-D0, summed in fp32 per thread
-  // Heavy tokens of each vector (8 or 4 per lane) are packed per warp by
-  // ballot into a shared queue as (bin, mass) and added to the histogram
-  // after the vector, one per lane: a warp-wide 64-bit shared add costs
-  // about the same however few of its lanes are active, so one add per 32
-  // heavy tokens instead of one per token position.
-  // (with a top-k count cut every token is heavy: no queue, direct adds)
-  __shared__ unsigned qbin[COUNT ? 1 : kWarps][COUNT ? 1 : 32 * IO::EPV];
-  __shared__ float qe[COUNT ? 1 : kWarps][COUNT ? 1 : 32 * IO::EPV];
-  auto add_mass = [&](unsigned bin, float e) {
-    const unsigned long long f = to_fixed(e * 256.f);  // < 2^41
-    if (f) {
-      atomicAdd(&hm[0][bin], (unsigned)f & 0x3fffu);
-      atomicAdd(&hm[1][bin], (unsigned)(f >> 14) & 0x3fffu);
-      atomicAdd(&hm[2][bin], (unsigned)(f >> 28));
-    }
-  };
-  const unsigned below = (1u << lane) - 1u;
-  const float2 nM = make_float2(-M, -M), chi = make_float2(a.c_hi, a.c_hi), clo = make_float2(a.c_lo, a.c_lo),
-               ncR = make_float2(-cR, -cR);
-#pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    float x[IO::EPV];
-    IO::unpack(w[u], x);
-    int qn = 0;  // warp-uniform
-#pragma unroll
-    for (int i = 0; i < IO::EPV; i += 2) {
-      // two tokens at a time in packed fp32x2: d = x - M, the exponent
-      // scaled(d) = d c_hi + d c_lo and the bin (M - x) cR = d (-cR), each
-      // the same rounding as the scalar operations of mass_fix / mass_bin
-      const float x1 = i + 1 < IO::EPV ? x[i + 1 < IO::EPV ? i + 1 : i] : -INFINITY;  // (EPV may be 1)
-      const float2 d = add2(make_float2(x[i], x1), nM);
-      const float2 y = fma2(d, chi, mul2(d, clo));
-      const float2 fb = mul2(d, ncR);
-      const float e2[2] = {ex2(y.x), ex2(y.y)};
-      const float fbin2[2] = {fb.x, fb.y};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (i + h >= IO::EPV) break;
-        const float e = e2[h], fbin = fbin2[h];
-        if constexpr (MINP) {
-          if (e >= a.min_p) {
-            zmin += to_fixed(e * 256.f);
-            kinv = max(kinv, ~ord32(h ? x1 : x[i]));
-          }
-        }
-        if constexpr (!BINS) {
-          // min_p alone: the cut is the smallest key with e >= min_p
-        } else if constexpr (COUNT) {  // every token of the row is counted
-          if (vbeg + tid + u * kThreads < vend) {
-            const unsigned bin = (unsigned)(int)fminf(fbin, (float)(kWideBins - 1));
-            add_mass(bin, e);
-            atomicAdd(&hc[bin], 1u);
-          }
-        } else {  // past the row: x = -inf, so fbin = +inf, light, no mass
-          const bool heavy = fbin < fb0;
-          light += heavy ? 0.f : e;
-          const unsigned hmask = __ballot_sync(0xffffffffu, heavy);
-          if (heavy) {
-            const int slot = qn + __popc(hmask & below);
-            qbin[warp][slot] = __float_as_uint(fbin);
-            qe[warp][slot] = e;
-          }
-          qn += __popc(hmask);
-        }
-      }
-    }
-    if constexpr (!COUNT && BINS) {
-      __syncwarp();
-      for (int q = lane; q < qn; q += 32)
-        add_mass((unsigned)(int)__uint_as_float(qbin[warp][q]), qe[warp][q]);  // fbin < b0 <= 2047
-      __syncwarp();
-    }
-  }
-  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
-  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
-  if (b0 < kWideBins) {  // the light tokens' mass, into the last bin
-    unsigned long long tot;
-    block_excl_u64(to_fixed(light * 256.f), &tot);  // (its barriers also order the adds above)
-    if (tid == 0 && tot) atomicAdd(gh + kWideBins - 1, tot);
-  } else {
+  hist_slice<DT, VEC, MINP, BINS>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vbeg + tid, vend, h, zmin,
+                                  kinv);
+  if constexpr (BINS) {
+    unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
+    unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
     __syncthreads();
-  }
-  for (int i = tid; i < min(b0, kWideBins); i += kThreads) {
-    const unsigned long long m = ((unsigned long long)hm[2][i] << 28) + ((unsigned long long)hm[1][i] << 14) + hm[0][i];
-    if (m) atomicAdd(gh + i, m);
-    if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
+    for (int i = tid; i < min(b1, kWideBins); i += kThreads) {  // heavy bins lie below b1
+      const unsigned long long m =
+          ((unsigned long long)hm[2][i] << 28) + ((unsigned long long)hm[1][i] << 14) + hm[0][i];
+      if (m) atomicAdd(gh + i, m);
+      if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
+    }
   }
   if (MINP) {
 #pragma unroll
@@ -295,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
         z += s_z[i];
         kk = max(kk, s_k[i]);
       }
-      WideRow* wr = a.ws.wrow + rr;
       if (z) atomicAdd(&wr->zmin, z);
       if (kk) atomicMax(&wr->kmin_inv, kk);
     }
@@ -307,7 +497,48 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
 constexpr int kBinsPerThread = kWideBins / kThreads;
 static_assert(kBinsPerThread * kThreads == kWideBins, "bins per thread");
 
-__global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) {
+// The row's histogram rebuilt by this one CTA with light depth b0 (every
+// token heavy when b0 = kWideBins), its slices streaming through the
+// registers in turn, straight into the row's global bins (cleared first).
+template <int DT, bool VEC, bool COUNT>
+__device__ void rebuild_row(const ChainArgs& a, int rr, float M, int b0, uint4* q, float* hq,
+                            unsigned long long* gh, unsigned* gc) {
+  using IO = Io<DT, VEC>;
+  const int tid = threadIdx.x;
+  int b, r;
+  slice_row(a, rr, b, r);
+  const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
+  for (int i = tid; i < kWideBins; i += kThreads) {
+    gh[i] = 0;
+    if (COUNT) gc[i] = 0;
+  }
+  __syncthreads();
+  const HistParams h = hist_params(a, M, b0, true, false);
+  for (int s = 0; s < a.nsplit; ++s) {
+    const int vbeg = s * a.vps;
+    const int vend = min(a.nvec, vbeg + a.vps);
+    uint32_t w[kVecPerThread][IO::NW];
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int v = vbeg + tid + u * kThreads;
+      if (v < vend) {
+        IO::load(row, v, w[u]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < IO::NW; ++k) w[u][k] = (VEC && DT == SPEC_BF16) ? 0xff80ff80u : 0xff800000u;
+      }
+    }
+    unsigned long long zd = 0;
+    unsigned kd = 0;
+    hist_slice<DT, VEC, false, true>(GlobalBins<COUNT>{gh, gc}, q, hq, w, vbeg + tid, vend, h, zd, kd);
+  }
+  __syncthreads();  // the adds above before the reads after
+}
+
+template <int DT, bool VEC, bool COUNT>
+__global__ void __launch_bounds__(kThreads, 4) wide_bins_kernel(const ChainArgs a) {
+  __shared__ uint4 sq[kWarps][kQueue];
+  __shared__ float shq[kWarps][64];
   __shared__ int s_bk, s_blo, s_bhi;
   __shared__ unsigned long long s_mb, s_mbin;
   const int tid = threadIdx.x;
@@ -315,28 +546,80 @@ __global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
-  unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins + kBinsPerThread * tid;
-  unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins + kBinsPerThread * tid;
-  const bool count_cut = a.top_k > 0;
-  unsigned long long m[kBinsPerThread], tm = 0, tc = 0;
+  unsigned long long* gh0 = a.ws.whist + (size_t)rr * kWideBins;
+  unsigned* gc0 = a.ws.wcount + (size_t)rr * kWideBins;
+  unsigned long long* gh = gh0 + kBinsPerThread * tid;
+  unsigned* gc = gc0 + kBinsPerThread * tid;
+  WideRow* wr = a.ws.wrow + rr;
+  const bool count_cut = COUNT && a.top_k < a.V;
+  // The row's shallowest light depth: bins below b1 hold every token of
+  // theirs; deeper bins hold only some slices' tokens.
+  int b1 = kWideBins + 1 - wr->b0;
+  // Top-p: the row's total mass is pass 1's (its slice sums), never below
+  // the heavy tokens' exact sum; the light tokens' share of it is not
+  // binned.  Top-k: the count decides, and with top_k >= V every token is
+  // heavy (the exact sum).
+  float Zs = 0.f;
+  if (!COUNT) row_stats(a, rr, &Zs);
+  unsigned long long m[kBinsPerThread];
   unsigned c[kBinsPerThread];
+  unsigned long long Z = 0, C = 0, NC = 0;
+  auto gather = [&]() {  // this thread's bins, the heavy total, the complete region's mass (count)
+    unsigned long long tm = 0, cm = 0, cc = 0;
 #pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    m[j] = gh[j];
-    c[j] = count_cut ? gc[j] : 0u;
-    tm += m[j];
-    tc += c[j];
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      m[j] = gh[j];
+      c[j] = COUNT ? gc[j] : 0u;
+      tm += m[j];
+      if (kBinsPerThread * tid + j < b1) {
+        cm += m[j];
+        cc += c[j];
+      }
+    }
+    unsigned long long zh;
+    block_excl_u64(tm, &zh);
+    block_excl_u64(cm, &C);
+    if (count_cut) block_excl_u64(cc, &NC);
+    Z = COUNT ? zh : max(zh, to_fixed(Zs * 256.f));
+  };
+  gather();
+  // The cut lies above depth b1 iff the bins above it reach the top-k count
+  // (top-k) or the top-p threshold of the total mass (top-p alone); when it
+  // does not, the row is rebuilt with the a-priori depth (an empty row has
+  // nothing to rebuild).
+  const bool ok = b1 >= kWideBins || Z == 0 ||
+                  (count_cut ? NC >= (unsigned long long)a.top_k : C >= top_p_threshold(a.top_p, Z));
+  if (!ok) {  // (uniform)
+    b1 = COUNT ? kWideBins : safe_depth_bin(a, Zs);
+    rebuild_row<DT, VEC, COUNT>(a, rr, wr->M, b1, sq[tid >> 5], shq[tid >> 5], gh0, gc0);
+    gather();
+  }
+  if (b1 < kWideBins) {  // the bins from b1 on merge into the last bin
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      const int bin = kBinsPerThread * tid + j;
+      if (bin >= b1) {
+        m[j] = bin == kWideBins - 1 ? Z - C : 0;
+        c[j] = 0;
+      }
+    }
   }
   if (tid == 0) {
     s_bk = s_blo = s_bhi = -1;
     s_mb = 0;
     s_mbin = 0;
   }
-  unsigned long long Z, N;
+  unsigned long long tm = 0, tc = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    tm += m[j];
+    tc += c[j];
+  }
+  unsigned long long N;
   const unsigned long long pm = block_excl_u64(tm, &Z);
-  const unsigned long long pc = block_excl_u64(tc, &N);
+  const unsigned long long pc = COUNT ? block_excl_u64(tc, &N) : 0;
   // top-k: the bin where the running count reaches top_k
-  if (count_cut && (unsigned long long)a.top_k < N) {
+  if (count_cut) {
     unsigned long long cb = pc, mb = pm;
 #pragma unroll
     for (int j = 0; j < kBinsPerThread; ++j) {
@@ -369,17 +652,17 @@ __global__ void __launch_bounds__(kThreads) wide_bins_kernel(const ChainArgs a) 
 #pragma unroll
     for (int j = 0; j < kBinsPerThread; ++j) {
       gh[j] = mb;
-      if (count_cut) gc[j] = (unsigned)cb;
+      if (COUNT) gc[j] = (unsigned)cb;
       mb += m[j];
       cb += c[j];
     }
   }
   __syncthreads();
   if (tid == 0) {
-    WideRow* wr = a.ws.wrow + rr;
     wr->bk = s_bk;
     wr->blo = s_blo;
     wr->bhi = s_blo >= 0 ? s_bhi : -1;
+    wr->b0 = b1;  // from here on: the row's light depth
     wr->ztot = Z;
   }
 }
@@ -602,7 +885,8 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
   if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
   const char* row = row_ptr(a, b, r, (size_t)a.V * ES);
   WideRow* wr = a.ws.wrow + rr;
-  const int bk = wr->bk, blo = wr->blo, bhi = wr->bhi, b0 = wr->b0;
+  const bool bins = a.top_k > 0 || a.top_p < 1.f;  // min_p alone has no histogram
+  const int bk = bins ? wr->bk : -1, blo = bins ? wr->blo : -1, bhi = bins ? wr->bhi : -1, b0 = wr->b0;
   const unsigned ncand = wr->ncand;
   const unsigned long long zmin = wr->zmin, Z = wr->ztot;
   const unsigned kinv = wr->kmin_inv;
@@ -695,10 +979,11 @@ __global__ void __launch_bounds__(kThreads) wide_cut_kernel(const ChainArgs a) {
   // were written).
   for (int i = tid; i < (int)min(ncand, (unsigned)kWideCandCap); i += kThreads)
     const_cast<unsigned*>(cand)[i] = 0;
-  for (int i = tid; i < kWideBins; i += kThreads) {
-    gh[i] = 0;
-    if (count_cut) gc[i] = 0;
-  }
+  if (bins)
+    for (int i = tid; i < kWideBins; i += kThreads) {
+      gh[i] = 0;
+      if (count_cut) gc[i] = 0;
+    }
   for (int u = tid; u < a.nsplit; u += kThreads) a.ws.stats[(size_t)rr * a.nsplit + u] = 0;
   if (tid == 0) {
     if (!ok) {  // the selection's bins disagree (not expected): the request fails closed
@@ -909,8 +1194,12 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
   else  // min_p alone
     e = launch_dep(wide_hist_kernel<DT, VEC, false, true, false>, slices, a, st);
   if (e != cudaSuccess) return e;
-  if ((e = launch_dep(wide_bins_kernel, rows, a, st)) != cudaSuccess) return e;
-  if ((e = launch_dep(wide_cand_kernel<DT, VEC>, slices, a, st)) != cudaSuccess) return e;
+  if (cnt || a.top_p < 1.f) {  // (min_p alone: no bins, no candidates)
+    e = cnt ? launch_dep(wide_bins_kernel<DT, VEC, true>, rows, a, st)
+            : launch_dep(wide_bins_kernel<DT, VEC, false>, rows, a, st);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_dep(wide_cand_kernel<DT, VEC>, slices, a, st)) != cudaSuccess) return e;
+  }
   if ((e = launch_dep(wide_cut_kernel<DT>, rows, a, st)) != cudaSuccess) return e;
   return launch_dep(wide_draw_kernel<DT, VEC>, items < slots ? items : slots, a, st);
 }

@@ -26,6 +26,10 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     tot = {key: sum(r[key] for r in recs) for key in ("requests", "flagged", "mismatched")}
     tr.write_line(f"{len(recs)} stochastic cases, {tot['requests']} requests: "
                   f"{tot['flagged']} flagged, {tot['mismatched']} mismatched (each one flagged and valid)")
+    tied = sum(r.get("tied_pq", 0) for r in recs)
+    if tied:
+        tr.write_line(f"  {tied} p/q entries beyond 1e-5 on rows whose filter cut the oracle flags "
+                      f"(either kept set valid)")
     for r in recs:
         if r.get("full_size"):
             tr.write_line(f"  {r['case']}: {r['requests']} requests, {r['flagged']} flagged "

@@ -129,16 +129,28 @@ def check_chain(w, g, o, label, full_size=None):
     po = o["probs"][ok]
     pg = g["probs"][ok].astype(np.float64)
     big = po > 1e-30
-    rel = np.abs(pg[big] - po[big]) / po[big]
-    assert np.all(np.abs(pg[~big] - po[~big]) <= 1e-30)
-    assert rel.max(initial=0.0) <= PROB_RTOL, f"{label}: p/q relative error {rel.max()}"
+    err = np.where(big, np.abs(pg - po) / np.where(big, po, 1.0), np.abs(pg - po))
+    bad = np.where(big, err > PROB_RTOL, err > 1e-30)
+    # A filtered row whose cut the oracle flags as a near tie (reading F5 /
+    # F6: either kept set is a valid result) may hold one token more or less,
+    # which moves its p or q by that token's share; every other entry must
+    # agree to PROB_RTOL.
+    for bi, i, side in zip(*np.nonzero(bad)):
+        b = int(np.flatnonzero(ok)[bi])
+        msg = f"{label}: request {b} position {i} {'pq'[side]}: gpu {pg[bi, i, side]} oracle {po[bi, i, side]}"
+        assert filt is not None, "p/q relative error above PROB_RTOL: " + msg
+        row = w["target"][b, i] if side == 0 else w["draft"][b, i]
+        _, tie = oracle.filtered_softmax(row, w["temperature"], filt[0], filt[1], w["dtype"],
+                                         min_p=filt[2] if len(filt) > 2 else 0.0)
+        assert tie, "p/q differ on a row without a cut near tie: " + msg
+    rel = err[big & ~bad]
     want_seq = oracle.rollback(w["seq_lens"], g["num_accepted"], k)["new_lens"]
     assert np.array_equal(g["seq_lens"], want_seq), f"{label}: seq_lens"
     if full_size in FLAG_CEILING:
         assert flagged <= FLAG_CEILING[full_size] * B, \
             f"{label}: {flagged} of {B} requests flagged, above the stated {FLAG_CEILING[full_size]:.0%}"
     _report.record(case=label, kind="filtered" if filt else "chain", requests=B, flagged=flagged,
-                   mismatched=mism, max_prob_rel_err=float(rel.max(initial=0.0)),
+                   mismatched=mism, max_prob_rel_err=float(rel.max(initial=0.0)), tied_pq=int(bad.sum()),
                    full_size=bool(full_size),
                    mean_accepted=float(np.mean(n_o[ok])) if ok.any() else 0.0)
     return flagged, mism
