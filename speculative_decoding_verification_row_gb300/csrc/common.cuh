@@ -86,8 +86,7 @@ struct WideRow {
   unsigned kmin_inv;        // ~ the smallest order key (ord32) among those tokens
   unsigned ncand;           // tokens appended to the row's candidate list
   int bk, blo, bhi;         // the top-k bin, the top-p bin range (-1: none)
-  int b0;                   // bins >= b0 are merged into the last bin (light tokens); while
-                            // the histogram is built, kWideBins + 1 - the slices' smallest b0
+  int b0;                   // bins >= b0 are merged into the last bin (light tokens)
   unsigned long long kcut;  // token t is kept iff make_key(x_t, t) >= kcut
   float M, Z;               // row maximum and (after the cut) kept mass, 2^(c(x - M)) units
   unsigned long long ztot;  // the row's total fixed-point mass

@@ -449,7 +449,9 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   WideRow* wr = a.ws.wrow + rr;
   if (tid == 0) {
     if (s == 0) wr->M = M;                          // every slice of the row computes the same
-    if (BINS) atomicMax(&wr->b0, kWideBins + 1 - b1);  // the row's shallowest light depth, encoded
+    // The record's b0 holds kWideBins + 1 - (the smallest light depth of the
+    // row's slices) until the bins grid replaces it with the row's depth.
+    if (BINS) atomicMax(&wr->b0, kWideBins + 1 - b1);
   }
   const HistParams h = hist_params(a, M, b1, BINS, MINP);
   unsigned long long zmin = 0;
