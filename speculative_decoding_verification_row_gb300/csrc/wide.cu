@@ -34,7 +34,9 @@
 //      shallowest slice depth) and otherwise rebuilds the row's histogram
 //      itself with the a-priori depth D0 = log2(V / ((1 - top_p) Z)) + 1
 //      (the V tokens below it weigh at most (1 - top_p) Z / 2) or, for
-//      top-k, every token counted.  Then prefix sums give the bin where the
+//      top-k, every token counted (and, should the cut still lie deeper --
+//      top_p within pass 1's rounding of 1 -- every token binned, the total
+//      then exact).  Then prefix sums give the bin where the
 //      top-k count is reached and the range of bins the top-p threshold can
 //      fall in (the top-k mass is known to within the top-k bin); the bins
 //      are rewritten as their exclusive prefix sums.
@@ -386,7 +388,7 @@ __device__ int sample_depth(const uint32_t (&w0)[Io<DT, VEC>::NW], bool valid, c
 }
 
 // BINS = false (min_p alone): no histogram, only the min_p mass and key.
-// COUNT: top-k cuts (the light tokens then need no mass unless top_k >= V).
+// COUNT: top-k cuts (every token counted and binned when top_k >= V).
 template <int DT, bool VEC, bool COUNT, bool MINP, bool BINS>
 __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs a) {
   __shared__ unsigned hm[3][kWideBins];
@@ -582,19 +584,27 @@ __global__ void __launch_bounds__(kThreads, 4) wide_bins_kernel(const ChainArgs 
     block_excl_u64(tm, &zh);
     block_excl_u64(cm, &C);
     if (count_cut) block_excl_u64(cc, &NC);
-    Z = COUNT ? zh : max(zh, to_fixed(Zs * 256.f));
+    Z = COUNT || b1 >= kWideBins ? zh : max(zh, to_fixed(Zs * 256.f));  // (every token heavy: exact)
+  };
+  // The cut lies above depth b1 iff the bins above it reach the top-k count
+  // (top-k) or the top-p threshold of the total mass (top-p alone); an
+  // empty row has no cut.
+  auto cut_above = [&]() {
+    return b1 >= kWideBins || Z == 0 ||
+           (count_cut ? NC >= (unsigned long long)a.top_k : C >= top_p_threshold(a.top_p, Z));
   };
   gather();
-  // The cut lies above depth b1 iff the bins above it reach the top-k count
-  // (top-k) or the top-p threshold of the total mass (top-p alone); when it
-  // does not, the row is rebuilt with the a-priori depth (an empty row has
-  // nothing to rebuild).
-  const bool ok = b1 >= kWideBins || Z == 0 ||
-                  (count_cut ? NC >= (unsigned long long)a.top_k : C >= top_p_threshold(a.top_p, Z));
-  if (!ok) {  // (uniform)
+  if (!cut_above()) {  // (uniform) rebuilt with the a-priori depth
     b1 = COUNT ? kWideBins : safe_depth_bin(a, Zs);
     rebuild_row<DT, VEC, COUNT>(a, rr, wr->M, b1, sq[tid >> 5], shq[tid >> 5], gh0, gc0);
     gather();
+    // top_p so close to 1 that the a-priori depth's margin, (1 - top_p) Z / 2,
+    // is within the rounding of pass 1's total: every token binned, exactly
+    if (!cut_above()) {
+      b1 = kWideBins;
+      rebuild_row<DT, VEC, COUNT>(a, rr, wr->M, b1, sq[tid >> 5], shq[tid >> 5], gh0, gc0);
+      gather();
+    }
   }
   if (b1 < kWideBins) {  // the bins from b1 on merge into the last bin
 #pragma unroll

@@ -95,11 +95,15 @@ def test_cuda_wide_filter_leaves_the_workspace_zero(V, top_k, top_p):
 
 
 @pytest.mark.parametrize("T,top_k,top_p,min_p", [(0.7, 0, 1.0, 0.999), (1.5, 0, 0.95, 0.0), (0.05, 0, 0.9, 0.0),
-                                                  (5.0, 0, 0.9, 0.0), (5.0, 3000, 0.95, 0.01)])
+                                                  (5.0, 0, 0.9, 0.0), (5.0, 3000, 0.95, 0.01),
+                                                  (1.0, 0, float(np.nextafter(np.float32(1), np.float32(0))), 0.0)])
 def test_cuda_wide_filter_edge_parameters(T, top_k, top_p, min_p):
     # min_p near 1 keeps the maxima only; a very low temperature (a few
     # tokens hold the mass) and high ones (flat rows: tens of thousands of
-    # tokens kept, the tail bound deep in the row).
+    # tokens kept, the tail bound deep in the row); top_p one float below 1
+    # (the a-priori tail bound, (1 - top_p) Z / 2, is then within the
+    # rounding of the row's total; a row whose cut the bound does not place
+    # is binned token by token).
     from test_gpu_parity import check_chain
     w = workloads.make("chain_b64_k7_v128256_bf16", seed=60, B=4, V=50000)
     w["temperature"] = T
@@ -234,3 +238,40 @@ def test_cuda_wide_filter_b256_full_size_sampled():
                seq_lens=w["seq_lens"][sel])
     check_chain(sub, {key: g[key][sel] for key in g}, _oracle_filtered(sub, 0, 0.7),
                 "wide filter b256 full size (sampled)", full_size="wide top-p b256")
+
+
+def _misleading_rows(w, ntop, seed):
+    """Rows whose first 2048 logits of every 16384 (each slice's sample, for
+    bf16 rows of a multiple of 16384) hold `ntop` tokens at the top and
+    nothing else of weight, while the rest of the row carries most of the
+    mass a little lower: a depth estimated from those 2048 falls far above
+    the cut, so the exact check must send the row to the rebuild."""
+    rng = np.random.default_rng(seed)
+    B, k, V = w["B"], w["k"], w["V"]
+    tgt = (-3.0 + 0.5 * rng.standard_normal((B, k + 1, V))).astype(np.float32)
+    for s in range(0, V, 16384):
+        hi = min(V, s + 2048)
+        tgt[..., s:hi] = -60.0
+        for b in range(B):
+            for r in range(k + 1):
+                pos = s + rng.choice(hi - s, size=min(ntop, hi - s), replace=False)
+                tgt[b, r, pos] = (0.1 * rng.standard_normal(pos.size)).astype(np.float32)
+    drf = tgt[:, :k] + (0.3 * rng.standard_normal((B, k, V))).astype(np.float32)
+    w["target"] = workloads.f32_to_bf16_bits(tgt)
+    w["draft"] = workloads.f32_to_bf16_bits(drf)
+    w["temperature"] = 1.0
+
+
+@pytest.mark.parametrize("ntop,top_k,top_p", [(40, 0, 0.9), (250, 1000, 0.95)])
+def test_cuda_wide_filter_misleading_sample(ntop, top_k, top_p):
+    # The histogram grid bins only the tokens above a light depth each slice
+    # estimates from a sample of itself; the bins grid checks exactly that
+    # the cut lies above the row's shallowest such depth and otherwise
+    # rebuilds the row's histogram with the a-priori depth (or every token
+    # counted, for top-k).  These rows take that path.
+    from test_gpu_parity import check_chain
+    w = workloads.make("chain_b64_k7_v128256_bf16", seed=63, B=3, V=49152)  # three full slices
+    _misleading_rows(w, ntop, 63)
+    w["draft_tokens"] = _filtered_tokens(w, top_k, top_p, 63)
+    g = _run_filtered(w, top_k, top_p)
+    check_chain(w, g, _oracle_filtered(w, top_k, top_p), f"wide misleading sample {ntop} {top_k} {top_p}")
