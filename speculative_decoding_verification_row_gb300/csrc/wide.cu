@@ -16,7 +16,7 @@
 // min_p alone), each a programmatic dependent that waits for its
 // predecessor before reading (no polling):
 //   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima and sums.
-//   2. wide_hist_kernel, one CTA per 32 KB slice.  Only the heavy tokens,
+//   2. wide_hist_kernel, one CTA per two 32 KB slices.  Only the heavy tokens,
 //      those above a light depth, are binned: bin floor(32 c (M - x)) (2048
 //      bins of 1/32 log2 unit), exact mass (and count when top-k cuts).  The
 //      depth comes from a sample of the slice (an eighth): where the row's
@@ -186,8 +186,8 @@ __device__ __forceinline__ HistParams hist_params(const ChainArgs& a, float M, i
 }
 
 // Where heavy tokens go: the CTA's shared histogram (three 14-bit parts of
-// the 2^-40 fixed point in 32-bit adds; at most 2^14 tokens reach it between
-// two flushes, so each part's sum stays below 2^28) ...
+// the 2^-40 fixed point in 32-bit adds; at most 2^15 tokens -- two slices --
+// reach it between two flushes, so each part's sum stays below 2^29) ...
 template <bool COUNT>
 struct SharedBins {
   unsigned (*hm)[kWideBins];
@@ -404,7 +404,10 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   __shared__ unsigned s_k[kWarps];
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rr = blockIdx.x / a.nsplit, s = blockIdx.x - rr * a.nsplit;
+  // two slices per CTA (2c, 2c + 1), in turn: the row statistics, the
+  // sampled depth (from the first) and the shared bins serve both
+  const int pairs = (a.nsplit + 1) >> 1;
+  const int rr = blockIdx.x / pairs, c = blockIdx.x - rr * pairs;
   int b, r;
   slice_row(a, rr, b, r);
   if (BINS)
@@ -424,19 +427,22 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   asm volatile("griddepcontrol.launch_dependents;");
   if (a.draft_lens && !row_used(a.k, a.draft_lens[b], r)) return;
   const char* row = row_ptr(a, b, r, (size_t)a.V * IO::ES);
-  const int vbeg = s * a.vps;
-  const int vend = min(a.nvec, vbeg + a.vps);
   uint32_t w[kVecPerThread][IO::NW];
+  auto load_slice = [&](int s) {
+    const int vbeg = s * a.vps, vend = min(a.nvec, vbeg + a.vps);
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int v = vbeg + tid + u * kThreads;
-    if (v < vend) {
-      IO::load(row, v, w[u]);
-    } else {  // past the row: -inf (no mass; never queued)
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int v = vbeg + tid + u * kThreads;
+      if (v < vend) {
+        IO::load(row, v, w[u]);
+      } else {  // past the row: -inf (no mass; never queued)
 #pragma unroll
-      for (int q = 0; q < IO::NW; ++q) w[u][q] = (VEC && DT == SPEC_BF16) ? 0xff80ff80u : 0xff800000u;
+        for (int q = 0; q < IO::NW; ++q) w[u][q] = (VEC && DT == SPEC_BF16) ? 0xff80ff80u : 0xff800000u;
+      }
     }
-  }
+  };
+  int vbeg = 2 * c * a.vps, vend = min(a.nvec, vbeg + a.vps);
+  load_slice(2 * c);
   float Zs;
   const float M = row_stats(a, rr, &Zs);  // also orders the clearing above before the adds
   const bool count_active = COUNT && a.top_k < a.V;  // (else every token is counted)
@@ -450,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   }
   WideRow* wr = a.ws.wrow + rr;
   if (tid == 0) {
-    if (s == 0) wr->M = M;                          // every slice of the row computes the same
+    if (c == 0) wr->M = M;                          // every CTA of the row computes the same
     // The record's b0 holds kWideBins + 1 - (the smallest light depth of the
     // row's slices) until the bins grid replaces it with the row's depth.
     if (BINS) atomicMax(&wr->b0, kWideBins + 1 - b1);
@@ -460,6 +466,13 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   unsigned kinv = 0;
   hist_slice<DT, VEC, MINP, BINS>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vbeg + tid, vend, h, zmin,
                                   kinv);
+  if (2 * c + 1 < a.nsplit) {  // (uniform) the second slice
+    load_slice(2 * c + 1);
+    vbeg = (2 * c + 1) * a.vps;
+    vend = min(a.nvec, vbeg + a.vps);
+    hist_slice<DT, VEC, MINP, BINS>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vbeg + tid, vend, h,
+                                    zmin, kinv);
+  }
   if constexpr (BINS) {
     unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
     unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
@@ -1197,14 +1210,15 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
   const long items = (long)a.B * a.nsplit2;
   if ((e = launch_first(chain_rowstats_kernel<DT, VEC>, slices, kThreads, st, a)) != cudaSuccess) return e;
   const bool cnt = a.top_k > 0, mp = a.min_p > 0.f;
+  const long hist = rows * ((a.nsplit + 1) / 2);  // two slices per CTA
   if (cnt)
-    e = mp ? launch_dep(wide_hist_kernel<DT, VEC, true, true, true>, slices, a, st)
-           : launch_dep(wide_hist_kernel<DT, VEC, true, false, true>, slices, a, st);
+    e = mp ? launch_dep(wide_hist_kernel<DT, VEC, true, true, true>, hist, a, st)
+           : launch_dep(wide_hist_kernel<DT, VEC, true, false, true>, hist, a, st);
   else if (a.top_p < 1.f)
-    e = mp ? launch_dep(wide_hist_kernel<DT, VEC, false, true, true>, slices, a, st)
-           : launch_dep(wide_hist_kernel<DT, VEC, false, false, true>, slices, a, st);
+    e = mp ? launch_dep(wide_hist_kernel<DT, VEC, false, true, true>, hist, a, st)
+           : launch_dep(wide_hist_kernel<DT, VEC, false, false, true>, hist, a, st);
   else  // min_p alone
-    e = launch_dep(wide_hist_kernel<DT, VEC, false, true, false>, slices, a, st);
+    e = launch_dep(wide_hist_kernel<DT, VEC, false, true, false>, hist, a, st);
   if (e != cudaSuccess) return e;
   if (cnt || a.top_p < 1.f) {  // (min_p alone: no bins, no candidates)
     e = cnt ? launch_dep(wide_bins_kernel<DT, VEC, true>, rows, a, st)
