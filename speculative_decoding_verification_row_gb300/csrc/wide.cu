@@ -16,7 +16,7 @@
 // min_p alone), each a programmatic dependent that waits for its
 // predecessor before reading (no polling):
 //   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima and sums.
-//   2. wide_hist_kernel, one CTA per two 32 KB slices.  Only the heavy tokens,
+//   2. wide_hist_kernel, one CTA per four 32 KB slices.  Only the heavy tokens,
 //      those above a light depth, are binned: bin floor(32 c (M - x)) (2048
 //      bins of 1/32 log2 unit), exact mass (and count when top-k cuts).  The
 //      depth comes from a sample of the slice (an eighth): where the row's
@@ -140,6 +140,7 @@ __device__ __forceinline__ unsigned long long top_p_threshold(float top_p, unsig
 
 // ------------------------------------------------------------------ 2
 constexpr int kQueue = 64;   // queued vectors a warp holds before binning them
+constexpr int kHistSlices = 4;  // 32 KB slices per histogram CTA
 constexpr int kLevels = 64;  // the sample's depth levels, half a log2 unit each
 
 // The light depth that bounds the mass below it a priori: the V tokens
@@ -186,8 +187,8 @@ __device__ __forceinline__ HistParams hist_params(const ChainArgs& a, float M, i
 }
 
 // Where heavy tokens go: the CTA's shared histogram (three 14-bit parts of
-// the 2^-40 fixed point in 32-bit adds; at most 2^15 tokens -- two slices --
-// reach it between two flushes, so each part's sum stays below 2^29) ...
+// the 2^-40 fixed point in 32-bit adds; at most 2^16 tokens -- four slices --
+// reach it between two flushes, so each part's sum stays below 2^30) ...
 template <bool COUNT>
 struct SharedBins {
   unsigned (*hm)[kWideBins];
@@ -404,10 +405,11 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   __shared__ unsigned s_k[kWarps];
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // two slices per CTA (2c, 2c + 1), in turn: the row statistics, the
-  // sampled depth (from the first) and the shared bins serve both
-  const int pairs = (a.nsplit + 1) >> 1;
-  const int rr = blockIdx.x / pairs, c = blockIdx.x - rr * pairs;
+  // kHistSlices slices per CTA (c kHistSlices ..), in turn: the row
+  // statistics, the sampled depth (from the first) and the shared bins
+  // serve them all
+  const int groups = (a.nsplit + kHistSlices - 1) / kHistSlices;
+  const int rr = blockIdx.x / groups, c = blockIdx.x - rr * groups;
   int b, r;
   slice_row(a, rr, b, r);
   if (BINS)
@@ -441,8 +443,9 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
       }
     }
   };
-  int vbeg = 2 * c * a.vps, vend = min(a.nvec, vbeg + a.vps);
-  load_slice(2 * c);
+  const int s0 = c * kHistSlices;
+  int vbeg = s0 * a.vps, vend = min(a.nvec, vbeg + a.vps);
+  load_slice(s0);
   float Zs;
   const float M = row_stats(a, rr, &Zs);  // also orders the clearing above before the adds
   const bool count_active = COUNT && a.top_k < a.V;  // (else every token is counted)
@@ -466,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   unsigned kinv = 0;
   hist_slice<DT, VEC, MINP, BINS>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vbeg + tid, vend, h, zmin,
                                   kinv);
-  if (2 * c + 1 < a.nsplit) {  // (uniform) the second slice
-    load_slice(2 * c + 1);
-    vbeg = (2 * c + 1) * a.vps;
+  for (int s = s0 + 1; s < min(a.nsplit, s0 + kHistSlices); ++s) {  // (uniform) the others
+    load_slice(s);
+    vbeg = s * a.vps;
     vend = min(a.nvec, vbeg + a.vps);
     hist_slice<DT, VEC, MINP, BINS>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vbeg + tid, vend, h,
                                     zmin, kinv);
@@ -1210,7 +1213,7 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
   const long items = (long)a.B * a.nsplit2;
   if ((e = launch_first(chain_rowstats_kernel<DT, VEC>, slices, kThreads, st, a)) != cudaSuccess) return e;
   const bool cnt = a.top_k > 0, mp = a.min_p > 0.f;
-  const long hist = rows * ((a.nsplit + 1) / 2);  // two slices per CTA
+  const long hist = rows * ((a.nsplit + kHistSlices - 1) / kHistSlices);
   if (cnt)
     e = mp ? launch_dep(wide_hist_kernel<DT, VEC, true, true, true>, hist, a, st)
            : launch_dep(wide_hist_kernel<DT, VEC, true, false, true>, hist, a, st);
