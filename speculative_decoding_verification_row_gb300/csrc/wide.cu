@@ -16,7 +16,8 @@
 // min_p alone), each a programmatic dependent that waits for its
 // predecessor before reading (no polling):
 //   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima and sums.
-//   2. wide_hist_kernel, one CTA per four 32 KB slices.  Only the heavy tokens,
+//   2. wide_hist_kernel, one CTA per 1 to 8 32 KB slices of a row (as many
+//      as keep the grid at a full wave or more).  Only the heavy tokens,
 //      those above a light depth, are binned: bin floor(32 c (M - x)) (2048
 //      bins of 1/32 log2 unit), exact mass (and count when top-k cuts).  The
 //      depth comes from a sample of the slice (an eighth): where the row's
@@ -56,6 +57,7 @@
 // Every call leaves the histograms, candidate lists, row records and
 // statistics words zero, as the chain path does (a later call's layout may
 // place its statistics words there).
+#include <algorithm>
 #include <mutex>
 
 #include "draw.cuh"
@@ -140,7 +142,7 @@ __device__ __forceinline__ unsigned long long top_p_threshold(float top_p, unsig
 
 // ------------------------------------------------------------------ 2
 constexpr int kQueue = 64;   // queued vectors a warp holds before binning them
-constexpr int kHistSlices = 4;  // 32 KB slices per histogram CTA
+constexpr int kHistSlices = 8;  // 32 KB slices per histogram CTA, at most
 constexpr int kLevels = 64;  // the sample's depth levels, half a log2 unit each
 
 // The light depth that bounds the mass below it a priori: the V tokens
@@ -187,8 +189,9 @@ __device__ __forceinline__ HistParams hist_params(const ChainArgs& a, float M, i
 }
 
 // Where heavy tokens go: the CTA's shared histogram (three 14-bit parts of
-// the 2^-40 fixed point in 32-bit adds; at most 2^16 tokens -- four slices --
-// reach it between two flushes, so each part's sum stays below 2^30) ...
+// the 2^-40 fixed point in 32-bit adds; at most 2^17 tokens -- kHistSlices
+// slices -- reach it between two flushes, so each part's sum stays below
+// 2^31) ...
 template <bool COUNT>
 struct SharedBins {
   unsigned (*hm)[kWideBins];
@@ -405,10 +408,12 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   __shared__ unsigned s_k[kWarps];
   using IO = Io<DT, VEC>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // kHistSlices slices per CTA (c kHistSlices ..), in turn: the row
-  // statistics, the sampled depth (from the first) and the shared bins
-  // serve them all
-  const int groups = (a.nsplit + kHistSlices - 1) / kHistSlices;
+  // Each row's slices are split among `groups` CTAs (the grid's size over
+  // the rows), spc consecutive slices each, taken in turn: the row
+  // statistics, the sampled depth (from the first) and the shared bins serve
+  // them all.
+  const int groups = (int)(gridDim.x / ((unsigned)a.B * (unsigned)a.rows));
+  const int spc = (a.nsplit + groups - 1) / groups;
   const int rr = blockIdx.x / groups, c = blockIdx.x - rr * groups;
   int b, r;
   slice_row(a, rr, b, r);
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
       }
     }
   };
-  const int s0 = c * kHistSlices;
+  const int s0 = c * spc;
   int vbeg = s0 * a.vps, vend = min(a.nvec, vbeg + a.vps);
   load_slice(s0);
   float Zs;
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
   unsigned kinv = 0;
   hist_slice<DT, VEC, MINP, BINS>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vbeg + tid, vend, h, zmin,
                                   kinv);
-  for (int s = s0 + 1; s < min(a.nsplit, s0 + kHistSlices); ++s) {  // (uniform) the others
+  for (int s = s0 + 1; s < min(a.nsplit, s0 + spc); ++s) {  // (uniform) the others
     load_slice(s);
     vbeg = s * a.vps;
     vend = min(a.nvec, vbeg + a.vps);
@@ -1177,6 +1182,23 @@ cudaError_t launch_dep(K kernel, long grid, const ChainArgs& a, cudaStream_t st)
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// The current device's SM count (cached per device).
+cudaError_t sm_count(int* out) {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    e = cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  *out = cached[dev];
+  return cudaSuccess;
+}
+
 template <int DT, bool VEC>
 cudaError_t wide_draw_grid(int* grid) {
   static std::mutex mu;
@@ -1213,7 +1235,12 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
   const long items = (long)a.B * a.nsplit2;
   if ((e = launch_first(chain_rowstats_kernel<DT, VEC>, slices, kThreads, st, a)) != cudaSuccess) return e;
   const bool cnt = a.top_k > 0, mp = a.min_p > 0.f;
-  const long hist = rows * ((a.nsplit + kHistSlices - 1) / kHistSlices);
+  // Slices per histogram CTA: up to kHistSlices, while the grid still fills
+  // every SM with four CTAs.
+  int sms = 0;
+  if ((e = sm_count(&sms)) != cudaSuccess) return e;
+  const long spc = std::max(1L, std::min((long)kHistSlices, slices / (4L * sms)));
+  const long hist = rows * ((a.nsplit + spc - 1) / spc);
   if (cnt)
     e = mp ? launch_dep(wide_hist_kernel<DT, VEC, true, true, true>, hist, a, st)
            : launch_dep(wide_hist_kernel<DT, VEC, true, false, true>, hist, a, st);
