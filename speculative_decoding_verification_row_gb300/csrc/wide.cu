@@ -12,9 +12,10 @@
 // maximum).  Masses that decide a cut are summed in 2^-40 fixed point, so
 // those sums are exact whatever their order; a row's total mass comes from
 // pass 1's slice sums (fp32, about 1e-7 relative, far inside the oracle's
-// 1e-6 near-tie window on the top-p cut).  Six stream-ordered grids (four for
-// min_p alone), each a programmatic dependent that waits for its
-// predecessor before reading (no polling):
+// 1e-6 near-tie window on the top-p cut).  Up to six stream-ordered grids
+// (five when each row has one histogram CTA, four for min_p alone), each a
+// programmatic dependent that waits for its predecessor before reading (no
+// polling):
 //   1. chain_rowstats_kernel (the chain's pass 1): the slice maxima and sums.
 //   2. wide_hist_kernel, one CTA per 1 to 8 32 KB slices of a row (as many
 //      as keep the grid at a full wave or more).  Only the heavy tokens,
@@ -28,19 +29,20 @@
 //      compare; the others are queued per warp and their tokens binned one
 //      per lane.  The same pass sums min_p's mass and key.  min_p alone
 //      needs no bins.
-//   3. wide_bins_kernel, one CTA per row: the row's total mass is pass 1's
-//      (never below the heavy tokens' exact sum: the light ones are the
-//      rest); it checks exactly that the cut lies among the bins every slice
-//      filled (the top-k count or the top-p threshold is reached above the
-//      shallowest slice depth) and otherwise rebuilds the row's histogram
-//      itself with the a-priori depth D0 = log2(V / ((1 - top_p) Z)) + 1
+//   3. the bins step (bins_step): by the histogram CTA itself when it holds
+//      the whole row, else by wide_bins_kernel, one CTA per row.  The row's
+//      total mass is pass 1's (never below the heavy tokens' exact sum: the
+//      light ones are the rest).  It checks exactly that the cut lies among
+//      the bins every CTA filled (the top-k count or the top-p threshold is
+//      reached above the shallowest depth) and otherwise rebuilds the row's
+//      histogram with the a-priori depth D0 = log2(V / ((1 - top_p) Z)) + 1
 //      (the V tokens below it weigh at most (1 - top_p) Z / 2) or, for
 //      top-k, every token counted (and, should the cut still lie deeper --
 //      top_p within pass 1's rounding of 1 -- every token binned, the total
-//      then exact).  Then prefix sums give the bin where the
-//      top-k count is reached and the range of bins the top-p threshold can
-//      fall in (the top-k mass is known to within the top-k bin); the bins
-//      are rewritten as their exclusive prefix sums.
+//      then exact).  Then prefix sums give the bin where the top-k count is
+//      reached and the range of bins the top-p threshold can fall in (the
+//      top-k mass is known to within the top-k bin); the bins are rewritten
+//      as their exclusive prefix sums.
 //   4. wide_cand_kernel, one CTA per slice: the tokens of those bins (as
 //      logit intervals, slightly widened) are listed per row (most rows:
 //      tens to hundreds).
@@ -391,6 +393,138 @@ __device__ int sample_depth(const uint32_t (&w0)[Io<DT, VEC>::NW], bool valid, c
   return *b1out;
 }
 
+// Bins b of a row are held 8 per thread (thread t: 8t .. 8t + 7).
+constexpr int kBinsPerThread = kWideBins / kThreads;
+static_assert(kBinsPerThread * kThreads == kWideBins, "bins per thread");
+
+// The bins step of one row, by one CTA.  load(m, c) gives this thread's
+// bins 8 tid .. 8 tid + 7 (mass, count) as the histogram left them (bins
+// below b1 complete, the deeper ones partial); rebuild(b) rebuilds the
+// histogram with light depth b.  The row's total mass is pass 1's (Zs,
+// never below the heavy tokens' exact sum; the light tokens' share of it is
+// not binned) for top-p, the exact sum when every token is heavy (top-k, or
+// b = kWideBins).  The cut must lie above b1: the bins above it must reach
+// the top-k count (top-k) or the top-p threshold of the total (top-p alone);
+// if not, the row is rebuilt with the a-priori depth (every token counted,
+// for top-k), and, should top_p be within pass 1's rounding of 1, with every
+// token binned.  Then the bins become their exclusive prefix sums (gh, gc:
+// this thread's eight) and the row's record gets the top-k bin, the top-p
+// bin range, the light depth and the total.
+template <bool COUNT, class Load, class Rebuild>
+__device__ __forceinline__ void bins_step(const ChainArgs& a, WideRow* wr, int b1, float Zs, const Load& load,
+                                          const Rebuild& rebuild, unsigned long long* gh, unsigned* gc) {
+  __shared__ int s_bk, s_blo, s_bhi;
+  __shared__ unsigned long long s_mb, s_mbin;
+  const int tid = threadIdx.x;
+  const bool count_cut = COUNT && a.top_k < a.V;
+  unsigned long long m[kBinsPerThread];
+  unsigned c[kBinsPerThread];
+  unsigned long long Z = 0, C = 0, NC = 0;
+  auto gather = [&]() {  // the bins, the heavy total, the complete region's mass (count)
+    load(m, c);
+    unsigned long long tm = 0, cm = 0, cc = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      tm += m[j];
+      if (kBinsPerThread * tid + j < b1) {
+        cm += m[j];
+        cc += c[j];
+      }
+    }
+    unsigned long long zh;
+    block_excl_u64(tm, &zh);
+    block_excl_u64(cm, &C);
+    if (count_cut) block_excl_u64(cc, &NC);
+    Z = COUNT || b1 >= kWideBins ? zh : max(zh, to_fixed(Zs * 256.f));  // (every token heavy: exact)
+  };
+  auto cut_above = [&]() {  // (an empty row has no cut)
+    return b1 >= kWideBins || Z == 0 ||
+           (count_cut ? NC >= (unsigned long long)a.top_k : C >= top_p_threshold(a.top_p, Z));
+  };
+  gather();
+  if (!cut_above()) {  // (uniform)
+    b1 = COUNT ? kWideBins : safe_depth_bin(a, Zs);
+    rebuild(b1);
+    gather();
+    if (!cut_above()) {
+      b1 = kWideBins;
+      rebuild(b1);
+      gather();
+    }
+  }
+  if (b1 < kWideBins) {  // the bins from b1 on merge into the last bin
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      const int bin = kBinsPerThread * tid + j;
+      if (bin >= b1) {
+        m[j] = bin == kWideBins - 1 ? Z - C : 0;
+        c[j] = 0;
+      }
+    }
+  }
+  if (tid == 0) {
+    s_bk = s_blo = s_bhi = -1;
+    s_mb = 0;
+    s_mbin = 0;
+  }
+  unsigned long long tm = 0, tc = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    tm += m[j];
+    tc += c[j];
+  }
+  unsigned long long N;
+  const unsigned long long pm = block_excl_u64(tm, &Z);
+  const unsigned long long pc = COUNT ? block_excl_u64(tc, &N) : 0;
+  // top-k: the bin where the running count reaches top_k
+  if (count_cut) {
+    unsigned long long cb = pc, mb = pm;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      if (cb < (unsigned long long)a.top_k && (unsigned long long)a.top_k <= cb + c[j]) {
+        s_bk = kBinsPerThread * tid + j;
+        s_mb = mb;
+        s_mbin = m[j];
+      }
+      cb += c[j];
+      mb += m[j];
+    }
+  }
+  __syncthreads();
+  if (a.top_p < 1.f) {
+    // the top-k mass lies in [zlo, zhi]; so does the threshold's bin range
+    const unsigned long long zlo = s_bk >= 0 ? s_mb : Z, zhi = s_bk >= 0 ? s_mb + s_mbin : Z;
+    const unsigned long long tl = top_p_threshold(a.top_p, zlo), th = top_p_threshold(a.top_p, zhi);
+    unsigned long long mb = pm;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      if (mb < tl && tl <= mb + m[j]) s_blo = kBinsPerThread * tid + j;
+      if (mb < th && th <= mb + m[j]) s_bhi = kBinsPerThread * tid + j;
+      mb += m[j];
+    }
+  }
+  // The bins become their exclusive prefix sums (mass, and count when top-k
+  // cuts): the cut kernel reads the few it needs.
+  {
+    unsigned long long mb = pm, cb = pc;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      gh[j] = mb;
+      if (COUNT) gc[j] = (unsigned)cb;
+      mb += m[j];
+      cb += c[j];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    wr->bk = s_bk;
+    wr->blo = s_blo;
+    wr->bhi = s_blo >= 0 ? s_bhi : -1;
+    wr->b0 = b1;  // from here on: the row's light depth
+    wr->ztot = Z;
+  }
+}
+
 // BINS = false (min_p alone): no histogram, only the min_p mass and key.
 // COUNT: top-k cuts (every token counted and binned when top_k >= V).
 template <int DT, bool VEC, bool COUNT, bool MINP, bool BINS>
@@ -485,11 +619,44 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
     unsigned long long* gh = a.ws.whist + (size_t)rr * kWideBins;
     unsigned* gc = a.ws.wcount + (size_t)rr * kWideBins;
     __syncthreads();
-    for (int i = tid; i < min(b1, kWideBins); i += kThreads) {  // heavy bins lie below b1
-      const unsigned long long m =
-          ((unsigned long long)hm[2][i] << 28) + ((unsigned long long)hm[1][i] << 14) + hm[0][i];
-      if (m) atomicAdd(gh + i, m);
-      if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
+    auto bin_mass = [&](int i) {
+      return ((unsigned long long)hm[2][i] << 28) + ((unsigned long long)hm[1][i] << 14) + hm[0][i];
+    };
+    if (groups == 1) {
+      // (uniform) The whole row is here: the bins step in place, from the
+      // shared bins, a rebuild re-reading this CTA's slices into them.
+      auto load = [&](unsigned long long (&m)[kBinsPerThread], unsigned (&cn)[kBinsPerThread]) {
+#pragma unroll
+        for (int j = 0; j < kBinsPerThread; ++j) {
+          m[j] = bin_mass(kBinsPerThread * tid + j);
+          cn[j] = COUNT ? hc[kBinsPerThread * tid + j] : 0u;
+        }
+      };
+      auto rebuild = [&](int depth) {
+        __syncthreads();  // every thread has read the bins
+        for (int i = tid; i < kWideBins; i += kThreads) {
+          hm[0][i] = hm[1][i] = hm[2][i] = 0u;
+          if (COUNT) hc[i] = 0;
+        }
+        __syncthreads();
+        const HistParams hb = hist_params(a, M, depth, true, false);
+        for (int s = s0; s < min(a.nsplit, s0 + spc); ++s) {
+          load_slice(s);
+          const int vb = s * a.vps, ve = min(a.nvec, vb + a.vps);
+          unsigned long long zd = 0;
+          unsigned kd = 0;
+          hist_slice<DT, VEC, false, true>(SharedBins<COUNT>{hm, hc}, sq[warp], shq[warp], w, vb + tid, ve, hb,
+                                           zd, kd);
+        }
+        __syncthreads();
+      };
+      bins_step<COUNT>(a, wr, b1, Zs, load, rebuild, gh + kBinsPerThread * tid, gc + kBinsPerThread * tid);
+    } else {
+      for (int i = tid; i < min(b1, kWideBins); i += kThreads) {  // heavy bins lie below b1
+        const unsigned long long m = bin_mass(i);
+        if (m) atomicAdd(gh + i, m);
+        if (COUNT && hc[i]) atomicAdd(gc + i, hc[i]);
+      }
     }
   }
   if (MINP) {
@@ -518,9 +685,6 @@ __global__ void __launch_bounds__(kThreads, 4) wide_hist_kernel(const ChainArgs 
 }
 
 // ------------------------------------------------------------------ 3
-// Bins b of a row are held 8 per thread (thread t: 8t .. 8t + 7).
-constexpr int kBinsPerThread = kWideBins / kThreads;
-static_assert(kBinsPerThread * kThreads == kWideBins, "bins per thread");
 
 // The row's histogram rebuilt by this one CTA with light depth b0 (every
 // token heavy when b0 = kWideBins), its slices streaming through the
@@ -560,12 +724,12 @@ __device__ void rebuild_row(const ChainArgs& a, int rr, float M, int b0, uint4* 
   __syncthreads();  // the adds above before the reads after
 }
 
+// Rows split over several histogram CTAs: the bins step on the row's global
+// histogram, a rebuild streaming the row through this CTA.
 template <int DT, bool VEC, bool COUNT>
 __global__ void __launch_bounds__(kThreads, 4) wide_bins_kernel(const ChainArgs a) {
   __shared__ uint4 sq[kWarps][kQueue];
   __shared__ float shq[kWarps][64];
-  __shared__ int s_bk, s_blo, s_bhi;
-  __shared__ unsigned long long s_mb, s_mbin;
   const int tid = threadIdx.x;
   const int rr = blockIdx.x, b = rr / a.rows, r = rr - b * a.rows;
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -576,128 +740,20 @@ __global__ void __launch_bounds__(kThreads, 4) wide_bins_kernel(const ChainArgs 
   unsigned long long* gh = gh0 + kBinsPerThread * tid;
   unsigned* gc = gc0 + kBinsPerThread * tid;
   WideRow* wr = a.ws.wrow + rr;
-  const bool count_cut = COUNT && a.top_k < a.V;
-  // The row's shallowest light depth: bins below b1 hold every token of
-  // theirs; deeper bins hold only some slices' tokens.
-  int b1 = kWideBins + 1 - wr->b0;
-  // Top-p: the row's total mass is pass 1's (its slice sums), never below
-  // the heavy tokens' exact sum; the light tokens' share of it is not
-  // binned.  Top-k: the count decides, and with top_k >= V every token is
-  // heavy (the exact sum).
+  const int b1 = kWideBins + 1 - wr->b0;  // the row's shallowest slice depth (encoded by the slices)
   float Zs = 0.f;
   if (!COUNT) row_stats(a, rr, &Zs);
-  unsigned long long m[kBinsPerThread];
-  unsigned c[kBinsPerThread];
-  unsigned long long Z = 0, C = 0, NC = 0;
-  auto gather = [&]() {  // this thread's bins, the heavy total, the complete region's mass (count)
-    unsigned long long tm = 0, cm = 0, cc = 0;
+  auto load = [&](unsigned long long (&m)[kBinsPerThread], unsigned (&c)[kBinsPerThread]) {
 #pragma unroll
     for (int j = 0; j < kBinsPerThread; ++j) {
       m[j] = gh[j];
       c[j] = COUNT ? gc[j] : 0u;
-      tm += m[j];
-      if (kBinsPerThread * tid + j < b1) {
-        cm += m[j];
-        cc += c[j];
-      }
     }
-    unsigned long long zh;
-    block_excl_u64(tm, &zh);
-    block_excl_u64(cm, &C);
-    if (count_cut) block_excl_u64(cc, &NC);
-    Z = COUNT || b1 >= kWideBins ? zh : max(zh, to_fixed(Zs * 256.f));  // (every token heavy: exact)
   };
-  // The cut lies above depth b1 iff the bins above it reach the top-k count
-  // (top-k) or the top-p threshold of the total mass (top-p alone); an
-  // empty row has no cut.
-  auto cut_above = [&]() {
-    return b1 >= kWideBins || Z == 0 ||
-           (count_cut ? NC >= (unsigned long long)a.top_k : C >= top_p_threshold(a.top_p, Z));
+  auto rebuild = [&](int depth) {
+    rebuild_row<DT, VEC, COUNT>(a, rr, wr->M, depth, sq[tid >> 5], shq[tid >> 5], gh0, gc0);
   };
-  gather();
-  if (!cut_above()) {  // (uniform) rebuilt with the a-priori depth
-    b1 = COUNT ? kWideBins : safe_depth_bin(a, Zs);
-    rebuild_row<DT, VEC, COUNT>(a, rr, wr->M, b1, sq[tid >> 5], shq[tid >> 5], gh0, gc0);
-    gather();
-    // top_p so close to 1 that the a-priori depth's margin, (1 - top_p) Z / 2,
-    // is within the rounding of pass 1's total: every token binned, exactly
-    if (!cut_above()) {
-      b1 = kWideBins;
-      rebuild_row<DT, VEC, COUNT>(a, rr, wr->M, b1, sq[tid >> 5], shq[tid >> 5], gh0, gc0);
-      gather();
-    }
-  }
-  if (b1 < kWideBins) {  // the bins from b1 on merge into the last bin
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-      const int bin = kBinsPerThread * tid + j;
-      if (bin >= b1) {
-        m[j] = bin == kWideBins - 1 ? Z - C : 0;
-        c[j] = 0;
-      }
-    }
-  }
-  if (tid == 0) {
-    s_bk = s_blo = s_bhi = -1;
-    s_mb = 0;
-    s_mbin = 0;
-  }
-  unsigned long long tm = 0, tc = 0;
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; ++j) {
-    tm += m[j];
-    tc += c[j];
-  }
-  unsigned long long N;
-  const unsigned long long pm = block_excl_u64(tm, &Z);
-  const unsigned long long pc = COUNT ? block_excl_u64(tc, &N) : 0;
-  // top-k: the bin where the running count reaches top_k
-  if (count_cut) {
-    unsigned long long cb = pc, mb = pm;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-      if (cb < (unsigned long long)a.top_k && (unsigned long long)a.top_k <= cb + c[j]) {
-        s_bk = kBinsPerThread * tid + j;
-        s_mb = mb;
-        s_mbin = m[j];
-      }
-      cb += c[j];
-      mb += m[j];
-    }
-  }
-  __syncthreads();
-  if (a.top_p < 1.f) {
-    // the top-k mass lies in [zlo, zhi]; so does the threshold's bin range
-    const unsigned long long zlo = s_bk >= 0 ? s_mb : Z, zhi = s_bk >= 0 ? s_mb + s_mbin : Z;
-    const unsigned long long tl = top_p_threshold(a.top_p, zlo), th = top_p_threshold(a.top_p, zhi);
-    unsigned long long mb = pm;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-      if (mb < tl && tl <= mb + m[j]) s_blo = kBinsPerThread * tid + j;
-      if (mb < th && th <= mb + m[j]) s_bhi = kBinsPerThread * tid + j;
-      mb += m[j];
-    }
-  }
-  // The bins become their exclusive prefix sums (mass, and count when top-k
-  // cuts): the cut kernel reads the few it needs.
-  {
-    unsigned long long mb = pm, cb = pc;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-      gh[j] = mb;
-      if (COUNT) gc[j] = (unsigned)cb;
-      mb += m[j];
-      cb += c[j];
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    wr->bk = s_bk;
-    wr->blo = s_blo;
-    wr->bhi = s_blo >= 0 ? s_bhi : -1;
-    wr->b0 = b1;  // from here on: the row's light depth
-    wr->ztot = Z;
-  }
+  bins_step<COUNT>(a, wr, b1, Zs, load, rebuild, gh, gc);
 }
 
 // ------------------------------------------------------------------ 4
@@ -1251,9 +1307,12 @@ cudaError_t launch_wide_t(const ChainArgs& args, cudaStream_t st) {
     e = launch_dep(wide_hist_kernel<DT, VEC, false, true, false>, hist, a, st);
   if (e != cudaSuccess) return e;
   if (cnt || a.top_p < 1.f) {  // (min_p alone: no bins, no candidates)
-    e = cnt ? launch_dep(wide_bins_kernel<DT, VEC, true>, rows, a, st)
-            : launch_dep(wide_bins_kernel<DT, VEC, false>, rows, a, st);
-    if (e != cudaSuccess) return e;
+    // one histogram CTA per row runs the bins step itself
+    if (hist > rows) {
+      e = cnt ? launch_dep(wide_bins_kernel<DT, VEC, true>, rows, a, st)
+              : launch_dep(wide_bins_kernel<DT, VEC, false>, rows, a, st);
+      if (e != cudaSuccess) return e;
+    }
     if ((e = launch_dep(wide_cand_kernel<DT, VEC>, slices, a, st)) != cudaSuccess) return e;
   }
   if ((e = launch_dep(wide_cut_kernel<DT>, rows, a, st)) != cudaSuccess) return e;

@@ -262,16 +262,19 @@ def _misleading_rows(w, ntop, seed):
     w["temperature"] = 1.0
 
 
-@pytest.mark.parametrize("ntop,top_k,top_p", [(40, 0, 0.9), (250, 1000, 0.95)])
-def test_cuda_wide_filter_misleading_sample(ntop, top_k, top_p):
-    # The histogram grid bins only the tokens above a light depth each slice
-    # estimates from a sample of itself; the bins grid checks exactly that
-    # the cut lies above the row's shallowest such depth and otherwise
-    # rebuilds the row's histogram with the a-priori depth (or every token
-    # counted, for top-k).  These rows take that path.
+@pytest.mark.parametrize("V,ntop,top_k,top_p", [(49152, 40, 0, 0.9), (49152, 250, 1000, 0.95),
+                                                (16384, 40, 0, 0.9), (16384, 450, 1000, 0.95)])
+def test_cuda_wide_filter_misleading_sample(V, ntop, top_k, top_p):
+    # The histogram grid bins only the tokens above a light depth each CTA
+    # estimates from a sample of its first slice; the bins step checks
+    # exactly that the cut lies above the row's shallowest such depth and
+    # otherwise rebuilds the row's histogram with the a-priori depth (or
+    # every token counted, for top-k).  These rows take that path: in the
+    # bins grid (three slices, several histogram CTAs per row) and in the
+    # histogram CTA itself (one slice: the CTA holds the whole row).
     from test_gpu_parity import check_chain
-    w = workloads.make("chain_b64_k7_v128256_bf16", seed=63, B=3, V=49152)  # three full slices
+    w = workloads.make("chain_b64_k7_v128256_bf16", seed=63, B=3, V=V)
     _misleading_rows(w, ntop, 63)
     w["draft_tokens"] = _filtered_tokens(w, top_k, top_p, 63)
     g = _run_filtered(w, top_k, top_p)
-    check_chain(w, g, _oracle_filtered(w, top_k, top_p), f"wide misleading sample {ntop} {top_k} {top_p}")
+    check_chain(w, g, _oracle_filtered(w, top_k, top_p), f"wide misleading sample V={V} {ntop} {top_k} {top_p}")
