@@ -285,9 +285,10 @@ def run_ours(args, rank, world, local):
             call_args.append((ptr(c["target"]), ptr(c["draft"]), code, ptr(c["tokens"]),
                               ptr(c["uniforms"]), ctypes.c_float(w["temperature"]), B, k, V,
                               ptr(out_tok), ptr(out_n), None, ptr(seq), ptr(buf), buf.numel(), sh))
-    # pass 1 and its programmatic-dependent finish/draw grid; the wide filter:
-    # pass 1, histogram, bins, candidates, cut, draw
-    launches_per_step = 6 if wide else 2
+    # pass 1 and its programmatic-dependent finish/draw grid; the wide filter
+    # as wide_launches counts it
+    launches_per_step = wide_launches(w, args, torch.cuda.get_device_properties(device).multi_processor_count) \
+        if wide else 2
 
     for i in range(args.warmup):
         rc = fn(*call_args[i & 1])
@@ -439,7 +440,8 @@ def run_ours(args, rank, world, local):
             "kernel": {"chain": "spec_verify_chain call (chain_rowstats_kernel + chain_draw_kernel)",
                        "filtered": "spec_verify_chain_ex call (filter_max_kernel + filter_pick_kernel)",
                        "wide": "spec_verify_chain_ex call (chain_rowstats_kernel + wide_hist_kernel + "
-                               "wide_bins_kernel + wide_cand_kernel + wide_cut_kernel + wide_draw_kernel)",
+                               "[wide_bins_kernel] + wide_cand_kernel + wide_cut_kernel + wide_draw_kernel; "
+                               "min_p alone: no bins, no candidates)",
                        "greedy": "spec_verify_greedy call (argmax_kernel + argmax_finish_kernel)",
                        "tree": "spec_verify_tree call (argmax_kernel + argmax_finish_kernel)",
                        "tree_sampled": "spec_verify_tree_sampled call (chain_rowstats_kernel + tree_draw_kernel)"}[kernel_key],
@@ -456,6 +458,22 @@ def run_ours(args, rank, world, local):
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
+
+
+def wide_launches(w, args, sms: int) -> int:
+    """Grids one per-row-cut verify launches (the rule of wide.cu's launch):
+    pass 1, the histogram, the bins grid when a row's slices are split over
+    several histogram CTAs (up to 8 slices of 2048 16-byte vectors per CTA,
+    as many as keep the grid at 4 CTAs per SM), the candidates, the cut and
+    the draw; min_p alone has no bins and no candidates."""
+    if args.top_k == 0 and args.top_p >= 1.0 and args.min_p > 0.0:
+        return 4
+    es = 2 if w["dtype"] == workloads.BF16 else 4
+    nvec = w["V"] * es // 16 if (w["V"] * es) % 16 == 0 else w["V"]  # (the bench's rows are aligned)
+    nsplit = -(-nvec // 2048)
+    rows = w["B"] * (2 * w["k"] + 1)
+    spc = max(1, min(8, rows * nsplit // (4 * sms)))
+    return 6 if -(-nsplit // spc) > 1 else 5
 
 
 def is_filtered(args):

@@ -170,3 +170,18 @@ def test_param_structs_match_the_header(tmp_path):
         want.append(ctypes.sizeof(py))
         want += [getattr(py, f).offset for f, _ in py._fields_]
     assert got == want
+
+
+def test_bench_counts_the_wide_launches():
+    # bench.py's gpu_launches claim for per-row cuts follows wide.cu's launch
+    # rule: the bins grid only when a row's slices are split over several
+    # histogram CTAs, no bins and no candidates for min_p alone.
+    import types
+    import bench
+    import workloads
+    w = dict(B=64, k=7, V=128256, dtype=workloads.BF16)
+    args = types.SimpleNamespace(top_k=0, top_p=0.9, min_p=0.0)
+    assert bench.wide_launches(w, args, 152) == 5        # 8 slices, one CTA per row
+    assert bench.wide_launches(dict(w, B=2), args, 152) == 6  # small batch: rows split
+    assert bench.wide_launches(w, types.SimpleNamespace(top_k=1000, top_p=1.0, min_p=0.0), 152) == 5
+    assert bench.wide_launches(w, types.SimpleNamespace(top_k=0, top_p=1.0, min_p=0.05), 152) == 4
